@@ -1,0 +1,227 @@
+/*
+ * qsfm.h — C ABI of the quantized shared-KV sparse MLA attention forward
+ * (QuantSparseFlashMla / KvQuantSparseAttnSharedKv) for sm_103a.
+ *
+ * What is computed (QuantSparseFlashMla, "功能说明" (function description),
+ * formula O = softmax(Q K~^T * softmax_scale) V~ with K~ = V~; the per-head
+ * sink is the "sinks" row of its "参数说明" (parameter) table):
+ *
+ *   for every query token t (batch b, position s) and head h (N1 = 64 heads,
+ *   D = 512, one latent KV head, N2 = 1):
+ *     rows(t) = ori rows inside the band / causal window of t
+ *             ++ cmp rows (CSA: the valid entries of cmp_sparse_indices[t];
+ *                          HCA: every causally visible compressed row)
+ *     K~[j, d] = e4m3fn(kv[j, d]) * scale[j, d / 64]
+ *     x_j      = softmax_scale * sum_d Q[t, h, d] K~[j, d]
+ *     O[t, h]  = sum_j e^{x_j} K~[j, :] / (sum_j e^{x_j} + e^{sink_h})
+ *     lse[t,h] = log sum_j e^{x_j}          (the sink is not included)
+ *   A token with no attended row gets O = 0 and lse = -inf.
+ *
+ * Modes (QuantSparseFlashMla, "约束说明" (constraints), third bullet):
+ *   SWA  cmp_kv == NULL                        ori window only
+ *   CSA  cmp_kv != NULL, cmp_sparse_indices    window + top-k compressed rows
+ *   HCA  cmp_kv != NULL, indices == NULL       window + all visible cmp rows
+ *
+ * Data layout (all device memory is owned by the caller; the library never
+ * allocates, frees or keeps pointers after a call returns):
+ *   q            bf16  BSND [B, S1, 64, 512] or TND [T1, 64, 512]
+ *   attn_out     bf16  same shape as q
+ *   softmax_lse  fp32  BSND [B, 1, S1, 64] / TND [1, T1, 64]
+ *                      (KvQuantSparseAttnSharedKv, parameter table, row
+ *                      softmax_lse); element (token t, head h) at t*64 + h
+ *   ori_kv       fp8 e4m3fn, paged [ori_num_blocks, 128, 1, 512]
+ *   cmp_kv       fp8 e4m3fn, paged [cmp_num_blocks, 128, 1, 512]
+ *   ori_scale / cmp_scale
+ *                fp32 [num_blocks, 128, 1, 8]: one dequant scale per
+ *                64-element tile of a row, paged exactly like its KV
+ *                (KvQuantSparseAttnSharedKv, parameter table, rows
+ *                kv_quant_mode and tile_size: per-tile quantisation, tile 64)
+ *   *_block_table int32 [B, *_max_blocks]: logical block -> physical block
+ *                (QuantSparseFlashMla, "约束说明", PageAttention bullets)
+ *   cmp_sparse_indices int32 BSND [B, S1, 1, K2] / TND [T1, 1, K2];
+ *                an entry is a logical compressed-row index of the token's
+ *                own batch; -1 (or any value outside the visible range) is
+ *                ignored
+ *   cu_seqlens_q int32 [B + 1], prefix sums from 0 (required for TND)
+ *   seqused_q    int32 [B] or NULL (BSND: rows s >= seqused_q[b] are
+ *                padding; they get O = 0, lse = -inf)
+ *   seqused_ori_kv int32 [B], required (ori length S2 of each batch)
+ *   seqused_cmp_kv int32 [B] or NULL (default floor(S2 / cmp_ratio))
+ *   cmp_residual_kv int32 [B] or NULL (default 0), 0 <= r_b < cmp_ratio
+ *   cmp_topk_length int32 [T] or NULL: only the first n entries of the
+ *                token's index row are read
+ *   sinks        fp32 [64] or NULL (NULL: no sink)
+ *   metadata     int32 [1024] written by qsfm_metadata()
+ *
+ * Query position alignment is bottom-right: p = S2 - S1_b + s on the ori
+ * side and p_c = cmp_len * cmp_ratio + residual - S1_b + s on the cmp side.
+ * ori mask mode 4 (band) keeps rows max(0, p - wl) .. min(S2 - 1, p + wr),
+ * -1 meaning no bound on that side; mode 3 keeps rows <= p; mode 0 keeps all.
+ * cmp mask mode 3 keeps compressed rows c < floor((p_c + 1) / cmp_ratio)
+ * (clipped to [0, cmp_len]); mode 0 keeps all cmp_len rows.
+ *
+ * Every call is asynchronous on the given stream and never reads device
+ * memory back to the host, so the calls may be captured in a CUDA graph
+ * (QuantSparseFlashMla, "约束说明": aclgraph mode). Argument errors are found
+ * on the host before anything is launched and are returned as status codes.
+ * Bad device data (a block id outside the pool, a block-table column past
+ * its width) is not trapped: the row is skipped and a bit is set in the
+ * device fault word, which qsfm_get_device_status() reads.
+ */
+#ifndef QSFM_H
+#define QSFM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QSFM_ABI_VERSION 1
+#define QSFM_NUM_HEADS 64
+#define QSFM_HEAD_DIM 512
+#define QSFM_BLOCK_SIZE 128
+#define QSFM_SCALES_PER_ROW 8
+#define QSFM_METADATA_INTS 1024
+#define QSFM_MAX_CTAS 256
+
+typedef enum {
+  QSFM_OK = 0,
+  QSFM_ERR_INVALID_ARG = 1,  /* a constraint of the op is violated        */
+  QSFM_ERR_UNSUPPORTED = 2,  /* valid for the op but not built (n1 != 64) */
+  QSFM_ERR_CUDA = 3,         /* a CUDA runtime call failed                */
+  QSFM_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than required   */
+  QSFM_ERR_DEVICE_FAULT = 5, /* the device fault word is non-zero         */
+  QSFM_ERR_TIMEOUT = 6       /* reserved for bounded device waits         */
+} qsfm_status;
+
+typedef enum { QSFM_LAYOUT_BSND = 0, QSFM_LAYOUT_TND = 1 } qsfm_q_layout;
+
+/* Device fault word bits (qsfm_get_device_status). */
+#define QSFM_FAULT_ORI_BLOCK_ID   0x1  /* ori block table entry outside pool */
+#define QSFM_FAULT_CMP_BLOCK_ID   0x2  /* cmp block table entry outside pool */
+#define QSFM_FAULT_ORI_TABLE_COL  0x4  /* ori row beyond the table width     */
+#define QSFM_FAULT_CMP_TABLE_COL  0x8  /* cmp row beyond the table width     */
+#define QSFM_FAULT_METADATA       0x10 /* metadata header does not match     */
+
+/*
+ * All inputs, attributes and outputs of one forward call. Pointers are
+ * device pointers; NULL marks an absent optional input. The parameter names
+ * follow QuantSparseFlashMla, "参数说明" (parameter table).
+ */
+typedef struct qsfm_params {
+  /* shapes */
+  int32_t batch;          /* B                                               */
+  int32_t max_s1;         /* BSND: S1. TND: unused                           */
+  int32_t total_t;        /* TND: T1 (= q.shape[0]). BSND: unused            */
+  int32_t n1;             /* query heads; only 64 is built                   */
+  int32_t d;              /* head dim; must be 512                           */
+  int32_t k2;             /* index row length K2 (CSA); 0 otherwise          */
+  int32_t ori_block_size; /* tokens per ori block; only 128 is built         */
+  int32_t cmp_block_size; /* tokens per cmp block; only 128 is built         */
+  int32_t ori_max_blocks; /* ori_block_table row width                       */
+  int32_t cmp_max_blocks; /* cmp_block_table row width                       */
+  int32_t ori_num_blocks; /* physical blocks in the ori pool                 */
+  int32_t cmp_num_blocks; /* physical blocks in the cmp pool                 */
+  int32_t num_ctas;       /* CTAs the work is planned over; 0 = SM count    */
+  /* inputs (device) */
+  const void* q;
+  const void* ori_kv;
+  const float* ori_scale;
+  const void* cmp_kv;
+  const float* cmp_scale;
+  const int32_t* cmp_sparse_indices;
+  const int32_t* ori_block_table;
+  const int32_t* cmp_block_table;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqused_q;
+  const int32_t* seqused_ori_kv;
+  const int32_t* seqused_cmp_kv;
+  const int32_t* cmp_residual_kv;
+  const int32_t* cmp_topk_length;
+  const float* sinks;
+  const int32_t* metadata;
+  /* attributes */
+  float softmax_scale;
+  int32_t cmp_ratio;      /* 1..128; must be 1 when cmp_kv is NULL           */
+  int32_t ori_mask_mode;  /* 0, 3 or 4                                       */
+  int32_t cmp_mask_mode;  /* 0 or 3                                          */
+  int32_t ori_win_left;   /* -1 or >= 0; >= 0 only with ori_mask_mode 4      */
+  int32_t ori_win_right;  /* -1 or >= 0; >= 0 only with ori_mask_mode 4      */
+  int32_t layout_q;       /* qsfm_q_layout                                   */
+  int32_t return_lse;     /* non-zero: write softmax_lse                     */
+  /* outputs (device) */
+  void* attn_out;
+  float* softmax_lse;
+} qsfm_params;
+
+/* Fill *p with the defaults of the op: n1 64, d 512, block size 128,
+ * cmp_ratio 1, ori mask 4 with window 127/0 (KvQuantSparseAttnSharedKv,
+ * parameter table rows ori_mask_mode, ori_win_left, ori_win_right), cmp mask
+ * 3, softmax_scale 1/sqrt(512), layout BSND, all pointers NULL. */
+void qsfm_params_init(qsfm_params* p);
+
+/*
+ * Plan the work of one forward call over p->num_ctas CTAs (the split-core
+ * plan of QuantSparseFlashMlaMetadata, QuantSparseFlashMla "功能说明",
+ * calling sequence steps 1-3). Reads cu_seqlens_q / seqused_* /
+ * cmp_residual_kv / cmp_topk_length on the device and writes the int32[1024]
+ * plan to metadata_out (device memory, caller-owned). Launches one small
+ * kernel on `stream`; nothing is read back.
+ * Errors: QSFM_ERR_INVALID_ARG for a NULL metadata_out or invalid params.
+ */
+qsfm_status qsfm_metadata(const qsfm_params* p, int32_t* metadata_out,
+                          void* stream /* cudaStream_t */);
+
+/* Bytes of device workspace qsfm_forward() needs for p (partial outputs of
+ * work split across CTAs). May be 0. */
+qsfm_status qsfm_forward_workspace_size(const qsfm_params* p, size_t* bytes);
+
+/*
+ * The forward pass: attention kernel, then (only when the plan may split a
+ * token across CTAs) the log-sum-exp combine kernel. Writes attn_out and,
+ * when return_lse is set, softmax_lse. p->metadata must come from
+ * qsfm_metadata() with the same shapes and lengths (QuantSparseFlashMla,
+ * "约束说明": metadata is required, shape [1024]).
+ * workspace: device memory of at least qsfm_forward_workspace_size() bytes.
+ */
+qsfm_status qsfm_forward(const qsfm_params* p, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* The two stages of qsfm_forward(), callable separately (for timing). */
+qsfm_status qsfm_attention(const qsfm_params* p, void* workspace,
+                           size_t workspace_bytes, void* stream);
+qsfm_status qsfm_combine(const qsfm_params* p, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
+ * Debug export of the row resolution the attention kernel uses. For each
+ * of the n query tokens in tokens[] (device int32), writes the token's row
+ * slots in the kernel's order (ori window rows, then cmp slots), up to
+ * max_rows of them:
+ *   rows_out    uint8 [n, max_rows, 512]  the fp8 bytes of the resolved row
+ *   scales_out  fp32  [n, max_rows, 8]    its dequant scales
+ *   row_ids_out int32 [n, max_rows]       (source << 30) | logical row, with
+ *                                         source 0 = ori, 1 = cmp; -1 for a
+ *                                         slot that is masked out
+ *   counts_out  int32 [n]                 number of slots of the token
+ * Masked slots get zero bytes and zero scales. All buffers are device memory.
+ */
+qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens,
+                              int32_t n, int32_t max_rows, uint8_t* rows_out,
+                              float* scales_out, int32_t* row_ids_out,
+                              int32_t* counts_out, void* stream);
+
+/* Synchronously read and clear the device fault word of the current
+ * device (QSFM_FAULT_* bits). Returns QSFM_ERR_DEVICE_FAULT when non-zero. */
+qsfm_status qsfm_get_device_status(int32_t* fault_word);
+
+const char* qsfm_status_string(qsfm_status s);
+int32_t qsfm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSFM_H */

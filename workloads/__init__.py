@@ -1,0 +1,276 @@
+"""Seeded synthetic inputs for the quantized shared-KV sparse MLA attention.
+
+This module builds inputs only. It holds none of the attention arithmetic:
+no masking, no dequantisation, no softmax. The oracle and the CUDA path both
+take what it returns. Everything is drawn on the CPU from one
+``torch.Generator`` seeded per workload.
+
+Value distributions follow the five workloads of the spec description
+(tiny CSA decode, SWA prefill, CSA decode batch, HCA long decode, CSA chunked
+prefill):
+
+* q ~ N(0, 1) in bf16.
+* KV rows ~ N(0, 1), quantised per 64-element tile to fp8 e4m3fn with
+  scale = amax / 448 (KvQuantSparseAttnSharedKv, parameter table rows
+  kv_quant_mode / tile_size: per-tile quantisation, tile 64). The fp32 scales
+  are stored beside the KV in a [blocks, 128, 1, 8] tensor paged like it.
+* sinks ~ N(0, 1) fp32 [64].
+* KV lives in 128-token blocks. Each batch takes its blocks from a randomly
+  permuted physical pool sized to the exact total, so block tables are
+  shuffled.
+* CSA indices are drawn distinct and uniform from the compressed rows a token
+  can see. The bound used for drawing is computed here from the
+  bottom-right-aligned position; the oracle and the kernel each apply their
+  own visibility rule, so a wrong bound here would show up as a mismatch or
+  as masked entries, never be hidden.
+
+Large pools (more than ``BANK_ROWS`` rows) are filled from a bank of
+``BANK_ROWS`` distinct random rows through a seeded random map. Each row is
+still a quantised N(0, 1) row; rows repeat across the pool. The attention
+output depends only on the rows a token attends to, so this changes neither
+the results' distribution nor the memory traffic of the kernel.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+NUM_HEADS = 64
+HEAD_DIM = 512
+BLOCK = 128
+TILE = 64
+SCALES_PER_ROW = HEAD_DIM // TILE
+FP8_MAX = 448.0
+BANK_ROWS = 1 << 18
+
+
+@dataclasses.dataclass
+class Workload:
+    """All inputs of one forward call, as CPU tensors (numpy-convertible)."""
+
+    name: str
+    layout: str  # "BSND" or "TND"
+    batch: int
+    max_s1: int  # BSND: S1; TND: max chunk length
+    q_lens: np.ndarray  # int64 [B]: query tokens per batch
+    cu_seqlens_q: Optional[torch.Tensor]  # int32 [B+1] (TND)
+    q: torch.Tensor  # bf16 [T, 64, 512] (BSND memory is identical)
+    ori_kv: torch.Tensor  # uint8 [nb, 128, 1, 512]
+    ori_scale: torch.Tensor  # fp32 [nb, 128, 1, 8]
+    ori_block_table: torch.Tensor  # int32 [B, wo]
+    seqused_ori_kv: torch.Tensor  # int32 [B]
+    cmp_kv: Optional[torch.Tensor]
+    cmp_scale: Optional[torch.Tensor]
+    cmp_block_table: Optional[torch.Tensor]
+    cmp_sparse_indices: Optional[torch.Tensor]  # int32 [T, 1, K2]
+    seqused_cmp_kv: Optional[torch.Tensor]
+    cmp_residual_kv: Optional[torch.Tensor]
+    cmp_topk_length: Optional[torch.Tensor]
+    seqused_q: Optional[torch.Tensor]
+    sinks: Optional[torch.Tensor]  # fp32 [64]
+    softmax_scale: float
+    cmp_ratio: int
+    ori_mask_mode: int
+    cmp_mask_mode: int
+    ori_win_left: int
+    ori_win_right: int
+    return_lse: bool
+    seed: int
+
+    @property
+    def total_t(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def k2(self) -> int:
+        return 0 if self.cmp_sparse_indices is None else int(self.cmp_sparse_indices.shape[-1])
+
+    @property
+    def mode(self) -> str:
+        if self.cmp_kv is None:
+            return "SWA"
+        return "CSA" if self.cmp_sparse_indices is not None else "HCA"
+
+    def token_batch(self) -> np.ndarray:
+        """Batch index of every query token (int64 [T])."""
+        return np.repeat(np.arange(self.batch), self.q_lens)
+
+    def token_pos(self) -> np.ndarray:
+        """Position s of every query token inside its batch's chunk."""
+        return np.concatenate([np.arange(n) for n in self.q_lens]) if self.total_t else np.zeros(0, np.int64)
+
+
+def _quantize_rows(x: torch.Tensor):
+    """Quantise fp32 rows [n, 512] per 64-tile to e4m3fn bytes + fp32 scales."""
+    n = x.shape[0]
+    t = x.view(n, SCALES_PER_ROW, TILE)
+    amax = t.abs().amax(dim=-1)
+    scale = torch.clamp(amax, min=1e-12) / FP8_MAX
+    q8 = (t / scale.unsqueeze(-1)).to(torch.float8_e4m3fn)
+    return q8.view(torch.uint8).view(n, HEAD_DIM), scale.to(torch.float32)
+
+
+def _random_rows(n: int, gen: torch.Generator, chunk: int = 1 << 16):
+    rows = torch.empty(n, HEAD_DIM, dtype=torch.uint8)
+    scales = torch.empty(n, SCALES_PER_ROW, dtype=torch.float32)
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        x = torch.randn(hi - lo, HEAD_DIM, generator=gen, dtype=torch.float32)
+        r, s = _quantize_rows(x)
+        rows[lo:hi] = r
+        scales[lo:hi] = s
+    return rows, scales
+
+
+def _paged_pool(lengths: np.ndarray, gen: torch.Generator, min_width: int = 0,
+                block: int = BLOCK):
+    """Pool + shuffled block table holding lengths[b] rows for each batch."""
+    nblk = [(int(l) + block - 1) // block for l in lengths]
+    total = sum(nblk)
+    width = max([min_width] + nblk + [1])
+    perm = torch.randperm(max(total, 1), generator=gen)[:total].to(torch.int32)
+    table = torch.full((len(lengths), width), -1, dtype=torch.int32)
+    off = 0
+    for b, k in enumerate(nblk):
+        table[b, :k] = perm[off:off + k]
+        off += k
+    nrows = max(total, 1) * block
+    if nrows <= BANK_ROWS:
+        rows, scales = _random_rows(nrows, gen)
+    else:
+        bank_r, bank_s = _random_rows(BANK_ROWS, gen)
+        pick = torch.randint(0, BANK_ROWS, (nrows,), generator=gen)
+        rows, scales = bank_r[pick], bank_s[pick]
+    kv = rows.view(max(total, 1), block, 1, HEAD_DIM)
+    sc = scales.view(max(total, 1), block, 1, SCALES_PER_ROW)
+    return kv, sc, table
+
+
+def _index_draw_bound(s2: int, s1: int, s: int, cmp_len: int, res: int, r: int) -> int:
+    """Number of compressed rows token s may draw indices from (see module doc)."""
+    p_c = cmp_len * r + res - s1 + s
+    return max(0, min(cmp_len, (p_c + 1) // r))
+
+
+def build(
+    name: str,
+    *,
+    layout: str,
+    q_lens,
+    s2,
+    cmp_ratio: int = 1,
+    mode: str = "SWA",
+    k2: int = 512,
+    n_valid: Optional[int] = None,
+    seed: int = 0,
+    ori_mask_mode: int = 4,
+    cmp_mask_mode: int = 3,
+    ori_win_left: int = 127,
+    ori_win_right: int = 0,
+    return_lse: bool = False,
+    sinks: bool = True,
+    with_residual: bool = True,
+    softmax_scale: Optional[float] = None,
+    cmp_topk_length: Optional[list] = None,
+    seqused_q: Optional[list] = None,
+    q_scale: float = 1.0,
+    block_size: int = BLOCK,
+) -> Workload:
+    """Build one workload. q_lens / s2 are per-batch query and ori lengths."""
+    gen = torch.Generator().manual_seed(seed)
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    s2 = np.asarray(s2, dtype=np.int64)
+    B = len(q_lens)
+    assert len(s2) == B
+    T = int(q_lens.sum())
+    q = (torch.randn(T, NUM_HEADS, HEAD_DIM, generator=gen) * q_scale).to(torch.bfloat16)
+    ori_kv, ori_scale, ori_table = _paged_pool(s2, gen, block=block_size)
+    sink = torch.randn(NUM_HEADS, generator=gen, dtype=torch.float32) if sinks else None
+    cu = None
+    if layout == "TND":
+        cu = torch.zeros(B + 1, dtype=torch.int32)
+        cu[1:] = torch.from_numpy(np.cumsum(q_lens)).to(torch.int32)
+    else:
+        assert len(set(q_lens.tolist())) <= 1, "BSND needs equal S1"
+    cmp_kv = cmp_scale = cmp_table = idx = used_cmp = resid = topk = None
+    if mode in ("CSA", "HCA"):
+        cmp_len = s2 // cmp_ratio
+        res = (s2 % cmp_ratio) if with_residual else np.zeros_like(s2)
+        cmp_w = (int(s2.max()) // cmp_ratio + block_size - 1) // block_size if B else 1
+        cmp_kv, cmp_scale, cmp_table = _paged_pool(cmp_len, gen, min_width=cmp_w,
+                                                   block=block_size)
+        resid = torch.from_numpy(res.astype(np.int32))
+        if mode == "CSA":
+            idx = torch.full((T, 1, k2), -1, dtype=torch.int32)
+            t = 0
+            for b in range(B):
+                for s in range(int(q_lens[b])):
+                    v = _index_draw_bound(int(s2[b]), int(q_lens[b]), s, int(cmp_len[b]), int(res[b]), cmp_ratio)
+                    n = min(k2 if n_valid is None else n_valid, v)
+                    if n > 0:
+                        idx[t, 0, :n] = torch.randperm(v, generator=gen)[:n].to(torch.int32)
+                    t += 1
+        if cmp_topk_length is not None:
+            topk = torch.tensor(cmp_topk_length, dtype=torch.int32)
+    used_q = torch.tensor(seqused_q, dtype=torch.int32) if seqused_q is not None else None
+    return Workload(
+        name=name, layout=layout, batch=B, max_s1=int(q_lens.max()) if B else 0,
+        q_lens=q_lens, cu_seqlens_q=cu, q=q,
+        ori_kv=ori_kv, ori_scale=ori_scale, ori_block_table=ori_table,
+        seqused_ori_kv=torch.from_numpy(s2.astype(np.int32)),
+        cmp_kv=cmp_kv, cmp_scale=cmp_scale, cmp_block_table=cmp_table,
+        cmp_sparse_indices=idx, seqused_cmp_kv=used_cmp, cmp_residual_kv=resid,
+        cmp_topk_length=topk, seqused_q=used_q, sinks=sink,
+        softmax_scale=(1.0 / math.sqrt(HEAD_DIM)) if softmax_scale is None else softmax_scale,
+        cmp_ratio=cmp_ratio if mode != "SWA" else 1,
+        ori_mask_mode=ori_mask_mode, cmp_mask_mode=cmp_mask_mode,
+        ori_win_left=ori_win_left, ori_win_right=ori_win_right,
+        return_lse=return_lse, seed=seed,
+    )
+
+
+def _uniform_int(gen: torch.Generator, lo: int, hi: int, n: int) -> np.ndarray:
+    """n integers uniform on the inclusive range [lo, hi]."""
+    return torch.randint(lo, hi + 1, (n,), generator=gen).numpy().astype(np.int64)
+
+
+def config(index: int, seed: Optional[int] = None) -> Workload:
+    """The five spec workloads; seed defaults to the workload index."""
+    seed = index if seed is None else seed
+    gen = torch.Generator().manual_seed(10_000 + seed)
+    if index == 0:  # tiny CSA decode
+        return build("tiny CSA decode B=2 S1=1 S2=4096 r=4 K2=512 (384 valid)",
+                     layout="BSND", q_lens=[1, 1], s2=[4096, 4096], cmp_ratio=4,
+                     mode="CSA", k2=512, n_valid=384, seed=seed)
+    if index == 1:  # SWA-only prefill
+        return build("SWA prefill TND B=4 S1=S2=2048",
+                     layout="TND", q_lens=[2048] * 4, s2=[2048] * 4, mode="SWA", seed=seed)
+    if index == 2:  # CSA decode batch
+        s2 = _uniform_int(gen, 4096, 65536, 128)
+        return build("CSA decode batch B=128 S1=2 S2~U[4K,64K] r=4 K2=512",
+                     layout="BSND", q_lens=[2] * 128, s2=s2, cmp_ratio=4, mode="CSA",
+                     k2=512, seed=seed)
+    if index == 3:  # HCA long-context decode
+        s2 = _uniform_int(gen, 32768, 131072, 64)
+        return build("HCA long decode B=64 S1=1 S2~U[32K,128K] r=128",
+                     layout="BSND", q_lens=[1] * 64, s2=s2, cmp_ratio=128, mode="HCA", seed=seed)
+    if index == 4:  # CSA chunked prefill
+        q_lens = _uniform_int(gen, 512, 4096, 8)
+        s2 = _uniform_int(gen, 8192, 32768, 8)
+        s2 = np.maximum(s2, q_lens)
+        return build("CSA chunked prefill TND B=8 S1~U[512,4096] S2~U[8K,32K] r=4 K2=512 lse",
+                     layout="TND", q_lens=q_lens, s2=s2, cmp_ratio=4, mode="CSA",
+                     k2=512, seed=seed, return_lse=True)
+    raise ValueError(index)
+
+
+def subset_tokens(w: Workload, n: int, seed: int = 0) -> np.ndarray:
+    """A seeded sample of n query-token indices of w (sorted)."""
+    gen = torch.Generator().manual_seed(20_000 + seed)
+    n = min(n, w.total_t)
+    return np.sort(torch.randperm(w.total_t, generator=gen)[:n].numpy())
