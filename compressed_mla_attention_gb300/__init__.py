@@ -1,0 +1,330 @@
+"""Python binding of libqsfm, the quantized shared-KV sparse MLA attention
+forward for sm_103a (QuantSparseFlashMla / KvQuantSparseAttnSharedKv).
+
+This module only marshals arguments: it fills the C ``qsfm_params`` struct
+from torch tensors (device pointers, shapes) and calls the C ABI declared in
+``include/qsfm.h`` through ctypes. Every step of the computation runs in the
+library's CUDA kernels. There is no CPU or PyTorch fallback: if the library
+is missing, importing the op functions raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_lib", "libqsfm.so")
+
+NUM_HEADS = 64
+HEAD_DIM = 512
+BLOCK_SIZE = 128
+METADATA_INTS = 1024
+MAX_CTAS = 256
+LAYOUT_BSND = 0
+LAYOUT_TND = 1
+
+STATUS = {
+    0: "QSFM_OK",
+    1: "QSFM_ERR_INVALID_ARG",
+    2: "QSFM_ERR_UNSUPPORTED",
+    3: "QSFM_ERR_CUDA",
+    4: "QSFM_ERR_WORKSPACE",
+    5: "QSFM_ERR_DEVICE_FAULT",
+    6: "QSFM_ERR_TIMEOUT",
+}
+FAULT_ORI_BLOCK_ID = 0x1
+FAULT_CMP_BLOCK_ID = 0x2
+FAULT_ORI_TABLE_COL = 0x4
+FAULT_CMP_TABLE_COL = 0x8
+FAULT_METADATA = 0x10
+FAULT_TIMEOUT = 0x20
+
+_i32 = ctypes.c_int32
+_ptr = ctypes.c_void_p
+
+
+class QsfmParams(ctypes.Structure):
+    """Mirror of ``qsfm_params`` (include/qsfm.h); field order must match."""
+
+    _fields_ = [
+        ("batch", _i32), ("max_s1", _i32), ("total_t", _i32), ("n1", _i32), ("d", _i32),
+        ("k2", _i32), ("ori_block_size", _i32), ("cmp_block_size", _i32),
+        ("ori_max_blocks", _i32), ("cmp_max_blocks", _i32), ("ori_num_blocks", _i32),
+        ("cmp_num_blocks", _i32), ("num_ctas", _i32),
+        ("q", _ptr), ("ori_kv", _ptr), ("ori_scale", _ptr), ("cmp_kv", _ptr), ("cmp_scale", _ptr),
+        ("cmp_sparse_indices", _ptr), ("ori_block_table", _ptr), ("cmp_block_table", _ptr),
+        ("cu_seqlens_q", _ptr), ("seqused_q", _ptr), ("seqused_ori_kv", _ptr),
+        ("seqused_cmp_kv", _ptr), ("cmp_residual_kv", _ptr), ("cmp_topk_length", _ptr),
+        ("sinks", _ptr), ("metadata", _ptr),
+        ("softmax_scale", ctypes.c_float), ("cmp_ratio", _i32), ("ori_mask_mode", _i32),
+        ("cmp_mask_mode", _i32), ("ori_win_left", _i32), ("ori_win_right", _i32),
+        ("layout_q", _i32), ("return_lse", _i32),
+        ("attn_out", _ptr), ("softmax_lse", _ptr),
+    ]
+
+
+class QsfmError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+EXPORTS = {
+    "qsfm_params_init": (None, [ctypes.POINTER(QsfmParams)]),
+    "qsfm_metadata": (_i32, [ctypes.POINTER(QsfmParams), _ptr, _ptr]),
+    "qsfm_forward_workspace_size": (_i32, [ctypes.POINTER(QsfmParams), ctypes.POINTER(ctypes.c_size_t)]),
+    "qsfm_forward": (_i32, [ctypes.POINTER(QsfmParams), _ptr, ctypes.c_size_t, _ptr]),
+    "qsfm_attention": (_i32, [ctypes.POINTER(QsfmParams), _ptr, ctypes.c_size_t, _ptr]),
+    "qsfm_combine": (_i32, [ctypes.POINTER(QsfmParams), _ptr, ctypes.c_size_t, _ptr]),
+    "qsfm_debug_gather": (_i32, [ctypes.POINTER(QsfmParams), _ptr, _i32, _i32, _ptr, _ptr, _ptr, _ptr, _ptr]),
+    "qsfm_get_device_status": (_i32, [ctypes.POINTER(_i32)]),
+    "qsfm_status_string": (ctypes.c_char_p, [_i32]),
+    "qsfm_abi_version": (_i32, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library. Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m compressed_mla_attention_gb300.build` (no fallback exists)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise QsfmError(fn, code)
+
+
+def _dptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to qsfm must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_params(
+    *,
+    q,
+    attn_out,
+    ori_kv,
+    ori_scale,
+    ori_block_table,
+    seqused_ori_kv,
+    layout: str = "BSND",
+    batch: Optional[int] = None,
+    cmp_kv=None,
+    cmp_scale=None,
+    cmp_block_table=None,
+    cmp_sparse_indices=None,
+    cu_seqlens_q=None,
+    seqused_q=None,
+    seqused_cmp_kv=None,
+    cmp_residual_kv=None,
+    cmp_topk_length=None,
+    sinks=None,
+    metadata=None,
+    softmax_lse=None,
+    softmax_scale: float = HEAD_DIM ** -0.5,
+    cmp_ratio: int = 1,
+    ori_mask_mode: int = 4,
+    cmp_mask_mode: int = 3,
+    ori_win_left: int = 127,
+    ori_win_right: int = 0,
+    return_lse: bool = False,
+    num_ctas: int = 0,
+) -> QsfmParams:
+    """Fill a QsfmParams from device tensors (shapes as in include/qsfm.h).
+
+    q / attn_out: BSND [B, S1, 64, 512] or TND [T1, 64, 512] bf16.
+    Paged KV: [blocks, 128, 1, 512] uint8 (fp8 e4m3fn bytes) with fp32 scales
+    [blocks, 128, 1, 8]; block tables int32 [B, width].
+    """
+    p = QsfmParams()
+    lib().qsfm_params_init(ctypes.byref(p))
+    if layout == "BSND":
+        p.layout_q = LAYOUT_BSND
+        if q.dim() == 4:
+            p.batch, p.max_s1 = int(q.shape[0]), int(q.shape[1])
+        else:  # flat [B * S1, 64, 512]
+            if batch is None:
+                raise ValueError("flat BSND q needs batch=")
+            p.batch = int(batch)
+            p.max_s1 = int(q.shape[0]) // max(1, p.batch)
+        p.total_t = p.batch * p.max_s1
+    elif layout == "TND":
+        p.layout_q = LAYOUT_TND
+        p.total_t = int(q.shape[0])
+        p.batch = int(cu_seqlens_q.shape[0]) - 1 if cu_seqlens_q is not None else int(batch or 0)
+        p.max_s1 = 0
+    else:
+        raise ValueError(layout)
+    p.n1, p.d = int(q.shape[-2]), int(q.shape[-1])
+    p.k2 = int(cmp_sparse_indices.shape[-1]) if cmp_sparse_indices is not None else 0
+    p.ori_block_size = int(ori_kv.shape[1])
+    p.ori_max_blocks = int(ori_block_table.shape[-1])
+    p.ori_num_blocks = int(ori_kv.shape[0])
+    if cmp_kv is not None:
+        p.cmp_block_size = int(cmp_kv.shape[1])
+        p.cmp_max_blocks = int(cmp_block_table.shape[-1])
+        p.cmp_num_blocks = int(cmp_kv.shape[0])
+    p.num_ctas = int(num_ctas)
+    p.q, p.attn_out = _dptr(q), _dptr(attn_out)
+    p.ori_kv, p.ori_scale = _dptr(ori_kv), _dptr(ori_scale)
+    p.cmp_kv, p.cmp_scale = _dptr(cmp_kv), _dptr(cmp_scale)
+    p.cmp_sparse_indices = _dptr(cmp_sparse_indices)
+    p.ori_block_table, p.cmp_block_table = _dptr(ori_block_table), _dptr(cmp_block_table)
+    p.cu_seqlens_q, p.seqused_q = _dptr(cu_seqlens_q), _dptr(seqused_q)
+    p.seqused_ori_kv, p.seqused_cmp_kv = _dptr(seqused_ori_kv), _dptr(seqused_cmp_kv)
+    p.cmp_residual_kv, p.cmp_topk_length = _dptr(cmp_residual_kv), _dptr(cmp_topk_length)
+    p.sinks, p.metadata, p.softmax_lse = _dptr(sinks), _dptr(metadata), _dptr(softmax_lse)
+    p.softmax_scale = float(softmax_scale)
+    p.cmp_ratio = int(cmp_ratio)
+    p.ori_mask_mode, p.cmp_mask_mode = int(ori_mask_mode), int(cmp_mask_mode)
+    p.ori_win_left, p.ori_win_right = int(ori_win_left), int(ori_win_right)
+    p.return_lse = int(bool(return_lse))
+    return p
+
+
+def metadata(params: QsfmParams, metadata_out, stream=None) -> None:
+    """qsfm_metadata(): plan the split over CTAs into metadata_out (int32[1024])."""
+    _check("qsfm_metadata", lib().qsfm_metadata(ctypes.byref(params), _dptr(metadata_out),
+                                                _stream_ptr(stream)))
+
+
+def workspace_size(params: QsfmParams) -> int:
+    n = ctypes.c_size_t(0)
+    _check("qsfm_forward_workspace_size",
+           lib().qsfm_forward_workspace_size(ctypes.byref(params), ctypes.byref(n)))
+    return int(n.value)
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return _dptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def forward(params: QsfmParams, workspace=None, stream=None) -> None:
+    """qsfm_forward(): attention + combine into params' output pointers."""
+    w, n = _ws(workspace)
+    _check("qsfm_forward", lib().qsfm_forward(ctypes.byref(params), w, n, _stream_ptr(stream)))
+
+
+def attention(params: QsfmParams, workspace=None, stream=None) -> None:
+    w, n = _ws(workspace)
+    _check("qsfm_attention", lib().qsfm_attention(ctypes.byref(params), w, n, _stream_ptr(stream)))
+
+
+def combine(params: QsfmParams, workspace=None, stream=None) -> None:
+    w, n = _ws(workspace)
+    _check("qsfm_combine", lib().qsfm_combine(ctypes.byref(params), w, n, _stream_ptr(stream)))
+
+
+def debug_gather(params: QsfmParams, tokens, max_rows: int, rows_out, scales_out, row_ids_out,
+                 counts_out, stream=None) -> None:
+    """qsfm_debug_gather(): the rows the attention kernel resolves per token."""
+    _check("qsfm_debug_gather", lib().qsfm_debug_gather(
+        ctypes.byref(params), _dptr(tokens), int(tokens.numel()), int(max_rows), _dptr(rows_out),
+        _dptr(scales_out), _dptr(row_ids_out), _dptr(counts_out), _stream_ptr(stream)))
+
+
+def device_status() -> int:
+    """Read and clear the device fault word (synchronous)."""
+    v = _i32(0)
+    code = lib().qsfm_get_device_status(ctypes.byref(v))
+    if code not in (0, 5):
+        raise QsfmError("qsfm_get_device_status", code)
+    return int(v.value)
+
+
+def status_string(code: int) -> str:
+    return lib().qsfm_status_string(int(code)).decode()
+
+
+def quant_sparse_flash_mla(
+    q,
+    ori_kv,
+    ori_scale,
+    ori_block_table,
+    seqused_ori_kv,
+    *,
+    layout: str = "BSND",
+    batch: Optional[int] = None,
+    cmp_kv=None,
+    cmp_scale=None,
+    cmp_block_table=None,
+    cmp_sparse_indices=None,
+    cu_seqlens_q=None,
+    seqused_q=None,
+    seqused_cmp_kv=None,
+    cmp_residual_kv=None,
+    cmp_topk_length=None,
+    sinks=None,
+    softmax_scale: float = HEAD_DIM ** -0.5,
+    cmp_ratio: int = 1,
+    ori_mask_mode: int = 4,
+    cmp_mask_mode: int = 3,
+    ori_win_left: int = 127,
+    ori_win_right: int = 0,
+    return_softmax_lse: bool = False,
+    metadata=None,
+    workspace=None,
+    num_ctas: int = 0,
+    out=None,
+    stream=None,
+):
+    """One forward call: plan (unless metadata is given), attention, combine.
+
+    Allocates the outputs (and the plan / workspace when not given) with
+    torch on q's device and returns (attn_out, softmax_lse or None). The
+    argument names are those of QuantSparseFlashMla's parameter table.
+    """
+    import torch
+
+    dev = q.device
+    attn_out = torch.empty_like(q) if out is None else out
+    lse = None
+    if return_softmax_lse:
+        T = int(q.shape[0] * q.shape[1]) if (layout == "BSND" and q.dim() == 4) else int(q.shape[0])
+        lse = torch.empty(T, NUM_HEADS, dtype=torch.float32, device=dev)
+    plan = metadata if metadata is not None else torch.empty(METADATA_INTS, dtype=torch.int32, device=dev)
+    p = make_params(
+        q=q, attn_out=attn_out, ori_kv=ori_kv, ori_scale=ori_scale, ori_block_table=ori_block_table,
+        seqused_ori_kv=seqused_ori_kv, layout=layout, batch=batch, cmp_kv=cmp_kv,
+        cmp_scale=cmp_scale, cmp_block_table=cmp_block_table,
+        cmp_sparse_indices=cmp_sparse_indices, cu_seqlens_q=cu_seqlens_q, seqused_q=seqused_q,
+        seqused_cmp_kv=seqused_cmp_kv, cmp_residual_kv=cmp_residual_kv,
+        cmp_topk_length=cmp_topk_length, sinks=sinks, metadata=plan, softmax_lse=lse,
+        softmax_scale=softmax_scale, cmp_ratio=cmp_ratio, ori_mask_mode=ori_mask_mode,
+        cmp_mask_mode=cmp_mask_mode, ori_win_left=ori_win_left, ori_win_right=ori_win_right,
+        return_lse=return_softmax_lse, num_ctas=num_ctas)
+    if metadata is None:
+        globals()["metadata"](p, plan, stream)
+    if workspace is None:
+        nbytes = workspace_size(p)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev) if nbytes else None
+    forward(p, workspace, stream)
+    return attn_out, lse

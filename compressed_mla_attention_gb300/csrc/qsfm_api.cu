@@ -1,0 +1,245 @@
+// C-ABI entry points: argument validation on the host, then kernel launches
+// on the caller's stream. Nothing here reads device memory back, so every
+// call can be captured in a CUDA graph (QuantSparseFlashMla, constraints:
+// aclgraph mode is supported).
+//
+// Validation follows QuantSparseFlashMla's constraints section: N2 = 1 and
+// D = 512; cmp_ratio in [1, 128] and 1 when only ori_kv is passed; ori mask
+// mode 0/3/4 and cmp mask mode 0/3; windows -1 or >= 0, and >= 0 only with
+// ori mask mode 4; cu_seqlens_q required for TND; seqused_ori_kv and the
+// block table required for paged KV; metadata required.
+#include <cmath>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "qsfm.h"
+#include "qsfm_internal.h"
+
+namespace {
+
+// Device fault word (QSFM_FAULT_* bits), one per device that loads the
+// library. Kernels get its address as an argument.
+__device__ int g_fault_word;
+
+int* fault_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  static int* ptrs[64] = {nullptr};
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int num_tokens(const qsfm_params& p) {
+  return p.layout_q == QSFM_LAYOUT_BSND ? p.batch * p.max_s1 : p.total_t;
+}
+
+qsfm_status resolve_ctas(const qsfm_params& p, int* out) {
+  if (p.num_ctas > 0) {
+    *out = p.num_ctas;
+    return QSFM_OK;
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QSFM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return QSFM_ERR_CUDA;
+  *out = sms < QSFM_MAX_CTAS ? sms : QSFM_MAX_CTAS;
+  return QSFM_OK;
+}
+
+// Shape / attribute / pointer checks shared by every entry point.
+qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
+  if (pp == nullptr) return QSFM_ERR_INVALID_ARG;
+  const qsfm_params& p = *pp;
+  if (p.n1 <= 0 || p.d <= 0) return QSFM_ERR_INVALID_ARG;
+  if (p.d != QSFM_HEAD_DIM) return QSFM_ERR_INVALID_ARG;  // "D only supports 512"
+  if (p.n1 != QSFM_NUM_HEADS) return QSFM_ERR_UNSUPPORTED;
+  if (p.batch < 0) return QSFM_ERR_INVALID_ARG;
+  if (p.layout_q != QSFM_LAYOUT_BSND && p.layout_q != QSFM_LAYOUT_TND) return QSFM_ERR_INVALID_ARG;
+  if (p.layout_q == QSFM_LAYOUT_BSND && p.max_s1 < 0) return QSFM_ERR_INVALID_ARG;
+  if (p.layout_q == QSFM_LAYOUT_TND) {
+    if (p.total_t < 0) return QSFM_ERR_INVALID_ARG;
+    if (p.cu_seqlens_q == nullptr && p.batch > 0) return QSFM_ERR_INVALID_ARG;
+  }
+  if (p.num_ctas < 0 || p.num_ctas > QSFM_MAX_CTAS) return QSFM_ERR_INVALID_ARG;
+  // paged ori KV is always present
+  if (p.ori_block_size < 1 || p.ori_block_size > 1024) return QSFM_ERR_INVALID_ARG;
+  if (p.ori_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
+  if (p.ori_kv == nullptr || p.ori_scale == nullptr || p.ori_block_table == nullptr ||
+      p.seqused_ori_kv == nullptr)
+    return QSFM_ERR_INVALID_ARG;
+  if (p.ori_max_blocks < 1 || p.ori_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
+  if (p.cmp_ratio < 1 || p.cmp_ratio > 128) return QSFM_ERR_INVALID_ARG;
+  if (p.cmp_kv == nullptr) {
+    if (p.cmp_ratio != 1) return QSFM_ERR_INVALID_ARG;  // SWA keeps the default 1
+    if (p.cmp_sparse_indices != nullptr) return QSFM_ERR_INVALID_ARG;  // CSA needs cmp_kv
+  } else {
+    if (p.cmp_block_size < 1 || p.cmp_block_size > 1024) return QSFM_ERR_INVALID_ARG;
+    if (p.cmp_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
+    if (p.cmp_scale == nullptr || p.cmp_block_table == nullptr) return QSFM_ERR_INVALID_ARG;
+    if (p.cmp_max_blocks < 1 || p.cmp_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
+    if (p.cmp_sparse_indices != nullptr && p.k2 < 1) return QSFM_ERR_INVALID_ARG;
+  }
+  if (p.ori_mask_mode != 0 && p.ori_mask_mode != 3 && p.ori_mask_mode != 4)
+    return QSFM_ERR_INVALID_ARG;
+  if (p.cmp_mask_mode != 0 && p.cmp_mask_mode != 3) return QSFM_ERR_INVALID_ARG;
+  if (p.ori_win_left < -1 || p.ori_win_right < -1) return QSFM_ERR_INVALID_ARG;
+  if (p.ori_mask_mode != 4 && (p.ori_win_left >= 0 || p.ori_win_right >= 0))
+    return QSFM_ERR_INVALID_ARG;
+  if (!std::isfinite(p.softmax_scale)) return QSFM_ERR_INVALID_ARG;
+  if (need_outputs && num_tokens(p) > 0) {
+    if (p.q == nullptr || p.attn_out == nullptr) return QSFM_ERR_INVALID_ARG;
+    if (p.return_lse && p.softmax_lse == nullptr) return QSFM_ERR_INVALID_ARG;
+  }
+  return QSFM_OK;
+}
+
+// Whether the plan may cut inside a token: only when there are fewer query
+// tokens than CTAs (decode); longer batches are cut at token starts.
+int split_mode(int tokens, int ctas) { return tokens < ctas ? 1 : 0; }
+
+qsfm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QSFM_OK : QSFM_ERR_CUDA; }
+
+qsfm_status prepare_forward(const qsfm_params* p, void* workspace, size_t ws_bytes, int* ctas,
+                            qsfm::Workspace* ws, int** fault) {
+  qsfm_status st = validate(p, true);
+  if (st != QSFM_OK) return st;
+  if (p->metadata == nullptr) return QSFM_ERR_INVALID_ARG;
+  st = resolve_ctas(*p, ctas);
+  if (st != QSFM_OK) return st;
+  const int T = num_tokens(*p);
+  if (split_mode(T, *ctas)) {
+    if (workspace == nullptr || ws_bytes < qsfm::workspace_bytes(*ctas)) return QSFM_ERR_WORKSPACE;
+    *ws = qsfm::workspace_view(workspace, *ctas);
+  } else {
+    *ws = qsfm::Workspace{nullptr, nullptr, 0};
+  }
+  *fault = fault_ptr();
+  if (*fault == nullptr) return QSFM_ERR_CUDA;
+  return QSFM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void qsfm_params_init(qsfm_params* p) {
+  if (p == nullptr) return;
+  std::memset(p, 0, sizeof(*p));
+  p->n1 = QSFM_NUM_HEADS;
+  p->d = QSFM_HEAD_DIM;
+  p->ori_block_size = QSFM_BLOCK_SIZE;
+  p->cmp_block_size = QSFM_BLOCK_SIZE;
+  p->softmax_scale = 1.0f / std::sqrt(float(QSFM_HEAD_DIM));
+  p->cmp_ratio = 1;
+  p->ori_mask_mode = 4;
+  p->cmp_mask_mode = 3;
+  p->ori_win_left = 127;
+  p->ori_win_right = 0;
+  p->layout_q = QSFM_LAYOUT_BSND;
+}
+
+qsfm_status qsfm_metadata(const qsfm_params* p, int32_t* metadata_out, void* stream) {
+  qsfm_status st = validate(p, false);
+  if (st != QSFM_OK) return st;
+  if (metadata_out == nullptr) return QSFM_ERR_INVALID_ARG;
+  int ctas = 0;
+  st = resolve_ctas(*p, &ctas);
+  if (st != QSFM_OK) return st;
+  int* fault = fault_ptr();
+  if (fault == nullptr) return QSFM_ERR_CUDA;
+  const int T = num_tokens(*p);
+  return cuda_status(qsfm::launch_plan(*p, T, ctas, split_mode(T, ctas), metadata_out, fault,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+qsfm_status qsfm_forward_workspace_size(const qsfm_params* p, size_t* bytes) {
+  qsfm_status st = validate(p, false);
+  if (st != QSFM_OK) return st;
+  if (bytes == nullptr) return QSFM_ERR_INVALID_ARG;
+  int ctas = 0;
+  st = resolve_ctas(*p, &ctas);
+  if (st != QSFM_OK) return st;
+  *bytes = split_mode(num_tokens(*p), ctas) ? qsfm::workspace_bytes(ctas) : 0;
+  return QSFM_OK;
+}
+
+qsfm_status qsfm_attention(const qsfm_params* p, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  int ctas = 0;
+  qsfm::Workspace ws{};
+  int* fault = nullptr;
+  qsfm_status st = prepare_forward(p, workspace, workspace_bytes, &ctas, &ws, &fault);
+  if (st != QSFM_OK) return st;
+  const int T = num_tokens(*p);
+  if (T == 0) return QSFM_OK;
+  return cuda_status(
+      qsfm::launch_attention(*p, T, ctas, ws, fault, static_cast<cudaStream_t>(stream)));
+}
+
+qsfm_status qsfm_combine(const qsfm_params* p, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  int ctas = 0;
+  qsfm::Workspace ws{};
+  int* fault = nullptr;
+  qsfm_status st = prepare_forward(p, workspace, workspace_bytes, &ctas, &ws, &fault);
+  if (st != QSFM_OK) return st;
+  const int T = num_tokens(*p);
+  if (T == 0 || !split_mode(T, ctas)) return QSFM_OK;  // no token can be split
+  return cuda_status(
+      qsfm::launch_combine(*p, T, ctas, ws, fault, static_cast<cudaStream_t>(stream)));
+}
+
+qsfm_status qsfm_forward(const qsfm_params* p, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  qsfm_status st = qsfm_attention(p, workspace, workspace_bytes, stream);
+  if (st != QSFM_OK) return st;
+  return qsfm_combine(p, workspace, workspace_bytes, stream);
+}
+
+qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens, int32_t n,
+                              int32_t max_rows, uint8_t* rows_out, float* scales_out,
+                              int32_t* row_ids_out, int32_t* counts_out, void* stream) {
+  qsfm_status st = validate(p, false);
+  if (st != QSFM_OK) return st;
+  if (n < 0 || max_rows < 0) return QSFM_ERR_INVALID_ARG;
+  if (n == 0) return QSFM_OK;
+  if (tokens == nullptr || counts_out == nullptr) return QSFM_ERR_INVALID_ARG;
+  if (max_rows > 0 && (rows_out == nullptr || scales_out == nullptr || row_ids_out == nullptr))
+    return QSFM_ERR_INVALID_ARG;
+  int* fault = fault_ptr();
+  if (fault == nullptr) return QSFM_ERR_CUDA;
+  return cuda_status(qsfm::launch_debug_gather(*p, tokens, n, max_rows, rows_out, scales_out,
+                                               row_ids_out, counts_out, fault,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+qsfm_status qsfm_get_device_status(int32_t* fault_word) {
+  if (fault_word == nullptr) return QSFM_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fault_word, sizeof(int)) != cudaSuccess) return QSFM_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(int)) != cudaSuccess) return QSFM_ERR_CUDA;
+  *fault_word = v;
+  return v == 0 ? QSFM_OK : QSFM_ERR_DEVICE_FAULT;
+}
+
+const char* qsfm_status_string(qsfm_status s) {
+  switch (s) {
+    case QSFM_OK: return "ok";
+    case QSFM_ERR_INVALID_ARG: return "invalid argument";
+    case QSFM_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case QSFM_ERR_CUDA: return "CUDA runtime error";
+    case QSFM_ERR_WORKSPACE: return "workspace missing or too small";
+    case QSFM_ERR_DEVICE_FAULT: return "device fault word set";
+    case QSFM_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int32_t qsfm_abi_version(void) { return QSFM_ABI_VERSION; }
+
+}  // extern "C"

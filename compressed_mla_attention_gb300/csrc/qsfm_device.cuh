@@ -1,0 +1,333 @@
+// Device-side building blocks shared by the qsfm kernels (sm_103a).
+//
+//  * token geometry: which ori rows and cmp slots a query token attends
+//    (QuantSparseFlashMla, parameter table rows ori_mask_mode, cmp_mask_mode,
+//    ori_win_left/right, cmp_residual_kv, cmp_topk_length; its constraints on
+//    the cmp length and cmp_len * cmp_ratio + residual; positions aligned
+//    bottom-right as a RightDownCausal mask is);
+//  * paged row resolution through the block tables (QuantSparseFlashMla
+//    constraints, PageAttention bullets);
+//  * thin inline-PTX wrappers for mbarrier and tcgen05 (TMEM allocation,
+//    MMA, commit, TMEM loads/stores, fences).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "qsfm.h"
+
+namespace qsfm {
+
+constexpr int kHeads = QSFM_NUM_HEADS;        // N1
+constexpr int kDim = QSFM_HEAD_DIM;           // D
+constexpr int kBlock = QSFM_BLOCK_SIZE;       // tokens per KV block
+constexpr int kScales = QSFM_SCALES_PER_ROW;  // fp32 scales per row
+constexpr int kTileRows = 128;                // KV rows per attention tile
+constexpr int kMetaMagic = 0x51534D31;        // "QSM1"
+constexpr int kMetaHeader = 8;
+// metadata layout (int32[1024]):
+//   [0] magic  [1] G (CTAs with work)  [2] T (query tokens)  [3] total cost
+//   [4] split flag  [5] total tiles (clipped)  [6..7] reserved
+//   [8 + 2c], [9 + 2c]  c = 0..G : (token, tile) where CTA c's range begins;
+//   CTA c covers [begin_c, begin_{c+1}) in (token, tile) order.
+
+// ---------------------------------------------------------------- geometry
+struct TokenGeom {
+  int b;          // batch of the token
+  int s2;         // ori length S2 of the batch
+  int ori_lo;     // first ori row attended
+  int n_ori;      // ori rows attended (contiguous from ori_lo)
+  int n_cmp;      // cmp slots: CSA index entries scanned, HCA visible rows
+  int cmp_vis;    // visible compressed rows V (CSA entries must be < V)
+  int ori_tiles;  // ceil(n_ori / 128)
+  int n_tiles;    // ori tiles + ceil(n_cmp / 128)
+};
+
+__device__ __forceinline__ int div_floor(int a, int b) {  // b > 0
+  int q = a / b;
+  return (a % b != 0 && a < 0) ? q - 1 : q;
+}
+
+// Batch, position in the batch's chunk and chunk length of query token t.
+__device__ __forceinline__ void token_batch(const qsfm_params& p, int t, int& b, int& s,
+                                            int& s1) {
+  if (p.layout_q == QSFM_LAYOUT_BSND) {
+    b = t / p.max_s1;
+    s = t - b * p.max_s1;
+    s1 = p.max_s1;
+  } else {
+    int lo = 0, hi = p.batch - 1;  // last b with cu[b] <= t
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (__ldg(p.cu_seqlens_q + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    int c0 = __ldg(p.cu_seqlens_q + b);
+    s = t - c0;
+    s1 = __ldg(p.cu_seqlens_q + b + 1) - c0;
+  }
+}
+
+__device__ __forceinline__ TokenGeom token_geom(const qsfm_params& p, int t) {
+  TokenGeom g;
+  int s, s1;
+  token_batch(p, t, g.b, s, s1);
+  g.s2 = __ldg(p.seqused_ori_kv + g.b);
+  g.ori_lo = 0; g.n_ori = 0; g.n_cmp = 0; g.cmp_vis = 0;
+  bool live = !(p.seqused_q != nullptr && s >= __ldg(p.seqused_q + g.b));
+  if (live) {
+    const int pos = g.s2 - s1 + s;  // bottom-right aligned position
+    int lo, hi;
+    if (p.ori_mask_mode == 0) {
+      lo = 0; hi = g.s2 - 1;
+    } else if (p.ori_mask_mode == 3) {
+      lo = 0; hi = min(g.s2 - 1, pos);
+    } else {
+      lo = p.ori_win_left < 0 ? 0 : max(0, pos - p.ori_win_left);
+      hi = p.ori_win_right < 0 ? g.s2 - 1 : min(g.s2 - 1, pos + p.ori_win_right);
+    }
+    g.ori_lo = lo;
+    g.n_ori = max(0, hi - lo + 1);
+    if (p.cmp_kv != nullptr) {
+      const int r = p.cmp_ratio;
+      const int cmp_len = p.seqused_cmp_kv ? __ldg(p.seqused_cmp_kv + g.b) : g.s2 / r;
+      const int res = p.cmp_residual_kv ? __ldg(p.cmp_residual_kv + g.b) : 0;
+      const int pc = cmp_len * r + res - s1 + s;
+      g.cmp_vis = p.cmp_mask_mode == 3 ? max(0, min(cmp_len, div_floor(pc + 1, r))) : cmp_len;
+      if (p.cmp_sparse_indices != nullptr) {
+        g.n_cmp = p.k2;
+        if (p.cmp_topk_length) g.n_cmp = max(0, min(p.k2, __ldg(p.cmp_topk_length + t)));
+      } else {
+        g.n_cmp = g.cmp_vis;
+      }
+    }
+  }
+  g.ori_tiles = (g.n_ori + kTileRows - 1) / kTileRows;
+  g.n_tiles = g.ori_tiles + (g.n_cmp + kTileRows - 1) / kTileRows;
+  return g;
+}
+
+// One resolved KV row: byte pointer to its 512 fp8 values and to its 8 scales.
+struct RowRef {
+  const uint8_t* kv;
+  const float* sc;
+  int row;     // logical row; -1 when the slot is masked out
+  int source;  // 0 ori, 1 cmp
+};
+
+// Row for slot `i` of tile `k` of token t. Slots past the token's rows, -1
+// or invisible CSA entries resolve to row = -1. Bad block ids set a fault
+// bit and also resolve to -1 (the row is skipped, never read).
+__device__ __forceinline__ RowRef resolve_slot(const qsfm_params& p, const TokenGeom& g,
+                                               int t, int k, int i, int* fault) {
+  RowRef r{nullptr, nullptr, -1, 0};
+  int row;
+  const uint8_t* pool;
+  const float* scales;
+  const int32_t* table;
+  int width, nblocks, src;
+  if (k < g.ori_tiles) {
+    const int slot = k * kTileRows + i;
+    if (slot >= g.n_ori) return r;
+    row = g.ori_lo + slot;
+    pool = static_cast<const uint8_t*>(p.ori_kv); scales = p.ori_scale;
+    table = p.ori_block_table; width = p.ori_max_blocks; nblocks = p.ori_num_blocks; src = 0;
+  } else {
+    const int slot = (k - g.ori_tiles) * kTileRows + i;
+    if (slot >= g.n_cmp) return r;
+    if (p.cmp_sparse_indices != nullptr) {
+      row = __ldg(p.cmp_sparse_indices + (size_t)t * p.k2 + slot);
+      if (row < 0 || row >= g.cmp_vis) return r;
+    } else {
+      row = slot;
+    }
+    pool = static_cast<const uint8_t*>(p.cmp_kv); scales = p.cmp_scale;
+    table = p.cmp_block_table; width = p.cmp_max_blocks; nblocks = p.cmp_num_blocks; src = 1;
+  }
+  const int col = row / kBlock;
+  if (col >= width) {
+    atomicOr(fault, src ? QSFM_FAULT_CMP_TABLE_COL : QSFM_FAULT_ORI_TABLE_COL);
+    return r;
+  }
+  const int blk = __ldg(table + (size_t)g.b * width + col);
+  if (blk < 0 || blk >= nblocks) {
+    atomicOr(fault, src ? QSFM_FAULT_CMP_BLOCK_ID : QSFM_FAULT_ORI_BLOCK_ID);
+    return r;
+  }
+  const size_t prow = (size_t)blk * kBlock + (row % kBlock);
+  r.kv = pool + prow * kDim;
+  r.sc = scales + prow * kScales;
+  r.row = row;
+  r.source = src;
+  return r;
+}
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Wait until the barrier's phase with the given parity has completed.
+// Bounded: returns false after `max_iters` polls (the caller reports a
+// timeout instead of spinning forever).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iters) {
+  const uint32_t addr = smem_u32(bar);
+  for (uint32_t it = 0; it < max_iters; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Whole-warp TMEM allocation; the base address is written to *dst (smem).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, fp32 acc).
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A/B bf16,
+// M x N, each operand K-major (0) or MN-major (1).
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int m, int n, int a_mn, int b_mn) {
+  return (1u << 4)                          // D format: f32
+         | (1u << 7)                        // A format: bf16
+         | (1u << 10)                       // B format: bf16
+         | (uint32_t(a_mn) << 15)           // A major
+         | (uint32_t(b_mn) << 16)           // B major
+         | (uint32_t(n >> 3) << 17)         // N / 8
+         | (uint32_t(m >> 4) << 24);        // M / 16
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle. Addresses are byte
+// offsets in the CTA's shared window; lbo / sbo are byte strides.
+__device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;  // descriptor version for tcgen05
+  d |= uint64_t(2) << 61;  // layout: SWIZZLE_128B
+  return d;
+}
+
+// 32 lanes x 32 bit, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ----------------------------------------------------------- fp8 dequant
+// 2 e4m3fn values (low byte first) times `scale`, rounded to a bf16 pair.
+__device__ __forceinline__ uint32_t dequant2(uint16_t two, float scale) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// 16 fp8 bytes -> 16 bf16 (two 16-byte chunks).
+__device__ __forceinline__ void dequant16(const uint4& in, float scale, uint4& lo, uint4& hi) {
+  lo.x = dequant2(uint16_t(in.x & 0xFFFF), scale);
+  lo.y = dequant2(uint16_t(in.x >> 16), scale);
+  lo.z = dequant2(uint16_t(in.y & 0xFFFF), scale);
+  lo.w = dequant2(uint16_t(in.y >> 16), scale);
+  hi.x = dequant2(uint16_t(in.z & 0xFFFF), scale);
+  hi.y = dequant2(uint16_t(in.z >> 16), scale);
+  hi.z = dequant2(uint16_t(in.w & 0xFFFF), scale);
+  hi.w = dequant2(uint16_t(in.w >> 16), scale);
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t saddr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+}  // namespace qsfm

@@ -1,0 +1,35 @@
+// Host-side interface between the C-ABI layer and the kernel translation
+// units. Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qsfm.h"
+
+namespace qsfm {
+
+// Partial-output workspace: per split piece slot, lse [64] fp32 then
+// O [64][512] fp32. Two slots per planned CTA.
+struct Workspace {
+  float* lse;  // [slots][64]
+  float* out;  // [slots][64][512]
+  int slots;
+};
+
+size_t workspace_bytes(int num_ctas);
+Workspace workspace_view(void* base, int num_ctas);
+
+cudaError_t launch_plan(const qsfm_params& p, int num_tokens, int num_ctas, int split,
+                        int32_t* metadata, int* fault, cudaStream_t s);
+cudaError_t launch_attention(const qsfm_params& p, int num_tokens, int num_ctas,
+                             const Workspace& ws, int* fault, cudaStream_t s);
+cudaError_t launch_combine(const qsfm_params& p, int num_tokens, int num_ctas,
+                           const Workspace& ws, int* fault, cudaStream_t s);
+cudaError_t launch_debug_gather(const qsfm_params& p, const int32_t* tokens, int n,
+                                int max_rows, uint8_t* rows_out, float* scales_out,
+                                int32_t* row_ids_out, int32_t* counts_out, int* fault,
+                                cudaStream_t s);
+
+}  // namespace qsfm

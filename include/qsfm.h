@@ -104,6 +104,7 @@ typedef enum { QSFM_LAYOUT_BSND = 0, QSFM_LAYOUT_TND = 1 } qsfm_q_layout;
 #define QSFM_FAULT_ORI_TABLE_COL  0x4  /* ori row beyond the table width     */
 #define QSFM_FAULT_CMP_TABLE_COL  0x8  /* cmp row beyond the table width     */
 #define QSFM_FAULT_METADATA       0x10 /* metadata header does not match     */
+#define QSFM_FAULT_TIMEOUT        0x20 /* a bounded device wait ran out      */
 
 /*
  * All inputs, attributes and outputs of one forward call. Pointers are

@@ -1,0 +1,166 @@
+"""The C-ABI library: exports, struct layout and host-side validation (CPU only).
+
+No kernel is launched here: every call below is rejected by the host checks
+before any CUDA call is made, so these tests run without a GPU.
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import compressed_mla_attention_gb300 as Q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qsfm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from compressed_mla_attention_gb300 import build
+
+    build.build()
+    return Q.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsfm_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert "qsfm_forward" in names and "qsfm_metadata" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(Q.EXPORTS)
+    assert lib.qsfm_abi_version() == 1
+
+
+def test_exports_are_c_symbols(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", Q.LIB_PATH], capture_output=True, text=True).stdout
+    for n in declared_functions():
+        assert re.search(rf"\bT {n}$", out, flags=re.M), n
+
+
+def test_struct_layout_matches_c(tmp_path):
+    src = tmp_path / "layout.c"
+    fields = [f[0] for f in Q.QsfmParams._fields_]
+    body = "\n".join(f'  printf("{f} %zu\\n", offsetof(qsfm_params, {f}));' for f in fields)
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "qsfm.h"\nint main(void){\n'
+                   + body + '\n  printf("sizeof %zu\\n", sizeof(qsfm_params));\n  return 0;\n}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = dict(line.split() for line in out if line)
+    for f in fields:
+        assert int(got[f]) == getattr(Q.QsfmParams, f).offset, f
+    assert int(got["sizeof"]) == ctypes.sizeof(Q.QsfmParams)
+
+
+def test_params_init_defaults(lib):
+    p = Q.QsfmParams()
+    lib.qsfm_params_init(ctypes.byref(p))
+    assert (p.n1, p.d, p.ori_block_size, p.cmp_ratio) == (64, 512, 128, 1)
+    assert (p.ori_mask_mode, p.cmp_mask_mode, p.ori_win_left, p.ori_win_right) == (4, 3, 127, 0)
+    assert abs(p.softmax_scale - 512 ** -0.5) < 1e-7
+
+
+def _valid(lib):
+    """A params struct that passes validation (fake non-null device pointers)."""
+    p = Q.QsfmParams()
+    lib.qsfm_params_init(ctypes.byref(p))
+    p.batch, p.max_s1, p.num_ctas = 2, 1, 8
+    p.ori_max_blocks, p.ori_num_blocks = 4, 8
+    for f in ("q", "attn_out", "ori_kv", "ori_scale", "ori_block_table", "seqused_ori_kv", "metadata"):
+        setattr(p, f, 0x1000)
+    return p
+
+
+def _status(lib, p, fn="qsfm_forward"):
+    if fn == "qsfm_forward":
+        return lib.qsfm_forward(ctypes.byref(p), None, 0, None)
+    if fn == "qsfm_metadata":
+        return lib.qsfm_metadata(ctypes.byref(p), None, None)
+    n = ctypes.c_size_t(0)
+    return lib.qsfm_forward_workspace_size(ctypes.byref(p), ctypes.byref(n))
+
+
+INVALID = [
+    ("d != 512", dict(d=256), 1),
+    ("n1 = 128 is valid but not built", dict(n1=128), 2),
+    ("n1 = 0", dict(n1=0), 1),
+    ("block size 64 not built", dict(ori_block_size=64), 2),
+    ("block size 2048 invalid", dict(ori_block_size=2048), 1),
+    ("cmp_ratio 0", dict(cmp_ratio=0), 1),
+    ("cmp_ratio 129", dict(cmp_ratio=129), 1),
+    ("cmp_ratio != 1 without cmp_kv", dict(cmp_ratio=4), 1),
+    ("ori mask mode 2", dict(ori_mask_mode=2), 1),
+    ("cmp mask mode 4", dict(cmp_mask_mode=4), 1),
+    ("window < -1", dict(ori_win_left=-2), 1),
+    ("window >= 0 with mode 3", dict(ori_mask_mode=3, ori_win_left=5, ori_win_right=-1), 1),
+    ("window >= 0 with mode 0", dict(ori_mask_mode=0, ori_win_left=-1, ori_win_right=0), 1),
+    ("TND without cu_seqlens_q", dict(layout_q=1, total_t=4), 1),
+    ("bad layout", dict(layout_q=7), 1),
+    ("no seqused_ori_kv", dict(seqused_ori_kv=None), 1),
+    ("no ori block table", dict(ori_block_table=None), 1),
+    ("no ori scale", dict(ori_scale=None), 1),
+    ("indices without cmp_kv", dict(cmp_sparse_indices=0x1000, k2=512), 1),
+    ("no q", dict(q=None), 1),
+    ("no output", dict(attn_out=None), 1),
+    ("lse requested without buffer", dict(return_lse=1), 1),
+    ("no metadata", dict(metadata=None), 1),
+    ("too many CTAs", dict(num_ctas=100000), 1),
+    ("nan scale", dict(softmax_scale=float("nan")), 1),
+]
+
+
+@pytest.mark.parametrize("why,change,code", INVALID, ids=[c[0] for c in INVALID])
+def test_forward_rejects_invalid_arguments(lib, why, change, code):
+    p = _valid(lib)
+    for k, v in change.items():
+        setattr(p, k, v)
+    assert _status(lib, p) == code
+
+
+def test_cmp_side_requirements(lib):
+    p = _valid(lib)
+    p.cmp_kv, p.cmp_ratio = 0x1000, 4
+    assert _status(lib, p) == 1  # no cmp scale / table
+    p.cmp_scale, p.cmp_block_table, p.cmp_max_blocks, p.cmp_num_blocks = 0x1000, 0x1000, 2, 4
+    p.cmp_sparse_indices, p.k2 = 0x1000, 0
+    assert _status(lib, p) == 1  # CSA needs K2 >= 1
+    p.cmp_block_size = 256
+    assert _status(lib, p, "size") == 2
+
+
+def test_null_params_and_outputs(lib):
+    assert lib.qsfm_forward(None, None, 0, None) == 1
+    assert lib.qsfm_metadata(ctypes.byref(_valid(lib)), None, None) == 1  # no metadata_out
+    assert lib.qsfm_forward_workspace_size(ctypes.byref(_valid(lib)), None) == 1
+    assert lib.qsfm_get_device_status(None) == 1
+
+
+def test_workspace_size_depends_on_split(lib):
+    p = _valid(lib)
+    n = ctypes.c_size_t(123)
+    p.batch, p.max_s1, p.num_ctas = 2, 1, 8  # 2 tokens < 8 CTAs: tokens may be split
+    assert lib.qsfm_forward_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    assert n.value >= 2 * 8 * 64 * 512 * 4
+    p.batch, p.max_s1 = 64, 1  # 64 tokens >= 8 CTAs: no split, no workspace
+    assert lib.qsfm_forward_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    assert n.value == 0
+
+
+def test_forward_needs_workspace_when_splitting(lib):
+    p = _valid(lib)
+    assert lib.qsfm_forward(ctypes.byref(p), None, 0, None) == 4
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert Q.status_string(code)
+    assert "invalid" in Q.status_string(1)

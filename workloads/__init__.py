@@ -274,3 +274,26 @@ def subset_tokens(w: Workload, n: int, seed: int = 0) -> np.ndarray:
     gen = torch.Generator().manual_seed(20_000 + seed)
     n = min(n, w.total_t)
     return np.sort(torch.randperm(w.total_t, generator=gen)[:n].numpy())
+
+
+def device_inputs(w: Workload, device) -> dict:
+    """The workload's tensors on `device`, keyed by the op's argument names.
+
+    Pure data movement (no arithmetic): uint8 fp8 bytes, fp32 scales, int32
+    tables / lengths / indices and the bf16 query are copied as they are.
+    """
+    def mv(t):
+        return None if t is None else t.contiguous().to(device)
+
+    return dict(
+        q=mv(w.q), ori_kv=mv(w.ori_kv), ori_scale=mv(w.ori_scale),
+        ori_block_table=mv(w.ori_block_table), seqused_ori_kv=mv(w.seqused_ori_kv),
+        layout=w.layout, batch=w.batch, cmp_kv=mv(w.cmp_kv), cmp_scale=mv(w.cmp_scale),
+        cmp_block_table=mv(w.cmp_block_table), cmp_sparse_indices=mv(w.cmp_sparse_indices),
+        cu_seqlens_q=mv(w.cu_seqlens_q), seqused_q=mv(w.seqused_q),
+        seqused_cmp_kv=mv(w.seqused_cmp_kv), cmp_residual_kv=mv(w.cmp_residual_kv),
+        cmp_topk_length=mv(w.cmp_topk_length), sinks=mv(w.sinks),
+        softmax_scale=w.softmax_scale, cmp_ratio=w.cmp_ratio, ori_mask_mode=w.ori_mask_mode,
+        cmp_mask_mode=w.cmp_mask_mode, ori_win_left=w.ori_win_left,
+        ori_win_right=w.ori_win_right, return_softmax_lse=w.return_lse,
+    )
