@@ -246,6 +246,14 @@ def logits(w, t: int) -> np.ndarray:
 _FORK_WORKLOAD = None
 
 
+def _worker_init():
+    # a forked worker must not enter the parent's OpenMP pool
+    import sys
+
+    if "torch" in sys.modules:
+        sys.modules["torch"].set_num_threads(1)
+
+
 def _reference_chunk(tokens):
     return reference(_FORK_WORKLOAD, tokens)
 
@@ -265,7 +273,7 @@ def reference_parallel(w, tokens, processes: int):
     chunks = [tokens[i::processes] for i in range(processes)]
     _FORK_WORKLOAD = w
     try:
-        with mp.get_context("fork").Pool(processes) as pool:
+        with mp.get_context("fork").Pool(processes, initializer=_worker_init) as pool:
             res = pool.map(_reference_chunk, chunks)
     finally:
         _FORK_WORKLOAD = None

@@ -272,3 +272,11 @@ def test_config_workloads_shapes():
     assert int((w.cmp_sparse_indices >= 0).sum()) == 2 * 384
     o, lse = O.reference(w)
     assert o.shape == (2, 64, 512) and np.all(np.isfinite(lse))
+
+
+def test_reference_parallel_matches_serial():
+    w = W.build("par", layout="BSND", q_lens=[2, 2], s2=[300, 500], cmp_ratio=4, mode="CSA", k2=32,
+                block_size=16, seed=13)
+    o1, l1 = O.reference(w)
+    o2, l2 = O.reference_parallel(w, range(w.total_t), 2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)

@@ -269,6 +269,16 @@ def config(index: int, seed: Optional[int] = None) -> Workload:
     raise ValueError(index)
 
 
+def profile_case(seed: int = 2) -> Workload:
+    """The CSA decode batch at profiling size: same B = 128, S1 = 2, K2 = 512
+    and per-token work (640 rows) as workload 2, with S2 ~ U[4K, 8K] so the
+    KV pools stay under 1 GB on the device."""
+    gen = torch.Generator().manual_seed(30_000 + seed)
+    s2 = _uniform_int(gen, 4096, 8192, 128)
+    return build("CSA decode batch (profiling size) B=128 S1=2 S2~U[4K,8K] r=4 K2=512",
+                 layout="BSND", q_lens=[2] * 128, s2=s2, cmp_ratio=4, mode="CSA", k2=512, seed=seed)
+
+
 def subset_tokens(w: Workload, n: int, seed: int = 0) -> np.ndarray:
     """A seeded sample of n query-token indices of w (sorted)."""
     gen = torch.Generator().manual_seed(20_000 + seed)
