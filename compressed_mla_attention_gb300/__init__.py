@@ -80,6 +80,7 @@ EXPORTS = {
     "qsfm_forward": (_i32, [ctypes.POINTER(QsfmParams), _ptr, ctypes.c_size_t, _ptr]),
     "qsfm_attention": (_i32, [ctypes.POINTER(QsfmParams), _ptr, ctypes.c_size_t, _ptr]),
     "qsfm_combine": (_i32, [ctypes.POINTER(QsfmParams), _ptr, ctypes.c_size_t, _ptr]),
+    "qsfm_forward_noalloc": (_i32, [ctypes.POINTER(QsfmParams), _ptr]),
     "qsfm_debug_gather": (_i32, [ctypes.POINTER(QsfmParams), _ptr, _i32, _i32, _ptr, _ptr, _ptr, _ptr, _ptr]),
     "qsfm_get_device_status": (_i32, [ctypes.POINTER(_i32)]),
     "qsfm_status_string": (ctypes.c_char_p, [_i32]),
@@ -241,6 +242,15 @@ def attention(params: QsfmParams, workspace=None, stream=None) -> None:
 def combine(params: QsfmParams, workspace=None, stream=None) -> None:
     w, n = _ws(workspace)
     _check("qsfm_combine", lib().qsfm_combine(ctypes.byref(params), w, n, _stream_ptr(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def forward_noalloc(params: QsfmParams, stream=None) -> None:
+    """qsfm_forward_noalloc(): the forward pass using the library's fixed
+    device scratch array instead of a caller workspace (allocates nothing)."""
+    _check("qsfm_forward_noalloc", lib().qsfm_forward_noalloc(ctypes.byref(params), _stream_ptr(stream)))
 
 
 def debug_gather(params: QsfmParams, tokens, max_rows: int, rows_out, scales_out, row_ids_out,

@@ -197,6 +197,32 @@ qsfm_status qsfm_combine(const qsfm_params* p, void* workspace,
                          size_t workspace_bytes, void* stream);
 
 /*
+ * qsfm_forward() for callers that cannot allocate device memory. The paper
+ * has no counterpart: this is an addition of this library.
+ *
+ * Some callers cannot call cudaMalloc: code that runs inside another
+ * framework's memory pool, plugin hosts that hand over only the input and
+ * output buffers, serving loops that forbid allocation once running. This
+ * entry point allocates nothing. Instead of a workspace argument it uses a
+ * fixed scratch array of QSFM_NOALLOC_SCRATCH_BYTES that the library
+ * reserves in the memory of every GPU that loads it, held until the process
+ * exits. The caller still passes all inputs and outputs (and the metadata
+ * from qsfm_metadata()) in p.
+ *   - Returns QSFM_ERR_WORKSPACE, launching nothing, when the plan needs
+ *     more than QSFM_NOALLOC_SCRATCH_BYTES of partial results (that happens
+ *     only when tokens may be split over CTAs, i.e. fewer query tokens than
+ *     p->num_ctas; the need is 2 * num_ctas * 131328 bytes rounded up, so at
+ *     most 31 CTAs fit). qsfm_forward_workspace_size() gives the need.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make it before any stream capture.
+ *   - All calls share the array, which keeps the last call's contents;
+ *     nothing in it needs to start at zero. Calls that overlap on the GPU
+ *     (other streams or threads) race on it.
+ */
+#define QSFM_NOALLOC_SCRATCH_BYTES (8u << 20)
+qsfm_status qsfm_forward_noalloc(const qsfm_params* p, void* stream);
+
+/*
  * Debug export of the row resolution the attention kernel uses. For each
  * of the n query tokens in tokens[] (device int32), writes the token's row
  * slots in the kernel's order (ori window rows, then cmp slots), up to
