@@ -11,18 +11,33 @@
 //   S^T[j, h]  = sum_d K~[j, d] Q[h, d]      (M = 128 rows, N = 64, K = 512)
 //   O^T[d, h] += sum_j V~[j, d] P[h, j]      (M = 128 d per chunk, N = 64,
 //                                             K = 128 rows, 4 chunks)
-// Both accumulators live in tensor memory: S^T in 64 columns, O^T in 256
-// columns. One dequantised bf16 tile in shared memory (128 rows x 512, 128-B
-// swizzle) is the K-major A operand of the first product and the MN-major A
-// operand of the second.
+// Both accumulators live in tensor memory: S^T in 64 columns, O^T in 256.
+// One dequantised bf16 tile (128 rows x 512, 128-B swizzle, 8 d-blocks of
+// 16 KB) is the K-major A operand of the first product and, read through an
+// MN-major descriptor, the A operand of the second.
 //
-// Per tile: gather 128 paged fp8 rows + their per-64 scales -> dequantise to
-// bf16 in the swizzled layout -> tcgen05 QK^T -> masked online softmax in
-// registers (thread = KV row; per-head max / sum over rows by warp
-// butterflies and a 4-warp exchange) -> P^T to shared memory -> tcgen05 PV.
-// The running max is only moved when a tile's max exceeds it by more than
-// 2^8 (exact: the rescale is applied to O and l whenever it is moved).
+// Warp roles (13 warps; at most 4 per SM sub-partition, so 128 registers):
+//   warps 0-3   softmax + epilogue. Thread i owns TMEM lane i: KV row i of the
+//               tile for S^T (all 64 heads), head-dim element i of a 128-d
+//               chunk for O^T.
+//   warps 4-11  producers: resolve the paged rows of a tile, load their fp8
+//               bytes and scales into registers one tile ahead, dequantise
+//               them chunk by chunk (a chunk = 128 rows x 128 d = 2 d-blocks)
+//               into the tile as soon as the previous tile's PV product has
+//               released that chunk.
+//   warp 12     tcgen05 issue (one thread): Q by TMA, QK^T per chunk as the
+//               chunks arrive, PV per chunk, commits that release chunks.
+// mbarriers carry every hand-off; every wait is bounded in time.
+//
+// Softmax: the running max m_used per head is moved only when a tile's max
+// exceeds it by more than 8 (log2 units); a named-barrier vote detects that
+// case, so most tiles need no cross-thread max reduction. When it moves, O^T
+// and the per-thread sums l are rescaled exactly. P <= 2^8 in bf16.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "qsfm_device.cuh"
 #include "qsfm_internal.h"
@@ -30,17 +45,36 @@
 namespace qsfm {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kSoftWarps = 4;
+constexpr int kProdWarps = 8;
+constexpr int kMmaWarp = kSoftWarps + kProdWarps;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kBarSoft = 1;  // named barrier id of the softmax warps
+
 // shared memory map (byte offsets from a 1024-aligned base)
-constexpr uint32_t kSK = 0;                        // K~: 8 d-blocks x 128 rows x 128 B
-constexpr uint32_t kSQ = kSK + 8 * 128 * 128;      // Q: 8 d-blocks x 64 heads x 128 B
-constexpr uint32_t kSP = kSQ + 8 * 64 * 128;       // P^T: 128 rows x 64 heads (bf16)
-constexpr uint32_t kSRed = kSP + 128 * 128;        // red_max[4][64], red_sum[4][64]
-constexpr uint32_t kSStat = kSRed + 2 * 4 * 64 * 4;  // m_used, l_run, alpha, inv [64] each
-constexpr uint32_t kSValid = kSStat + 4 * 64 * 4;  // row valid flags [128]
-constexpr uint32_t kSBar = kSValid + 128 * 4;      // 2 mbarriers, tmem base, flags
-constexpr uint32_t kSmemBytes = kSBar + 64;
+constexpr uint32_t kSK = 0;                      // K~: 8 d-blocks x 128 rows x 128 B
+constexpr uint32_t kSQ = kSK + 8 * 128 * 128;    // Q: 8 d-blocks x 64 heads x 128 B
+constexpr uint32_t kSP = kSQ + 8 * 64 * 128;     // P^T: 128 rows x 64 heads (bf16)
+constexpr uint32_t kSRedMax = kSP + 128 * 128;   // [4][64] f32
+constexpr uint32_t kSRedSum = kSRedMax + 1024;   // [2][4][64] f32 (per tile, double-buffered)
+constexpr uint32_t kSLRun = kSRedSum + 2048;     // [64] f32 running sums
+constexpr uint32_t kSMUsed = kSLRun + 256;       // [64] f32
+constexpr uint32_t kSAlpha = kSMUsed + 256;      // [64] f32
+constexpr uint32_t kSInv = kSAlpha + 256;        // [64] f32
+constexpr uint32_t kSValid = kSInv + 256;        // [2][128] i32
+constexpr uint32_t kSBar = kSValid + 1024;       // mbarriers, tmem base, flags
+constexpr uint32_t kSmemBytes = kSBar + 256;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+
+// mbarrier slots
+constexpr int kBarQFull = 0;
+constexpr int kBarKvFull = 1;   // 4 chunks
+constexpr int kBarKvEmpty = 5;  // 4 chunks
+constexpr int kBarSFull = 9;
+constexpr int kBarPFull = 10;
+constexpr int kBarODone = 11;
+constexpr int kBarOFree = 12;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
@@ -50,86 +84,514 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kIdescQK = make_idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, 64, /*a_mn=*/1, /*b_mn=*/1);
-constexpr uint32_t kWaitIters = 1u << 26;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
-// Reduce 64 per-thread values over the 32 lanes of a warp. Afterwards lane l
-// holds the result for heads 2l and 2l+1 in r0 / r1.
-template <bool kMax>
-__device__ __forceinline__ void warp_reduce64(const float (&v)[64], float& r0, float& r1) {
-  const int lane = threadIdx.x & 31;
-  float a[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const bool up = lane & 16;
-    const float keep = up ? v[32 + i] : v[i];
-    const float send = up ? v[i] : v[32 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 16);
-    a[i] = kMax ? fmaxf(keep, got) : keep + got;
+struct Range {
+  int t0, k0, t1, k1;
+};
+
+// Walks the (token, tile-range) pieces of a CTA's range in order.
+struct PieceIter {
+  const qsfm_params* p;
+  Range r;
+  int T;
+  int t;
+  __device__ PieceIter(const qsfm_params* p_, Range r_, int T_) : p(p_), r(r_), T(T_), t(r_.t0) {}
+  __device__ bool next(int& tok, TokenGeom& g, int& lo, int& hi) {
+    if (t > r.t1 || t >= T || (t == r.t1 && r.k1 == 0)) return false;
+    tok = t;
+    g = token_geom(*p, t);
+    lo = (t == r.t0) ? min(r.k0, g.n_tiles) : 0;
+    hi = (t == r.t1) ? min(r.k1, g.n_tiles) : g.n_tiles;
+    ++t;
+    return true;
   }
-  float b[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const bool up = lane & 8;
-    const float keep = up ? a[16 + i] : a[i];
-    const float send = up ? a[i] : a[16 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 8);
-    b[i] = kMax ? fmaxf(keep, got) : keep + got;
+};
+
+// Walks the (token, tile) jobs of the range, skipping tokens without tiles.
+struct JobIter {
+  PieceIter pieces;
+  int tok = -1, k = 0, hi = 0;
+  TokenGeom g;
+  __device__ JobIter(const qsfm_params* p, Range r, int T) : pieces(p, r, T) {}
+  __device__ bool next(int& tok_out, int& k_out, TokenGeom& g_out) {
+    while (tok < 0 || k >= hi) {
+      int lo;
+      if (!pieces.next(tok, g, lo, hi)) return false;
+      k = lo;
+    }
+    tok_out = tok;
+    k_out = k++;
+    g_out = g;
+    return true;
   }
-  float c[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const bool up = lane & 4;
-    const float keep = up ? b[8 + i] : b[i];
-    const float send = up ? b[i] : b[8 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 4);
-    c[i] = kMax ? fmaxf(keep, got) : keep + got;
-  }
-  float d[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const bool up = lane & 2;
-    const float keep = up ? c[4 + i] : c[i];
-    const float send = up ? c[i] : c[4 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 2);
-    d[i] = kMax ? fmaxf(keep, got) : keep + got;
-  }
-  float e[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const bool up = lane & 1;
-    const float keep = up ? d[2 + i] : d[i];
-    const float send = up ? d[i] : d[2 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 1);
-    e[i] = kMax ? fmaxf(keep, got) : keep + got;
-  }
-  r0 = e[0];
-  r1 = e[1];
-}
+};
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Max (kMax) or sum over the 32 lanes of a warp of 32 values per lane.
+// Afterwards lane l holds the result for value index l.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = lane & w;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float keep = up ? v[w + i] : v[i];
+      const float send = up ? v[i] : v[w + i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, w);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return v[0];
+}
+
+struct Smem {
+  uint32_t base;
+  uint8_t* ptr;
+  __device__ float* f(uint32_t off) const { return reinterpret_cast<float*>(ptr + off); }
+  __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(ptr + kSBar) + i; }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(ptr + kSBar + 128); }
+  __device__ volatile int* abort_flag() const {
+    return reinterpret_cast<volatile int*>(ptr + kSBar + 136);
+  }
+};
+
+// Bounded wait; on timeout raises the CTA's abort flag and the fault bit.
+__device__ __forceinline__ bool wait_or_abort(const Smem& sm, int bar, uint32_t parity, int* fault) {
+  if (mbar_wait_bounded(sm.bar(bar), parity, sm.abort_flag(), kTimeoutNs)) return true;
+  if (!*sm.abort_flag()) {
+    *sm.abort_flag() = 1;
+    atomicOr(fault, QSFM_FAULT_TIMEOUT);
+  }
+  return false;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast, so the
+// lanes of a warp never split on a timeout.
+__device__ __forceinline__ bool warp_wait_or_abort(const Smem& sm, int bar, uint32_t parity,
+                                                   int* fault) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_or_abort(sm, bar, parity, fault);
+  __syncwarp();  // the other lanes wait here (and are ordered after lane 0's acquire)
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// ------------------------------------------------------------- producers
+// One tile job: the physical row (block * 128 + offset, -1 = masked) of each
+// of this thread's 4 rows, and which pool the tile reads (a tile never mixes
+// ori and cmp rows).
+struct JobRows {
+  int prow[4];
+  int cmp;
+};
+
+__device__ __forceinline__ void resolve_job(const qsfm_params& p, int tok, int k, const TokenGeom& g,
+                                            int row_lo, int* fault, JobRows& jr) {
+  jr.cmp = k >= g.ori_tiles;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const RowRef ref = resolve_slot(p, g, tok, k, row_lo + 32 * u, fault);
+    const uint8_t* pool = static_cast<const uint8_t*>(jr.cmp ? p.cmp_kv : p.ori_kv);
+    jr.prow[u] = ref.row >= 0 ? int((ref.kv - pool) / kDim) : -1;
+  }
+}
+
+__device__ void producer_role(const qsfm_params& p, const Smem& sm, Range rg, int T, int* fault) {
+  const int ptid = threadIdx.x - kSoftThreads;  // 0..255 (8 producer warps)
+  const int lane = threadIdx.x & 31;
+  const int row_lo = ptid >> 3;   // this thread's rows: row_lo + 32u, u = 0..3
+  const int j = ptid & 7;         // its 16-byte slot inside each 128-byte chunk of a row
+  const int odd_first = j >> 2;   // j >= 4 stores its odd 16-B chunk first (no bank conflicts)
+  JobIter jobs(&p, rg, T);
+
+  JobRows cur, nxt;
+  float csc[4];  // scale j of each row (this lane's share of the row's 8 scales)
+  // fp8 bytes of chunks 0..3 for the 4 rows, loaded one tile ahead; the chunk
+  // loop always works on R0 and rotates the others down, so that its body is
+  // emitted once
+  uint4 R0[4], R1[4], R2[4], R3[4];
+
+  auto load_job = [&](const JobRows& jr) {
+    const uint8_t* pool = static_cast<const uint8_t*>(jr.cmp ? p.cmp_kv : p.ori_kv);
+    const float* spool = jr.cmp ? p.cmp_scale : p.ori_scale;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool v = jr.prow[u] >= 0;
+      const uint8_t* src = pool + size_t(v ? jr.prow[u] : 0) * kDim + 16 * j;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      R0[u] = v ? ldg_stream_v4(src) : z;
+      R1[u] = v ? ldg_stream_v4(src + 128) : z;
+      R2[u] = v ? ldg_stream_v4(src + 256) : z;
+      R3[u] = v ? ldg_stream_v4(src + 384) : z;
+      csc[u] = v ? __ldg(spool + size_t(jr.prow[u]) * kScales + j) : 0.f;
+    }
+  };
+
+  int tok, k;
+  TokenGeom g;
+  bool have_cur = jobs.next(tok, k, g);
+  if (!have_cur) return;
+  resolve_job(p, tok, k, g, row_lo, fault, cur);
+  load_job(cur);
+  bool have_nxt = jobs.next(tok, k, g);
+  if (have_nxt) resolve_job(p, tok, k, g, row_lo, fault, nxt);
+
+  // The next tile's rows are loaded only after this tile's last chunk has
+  // been published: the proxy fence and the release of each chunk's arrive
+  // wait for the thread's outstanding loads, so loads issued earlier would
+  // serialise every chunk on a memory round trip. Issued here, they overlap
+  // the softmax and PV product of the current tile instead.
+  uint32_t ph = 1;  // kv_empty starts free
+  uint32_t tiles = 0;
+  while (have_cur) {
+    int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + (tiles & 1) * 128;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      if (!warp_wait_or_abort(sm, kBarKvEmpty + c, ph, fault)) return;
+      if (c == 0 && j == 0) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) valid[row_lo + 32 * u] = cur.prow[u] >= 0;
+      }
+      const int src_lane = (lane & ~7) | (2 * c + (j >> 2));
+      const uint32_t blk = sm.base + kSK + (2 * c + (j >> 2)) * 16384;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float sc = __shfl_sync(0xffffffffu, csc[u], src_lane);
+        uint4 lo, hi;
+        dequant16(R0[u], sc, lo, hi);
+        const int r = row_lo + 32 * u;
+        const uint32_t sw = uint32_t(r & 7);
+        const uint32_t rowb = blk + r * 128;
+        const uint32_t c0 = 2 * (j & 3);
+        sts_v4(rowb + (((c0 + odd_first) ^ sw) << 4), odd_first ? hi : lo);
+        sts_v4(rowb + (((c0 + 1 - odd_first) ^ sw) << 4), odd_first ? lo : hi);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(kBarKvFull + c));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        R0[u] = R1[u];
+        R1[u] = R2[u];
+        R2[u] = R3[u];
+      }
+    }
+    ph ^= 1;
+    ++tiles;
+    have_cur = have_nxt;
+    if (have_cur) {
+      cur = nxt;
+      load_job(cur);
+      have_nxt = jobs.next(tok, k, g);
+      if (have_nxt) resolve_job(p, tok, k, g, row_lo, fault, nxt);
+    }
+  }
+}
+
+// ------------------------------------------------------------- MMA issue
+__device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
+                         const CUtensorMap* qmap, int* fault) {
+  if ((threadIdx.x & 31) != 0) return;
+  PieceIter pieces(&p, rg, T);
+  TokenGeom g;
+  // the next piece that has tiles
+  auto next_live = [&](int& t_, int& lo_, int& hi_) {
+    while (pieces.next(t_, g, lo_, hi_))
+      if (lo_ < hi_) return true;
+    return false;
+  };
+  auto load_q = [&](int t_) {
+    mbar_arrive_expect_tx(sm.bar(kBarQFull), 64 * 1024);
+#pragma unroll
+    for (int db = 0; db < 8; ++db)
+      tma_load_2d(sm.base + kSQ + db * 8192, qmap, db * 64, t_ * 64, sm.bar(kBarQFull));
+  };
+  int tok, lo, hi;
+  bool have = next_live(tok, lo, hi);
+  if (!have) return;
+  load_q(tok);
+  uint32_t tiles = 0, pieces_done = 0, ph_q = 0;
+  while (have) {
+    int ntok = 0, nlo = 0, nhi = 0;
+    const bool have_next = next_live(ntok, nlo, nhi);
+    if (!wait_or_abort(sm, kBarQFull, ph_q, fault)) return;
+    ph_q ^= 1;
+    for (int k = lo; k < hi; ++k) {
+      const uint32_t par = tiles & 1;
+      // descriptors advance by 32 B per k-step (16 elements), 16 KB / 8 KB per d-block
+      const uint64_t a0 = make_sdesc_sw128(sm.base + kSK, 16, 1024);
+      const uint64_t b0 = make_sdesc_sw128(sm.base + kSQ, 16, 1024);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        if (!wait_or_abort(sm, kBarKvFull + c, par, fault)) return;
+        tc_fence_after();
+#pragma unroll 1
+        for (int step = 8 * c; step < 8 * c + 8; ++step) {
+          const int db = step >> 2, kk = step & 3;
+          mma_bf16(tmem + kTmemS, a0 + uint64_t((db * 16384 + kk * 32) >> 4),
+                   b0 + uint64_t((db * 8192 + kk * 32) >> 4), kIdescQK, step != 0);
+        }
+      }
+      mma_commit(sm.bar(kBarSFull));
+      if (k == hi - 1 && have_next) {
+        // Q of the next token as soon as this token's last QK^T has read Q
+        if (!wait_or_abort(sm, kBarSFull, par, fault)) return;
+        load_q(ntok);
+      }
+      if (!wait_or_abort(sm, kBarPFull, par, fault)) return;
+      if (k == lo && pieces_done > 0) {
+        // the previous token's epilogue must have read O^T before it is overwritten
+        if (!wait_or_abort(sm, kBarOFree, (pieces_done - 1) & 1, fault)) return;
+      }
+      tc_fence_after();
+      const uint64_t pa0 = make_sdesc_sw128(sm.base + kSK, 16384, 1024);
+      const uint64_t pb0 = make_sdesc_sw128(sm.base + kSP, 16, 1024);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16(tmem + kTmemO + c * 64, pa0 + uint64_t((c * 32768 + ks * 2048) >> 4),
+                   pb0 + uint64_t((ks * 2048) >> 4), kIdescPV, (k == lo && ks == 0) ? 0u : 1u);
+        }
+        mma_commit(sm.bar(kBarKvEmpty + c));
+      }
+      if (k == hi - 1) mma_commit(sm.bar(kBarODone));
+      ++tiles;
+    }
+    ++pieces_done;
+    have = have_next;
+    tok = ntok;
+    lo = nlo;
+    hi = nhi;
+  }
+}
+
+// ------------------------------------------------------ softmax + epilogue
+// Thread i owns row i of the tile: its 64 scores are handled as two halves
+// of 32 heads, read from TMEM again for each pass to keep registers low.
+__device__ __forceinline__ void load_scores(uint32_t taddr, bool rv, float scale, float (&x)[32]) {
+  tmem_ld32(taddr, x);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = rv ? x[i] * scale : -INFINITY;
+}
+
+__device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
+                             const Workspace& ws, int c_idx, int* fault) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid;  // KV row of the tile / head-dim element inside a 128-d chunk
+  const uint32_t lane_base = uint32_t(32 * warp) << 16;
+  const float qk_scale = p.softmax_scale * kLog2e;
+  float* m_used = sm.f(kSMUsed);
+  float* alpha = sm.f(kSAlpha);
+  float* inv = sm.f(kSInv);
+  float* lrun = sm.f(kSLRun);
+  float* red_max = sm.f(kSRedMax);
+  float* red_sum = sm.f(kSRedSum);
+  PieceIter pieces(&p, rg, T);
+  uint32_t tiles = 0, pieces_live = 0;
+  int t, lo, hi;
+  TokenGeom g;
+  while (pieces.next(t, g, lo, hi)) {
+    const bool whole = (lo == 0 && hi == g.n_tiles);
+    const int slot = (t == rg.t0) ? 2 * c_idx : 2 * c_idx + 1;
+    const bool writable = whole || slot < ws.slots;  // split pieces need the workspace
+    if (!writable && tid == 0) atomicOr(fault, QSFM_FAULT_METADATA);
+    if (tid < 64) {
+      m_used[tid] = -INFINITY;
+      lrun[tid] = 0.f;
+    }
+    named_sync(kBarSoft, kSoftThreads);
+    bool pend = false;  // red_sum of the previous tile not yet added to lrun
+    for (int k = lo; k < hi; ++k) {
+      const uint32_t par = tiles & 1;
+      // Lane 0 of each warp polls. After an abort the waits fall through at
+      // once; the softmax warps keep running the same named-barrier sequence
+      // so that none of them blocks.
+      warp_wait_or_abort(sm, kBarKvFull, par, fault);
+      const bool rv = reinterpret_cast<int*>(sm.ptr + kSValid)[par * 128 + row] != 0;
+      warp_wait_or_abort(sm, kBarSFull, par, fault);
+      tc_fence_after();
+      bool exceed = false;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float x[32];
+        load_scores(tmem + kTmemS + lane_base + 32 * half, rv, qk_scale, x);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) exceed |= x[i] > m_used[32 * half + i] + kRescaleLog2;
+      }
+      const bool move = named_sync_or(kBarSoft, kSoftThreads, exceed);  // also true against -inf
+      if (pend && tid < 64) {
+        const float* rs = red_sum + (par ^ 1) * 256;
+        lrun[tid] += (rs[tid] + rs[64 + tid]) + (rs[128 + tid] + rs[192 + tid]);
+      }
+      if (move) {
+        // move the running max: tile max per head over the 128 rows
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          float x[32];
+          load_scores(tmem + kTmemS + lane_base + 32 * half, rv, qk_scale, x);
+          red_max[warp * 64 + 32 * half + lane] = warp_reduce32<true>(x);
+        }
+        named_sync(kBarSoft, kSoftThreads);
+        if (tid < 64) {
+          const float mt = fmaxf(fmaxf(red_max[tid], red_max[64 + tid]),
+                                 fmaxf(red_max[128 + tid], red_max[192 + tid]));
+          const float mu = m_used[tid];
+          float a = 1.f;
+          if (mt > -INFINITY && (mu == -INFINITY || mt > mu + kRescaleLog2)) {
+            a = (mu == -INFINITY) ? 0.f : exp2f(mu - mt);
+            m_used[tid] = mt;
+          }
+          alpha[tid] = a;
+          lrun[tid] *= a;
+        }
+        named_sync(kBarSoft, kSoftThreads);
+        if (k != lo) {
+          // O^T at this thread's head-dim lane, all heads (the previous PV
+          // product has completed: this tile's QK^T waited for it)
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              float o[32];
+              const uint32_t addr = tmem + kTmemO + 64 * c + 32 * half + lane_base;
+              tmem_ld32(addr, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= alpha[32 * half + i];
+              tmem_st16(addr, o);
+              tmem_st16(addr + 16, o + 16);
+            }
+          }
+          tmem_st_wait();
+        }
+      }
+      // P = exp2(x - m_used) -> the P^T row line (64 heads, 128 B, swizzled),
+      // and the per-head sums of this warp's 32 rows
+      const uint32_t prow = sm.base + kSP + row * 128;
+      const uint32_t sw = uint32_t(row & 7);
+      float* rs = red_sum + par * 256 + warp * 64;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float x[32];
+        load_scores(tmem + kTmemS + lane_base + 32 * half, rv, qk_scale, x);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float mu = m_used[32 * half + i];
+          x[i] = exp2f(x[i] - (mu == -INFINITY ? 0.f : mu));
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint4 v;
+          v.x = pack_bf16(x[8 * cc + 0], x[8 * cc + 1]);
+          v.y = pack_bf16(x[8 * cc + 2], x[8 * cc + 3]);
+          v.z = pack_bf16(x[8 * cc + 4], x[8 * cc + 5]);
+          v.w = pack_bf16(x[8 * cc + 6], x[8 * cc + 7]);
+          sts_v4(prow + ((uint32_t(4 * half + cc) ^ sw) << 4), v);
+        }
+        rs[32 * half + lane] = warp_reduce32<false>(x);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(kBarPFull));
+      pend = true;
+      ++tiles;
+    }
+    // ---------------- epilogue of the piece
+    const bool any = lo < hi;
+    named_sync(kBarSoft, kSoftThreads);
+    if (tid < 64 && writable) {
+      float lt = lrun[tid];
+      if (pend) {
+        const float* rs = red_sum + ((tiles - 1) & 1) * 256;
+        lt += (rs[tid] + rs[64 + tid]) + (rs[128 + tid] + rs[192 + tid]);
+      }
+      const float mu = m_used[tid];
+      const float lse2 = lt > 0.f ? mu + log2f(lt) : -INFINITY;
+      if (whole) {
+        float den = lt;
+        if (p.sinks != nullptr && lt > 0.f) den += exp2f(__ldg(p.sinks + tid) * kLog2e - mu);
+        inv[tid] = lt > 0.f ? 1.f / den : 0.f;
+        if (p.return_lse) p.softmax_lse[size_t(t) * 64 + tid] = lse2 * kLn2;
+      } else {
+        inv[tid] = lt > 0.f ? 1.f / lt : 0.f;
+        ws.lse[size_t(slot) * 64 + tid] = lse2 * kLn2;
+      }
+    }
+    named_sync(kBarSoft, kSoftThreads);
+    if (any) {
+      warp_wait_or_abort(sm, kBarODone, pieces_live & 1, fault);
+      tc_fence_after();
+    }
+    // O^T chunk by chunk: lane = head-dim element, columns = heads. Whole
+    // tokens go through the (now idle) P buffer as bf16 [64 heads][128 d] so
+    // that every head's 256-byte run is written with 16-byte stores; split
+    // pieces write fp32 partial rows straight to the workspace.
+    uint8_t* stage = sm.ptr + kSP;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float o[32];
+        if (any) {
+          tmem_ld32(tmem + kTmemO + 64 * c + 32 * half + lane_base, o);
+          tmem_ld_wait();
+        }
+        const int h0 = 32 * half;
+        if (whole) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            reinterpret_cast<__nv_bfloat16*>(stage)[(h0 + i) * 128 + row] =
+                __float2bfloat16_rn(any ? o[i] * inv[h0 + i] : 0.f);
+        } else if (writable) {
+          float* out = ws.out + (size_t(slot) * 64 + h0) * kDim + 128 * c + row;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[size_t(i) * kDim] = any ? o[i] * inv[h0 + i] : 0.f;
+        }
+      }
+      if (whole) {
+        named_sync(kBarSoft, kSoftThreads);
+        // 64 heads x 256 B = 1024 16-byte pieces, 8 per thread
+        uint8_t* gout = static_cast<uint8_t*>(p.attn_out) + size_t(t) * 64 * kDim * 2 + 256 * c;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int piece = it * kSoftThreads + tid;
+          const int h = piece >> 4, part = piece & 15;
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + h * 256 + part * 16);
+          *reinterpret_cast<uint4*>(gout + size_t(h) * kDim * 2 + part * 16) = v;
+        }
+        named_sync(kBarSoft, kSoftThreads);
+      }
+    }
+    if (any) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(kBarOFree));
+      ++pieces_live;
+    }
+    named_sync(kBarSoft, kSoftThreads);  // m_used / lrun / inv are reused by the next piece
+    if (*sm.abort_flag()) break;         // uniform: read after the barrier
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    attention_kernel(const qsfm_params p, const int T, const Workspace ws, int* fault) {
+    attention_kernel(const qsfm_params p, const int T, const Workspace ws, int* fault,
+                     const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
-  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (sbase - raw_addr);
-  float* red_max = reinterpret_cast<float*>(smem + kSRed);
-  float* red_sum = red_max + 4 * 64;
-  float* m_used = reinterpret_cast<float*>(smem + kSStat);
-  float* l_run = m_used + 64;
-  float* alpha = l_run + 64;
-  float* inv = alpha + 64;
-  int* row_valid = reinterpret_cast<int*>(smem + kSValid);
-  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + kSBar);
-  uint64_t* bar_o = bar_s + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSBar + 16);
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + kSBar + 32);  // [0] rescale [1] abort
+  Smem sm;
+  sm.base = (raw_addr + 1023u) & ~1023u;
+  sm.ptr = smem_raw + (sm.base - raw_addr);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int* meta = p.metadata;
   if (meta[0] != kMetaMagic || meta[2] != T) {
     if (tid == 0 && blockIdx.x == 0) atomicOr(fault, QSFM_FAULT_METADATA);
@@ -142,261 +604,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int c = blockIdx.x;
   if (c >= G) return;
-  const int t0 = meta[kMetaHeader + 2 * c], k0 = meta[kMetaHeader + 2 * c + 1];
-  const int t1 = meta[kMetaHeader + 2 * c + 2], k1 = meta[kMetaHeader + 2 * c + 3];
-  if (t0 < 0 || t1 > T || t0 > t1 || k0 < 0 || k1 < 0 || (t1 == T && k1 != 0)) {
+  const Range rg{meta[kMetaHeader + 2 * c], meta[kMetaHeader + 2 * c + 1],
+                 meta[kMetaHeader + 2 * c + 2], meta[kMetaHeader + 2 * c + 3]};
+  if (rg.t0 < 0 || rg.t1 > T || rg.t0 > rg.t1 || rg.k0 < 0 || rg.k1 < 0 ||
+      (rg.t1 == T && rg.k1 != 0)) {
     if (tid == 0) atomicOr(fault, QSFM_FAULT_METADATA);
     return;
   }
-  if (t0 == t1 && k0 == k1) return;
+  if (rg.t0 == rg.t1 && rg.k0 == rg.k1) return;
 
   if (tid == 0) {
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+    mbar_init(sm.bar(kBarQFull), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(sm.bar(kBarKvFull + i), kProdWarps);
+      mbar_init(sm.bar(kBarKvEmpty + i), 1);
+    }
+    mbar_init(sm.bar(kBarSFull), 1);
+    mbar_init(sm.bar(kBarPFull), kSoftWarps);
+    mbar_init(sm.bar(kBarODone), 1);
+    mbar_init(sm.bar(kBarOFree), kSoftWarps);
+    *sm.abort_flag() = 0;
     fence_mbar_init();
-    flags[0] = 0;
-    flags[1] = 0;
   }
-  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(sm.tmem_slot(), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = uint32_t(warp * 32) << 16;
-  const float qk_scale = p.softmax_scale * kLog2e;
-  uint32_t ph_s = 0, ph_o = 0;
-  bool aborted = false;
+  const uint32_t tmem = *sm.tmem_slot();
 
-  for (int t = t0; t <= t1 && t < T && !aborted; ++t) {
-    if (t == t1 && k1 == 0) break;
-    const TokenGeom g = token_geom(p, t);
-    const int klo = (t == t0) ? min(k0, g.n_tiles) : 0;
-    const int khi = (t == t1) ? min(k1, g.n_tiles) : g.n_tiles;
-    const bool whole = (klo == 0 && khi == g.n_tiles);
-    const int slot = (t == t0) ? 2 * c : 2 * c + 1;
-    if (!whole && slot >= ws.slots) {  // plan splits a token but no workspace was given
-      if (tid == 0) atomicOr(fault, QSFM_FAULT_METADATA);
-      break;
-    }
-
-    if (tid < 64) {
-      m_used[tid] = -INFINITY;
-      l_run[tid] = 0.f;
-    }
-    // Q of the token -> swizzled K-major [8 d-blocks][64 heads][128 B]
-    if (klo < khi) {
-      const uint8_t* qg = static_cast<const uint8_t*>(p.q) + size_t(t) * kHeads * kDim * 2;
-#pragma unroll 4
-      for (int i = tid; i < kHeads * kDim / 8; i += kThreads) {
-        const int h = i >> 6, c16 = i & 63;
-        const uint4 v = ldg_nc_v4(qg + size_t(i) * 16);
-        sts_v4(sbase + kSQ + (c16 >> 3) * 8192 + h * 128 + (((c16 & 7) ^ (h & 7)) << 4), v);
-      }
-    }
-
-    bool first = true;
-    for (int k = klo; k < khi; ++k) {
-      // ---- gather + dequantise 128 rows into the swizzled tile
-#pragma unroll 1
-      for (int gi = 0; gi < 4; ++gi) {
-        const int r = warp * 32 + gi * 8 + (lane & 7);
-        const RowRef ref = resolve_slot(p, g, t, k, r, fault);
-        const bool valid = ref.row >= 0;
-        if ((lane >> 3) == 0) row_valid[r] = valid ? 1 : 0;
-        const uint32_t sw = uint32_t(r & 7);
-#pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-          const int u = pp * 4 + (lane >> 3);
-          const uint32_t dst = sbase + kSK + u * 16384 + r * 128;
-          if (valid) {
-            const uint8_t* src = ref.kv + u * 64;
-            const float sc = __ldg(ref.sc + u);
-            uint4 in[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) in[m] = ldg_nc_v4(src + 16 * m);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              uint4 lo, hi;
-              dequant16(in[m], sc, lo, hi);
-              sts_v4(dst + (((2 * m) ^ sw) << 4), lo);
-              sts_v4(dst + (((2 * m + 1) ^ sw) << 4), hi);
-            }
-          } else {
-            const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) sts_v4(dst + ((ch ^ sw) << 4), z);
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      __syncthreads();
-
-      // ---- S^T = K~ Q^T
-      if (tid == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = make_sdesc_sw128(sbase + kSK + kb * 16384 + kk * 32, 16, 1024);
-            const uint64_t b = make_sdesc_sw128(sbase + kSQ + kb * 8192 + kk * 32, 16, 1024);
-            mma_bf16(tmem + kTmemS, a, b, kIdescQK, (kb | kk) != 0);
-          }
-        }
-        mma_commit(bar_s);
-        if (!mbar_wait(bar_s, ph_s, kWaitIters)) {
-          flags[1] = 1;
-          atomicOr(fault, QSFM_FAULT_TIMEOUT);
-        }
-      }
-      ph_s ^= 1;
-      __syncthreads();
-      if (flags[1]) { aborted = true; break; }
-      tc_fence_after();
-
-      // ---- masked online softmax (thread = KV row of the tile)
-      float x[64];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tmem_ld16(tmem + kTmemS + lane_base + j * 16, x + j * 16);
-      tmem_ld_wait();
-      const bool rv = row_valid[tid] != 0;
-#pragma unroll
-      for (int h = 0; h < 64; ++h) x[h] = rv ? x[h] * qk_scale : -INFINITY;
-      float r0, r1;
-      warp_reduce64<true>(x, r0, r1);
-      red_max[warp * 64 + 2 * lane] = r0;
-      red_max[warp * 64 + 2 * lane + 1] = r1;
-      __syncthreads();
-      if (tid < 64) {
-        const float mt = fmaxf(fmaxf(red_max[tid], red_max[64 + tid]),
-                               fmaxf(red_max[128 + tid], red_max[192 + tid]));
-        const float mu = m_used[tid];
-        float a = 1.f;
-        if (mt > -INFINITY && (mu == -INFINITY || mt > mu + kRescaleLog2)) {
-          a = (mu == -INFINITY) ? 0.f : exp2f(mu - mt);
-          m_used[tid] = mt;
-          if (!first) flags[0] = 1;
-        }
-        alpha[tid] = a;
-      }
-      __syncthreads();
-      float pr[64];
-#pragma unroll
-      for (int h = 0; h < 64; ++h) {
-        const float mu = m_used[h];
-        pr[h] = exp2f(x[h] - (mu == -INFINITY ? 0.f : mu));
-      }
-      warp_reduce64<false>(pr, r0, r1);
-      red_sum[warp * 64 + 2 * lane] = r0;
-      red_sum[warp * 64 + 2 * lane + 1] = r1;
-      {
-        const uint32_t prow = sbase + kSP + tid * 128;
-        const uint32_t sw = uint32_t(tid & 7);
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint4 v;
-          v.x = pack_bf16(pr[8 * cc + 0], pr[8 * cc + 1]);
-          v.y = pack_bf16(pr[8 * cc + 2], pr[8 * cc + 3]);
-          v.z = pack_bf16(pr[8 * cc + 4], pr[8 * cc + 5]);
-          v.w = pack_bf16(pr[8 * cc + 6], pr[8 * cc + 7]);
-          sts_v4(prow + ((uint32_t(cc) ^ sw) << 4), v);
-        }
-      }
-      __syncthreads();
-      if (tid < 64) {
-        l_run[tid] = l_run[tid] * alpha[tid] + (red_sum[tid] + red_sum[64 + tid]) +
-                     (red_sum[128 + tid] + red_sum[192 + tid]);
-      }
-      if (flags[0]) {  // move O^T to the new running max (previous PV has completed)
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float o[16];
-            const uint32_t addr = tmem + kTmemO + cc * 64 + j * 16 + lane_base;
-            tmem_ld16(addr, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha[j * 16 + i];
-            tmem_st16(addr, o);
-          }
-        }
-        tmem_st_wait();
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) flags[0] = 0;
-
-      // ---- O^T += V~^T P^T
-      if (tid == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t a = make_sdesc_sw128(sbase + kSK + cc * 32768 + ks * 2048, 16384, 1024);
-            const uint64_t b = make_sdesc_sw128(sbase + kSP + ks * 2048, 16, 1024);
-            mma_bf16(tmem + kTmemO + cc * 64, a, b, kIdescPV, (first && ks == 0) ? 0u : 1u);
-          }
-        }
-        mma_commit(bar_o);
-        if (!mbar_wait(bar_o, ph_o, kWaitIters)) {
-          flags[1] = 1;
-          atomicOr(fault, QSFM_FAULT_TIMEOUT);
-        }
-      }
-      ph_o ^= 1;
-      __syncthreads();
-      if (flags[1]) { aborted = true; break; }
-      tc_fence_after();
-      first = false;
-    }
-    if (aborted) break;
-
-    // ---- epilogue: normalise, add the sink (whole tokens), write out
-    const bool any = !first;  // at least one tile went through the MMAs
-    if (tid < 64) {
-      const float l = l_run[tid], mu = m_used[tid];
-      const float lse2 = l > 0.f ? mu + log2f(l) : -INFINITY;
-      if (whole) {
-        float den = l;
-        if (p.sinks != nullptr && l > 0.f) den += exp2f(__ldg(p.sinks + tid) * kLog2e - mu);
-        inv[tid] = l > 0.f ? 1.f / den : 0.f;
-        if (p.return_lse) p.softmax_lse[size_t(t) * 64 + tid] = lse2 * kLn2;
-      } else {
-        inv[tid] = l > 0.f ? 1.f / l : 0.f;
-        ws.lse[size_t(slot) * 64 + tid] = lse2 * kLn2;
-      }
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      float o[64];
-      if (any) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tmem_ld16(tmem + kTmemO + cc * 64 + j * 16 + lane_base, o + j * 16);
-        tmem_ld_wait();
-      }
-      const int d = cc * 128 + warp * 32 + lane;
-      if (whole) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.attn_out) + size_t(t) * 64 * kDim + d;
-#pragma unroll
-        for (int h = 0; h < 64; ++h) out[size_t(h) * kDim] = __float2bfloat16_rn(any ? o[h] * inv[h] : 0.f);
-      } else {
-        float* out = ws.out + size_t(slot) * 64 * kDim + d;
-#pragma unroll
-        for (int h = 0; h < 64; ++h) out[size_t(h) * kDim] = any ? o[h] * inv[h] : 0.f;
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+  if (warp < kSoftWarps) {
+    softmax_role(p, sm, rg, T, tmem, ws, c, fault);
+  } else if (warp < kMmaWarp) {
+    producer_role(p, sm, rg, T, fault);
+  } else {
+    mma_role(p, sm, rg, T, tmem, &qmap, fault);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Tensor map of q viewed as [T * 64 rows, 512 bf16 columns], boxes of
+// 64 rows x 64 columns (128 B) with the 128-B swizzle of the MMA operand.
+cudaError_t make_q_map(const void* q, int T, CUtensorMap* map) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult qres;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qres) == cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(T) * kHeads};
+  const cuuint64_t strides[1] = {cuuint64_t(kDim) * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -406,7 +680,10 @@ cudaError_t launch_attention(const qsfm_params& p, int num_tokens, int num_ctas,
   cudaError_t e = cudaFuncSetAttribute(attention_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e != cudaSuccess) return e;
-  attention_kernel<<<num_ctas, kThreads, kSmemAlloc, s>>>(p, num_tokens, ws, fault);
+  CUtensorMap qmap;
+  e = make_q_map(p.q, num_tokens, &qmap);
+  if (e != cudaSuccess) return e;
+  attention_kernel<<<num_ctas, kThreads, kSmemAlloc, s>>>(p, num_tokens, ws, fault, qmap);
   return cudaGetLastError();
 }
 
