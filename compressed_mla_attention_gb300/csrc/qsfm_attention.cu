@@ -212,10 +212,7 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, Range rg, in
 
   JobRows cur, nxt;
   float csc[4];  // scale j of each row (this lane's share of the row's 8 scales)
-  // fp8 bytes of chunks 0..3 for the 4 rows, loaded one tile ahead; the chunk
-  // loop always works on R0 and rotates the others down, so that its body is
-  // emitted once
-  uint4 R0[4], R1[4], R2[4], R3[4];
+  uint4 R[4][4];  // fp8 bytes [chunk][row unit], loaded one tile ahead
 
   auto load_job = [&](const JobRows& jr) {
     const uint8_t* pool = static_cast<const uint8_t*>(jr.cmp ? p.cmp_kv : p.ori_kv);
@@ -224,11 +221,8 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, Range rg, in
     for (int u = 0; u < 4; ++u) {
       const bool v = jr.prow[u] >= 0;
       const uint8_t* src = pool + size_t(v ? jr.prow[u] : 0) * kDim + 16 * j;
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      R0[u] = v ? ldg_stream_v4(src) : z;
-      R1[u] = v ? ldg_stream_v4(src + 128) : z;
-      R2[u] = v ? ldg_stream_v4(src + 256) : z;
-      R3[u] = v ? ldg_stream_v4(src + 384) : z;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) R[c][u] = v ? ldg_stream_v4(src + 128 * c) : make_uint4(0, 0, 0, 0);
       csc[u] = v ? __ldg(spool + size_t(jr.prow[u]) * kScales + j) : 0.f;
     }
   };
@@ -251,7 +245,7 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, Range rg, in
   uint32_t tiles = 0;
   while (have_cur) {
     int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + (tiles & 1) * 128;
-#pragma unroll 1
+#pragma unroll
     for (int c = 0; c < 4; ++c) {
       if (!warp_wait_or_abort(sm, kBarKvEmpty + c, ph, fault)) return;
       if (c == 0 && j == 0) {
@@ -264,7 +258,7 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, Range rg, in
       for (int u = 0; u < 4; ++u) {
         const float sc = __shfl_sync(0xffffffffu, csc[u], src_lane);
         uint4 lo, hi;
-        dequant16(R0[u], sc, lo, hi);
+        dequant16(R[c][u], sc, lo, hi);
         const int r = row_lo + 32 * u;
         const uint32_t sw = uint32_t(r & 7);
         const uint32_t rowb = blk + r * 128;
@@ -275,12 +269,6 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, Range rg, in
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(kBarKvFull + c));
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        R0[u] = R1[u];
-        R1[u] = R2[u];
-        R2[u] = R3[u];
-      }
     }
     ph ^= 1;
     ++tiles;
@@ -295,6 +283,44 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, Range rg, in
 }
 
 // ------------------------------------------------------------- MMA issue
+// k-step s of d-block db: A (K~) at +db*16 KB + s*32 B, B (Q) at +db*8 KB + s*32 B.
+template <int kDb, int kS>
+__device__ __forceinline__ void qk_mma(uint32_t d, uint64_t a0, uint64_t b0) {
+  mma_bf16_at<uint32_t((kDb * 16384 + kS * 32) >> 4), uint32_t((kDb * 8192 + kS * 32) >> 4)>(
+      d, a0, b0, kIdescQK, (kDb | kS) != 0);
+}
+
+// QK^T over chunk kC (d-blocks 2kC, 2kC+1) once the producers publish it.
+template <int kC>
+__device__ __forceinline__ bool qk_chunk(const Smem& sm, uint32_t tmem, uint64_t a0, uint64_t b0,
+                                         uint32_t par, int* fault) {
+  if (!wait_or_abort(sm, kBarKvFull + kC, par, fault)) return false;
+  tc_fence_after();
+  const uint32_t d = tmem + kTmemS;
+  qk_mma<2 * kC, 0>(d, a0, b0); qk_mma<2 * kC, 1>(d, a0, b0);
+  qk_mma<2 * kC, 2>(d, a0, b0); qk_mma<2 * kC, 3>(d, a0, b0);
+  qk_mma<2 * kC + 1, 0>(d, a0, b0); qk_mma<2 * kC + 1, 1>(d, a0, b0);
+  qk_mma<2 * kC + 1, 2>(d, a0, b0); qk_mma<2 * kC + 1, 3>(d, a0, b0);
+  return true;
+}
+
+// PV for head-dim chunk kC: A (V~^T, MN-major) at +kC*32 KB + ks*2 KB,
+// B (P^T) at +ks*2 KB; then release the chunk to the producers.
+template <int kC>
+__device__ __forceinline__ void pv_chunk(const Smem& sm, uint32_t tmem, uint64_t a0, uint64_t b0,
+                                         uint32_t acc0) {
+  const uint32_t d = tmem + kTmemO + kC * 64;
+  mma_bf16_at<uint32_t((kC * 32768 + 0 * 2048) >> 4), uint32_t((0 * 2048) >> 4)>(d, a0, b0, kIdescPV, acc0);
+  mma_bf16_at<uint32_t((kC * 32768 + 1 * 2048) >> 4), uint32_t((1 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_bf16_at<uint32_t((kC * 32768 + 2 * 2048) >> 4), uint32_t((2 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_bf16_at<uint32_t((kC * 32768 + 3 * 2048) >> 4), uint32_t((3 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_bf16_at<uint32_t((kC * 32768 + 4 * 2048) >> 4), uint32_t((4 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_bf16_at<uint32_t((kC * 32768 + 5 * 2048) >> 4), uint32_t((5 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_bf16_at<uint32_t((kC * 32768 + 6 * 2048) >> 4), uint32_t((6 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_bf16_at<uint32_t((kC * 32768 + 7 * 2048) >> 4), uint32_t((7 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_commit(sm.bar(kBarKvEmpty + kC));
+}
+
 __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
                          const CUtensorMap* qmap, int* fault) {
   if ((threadIdx.x & 31) != 0) return;
@@ -324,20 +350,15 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
     ph_q ^= 1;
     for (int k = lo; k < hi; ++k) {
       const uint32_t par = tiles & 1;
-      // descriptors advance by 32 B per k-step (16 elements), 16 KB / 8 KB per d-block
+      // Fully unrolled: descriptors are the base plus compile-time offsets
+      // (32 B per k-step, 16 KB / 8 KB per d-block), so one thread issues an
+      // MMA as fast as the pipe takes it.
       const uint64_t a0 = make_sdesc_sw128(sm.base + kSK, 16, 1024);
       const uint64_t b0 = make_sdesc_sw128(sm.base + kSQ, 16, 1024);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        if (!wait_or_abort(sm, kBarKvFull + c, par, fault)) return;
-        tc_fence_after();
-#pragma unroll 1
-        for (int step = 8 * c; step < 8 * c + 8; ++step) {
-          const int db = step >> 2, kk = step & 3;
-          mma_bf16(tmem + kTmemS, a0 + uint64_t((db * 16384 + kk * 32) >> 4),
-                   b0 + uint64_t((db * 8192 + kk * 32) >> 4), kIdescQK, step != 0);
-        }
-      }
+      if (!qk_chunk<0>(sm, tmem, a0, b0, par, fault)) return;
+      if (!qk_chunk<1>(sm, tmem, a0, b0, par, fault)) return;
+      if (!qk_chunk<2>(sm, tmem, a0, b0, par, fault)) return;
+      if (!qk_chunk<3>(sm, tmem, a0, b0, par, fault)) return;
       mma_commit(sm.bar(kBarSFull));
       if (k == hi - 1 && have_next) {
         // Q of the next token as soon as this token's last QK^T has read Q
@@ -352,15 +373,11 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
       tc_fence_after();
       const uint64_t pa0 = make_sdesc_sw128(sm.base + kSK, 16384, 1024);
       const uint64_t pb0 = make_sdesc_sw128(sm.base + kSP, 16, 1024);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks) {
-          mma_bf16(tmem + kTmemO + c * 64, pa0 + uint64_t((c * 32768 + ks * 2048) >> 4),
-                   pb0 + uint64_t((ks * 2048) >> 4), kIdescPV, (k == lo && ks == 0) ? 0u : 1u);
-        }
-        mma_commit(sm.bar(kBarKvEmpty + c));
-      }
+      const uint32_t acc0 = k == lo ? 0u : 1u;
+      pv_chunk<0>(sm, tmem, pa0, pb0, acc0);
+      pv_chunk<1>(sm, tmem, pa0, pb0, acc0);
+      pv_chunk<2>(sm, tmem, pa0, pb0, acc0);
+      pv_chunk<3>(sm, tmem, pa0, pb0, acc0);
       if (k == hi - 1) mma_commit(sm.bar(kBarODone));
       ++tiles;
     }

@@ -309,6 +309,22 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// As mma_bf16, with the descriptors given as a base plus compile-time
+// offsets (in 16-byte units) added inside the asm, so that an unrolled
+// sequence of MMAs keeps only the two base descriptors in registers.
+template <uint32_t kAOff, uint32_t kBOff>
+__device__ __forceinline__ void mma_bf16_at(uint32_t d_tmem, uint64_t a_base, uint64_t b_base,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 a, b;\n"
+      " add.u64 a, %1, %5;\n add.u64 b, %2, %6;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(uint64_t(kAOff)),
+      "n"(uint64_t(kBOff))
+      : "memory");
+}
+
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
