@@ -6,33 +6,45 @@
 // parameter table row "sinks"; lse from KvQuantSparseAttnSharedKv, parameter
 // table row softmax_lse).
 //
-// Orientation. The contractions run transposed so that the KV-row dimension
-// (128 rows per tile) is the MMA M dimension and the 64 heads are N:
-//   S^T[j, h]  = sum_d K~[j, d] Q[h, d]      (M = 128 rows, N = 64, K = 512)
+// Orientation. The contractions run transposed so that the KV rows of a tile
+// (64 rows) are the M dimension of the score product and the 64 heads are N:
+//   S^T[j, h]  = sum_d K~[j, d] Q[h, d]      (M = 64 rows, N = 64, K = 512)
 //   O^T[d, h] += sum_j V~[j, d] P[h, j]      (M = 128 d per chunk, N = 64,
-//                                             K = 128 rows, 4 chunks)
-// Both accumulators live in tensor memory: S^T in 64 columns, O^T in 256.
-// One dequantised bf16 tile (128 rows x 512, 128-B swizzle, 8 d-blocks of
-// 16 KB) is the K-major A operand of the first product and, read through an
-// MN-major descriptor, the A operand of the second.
+//                                             K = 64 rows, 4 chunks)
+// Both accumulators live in tensor memory: S^T in two buffers of 64 columns
+// (an M = 64 accumulator fills lanes 0-15 of each 32-lane quarter), O^T in
+// 256 columns. One dequantised bf16 tile (64 rows x 512, 128-B swizzle, 8
+// d-blocks of 8 KB) is the K-major A operand of the first product and, read
+// through an MN-major descriptor, the A operand of the second.
 //
-// Warp roles (13 warps; at most 4 per SM sub-partition, so 128 registers):
-//   warps 0-3   softmax + epilogue. Thread i owns TMEM lane i: KV row i of the
-//               tile for S^T (all 64 heads), head-dim element i of a 128-d
-//               chunk for O^T.
-//   warps 4-11  producers: resolve the paged rows of a tile, load their fp8
-//               bytes and scales into registers one tile ahead, dequantise
-//               them chunk by chunk (a chunk = 128 rows x 128 d = 2 d-blocks)
-//               into the tile as soon as the previous tile's PV product has
-//               released that chunk.
-//   warp 12     tcgen05 issue (one thread): Q by TMA, QK^T per chunk as the
-//               chunks arrive, PV per chunk, commits that release chunks.
+// Pipeline. Two tile stages in shared memory: while the tensor cores and the
+// softmax work on tile n, the producers fill the other stage with tile n+1.
+// The issue thread runs QK^T(n) before PV(n-1), so the softmax of tile n
+// overlaps the PV product of tile n-1 and the dequantisation of tile n+1.
+//
+// Warp roles (15 warps; at most 4 per SM sub-partition, so 128 registers):
+//   warps 0-3   softmax + epilogue. Warp q owns tile rows 16q..16q+15; each
+//               thread holds two rows x 16 heads of S^T (the accumulator-
+//               fragment layout), keeps the row sums of its 16 heads in
+//               registers and writes its P values with stmatrix. In the
+//               epilogue thread i owns head-dim lane i of O^T.
+//   warps 4-11  producers: take a tile's physical rows from the resolver,
+//               load their fp8 bytes and scales into registers while the
+//               tile's stage drains, then dequantise them chunk by chunk (a
+//               chunk = 64 rows x 128 d = 2 d-blocks) into the stage.
+//   warp 12     QK^T issue (one thread): Q by TMA, QK^T chunk by chunk as the
+//               producers publish the chunks.
+//   warp 14     PV issue (one thread): PV once the softmax has written P, and
+//               the commits that release stages and hand O^T to the epilogue.
+//   warp 13     resolver: runs up to 4 tiles ahead, turns each tile's slots
+//               into physical rows (sparse indices, block tables) in a
+//               shared-memory ring, and asks L2 for those rows' bytes.
 // mbarriers carry every hand-off; every wait is bounded in time.
 //
 // Softmax: the running max m_used per head is moved only when a tile's max
 // exceeds it by more than 8 (log2 units); a named-barrier vote detects that
 // case, so most tiles need no cross-thread max reduction. When it moves, O^T
-// and the per-thread sums l are rescaled exactly. P <= 2^8 in bf16.
+// and the row sums l are rescaled exactly. P <= 2^8 in bf16.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -45,44 +57,59 @@
 namespace qsfm {
 namespace {
 
+static_assert(kTileRows == 64, "the kernel's layouts assume 64-row tiles");
+
 constexpr int kSoftWarps = 4;
 constexpr int kProdWarps = 8;
 constexpr int kMmaWarp = kSoftWarps + kProdWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kResolverWarp = kMmaWarp + 1;
+constexpr int kPvWarp = kResolverWarp + 1;
+constexpr int kThreads = (kPvWarp + 1) * 32;
+constexpr int kRing = 4;  // tiles of resolved rows in flight
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kBarSoft = 1;  // named barrier id of the softmax warps
+constexpr int kStages = 2;
 
 // shared memory map (byte offsets from a 1024-aligned base)
-constexpr uint32_t kSK = 0;                      // K~: 8 d-blocks x 128 rows x 128 B
-constexpr uint32_t kSQ = kSK + 8 * 128 * 128;    // Q: 8 d-blocks x 64 heads x 128 B
-constexpr uint32_t kSP = kSQ + 8 * 64 * 128;     // P^T: 128 rows x 64 heads (bf16)
-constexpr uint32_t kSRedMax = kSP + 128 * 128;   // [4][64] f32
-constexpr uint32_t kSRedSum = kSRedMax + 1024;   // [2][4][64] f32 (per tile, double-buffered)
-constexpr uint32_t kSLRun = kSRedSum + 2048;     // [64] f32 running sums
-constexpr uint32_t kSMUsed = kSLRun + 256;       // [64] f32
-constexpr uint32_t kSAlpha = kSMUsed + 256;      // [64] f32
-constexpr uint32_t kSInv = kSAlpha + 256;        // [64] f32
-constexpr uint32_t kSValid = kSInv + 256;        // [2][128] i32
-constexpr uint32_t kSBar = kSValid + 1024;       // mbarriers, tmem base, flags
+constexpr uint32_t kDBlockBytes = kTileRows * 128;           // 64 rows x 64 d (bf16)
+constexpr uint32_t kStageBytes = 8 * kDBlockBytes;           // one tile: 64 KB
+constexpr uint32_t kPBytes = kTileRows * 128;                // P: 64 rows x 64 heads (bf16)
+constexpr uint32_t kSK = 0;                                  // K~ stages
+constexpr uint32_t kSQ = kSK + kStages * kStageBytes;        // Q: 8 d-blocks x 64 heads x 128 B
+constexpr uint32_t kSP = kSQ + 8 * 64 * 128;                 // P stages (epilogue: O staging)
+constexpr uint32_t kSRed = kSP + kStages * kPBytes;          // [4][64] f32 per-warp partials
+constexpr uint32_t kSMUsed = kSRed + 1024;                   // [64] f32
+constexpr uint32_t kSAlpha = kSMUsed + 256;                  // [64] f32
+constexpr uint32_t kSInv = kSAlpha + 256;                    // [64] f32
+constexpr uint32_t kSValid = kSInv + 256;                    // [2][64] i32
+constexpr uint32_t kSRows = kSValid + 512;                   // [kRing][64] i32 physical rows
+constexpr uint32_t kSRowKind = kSRows + kRing * kTileRows * 4;  // [kRing] i32: 0 ori, 1 cmp, -1 end
+constexpr uint32_t kSBar = kSRowKind + 64;                   // mbarriers, tmem base, flags
 constexpr uint32_t kSmemBytes = kSBar + 256;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+static_assert(kStages * kPBytes >= 64 * 128 * 2, "O staging: 64 heads x 128 d bf16");
 
 // mbarrier slots
 constexpr int kBarQFull = 0;
-constexpr int kBarKvFull = 1;   // 4 chunks
-constexpr int kBarKvEmpty = 5;  // 4 chunks
-constexpr int kBarSFull = 9;
-constexpr int kBarPFull = 10;
-constexpr int kBarODone = 11;
-constexpr int kBarOFree = 12;
+constexpr int kBarKvFull = 1;    // [stage][chunk], one arrive per producer warp
+constexpr int kBarKvEmpty = 9;   // [stage]: the PV product of the stage's tile completed
+constexpr int kBarSFull = 11;    // [stage]
+constexpr int kBarSFree = 13;    // [stage]
+constexpr int kBarPFull = 15;    // [stage]
+constexpr int kBarODone = 17;
+constexpr int kBarOFree = 18;
+constexpr int kBarRowsFull = 19;   // [ring slot]
+constexpr int kBarRowsEmpty = 23;  // [ring slot], one arrive per producer warp
+constexpr int kNumBars = 27;
+static_assert(kNumBars * 8 <= 224, "barriers overlap the tmem slot");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemS = 0;  // + 64 * stage
 constexpr uint32_t kTmemO = 256;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kIdescQK = make_idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);
+constexpr uint32_t kIdescQK = make_idesc_bf16(64, 64, /*a_mn=*/0, /*b_mn=*/0);
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, 64, /*a_mn=*/1, /*b_mn=*/1);
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -132,23 +159,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Max (kMax) or sum over the 32 lanes of a warp of 32 values per lane.
-// Afterwards lane l holds the result for value index l.
+// Max (kMax) or sum of 16 values per lane over the 8 lanes of a warp that
+// share lane % 4 (lane bits 2-4). Afterwards lane l holds, in v[0] and v[1],
+// the results for value indices 2 * (l >> 2) and 2 * (l >> 2) + 1.
 template <bool kMax>
-__device__ __forceinline__ float warp_reduce32(float (&v)[32]) {
+__device__ __forceinline__ void reduce_rows16(float (&v)[16]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
+  for (int w = 16, n = 8; w >= 4; w >>= 1, n >>= 1) {
     const bool up = lane & w;
 #pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float keep = up ? v[w + i] : v[i];
-      const float send = up ? v[i] : v[w + i];
+    for (int i = 0; i < n; ++i) {
+      const float keep = up ? v[n + i] : v[i];
+      const float send = up ? v[i] : v[n + i];
       const float got = __shfl_xor_sync(0xffffffffu, send, w);
       v[i] = kMax ? fmaxf(keep, got) : keep + got;
     }
   }
-  return v[0];
 }
 
 struct Smem {
@@ -156,9 +183,9 @@ struct Smem {
   uint8_t* ptr;
   __device__ float* f(uint32_t off) const { return reinterpret_cast<float*>(ptr + off); }
   __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(ptr + kSBar) + i; }
-  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(ptr + kSBar + 128); }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(ptr + kSBar + 224); }
   __device__ volatile int* abort_flag() const {
-    return reinterpret_cast<volatile int*>(ptr + kSBar + 136);
+    return reinterpret_cast<volatile int*>(ptr + kSBar + 232);
   }
 };
 
@@ -182,151 +209,175 @@ __device__ __forceinline__ bool warp_wait_or_abort(const Smem& sm, int bar, uint
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// ------------------------------------------------------------- producers
-// One tile job: the physical row (block * 128 + offset, -1 = masked) of each
-// of this thread's 4 rows, and which pool the tile reads (a tile never mixes
-// ori and cmp rows).
-struct JobRows {
-  int prow[4];
-  int cmp;
-};
-
-__device__ __forceinline__ void resolve_job(const qsfm_params& p, int tok, int k, const TokenGeom& g,
-                                            int row_lo, int* fault, JobRows& jr) {
-  jr.cmp = k >= g.ori_tiles;
+// ------------------------------------------------------------- resolver
+// Tile n's rows go to ring slot n % kRing: 64 physical rows (block * 128 +
+// offset, -1 = masked) and the pool they come from. After the CTA's last tile
+// the resolver writes an end mark (-1) in the next slot.
+__device__ void resolver_role(const qsfm_params& p, const Smem& sm, Range rg, int T, int* fault) {
+  const int lane = threadIdx.x & 31;
+  int* rows = reinterpret_cast<int*>(sm.ptr + kSRows);
+  int* kind = reinterpret_cast<int*>(sm.ptr + kSRowKind);
+  JobIter jobs(&p, rg, T);
+  int tok, k, last_tok = -1;
+  TokenGeom g;
+  for (uint32_t n = 0;; ++n) {
+    const bool more = jobs.next(tok, k, g);
+    const uint32_t slot = n % kRing;
+    if (!warp_wait_or_abort(sm, kBarRowsEmpty + slot, ((n / kRing) & 1) ^ 1, fault)) return;
+    if (!more) {
+      if (lane == 0) kind[slot] = -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(kBarRowsFull + slot));
+      return;
+    }
+    if (tok != last_tok) {
+      // the next token's index list goes to L2 while this token is resolved
+      if (p.cmp_sparse_indices != nullptr && tok + 1 < T) {
+        const uint8_t* ix = reinterpret_cast<const uint8_t*>(p.cmp_sparse_indices + (size_t)(tok + 1) * p.k2);
+        for (int off = 128 * lane; off < 4 * p.k2; off += 32 * 128) prefetch_l2(ix + off);
+      }
+      last_tok = tok;
+    }
+    const int cmp = k >= g.ori_tiles ? 1 : 0;
+    int pr[2];
+    resolve_two(p, g, tok, k, lane, fault, pr);
+    const uint8_t* pool = static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv);
+    const float* spool = cmp ? p.cmp_scale : p.ori_scale;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const RowRef ref = resolve_slot(p, g, tok, k, row_lo + 32 * u, fault);
-    const uint8_t* pool = static_cast<const uint8_t*>(jr.cmp ? p.cmp_kv : p.ori_kv);
-    jr.prow[u] = ref.row >= 0 ? int((ref.kv - pool) / kDim) : -1;
+    for (int u = 0; u < 2; ++u) {
+      rows[slot * kTileRows + lane + 32 * u] = pr[u];
+      if (pr[u] >= 0) {
+        const uint8_t* src = pool + size_t(pr[u]) * kDim;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) prefetch_l2(src + 128 * c);
+        prefetch_l2(spool + size_t(pr[u]) * kScales);
+      }
+    }
+    if (lane == 0) kind[slot] = cmp;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(kBarRowsFull + slot));
   }
 }
 
-__device__ void producer_role(const qsfm_params& p, const Smem& sm, Range rg, int T, int* fault) {
+// ------------------------------------------------------------- producers
+// Thread (row_lo, j) of the 8 producer warps: tile rows row_lo and row_lo +
+// 32, 16-byte slot j of each 128-byte chunk of those rows.
+__device__ void producer_role(const qsfm_params& p, const Smem& sm, int* fault) {
   const int ptid = threadIdx.x - kSoftThreads;  // 0..255 (8 producer warps)
   const int lane = threadIdx.x & 31;
-  const int row_lo = ptid >> 3;   // this thread's rows: row_lo + 32u, u = 0..3
-  const int j = ptid & 7;         // its 16-byte slot inside each 128-byte chunk of a row
+  const int row_lo = ptid >> 3;   // 0..31
+  const int j = ptid & 7;
   const int odd_first = j >> 2;   // j >= 4 stores its odd 16-B chunk first (no bank conflicts)
-  JobIter jobs(&p, rg, T);
+  const int* rows = reinterpret_cast<const int*>(sm.ptr + kSRows);
+  const int* kind = reinterpret_cast<const int*>(sm.ptr + kSRowKind);
 
-  JobRows cur, nxt;
-  float csc[4];  // scale j of each row (this lane's share of the row's 8 scales)
-  uint4 R[4][4];  // fp8 bytes [chunk][row unit], loaded one tile ahead
+  int pr[2];
+  float csc[2];  // scale j of each row (this lane's share of the row's 8 scales)
+  uint4 R0[2], R1[2], R2[2], R3[2];  // fp8 bytes of chunks 0..3 of the two rows
 
-  auto load_job = [&](const JobRows& jr) {
-    const uint8_t* pool = static_cast<const uint8_t*>(jr.cmp ? p.cmp_kv : p.ori_kv);
-    const float* spool = jr.cmp ? p.cmp_scale : p.ori_scale;
+  // Rows of tile n from the ring; their loads start at once. False at the
+  // end mark or on abort.
+  auto fetch = [&](uint32_t n) -> bool {
+    const uint32_t slot = n % kRing;
+    if (!warp_wait_or_abort(sm, kBarRowsFull + slot, (n / kRing) & 1, fault)) return false;
+    const int kd = kind[slot];
+    pr[0] = rows[slot * kTileRows + row_lo];
+    pr[1] = rows[slot * kTileRows + row_lo + 32];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(kBarRowsEmpty + slot));
+    if (kd < 0) return false;
+    const uint8_t* pool = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv);
+    const float* spool = kd ? p.cmp_scale : p.ori_scale;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const bool v = jr.prow[u] >= 0;
-      const uint8_t* src = pool + size_t(v ? jr.prow[u] : 0) * kDim + 16 * j;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) R[c][u] = v ? ldg_stream_v4(src + 128 * c) : make_uint4(0, 0, 0, 0);
-      csc[u] = v ? __ldg(spool + size_t(jr.prow[u]) * kScales + j) : 0.f;
+    for (int u = 0; u < 2; ++u) {
+      const bool v = pr[u] >= 0;
+      const uint8_t* src = pool + size_t(v ? pr[u] : 0) * kDim + 16 * j;
+      R0[u] = v ? ldg_stream_v4(src) : make_uint4(0, 0, 0, 0);
+      R1[u] = v ? ldg_stream_v4(src + 128) : make_uint4(0, 0, 0, 0);
+      R2[u] = v ? ldg_stream_v4(src + 256) : make_uint4(0, 0, 0, 0);
+      R3[u] = v ? ldg_stream_v4(src + 384) : make_uint4(0, 0, 0, 0);
+      csc[u] = v ? __ldg(spool + size_t(pr[u]) * kScales + j) : 0.f;
     }
+    return true;
   };
 
-  int tok, k;
-  TokenGeom g;
-  bool have_cur = jobs.next(tok, k, g);
-  if (!have_cur) return;
-  resolve_job(p, tok, k, g, row_lo, fault, cur);
-  load_job(cur);
-  bool have_nxt = jobs.next(tok, k, g);
-  if (have_nxt) resolve_job(p, tok, k, g, row_lo, fault, nxt);
-
-  // The next tile's rows are loaded only after this tile's last chunk has
-  // been published: the proxy fence and the release of each chunk's arrive
-  // wait for the thread's outstanding loads, so loads issued earlier would
-  // serialise every chunk on a memory round trip. Issued here, they overlap
-  // the softmax and PV product of the current tile instead.
-  uint32_t ph = 1;  // kv_empty starts free
-  uint32_t tiles = 0;
-  while (have_cur) {
-    int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + (tiles & 1) * 128;
-#pragma unroll
+  // The next tile's loads are issued only after this tile's last chunk has
+  // been published: each chunk's release waits for the thread's outstanding
+  // loads, so loads issued earlier would serialise every chunk on a memory
+  // round trip. Issued there, they overlap the wait for the next stage.
+  for (uint32_t n = 0; fetch(n); ++n) {
+    const uint32_t st = n & 1;
+    if (!warp_wait_or_abort(sm, kBarKvEmpty + st, ((n >> 1) & 1) ^ 1, fault)) return;
+    const uint32_t stage = sm.base + kSK + st * kStageBytes;
+    if (j == 0) {
+      int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + st * kTileRows;
+      valid[row_lo] = pr[0] >= 0;
+      valid[row_lo + 32] = pr[1] >= 0;
+    }
+#pragma unroll 1
     for (int c = 0; c < 4; ++c) {
-      if (!warp_wait_or_abort(sm, kBarKvEmpty + c, ph, fault)) return;
-      if (c == 0 && j == 0) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) valid[row_lo + 32 * u] = cur.prow[u] >= 0;
-      }
       const int src_lane = (lane & ~7) | (2 * c + (j >> 2));
-      const uint32_t blk = sm.base + kSK + (2 * c + (j >> 2)) * 16384;
+      const uint32_t blk = stage + (2 * c + (j >> 2)) * kDBlockBytes;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 2; ++u) {
         const float sc = __shfl_sync(0xffffffffu, csc[u], src_lane);
         uint4 lo, hi;
-        dequant16(R[c][u], sc, lo, hi);
+        dequant16(R0[u], sc, lo, hi);
         const int r = row_lo + 32 * u;
         const uint32_t sw = uint32_t(r & 7);
         const uint32_t rowb = blk + r * 128;
         const uint32_t c0 = 2 * (j & 3);
         sts_v4(rowb + (((c0 + odd_first) ^ sw) << 4), odd_first ? hi : lo);
         sts_v4(rowb + (((c0 + 1 - odd_first) ^ sw) << 4), odd_first ? lo : hi);
+        R0[u] = R1[u];
+        R1[u] = R2[u];
+        R2[u] = R3[u];
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(kBarKvFull + c));
-    }
-    ph ^= 1;
-    ++tiles;
-    have_cur = have_nxt;
-    if (have_cur) {
-      cur = nxt;
-      load_job(cur);
-      have_nxt = jobs.next(tok, k, g);
-      if (have_nxt) resolve_job(p, tok, k, g, row_lo, fault, nxt);
+      if (lane == 0) mbar_arrive(sm.bar(kBarKvFull + 4 * st + c));
     }
   }
 }
 
 // ------------------------------------------------------------- MMA issue
-// k-step s of d-block db: A (K~) at +db*16 KB + s*32 B, B (Q) at +db*8 KB + s*32 B.
+// k-step s of d-block db: A (K~) at +db*8 KB + s*32 B, B (Q) at +db*8 KB + s*32 B.
 template <int kDb, int kS>
 __device__ __forceinline__ void qk_mma(uint32_t d, uint64_t a0, uint64_t b0) {
-  mma_bf16_at<uint32_t((kDb * 16384 + kS * 32) >> 4), uint32_t((kDb * 8192 + kS * 32) >> 4)>(
+  mma_bf16_at<uint32_t((kDb * 8192 + kS * 32) >> 4), uint32_t((kDb * 8192 + kS * 32) >> 4)>(
       d, a0, b0, kIdescQK, (kDb | kS) != 0);
 }
 
-// QK^T over chunk kC (d-blocks 2kC, 2kC+1) once the producers publish it.
+// PV for head-dim chunk kC: A (V~^T, MN-major) at +kC*16 KB + ks*2 KB,
+// B (P, MN-major) at +ks*2 KB.
 template <int kC>
-__device__ __forceinline__ bool qk_chunk(const Smem& sm, uint32_t tmem, uint64_t a0, uint64_t b0,
-                                         uint32_t par, int* fault) {
-  if (!wait_or_abort(sm, kBarKvFull + kC, par, fault)) return false;
-  tc_fence_after();
-  const uint32_t d = tmem + kTmemS;
+__device__ __forceinline__ void pv_chunk(uint32_t tmem, uint64_t a0, uint64_t b0, uint32_t acc0) {
+  const uint32_t d = tmem + kTmemO + kC * 64;
+  mma_bf16_at<uint32_t((kC * 16384 + 0 * 2048) >> 4), uint32_t((0 * 2048) >> 4)>(d, a0, b0, kIdescPV, acc0);
+  mma_bf16_at<uint32_t((kC * 16384 + 1 * 2048) >> 4), uint32_t((1 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_bf16_at<uint32_t((kC * 16384 + 2 * 2048) >> 4), uint32_t((2 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_bf16_at<uint32_t((kC * 16384 + 3 * 2048) >> 4), uint32_t((3 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+}
+
+template <int kC>
+__device__ __forceinline__ void qk_issue(uint32_t d, uint64_t a0, uint64_t b0) {
   qk_mma<2 * kC, 0>(d, a0, b0); qk_mma<2 * kC, 1>(d, a0, b0);
   qk_mma<2 * kC, 2>(d, a0, b0); qk_mma<2 * kC, 3>(d, a0, b0);
   qk_mma<2 * kC + 1, 0>(d, a0, b0); qk_mma<2 * kC + 1, 1>(d, a0, b0);
   qk_mma<2 * kC + 1, 2>(d, a0, b0); qk_mma<2 * kC + 1, 3>(d, a0, b0);
-  return true;
 }
 
-// PV for head-dim chunk kC: A (V~^T, MN-major) at +kC*32 KB + ks*2 KB,
-// B (P^T) at +ks*2 KB; then release the chunk to the producers.
-template <int kC>
-__device__ __forceinline__ void pv_chunk(const Smem& sm, uint32_t tmem, uint64_t a0, uint64_t b0,
-                                         uint32_t acc0) {
-  const uint32_t d = tmem + kTmemO + kC * 64;
-  mma_bf16_at<uint32_t((kC * 32768 + 0 * 2048) >> 4), uint32_t((0 * 2048) >> 4)>(d, a0, b0, kIdescPV, acc0);
-  mma_bf16_at<uint32_t((kC * 32768 + 1 * 2048) >> 4), uint32_t((1 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
-  mma_bf16_at<uint32_t((kC * 32768 + 2 * 2048) >> 4), uint32_t((2 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
-  mma_bf16_at<uint32_t((kC * 32768 + 3 * 2048) >> 4), uint32_t((3 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
-  mma_bf16_at<uint32_t((kC * 32768 + 4 * 2048) >> 4), uint32_t((4 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
-  mma_bf16_at<uint32_t((kC * 32768 + 5 * 2048) >> 4), uint32_t((5 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
-  mma_bf16_at<uint32_t((kC * 32768 + 6 * 2048) >> 4), uint32_t((6 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
-  mma_bf16_at<uint32_t((kC * 32768 + 7 * 2048) >> 4), uint32_t((7 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
-  mma_commit(sm.bar(kBarKvEmpty + kC));
-}
-
-__device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
-                         const CUtensorMap* qmap, int* fault) {
+// Tile n of the CTA's sequence uses stage n & 1 (K~, S^T, P buffers); each
+// barrier of a stage completes once per tile of that stage, so tile n waits
+// for phase parity (n >> 1) & 1. Two threads issue tensor-core work, each
+// blocking on its own inputs in program order: this one QK^T (and Q), the PV
+// thread the PV products. QK^T(n) cannot run more than two tiles ahead of
+// PV: its stage is refilled only after PV(n - 2) has completed.
+__device__ void qk_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
+                        const CUtensorMap* qmap, int* fault) {
   if ((threadIdx.x & 31) != 0) return;
   PieceIter pieces(&p, rg, T);
   TokenGeom g;
-  // the next piece that has tiles
   auto next_live = [&](int& t_, int& lo_, int& hi_) {
     while (pieces.next(t_, g, lo_, hi_))
       if (lo_ < hi_) return true;
@@ -342,46 +393,38 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
   bool have = next_live(tok, lo, hi);
   if (!have) return;
   load_q(tok);
-  uint32_t tiles = 0, pieces_done = 0, ph_q = 0;
+  uint32_t n = 0, piece = 0;
   while (have) {
     int ntok = 0, nlo = 0, nhi = 0;
     const bool have_next = next_live(ntok, nlo, nhi);
-    if (!wait_or_abort(sm, kBarQFull, ph_q, fault)) return;
-    ph_q ^= 1;
-    for (int k = lo; k < hi; ++k) {
-      const uint32_t par = tiles & 1;
-      // Fully unrolled: descriptors are the base plus compile-time offsets
-      // (32 B per k-step, 16 KB / 8 KB per d-block), so one thread issues an
-      // MMA as fast as the pipe takes it.
-      const uint64_t a0 = make_sdesc_sw128(sm.base + kSK, 16, 1024);
+    if (!wait_or_abort(sm, kBarQFull, piece & 1, fault)) return;
+    for (int k = lo; k < hi; ++k, ++n) {
+      const uint32_t st = n & 1, par = (n >> 1) & 1;
+      // S^T buffer st is free once the softmax has read tile n - 2's scores
+      if (!wait_or_abort(sm, kBarSFree + st, par ^ 1, fault)) return;
+      const uint32_t d = tmem + kTmemS + 64 * st;
+      const uint64_t a0 = make_sdesc_sw128(sm.base + kSK + st * kStageBytes, 16, 1024);
       const uint64_t b0 = make_sdesc_sw128(sm.base + kSQ, 16, 1024);
-      if (!qk_chunk<0>(sm, tmem, a0, b0, par, fault)) return;
-      if (!qk_chunk<1>(sm, tmem, a0, b0, par, fault)) return;
-      if (!qk_chunk<2>(sm, tmem, a0, b0, par, fault)) return;
-      if (!qk_chunk<3>(sm, tmem, a0, b0, par, fault)) return;
-      mma_commit(sm.bar(kBarSFull));
+      if (!wait_or_abort(sm, kBarKvFull + 4 * st + 0, par, fault)) return;
+      tc_fence_after();
+      qk_issue<0>(d, a0, b0);
+      if (!wait_or_abort(sm, kBarKvFull + 4 * st + 1, par, fault)) return;
+      tc_fence_after();
+      qk_issue<1>(d, a0, b0);
+      if (!wait_or_abort(sm, kBarKvFull + 4 * st + 2, par, fault)) return;
+      tc_fence_after();
+      qk_issue<2>(d, a0, b0);
+      if (!wait_or_abort(sm, kBarKvFull + 4 * st + 3, par, fault)) return;
+      tc_fence_after();
+      qk_issue<3>(d, a0, b0);
+      mma_commit(sm.bar(kBarSFull + st));
       if (k == hi - 1 && have_next) {
-        // Q of the next token as soon as this token's last QK^T has read Q
-        if (!wait_or_abort(sm, kBarSFull, par, fault)) return;
+        // Q of the next token once this token's last QK^T has read Q
+        if (!wait_or_abort(sm, kBarSFull + st, par, fault)) return;
         load_q(ntok);
       }
-      if (!wait_or_abort(sm, kBarPFull, par, fault)) return;
-      if (k == lo && pieces_done > 0) {
-        // the previous token's epilogue must have read O^T before it is overwritten
-        if (!wait_or_abort(sm, kBarOFree, (pieces_done - 1) & 1, fault)) return;
-      }
-      tc_fence_after();
-      const uint64_t pa0 = make_sdesc_sw128(sm.base + kSK, 16384, 1024);
-      const uint64_t pb0 = make_sdesc_sw128(sm.base + kSP, 16, 1024);
-      const uint32_t acc0 = k == lo ? 0u : 1u;
-      pv_chunk<0>(sm, tmem, pa0, pb0, acc0);
-      pv_chunk<1>(sm, tmem, pa0, pb0, acc0);
-      pv_chunk<2>(sm, tmem, pa0, pb0, acc0);
-      pv_chunk<3>(sm, tmem, pa0, pb0, acc0);
-      if (k == hi - 1) mma_commit(sm.bar(kBarODone));
-      ++tiles;
     }
-    ++pieces_done;
+    ++piece;
     have = have_next;
     tok = ntok;
     lo = nlo;
@@ -389,30 +432,57 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
   }
 }
 
-// ------------------------------------------------------ softmax + epilogue
-// Thread i owns row i of the tile: its 64 scores are handled as two halves
-// of 32 heads, read from TMEM again for each pass to keep registers low.
-__device__ __forceinline__ void load_scores(uint32_t taddr, bool rv, float scale, float (&x)[32]) {
-  tmem_ld32(taddr, x);
-  tmem_ld_wait();
-#pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = rv ? x[i] * scale : -INFINITY;
+__device__ void pv_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
+                        int* fault) {
+  if ((threadIdx.x & 31) != 0) return;
+  PieceIter pieces(&p, rg, T);
+  TokenGeom g;
+  int tok, lo, hi;
+  uint32_t n = 0, piece = 0;
+  while (pieces.next(tok, g, lo, hi)) {
+    if (lo >= hi) continue;
+    for (int k = lo; k < hi; ++k, ++n) {
+      const uint32_t st = n & 1;
+      if (!wait_or_abort(sm, kBarPFull + st, (n >> 1) & 1, fault)) return;
+      if (k == lo && piece > 0) {
+        // the previous piece's epilogue must have read O^T before it is overwritten
+        if (!wait_or_abort(sm, kBarOFree, (piece - 1) & 1, fault)) return;
+      }
+      tc_fence_after();
+      const uint64_t a0 = make_sdesc_sw128(sm.base + kSK + st * kStageBytes, kDBlockBytes, 1024);
+      const uint64_t b0 = make_sdesc_sw128(sm.base + kSP + st * kPBytes, 16, 1024);
+      const uint32_t acc0 = k == lo ? 0u : 1u;
+      pv_chunk<0>(tmem, a0, b0, acc0);
+      pv_chunk<1>(tmem, a0, b0, acc0);
+      pv_chunk<2>(tmem, a0, b0, acc0);
+      pv_chunk<3>(tmem, a0, b0, acc0);
+      mma_commit(sm.bar(kBarKvEmpty + st));  // stage (K~ and P) released
+      if (k == hi - 1) mma_commit(sm.bar(kBarODone));
+    }
+    ++piece;
+  }
 }
 
+// ------------------------------------------------------ softmax + epilogue
+// Warp q reads the 16 tensor-memory lanes 32q..32q+15 of an S^T buffer, i.e.
+// tile rows 16q..16q+15. In the accumulator-fragment layout thread l holds
+// rows ra = 16q + l/4 and ra + 8, heads 8j + 2(l%4) + e (j = 0..7, e = 0, 1):
+//   x[4j + 2r + e] = S^T[ra + 8r, 8j + 2(l%4) + e].
+// Its 16 heads are indexed i = 2j + e in l[].
 __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
                              const Workspace& ws, int c_idx, int* fault) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = tid;  // KV row of the tile / head-dim element inside a 128-d chunk
+  const int row = tid;  // epilogue: head-dim element inside a 128-d chunk
+  const int ra = 16 * warp + (lane >> 2);
+  const int hq = 2 * (lane & 3);
   const uint32_t lane_base = uint32_t(32 * warp) << 16;
   const float qk_scale = p.softmax_scale * kLog2e;
   float* m_used = sm.f(kSMUsed);
   float* alpha = sm.f(kSAlpha);
   float* inv = sm.f(kSInv);
-  float* lrun = sm.f(kSLRun);
-  float* red_max = sm.f(kSRedMax);
-  float* red_sum = sm.f(kSRedSum);
+  float* red = sm.f(kSRed);
   PieceIter pieces(&p, rg, T);
-  uint32_t tiles = 0, pieces_live = 0;
+  uint32_t n = 0, pieces_live = 0;
   int t, lo, hi;
   TokenGeom g;
   while (pieces.next(t, g, lo, hi)) {
@@ -420,46 +490,56 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
     const int slot = (t == rg.t0) ? 2 * c_idx : 2 * c_idx + 1;
     const bool writable = whole || slot < ws.slots;  // split pieces need the workspace
     if (!writable && tid == 0) atomicOr(fault, QSFM_FAULT_METADATA);
-    if (tid < 64) {
-      m_used[tid] = -INFINITY;
-      lrun[tid] = 0.f;
-    }
+    float l[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) l[i] = 0.f;
+    if (tid < 64) m_used[tid] = -INFINITY;
     named_sync(kBarSoft, kSoftThreads);
-    bool pend = false;  // red_sum of the previous tile not yet added to lrun
-    for (int k = lo; k < hi; ++k) {
-      const uint32_t par = tiles & 1;
+    for (int k = lo; k < hi; ++k, ++n) {
+      const uint32_t st = n & 1, par = (n >> 1) & 1;
       // Lane 0 of each warp polls. After an abort the waits fall through at
       // once; the softmax warps keep running the same named-barrier sequence
       // so that none of them blocks.
-      warp_wait_or_abort(sm, kBarKvFull, par, fault);
-      const bool rv = reinterpret_cast<int*>(sm.ptr + kSValid)[par * 128 + row] != 0;
-      warp_wait_or_abort(sm, kBarSFull, par, fault);
+      warp_wait_or_abort(sm, kBarKvFull + 4 * st, par, fault);
+      const int* valid = reinterpret_cast<const int*>(sm.ptr + kSValid) + st * kTileRows;
+      const bool va = valid[ra] != 0, vb = valid[ra + 8] != 0;
+      warp_wait_or_abort(sm, kBarSFull + st, par, fault);
       tc_fence_after();
-      bool exceed = false;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        float x[32];
-        load_scores(tmem + kTmemS + lane_base + 32 * half, rv, qk_scale, x);
+      float x[32];
+      tmem_ld16x256b_x8(tmem + kTmemS + 64 * st + lane_base, x);
+      tmem_ld_wait();
+      // the scores are in registers: the buffer can take tile n + 2
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(kBarSFree + st));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) exceed |= x[i] > m_used[32 * half + i] + kRescaleLog2;
+      for (int jj = 0; jj < 8; ++jj) {
+        x[4 * jj + 0] = va ? x[4 * jj + 0] * qk_scale : -INFINITY;
+        x[4 * jj + 1] = va ? x[4 * jj + 1] * qk_scale : -INFINITY;
+        x[4 * jj + 2] = vb ? x[4 * jj + 2] * qk_scale : -INFINITY;
+        x[4 * jj + 3] = vb ? x[4 * jj + 3] * qk_scale : -INFINITY;
       }
-      const bool move = named_sync_or(kBarSoft, kSoftThreads, exceed);  // also true against -inf
-      if (pend && tid < 64) {
-        const float* rs = red_sum + (par ^ 1) * 256;
-        lrun[tid] += (rs[tid] + rs[64 + tid]) + (rs[128 + tid] + rs[192 + tid]);
+      bool move = true;  // the first tile of a piece always sets the max
+      if (k != lo) {
+        bool exceed = false;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          exceed |= fmaxf(x[4 * (i >> 1) + (i & 1)], x[4 * (i >> 1) + 2 + (i & 1)]) >
+                    m_used[8 * (i >> 1) + hq + (i & 1)] + kRescaleLog2;
+        move = named_sync_or(kBarSoft, kSoftThreads, exceed);  // also true against -inf
       }
       if (move) {
-        // move the running max: tile max per head over the 128 rows
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float x[32];
-          load_scores(tmem + kTmemS + lane_base + 32 * half, rv, qk_scale, x);
-          red_max[warp * 64 + 32 * half + lane] = warp_reduce32<true>(x);
-        }
+        // move the running max: tile max per head over the 64 rows
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          v[i] = fmaxf(x[4 * (i >> 1) + (i & 1)], x[4 * (i >> 1) + 2 + (i & 1)]);
+        reduce_rows16<true>(v);  // lane l: heads 2l, 2l + 1
+        red[warp * 64 + 2 * lane] = v[0];
+        red[warp * 64 + 2 * lane + 1] = v[1];
         named_sync(kBarSoft, kSoftThreads);
         if (tid < 64) {
-          const float mt = fmaxf(fmaxf(red_max[tid], red_max[64 + tid]),
-                                 fmaxf(red_max[128 + tid], red_max[192 + tid]));
+          const float mt = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
           const float mu = m_used[tid];
           float a = 1.f;
           if (mt > -INFINITY && (mu == -INFINITY || mt > mu + kRescaleLog2)) {
@@ -467,70 +547,64 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
             m_used[tid] = mt;
           }
           alpha[tid] = a;
-          lrun[tid] *= a;
         }
         named_sync(kBarSoft, kSoftThreads);
-        if (k != lo) {
-          // O^T at this thread's head-dim lane, all heads (the previous PV
-          // product has completed: this tile's QK^T waited for it)
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              float o[32];
-              const uint32_t addr = tmem + kTmemO + 64 * c + 32 * half + lane_base;
-              tmem_ld32(addr, o);
-              tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= alpha[32 * half + i];
-              tmem_st16(addr, o);
-              tmem_st16(addr + 16, o + 16);
-            }
+        for (int i = 0; i < 16; ++i) l[i] *= alpha[8 * (i >> 1) + hq + (i & 1)];
+        if (k != lo) {
+          // O^T at this thread's head-dim lane, all heads, once the PV product
+          // of tile n - 1 has completed
+          warp_wait_or_abort(sm, kBarKvEmpty + ((n - 1) & 1), ((n - 1) >> 1) & 1, fault);
+          tc_fence_after();
+#pragma unroll 1
+          for (int q16 = 0; q16 < 16; ++q16) {
+            float o[16];
+            const uint32_t addr = tmem + kTmemO + 16 * q16 + lane_base;
+            tmem_ld16(addr, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= alpha[16 * (q16 & 3) + i];
+            tmem_st16(addr, o);
           }
           tmem_st_wait();
         }
       }
-      // P = exp2(x - m_used) -> the P^T row line (64 heads, 128 B, swizzled),
-      // and the per-head sums of this warp's 32 rows
-      const uint32_t prow = sm.base + kSP + row * 128;
-      const uint32_t sw = uint32_t(row & 7);
-      float* rs = red_sum + par * 256 + warp * 64;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        float x[32];
-        load_scores(tmem + kTmemS + lane_base + 32 * half, rv, qk_scale, x);
+      // P = 2^(x - m_used), row sums, and P into its stage as [64 rows][64
+      // heads] bf16 with the 128-B swizzle (the MN-major B operand of PV)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float mu = m_used[32 * half + i];
-          x[i] = exp2f(x[i] - (mu == -INFINITY ? 0.f : mu));
-        }
+      for (int i = 0; i < 16; ++i) {
+        const float mi_ = m_used[8 * (i >> 1) + hq + (i & 1)];
+        const float mz = mi_ == -INFINITY ? 0.f : mi_;
+        const int ia = 4 * (i >> 1) + (i & 1);
+        x[ia] = ex2_approx(x[ia] - mz);
+        x[ia + 2] = ex2_approx(x[ia + 2] - mz);
+        l[i] += x[ia] + x[ia + 2];
+      }
+      const uint32_t pbase = sm.base + kSP + st * kPBytes;
+      const int mi = lane >> 3, jr = lane & 7;
+      const uint32_t prow = pbase + uint32_t(16 * warp + 8 * (mi & 1) + jr) * 128;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint4 v;
-          v.x = pack_bf16(x[8 * cc + 0], x[8 * cc + 1]);
-          v.y = pack_bf16(x[8 * cc + 2], x[8 * cc + 3]);
-          v.z = pack_bf16(x[8 * cc + 4], x[8 * cc + 5]);
-          v.w = pack_bf16(x[8 * cc + 6], x[8 * cc + 7]);
-          sts_v4(prow + ((uint32_t(4 * half + cc) ^ sw) << 4), v);
-        }
-        rs[32 * half + lane] = warp_reduce32<false>(x);
+      for (int gq = 0; gq < 4; ++gq) {
+        const uint32_t hg = uint32_t(2 * gq + (mi >> 1));
+        stmatrix_x4(prow + ((hg ^ uint32_t(jr)) << 4),
+                    pack_bf16(x[8 * gq + 0], x[8 * gq + 1]), pack_bf16(x[8 * gq + 2], x[8 * gq + 3]),
+                    pack_bf16(x[8 * gq + 4], x[8 * gq + 5]), pack_bf16(x[8 * gq + 6], x[8 * gq + 7]));
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(kBarPFull));
-      pend = true;
-      ++tiles;
+      if (lane == 0) mbar_arrive(sm.bar(kBarPFull + st));
     }
     // ---------------- epilogue of the piece
     const bool any = lo < hi;
+    if (any) {
+      reduce_rows16<false>(l);  // lane l: heads 2l, 2l + 1 of this warp's rows
+      red[warp * 64 + 2 * lane] = l[0];
+      red[warp * 64 + 2 * lane + 1] = l[1];
+    }
     named_sync(kBarSoft, kSoftThreads);
     if (tid < 64 && writable) {
-      float lt = lrun[tid];
-      if (pend) {
-        const float* rs = red_sum + ((tiles - 1) & 1) * 256;
-        lt += (rs[tid] + rs[64 + tid]) + (rs[128 + tid] + rs[192 + tid]);
-      }
+      const float lt = any ? (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]) : 0.f;
       const float mu = m_used[tid];
       const float lse2 = lt > 0.f ? mu + log2f(lt) : -INFINITY;
       if (whole) {
@@ -549,7 +623,7 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
       tc_fence_after();
     }
     // O^T chunk by chunk: lane = head-dim element, columns = heads. Whole
-    // tokens go through the (now idle) P buffer as bf16 [64 heads][128 d] so
+    // tokens go through the (now idle) P stages as bf16 [64 heads][128 d] so
     // that every head's 256-byte run is written with 16-byte stores; split
     // pieces write fp32 partial rows straight to the workspace.
     uint8_t* stage = sm.ptr + kSP;
@@ -594,7 +668,7 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
       if (lane == 0) mbar_arrive(sm.bar(kBarOFree));
       ++pieces_live;
     }
-    named_sync(kBarSoft, kSoftThreads);  // m_used / lrun / inv are reused by the next piece
+    named_sync(kBarSoft, kSoftThreads);  // m_used / inv / red are reused by the next piece
     if (*sm.abort_flag()) break;         // uniform: read after the barrier
   }
 }
@@ -632,14 +706,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(sm.bar(kBarQFull), 1);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(sm.bar(kBarKvFull + i), kProdWarps);
+    for (int i = 0; i < 4 * kStages; ++i) mbar_init(sm.bar(kBarKvFull + i), kProdWarps);
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(sm.bar(kBarKvEmpty + i), 1);
+      mbar_init(sm.bar(kBarSFull + i), 1);
+      mbar_init(sm.bar(kBarSFree + i), kSoftWarps);
+      mbar_init(sm.bar(kBarPFull + i), kSoftWarps);
     }
-    mbar_init(sm.bar(kBarSFull), 1);
-    mbar_init(sm.bar(kBarPFull), kSoftWarps);
     mbar_init(sm.bar(kBarODone), 1);
     mbar_init(sm.bar(kBarOFree), kSoftWarps);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(sm.bar(kBarRowsFull + i), 1);
+      mbar_init(sm.bar(kBarRowsEmpty + i), kProdWarps);
+    }
     *sm.abort_flag() = 0;
     fence_mbar_init();
   }
@@ -652,9 +731,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kSoftWarps) {
     softmax_role(p, sm, rg, T, tmem, ws, c, fault);
   } else if (warp < kMmaWarp) {
-    producer_role(p, sm, rg, T, fault);
+    producer_role(p, sm, fault);
+  } else if (warp == kMmaWarp) {
+    qk_role(p, sm, rg, T, tmem, &qmap, fault);
+  } else if (warp == kPvWarp) {
+    pv_role(p, sm, rg, T, tmem, fault);
   } else {
-    mma_role(p, sm, rg, T, tmem, &qmap, fault);
+    resolver_role(p, sm, rg, T, fault);
   }
 
   tc_fence_before();

@@ -24,7 +24,7 @@ constexpr int kHeads = QSFM_NUM_HEADS;        // N1
 constexpr int kDim = QSFM_HEAD_DIM;           // D
 constexpr int kBlock = QSFM_BLOCK_SIZE;       // tokens per KV block
 constexpr int kScales = QSFM_SCALES_PER_ROW;  // fp32 scales per row
-constexpr int kTileRows = 128;                // KV rows per attention tile
+constexpr int kTileRows = 64;                 // KV rows per attention tile
 constexpr int kMetaMagic = 0x51534D31;        // "QSM1"
 constexpr int kMetaHeader = 8;
 // metadata layout (int32[1024]):
@@ -41,8 +41,8 @@ struct TokenGeom {
   int n_ori;      // ori rows attended (contiguous from ori_lo)
   int n_cmp;      // cmp slots: CSA index entries scanned, HCA visible rows
   int cmp_vis;    // visible compressed rows V (CSA entries must be < V)
-  int ori_tiles;  // ceil(n_ori / 128)
-  int n_tiles;    // ori tiles + ceil(n_cmp / 128)
+  int ori_tiles;  // ceil(n_ori / kTileRows)
+  int n_tiles;    // ori tiles + ceil(n_cmp / kTileRows)
 };
 
 __device__ __forceinline__ int div_floor(int a, int b) {  // b > 0
@@ -166,6 +166,52 @@ static __device__ __noinline__ RowRef resolve_slot(const qsfm_params& p, const T
   return r;
 }
 
+// Physical rows (block * kBlock + offset; -1 when masked) of slots i0 and
+// i0 + 32 of tile k of token t, by the rules of resolve_slot, with the index
+// loads of both slots in flight together and then their block-table loads.
+__device__ __forceinline__ void resolve_two(const qsfm_params& p, const TokenGeom& g, int t, int k,
+                                            int i0, int* fault, int (&prow)[2]) {
+  const bool ori = k < g.ori_tiles;
+  const int base = (ori ? k : k - g.ori_tiles) * kTileRows + i0;
+  const int n = ori ? g.n_ori : g.n_cmp;
+  int row[2];
+  bool ok[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int slot = base + 32 * u;
+    ok[u] = slot < n;
+    row[u] = ori ? g.ori_lo + slot : slot;
+  }
+  if (!ori && p.cmp_sparse_indices != nullptr) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (ok[u]) row[u] = __ldg(p.cmp_sparse_indices + (size_t)t * p.k2 + base + 32 * u);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) ok[u] = ok[u] && row[u] >= 0 && row[u] < g.cmp_vis;
+  }
+  const int32_t* table = ori ? p.ori_block_table : p.cmp_block_table;
+  const int width = ori ? p.ori_max_blocks : p.cmp_max_blocks;
+  const int nblocks = ori ? p.ori_num_blocks : p.cmp_num_blocks;
+  int blk[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int col = row[u] / kBlock;
+    if (ok[u] && col >= width) {
+      atomicOr(fault, ori ? QSFM_FAULT_ORI_TABLE_COL : QSFM_FAULT_CMP_TABLE_COL);
+      ok[u] = false;
+    }
+    blk[u] = ok[u] ? __ldg(table + (size_t)g.b * width + col) : 0;
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    if (ok[u] && (blk[u] < 0 || blk[u] >= nblocks)) {
+      atomicOr(fault, ori ? QSFM_FAULT_ORI_BLOCK_ID : QSFM_FAULT_CMP_BLOCK_ID);
+      ok[u] = false;
+    }
+    prow[u] = ok[u] ? blk[u] * kBlock + row[u] % kBlock : -1;
+  }
+}
+
 // ------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
@@ -217,17 +263,35 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of a barrier phase (for a thread that polls several).
+__device__ __forceinline__ bool mbar_ready(uint32_t addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Hint: bring the 128-byte line holding `ptr` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // Wait for a barrier phase, bounded in time: gives up (returns false) after
-// `timeout_ns` or as soon as *abort becomes non-zero. After a few quick
-// polls it backs off with short sleeps, so that waiting threads do not crowd
-// the shared-memory pipe the working warps need.
+// `timeout_ns` or as soon as *abort becomes non-zero. try_wait suspends the
+// thread in hardware until the phase completes or a short time limit passes,
+// so the loop polls rarely; only long waits back off further with sleeps.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, uint64_t timeout_ns) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_test(addr, parity)) return true;
   const uint64_t start = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (it > 8) __nanosleep(it < 64 ? 32 : 128);
+    if (it > 256) __nanosleep(64);
     if (mbar_test(addr, parity)) return true;
     if ((it & 15u) == 0) {
       if (*abort) return false;
@@ -399,6 +463,46 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 lanes x 256 bit, 8 repetitions along the columns (64 columns). Thread t
+// of the warp receives, for repetition j, the accumulator-fragment quad
+//   v[4j+0] = (lane t/4,     column 8j + 2(t%4)),  v[4j+1] = its column + 1,
+//   v[4j+2] = (lane t/4 + 8, column 8j + 2(t%4)),  v[4j+3] = its column + 1,
+// lanes counted from the warp's base lane in `taddr`.
+__device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Four 8x8 b16 matrices to shared memory; thread t gives the address of row
+// t%8 of matrix t/8 and, in register i, the pair (row t/4, columns 2(t%4),
+// 2(t%4)+1) of matrix i.
+__device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                            uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(saddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; subnormal
+// results flush to zero, 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
