@@ -631,33 +631,52 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
     for (int c = 0; c < 4; ++c) {
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
+        const int h0 = 32 * half;
         float o[32];
         if (any) {
           tmem_ld32(tmem + kTmemO + 64 * c + 32 * half + lane_base, o);
           tmem_ld_wait();
-        }
-        const int h0 = 32 * half;
-        if (whole) {
+          // 1 / denominator per head, read into registers before any store
+          // (the stores below could alias inv[] as far as the compiler knows)
+          float iv[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            reinterpret_cast<__nv_bfloat16*>(stage)[(h0 + i) * 128 + row] =
-                __float2bfloat16_rn(any ? o[i] * inv[h0 + i] : 0.f);
+          for (int i = 0; i < 32; i += 4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(inv + h0 + i);
+            iv[i] = v4.x;
+            iv[i + 1] = v4.y;
+            iv[i + 2] = v4.z;
+            iv[i + 3] = v4.w;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= iv[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        }
+        if (whole) {
+          __nv_bfloat16* st16 = reinterpret_cast<__nv_bfloat16*>(stage) + h0 * 128 + row;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) st16[i * 128] = __float2bfloat16_rn(o[i]);
         } else if (writable) {
           float* out = ws.out + (size_t(slot) * 64 + h0) * kDim + 128 * c + row;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) out[size_t(i) * kDim] = any ? o[i] * inv[h0 + i] : 0.f;
+          for (int i = 0; i < 32; ++i) out[size_t(i) * kDim] = o[i];
         }
       }
       if (whole) {
         named_sync(kBarSoft, kSoftThreads);
         // 64 heads x 256 B = 1024 16-byte pieces, 8 per thread
         uint8_t* gout = static_cast<uint8_t*>(p.attn_out) + size_t(t) * 64 * kDim * 2 + 256 * c;
+        uint4 v[8];  // all loads before the stores: they could alias as far as the compiler knows
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
           const int piece = it * kSoftThreads + tid;
-          const int h = piece >> 4, part = piece & 15;
-          const uint4 v = *reinterpret_cast<const uint4*>(stage + h * 256 + part * 16);
-          *reinterpret_cast<uint4*>(gout + size_t(h) * kDim * 2 + part * 16) = v;
+          v[it] = *reinterpret_cast<const uint4*>(stage + (piece >> 4) * 256 + (piece & 15) * 16);
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int piece = it * kSoftThreads + tid;
+          *reinterpret_cast<uint4*>(gout + size_t(piece >> 4) * kDim * 2 + (piece & 15) * 16) = v[it];
         }
         named_sync(kBarSoft, kSoftThreads);
       }
