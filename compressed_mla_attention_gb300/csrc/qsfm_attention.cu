@@ -76,7 +76,7 @@ constexpr uint32_t kStageBytes = 8 * kDBlockBytes;           // one tile: 64 KB
 constexpr uint32_t kPBytes = kTileRows * 128;                // P: 64 rows x 64 heads (bf16)
 constexpr uint32_t kSK = 0;                                  // K~ stages
 constexpr uint32_t kSQ = kSK + kStages * kStageBytes;        // Q: 8 d-blocks x 64 heads x 128 B
-constexpr uint32_t kSP = kSQ + 8 * 64 * 128;                 // P stages (epilogue: O staging)
+constexpr uint32_t kSP = kSQ + 8 * 64 * 128;                 // P stages
 constexpr uint32_t kSRed = kSP + kStages * kPBytes;          // [4][64] f32 per-warp partials
 constexpr uint32_t kSMUsed = kSRed + 1024;                   // [64] f32
 constexpr uint32_t kSAlpha = kSMUsed + 256;                  // [64] f32
@@ -87,7 +87,6 @@ constexpr uint32_t kSRowKind = kSRows + kRing * kTileRows * 4;  // [kRing] i32: 
 constexpr uint32_t kSBar = kSRowKind + 64;                   // mbarriers, tmem base, flags
 constexpr uint32_t kSmemBytes = kSBar + 256;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
-static_assert(kStages * kPBytes >= 64 * 128 * 2, "O staging: 64 heads x 128 d bf16");
 
 // mbarrier slots
 constexpr int kBarQFull = 0;
@@ -622,11 +621,10 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
       warp_wait_or_abort(sm, kBarODone, pieces_live & 1, fault);
       tc_fence_after();
     }
-    // O^T chunk by chunk: lane = head-dim element, columns = heads. Whole
-    // tokens go through the (now idle) P stages as bf16 [64 heads][128 d] so
-    // that every head's 256-byte run is written with 16-byte stores; split
-    // pieces write fp32 partial rows straight to the workspace.
-    uint8_t* stage = sm.ptr + kSP;
+    // O^T chunk by chunk: lane = head-dim element, columns = heads. For each
+    // head the 32 lanes of a warp write 32 consecutive outputs (64 bytes of
+    // bf16, 128 bytes of fp32 for split pieces), so the stores coalesce
+    // without staging.
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
 #pragma unroll 1
@@ -654,31 +652,15 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
         }
         if (whole) {
-          __nv_bfloat16* st16 = reinterpret_cast<__nv_bfloat16*>(stage) + h0 * 128 + row;
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.attn_out) +
+                               (size_t(t) * 64 + h0) * kDim + 128 * c + row;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) st16[i * 128] = __float2bfloat16_rn(o[i]);
+          for (int i = 0; i < 32; ++i) out[size_t(i) * kDim] = __float2bfloat16_rn(o[i]);
         } else if (writable) {
           float* out = ws.out + (size_t(slot) * 64 + h0) * kDim + 128 * c + row;
 #pragma unroll
           for (int i = 0; i < 32; ++i) out[size_t(i) * kDim] = o[i];
         }
-      }
-      if (whole) {
-        named_sync(kBarSoft, kSoftThreads);
-        // 64 heads x 256 B = 1024 16-byte pieces, 8 per thread
-        uint8_t* gout = static_cast<uint8_t*>(p.attn_out) + size_t(t) * 64 * kDim * 2 + 256 * c;
-        uint4 v[8];  // all loads before the stores: they could alias as far as the compiler knows
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int piece = it * kSoftThreads + tid;
-          v[it] = *reinterpret_cast<const uint4*>(stage + (piece >> 4) * 256 + (piece & 15) * 16);
-        }
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int piece = it * kSoftThreads + tid;
-          *reinterpret_cast<uint4*>(gout + size_t(piece >> 4) * kDim * 2 + (piece & 15) * 16) = v[it];
-        }
-        named_sync(kBarSoft, kSoftThreads);
       }
     }
     if (any) {
