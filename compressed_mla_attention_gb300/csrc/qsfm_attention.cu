@@ -306,6 +306,19 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, int* fault) 
   // round trip. Issued there, they overlap the wait for the next stage.
   for (uint32_t n = 0; fetch(n); ++n) {
     const uint32_t st = n & 1;
+    // Dequantise the whole tile into registers first: this waits for the
+    // loads and runs while the stage is still in use by tile n - 2.
+    uint4 D[4][2][2];  // [chunk][row][16-byte half], bf16
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int src_lane = (lane & ~7) | (2 * c + (j >> 2));
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float sc = __shfl_sync(0xffffffffu, csc[u], src_lane);
+        const uint4 raw = c == 0 ? R0[u] : c == 1 ? R1[u] : c == 2 ? R2[u] : R3[u];
+        dequant16(raw, sc, D[c][u][0], D[c][u][1]);
+      }
+    }
     if (!warp_wait_or_abort(sm, kBarKvEmpty + st, ((n >> 1) & 1) ^ 1, fault)) return;
     const uint32_t stage = sm.base + kSK + st * kStageBytes;
     if (j == 0) {
@@ -313,24 +326,17 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, int* fault) 
       valid[row_lo] = pr[0] >= 0;
       valid[row_lo + 32] = pr[1] >= 0;
     }
-#pragma unroll 1
+#pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int src_lane = (lane & ~7) | (2 * c + (j >> 2));
       const uint32_t blk = stage + (2 * c + (j >> 2)) * kDBlockBytes;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const float sc = __shfl_sync(0xffffffffu, csc[u], src_lane);
-        uint4 lo, hi;
-        dequant16(R0[u], sc, lo, hi);
         const int r = row_lo + 32 * u;
         const uint32_t sw = uint32_t(r & 7);
         const uint32_t rowb = blk + r * 128;
         const uint32_t c0 = 2 * (j & 3);
-        sts_v4(rowb + (((c0 + odd_first) ^ sw) << 4), odd_first ? hi : lo);
-        sts_v4(rowb + (((c0 + 1 - odd_first) ^ sw) << 4), odd_first ? lo : hi);
-        R0[u] = R1[u];
-        R1[u] = R2[u];
-        R2[u] = R3[u];
+        sts_v4(rowb + (((c0 + odd_first) ^ sw) << 4), odd_first ? D[c][u][1] : D[c][u][0]);
+        sts_v4(rowb + (((c0 + 1 - odd_first) ^ sw) << 4), odd_first ? D[c][u][0] : D[c][u][1]);
       }
       fence_proxy_async_smem();
       __syncwarp();
