@@ -495,9 +495,12 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
     const int slot = (t == rg.t0) ? 2 * c_idx : 2 * c_idx + 1;
     const bool writable = whole || slot < ws.slots;  // split pieces need the workspace
     if (!writable && tid == 0) atomicOr(fault, QSFM_FAULT_METADATA);
-    float l[16];
+    float l[16], m[16];  // row sums and running max (log2 units) of this thread's 16 heads
 #pragma unroll
-    for (int i = 0; i < 16; ++i) l[i] = 0.f;
+    for (int i = 0; i < 16; ++i) {
+      l[i] = 0.f;
+      m[i] = -INFINITY;
+    }
     if (tid < 64) m_used[tid] = -INFINITY;
     named_sync(kBarSoft, kSoftThreads);
     for (int k = lo; k < hi; ++k, ++n) {
@@ -510,31 +513,48 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
       const bool va = valid[ra] != 0, vb = valid[ra + 8] != 0;
       warp_wait_or_abort(sm, kBarSFull + st, par, fault);
       tc_fence_after();
+      const uint32_t s_addr = tmem + kTmemS + 64 * st + lane_base;
       float x[32];
-      tmem_ld16x256b_x8(tmem + kTmemS + 64 * st + lane_base, x);
+      tmem_ld16x256b_x8(s_addr, x);
       tmem_ld_wait();
-      // the scores are in registers: the buffer can take tile n + 2
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(kBarSFree + st));
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        x[4 * jj + 0] = va ? x[4 * jj + 0] * qk_scale : -INFINITY;
-        x[4 * jj + 1] = va ? x[4 * jj + 1] * qk_scale : -INFINITY;
-        x[4 * jj + 2] = vb ? x[4 * jj + 2] * qk_scale : -INFINITY;
-        x[4 * jj + 3] = vb ? x[4 * jj + 3] * qk_scale : -INFINITY;
-      }
       bool move = true;  // the first tile of a piece always sets the max
       if (k != lo) {
-        bool exceed = false;
+        // Fast path: t = score * scale - m (log2 units), P = 2^t computed
+        // before the vote; valid only if no t exceeds 8 anywhere in the tile.
+        float tmax = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          exceed |= fmaxf(x[4 * (i >> 1) + (i & 1)], x[4 * (i >> 1) + 2 + (i & 1)]) >
-                    m_used[8 * (i >> 1) + hq + (i & 1)] + kRescaleLog2;
-        move = named_sync_or(kBarSoft, kSoftThreads, exceed);  // also true against -inf
+        for (int i = 0; i < 16; ++i) {
+          const int ia = 4 * (i >> 1) + (i & 1);
+          const float ta = va ? fmaf(x[ia], qk_scale, -m[i]) : -INFINITY;
+          const float tb = vb ? fmaf(x[ia + 2], qk_scale, -m[i]) : -INFINITY;
+          tmax = fmaxf(tmax, fmaxf(ta, tb));
+          x[ia] = ex2_approx(ta);
+          x[ia + 2] = ex2_approx(tb);
+        }
+        move = named_sync_or(kBarSoft, kSoftThreads, tmax > kRescaleLog2);  // also true against -inf
+        if (!move) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int ia = 4 * (i >> 1) + (i & 1);
+            l[i] += x[ia] + x[ia + 2];
+          }
+        }
       }
       if (move) {
-        // move the running max: tile max per head over the 64 rows
+        // Slow path: the scores again (S^T buffer st is not reused before
+        // this tile's PV has completed), then move the running max.
+        if (k != lo) {
+          tmem_ld16x256b_x8(s_addr, x);
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          x[4 * jj + 0] = va ? x[4 * jj + 0] * qk_scale : -INFINITY;
+          x[4 * jj + 1] = va ? x[4 * jj + 1] * qk_scale : -INFINITY;
+          x[4 * jj + 2] = vb ? x[4 * jj + 2] * qk_scale : -INFINITY;
+          x[4 * jj + 3] = vb ? x[4 * jj + 3] * qk_scale : -INFINITY;
+        }
+        // tile max per head over the 64 rows
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -555,7 +575,11 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
         }
         named_sync(kBarSoft, kSoftThreads);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) l[i] *= alpha[8 * (i >> 1) + hq + (i & 1)];
+        for (int i = 0; i < 16; ++i) {
+          const int h = 8 * (i >> 1) + hq + (i & 1);
+          l[i] *= alpha[h];
+          m[i] = m_used[h];
+        }
         if (k != lo) {
           // O^T at this thread's head-dim lane, all heads, once the PV product
           // of tile n - 1 has completed
@@ -573,18 +597,22 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
           }
           tmem_st_wait();
         }
-      }
-      // P = 2^(x - m_used), row sums, and P into its stage as [64 rows][64
-      // heads] bf16 with the 128-B swizzle (the MN-major B operand of PV)
+        // P = 2^(x - m_used) and the row sums
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float mi_ = m_used[8 * (i >> 1) + hq + (i & 1)];
-        const float mz = mi_ == -INFINITY ? 0.f : mi_;
-        const int ia = 4 * (i >> 1) + (i & 1);
-        x[ia] = ex2_approx(x[ia] - mz);
-        x[ia + 2] = ex2_approx(x[ia + 2] - mz);
-        l[i] += x[ia] + x[ia + 2];
+        for (int i = 0; i < 16; ++i) {
+          const float mz = m[i] == -INFINITY ? 0.f : m[i];
+          const int ia = 4 * (i >> 1) + (i & 1);
+          x[ia] = ex2_approx(x[ia] - mz);
+          x[ia + 2] = ex2_approx(x[ia + 2] - mz);
+          l[i] += x[ia] + x[ia + 2];
+        }
       }
+      // the scores are no longer needed: the buffer can take tile n + 2
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(kBarSFree + st));
+      // P into its stage as [64 rows][64 heads] bf16 with the 128-B swizzle
+      // (the MN-major B operand of PV)
       const uint32_t pbase = sm.base + kSP + st * kPBytes;
       const int mi = lane >> 3, jr = lane & 7;
       const uint32_t prow = pbase + uint32_t(16 * warp + 8 * (mi & 1) + jr) * 128;
