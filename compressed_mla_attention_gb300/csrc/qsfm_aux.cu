@@ -45,21 +45,21 @@ __global__ void __launch_bounds__(kPlanThreads)
   const int tid = threadIdx.x;
   const int per = (T + kPlanThreads - 1) / kPlanThreads;
   const int ta = min(T, tid * per), tb = min(T, ta + per);
-  long long cost = 0, tiles = 0;
+  // tiles per token, kept for the second pass for the first kKeep tokens
+  // (beyond them they are recomputed)
+  constexpr int kKeep = 6144;
+  __shared__ int s_tiles[kKeep];
+  long long cost = 0;
   for (int t = ta; t < tb; ++t) {
     const int n = token_geom(p, t).n_tiles;
+    if (t < kKeep) s_tiles[t] = n;
     cost += n + 1;
-    tiles += n;
   }
   long long pre, total;
   Scan(scan_tmp).ExclusiveSum(cost, pre, total);
-  __syncthreads();
-  long long pre_tiles, total_tiles;
-  Scan(scan_tmp).ExclusiveSum(tiles, pre_tiles, total_tiles);
-  (void)pre_tiles;
   if (tid == 0) {
     s_total[0] = total;
-    s_total[1] = total_tiles;
+    s_total[1] = total - T;  // every token costs its tiles + 1
   }
   __syncthreads();
   const long long W = s_total[0];
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   if (G == 0) return;
   long long pos = pre;
   for (int t = ta; t < tb; ++t) {
-    const int n = token_geom(p, t).n_tiles;
+    const int n = t < kKeep ? s_tiles[t] : token_geom(p, t).n_tiles;
     const long long ct = n + 1;
     // boundaries c with floor(c W / G) in [pos, pos + ct)
     long long c_lo = (pos * G + W - 1) / W;

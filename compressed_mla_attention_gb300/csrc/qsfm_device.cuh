@@ -76,9 +76,16 @@ static __device__ __noinline__ TokenGeom token_geom(const qsfm_params& p, int t)
   TokenGeom g;
   int s, s1;
   token_batch(p, t, g.b, s, s1);
-  g.s2 = __ldg(p.seqused_ori_kv + g.b);
+  // every per-batch / per-token length this token may need, loaded together
+  // (one memory round trip instead of a chain of them)
+  const int s2 = __ldg(p.seqused_ori_kv + g.b);
+  const int used_q = p.seqused_q != nullptr ? __ldg(p.seqused_q + g.b) : 0;
+  const int used_cmp = p.seqused_cmp_kv != nullptr ? __ldg(p.seqused_cmp_kv + g.b) : 0;
+  const int resid = p.cmp_residual_kv != nullptr ? __ldg(p.cmp_residual_kv + g.b) : 0;
+  const int topk = p.cmp_topk_length != nullptr ? __ldg(p.cmp_topk_length + t) : 0;
+  g.s2 = s2;
   g.ori_lo = 0; g.n_ori = 0; g.n_cmp = 0; g.cmp_vis = 0;
-  bool live = !(p.seqused_q != nullptr && s >= __ldg(p.seqused_q + g.b));
+  bool live = !(p.seqused_q != nullptr && s >= used_q);
   if (live) {
     const int pos = g.s2 - s1 + s;  // bottom-right aligned position
     int lo, hi;
@@ -94,13 +101,13 @@ static __device__ __noinline__ TokenGeom token_geom(const qsfm_params& p, int t)
     g.n_ori = max(0, hi - lo + 1);
     if (p.cmp_kv != nullptr) {
       const int r = p.cmp_ratio;
-      const int cmp_len = p.seqused_cmp_kv ? __ldg(p.seqused_cmp_kv + g.b) : g.s2 / r;
-      const int res = p.cmp_residual_kv ? __ldg(p.cmp_residual_kv + g.b) : 0;
+      const int cmp_len = p.seqused_cmp_kv ? used_cmp : g.s2 / r;
+      const int res = resid;
       const int pc = cmp_len * r + res - s1 + s;
       g.cmp_vis = p.cmp_mask_mode == 3 ? max(0, min(cmp_len, div_floor(pc + 1, r))) : cmp_len;
       if (p.cmp_sparse_indices != nullptr) {
         g.n_cmp = p.k2;
-        if (p.cmp_topk_length) g.n_cmp = max(0, min(p.k2, __ldg(p.cmp_topk_length + t)));
+        if (p.cmp_topk_length) g.n_cmp = max(0, min(p.k2, topk));
       } else {
         g.n_cmp = g.cmp_vis;
       }
