@@ -56,6 +56,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of `values` over all ranks (the step time of a weak
+    scaling run is its slowest rank); identity without a process group."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(world: int, tokens_per_rank: int, ms: float) -> float:
+    """Query tokens per second of the whole job: every rank runs its own
+    replica of the batch, so all ranks' tokens count, over the slowest
+    rank's step time."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -229,10 +247,7 @@ def run_gpu_arm(args, w, rank, world, local):
     t_step = [e[0].elapsed_time(e[3]) for e in evs]
     ms = statistics.mean(t_step)
     ms_attn = statistics.mean(t_attn)
-    if world > 1:
-        t = torch.tensor([ms, ms_attn], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_attn = float(t[0]), float(t[1])
+    ms, ms_attn = max_over_ranks([ms, ms_attn], dev)
     if Q.device_status() != 0:
         raise RuntimeError("device fault during the timed steps")
 
@@ -270,10 +285,7 @@ def run_gpu_arm(args, w, rank, world, local):
             if k >= args.warmup:
                 times.append(e0.elapsed_time(e1))
         e2e_ms = statistics.mean(times)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t[0])
+        (e2e_ms,) = max_over_ranks([e2e_ms], dev)
         res["e2e"] = dict(ms=e2e_ms, h2d=h2d, d2h=d2h)
         res["work"] = algorithmic_work(Q, p, w, dev)
     return res
@@ -353,7 +365,7 @@ def main():
     if rank != 0:
         return
     hbm, tf, kind = measured_peaks()
-    value = world * T / (res["ms"] / 1e3)
+    value = job_throughput(world, T, res["ms"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms"], "higher_is_better": True, "scaling": "weak",
@@ -380,7 +392,7 @@ def main():
                             "tensor_tflops": flops / (res["ms_attn"] / 1e3) / 1e12,
                             "tensor_frac": flops / (res["ms_attn"] / 1e3) / 1e12 / tf}
         e = res["e2e"]
-        line["e2e"] = {"value": world * T / (e["ms"] / 1e3), "unit": UNIT,
+        line["e2e"] = {"value": job_throughput(world, T, e["ms"]), "unit": UNIT,
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
     if res["clocks"] is not None:
         line["clocks"] = res["clocks"]
