@@ -101,84 +101,129 @@ __global__ void __launch_bounds__(kPlanThreads)
   }
 }
 
-// One CTA per cut: the CTA of the first cut that falls inside a token merges
-// all parts of that token.
-__global__ void __launch_bounds__(256)
+// A fixed grid of blocks, each holding the plan's cuts in shared memory.
+// Work item = (a token whose tiles were split over several CTAs, a head);
+// the items are dealt to the warps of all blocks. The token is owned by its
+// first cut that falls inside it; its parts are the ranges of that cut's
+// predecessor and of the following cuts that start inside it. Lane l of a
+// warp holds head-dim elements 4l..4l+3 of each 128-wide quarter, so each
+// part's partial row is read with coalesced 512-byte loads.
+constexpr int kCombineThreads = 256;
+__global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const qsfm_params p, const int T, const Workspace ws, int* fault) {
+  using Scan = cub::BlockScan<int, kCombineThreads>;
+  __shared__ typename Scan::TempStorage scan_tmp;
+  __shared__ int s_cut[2 * (QSFM_MAX_CTAS + 1)];
+  __shared__ int s_owner[QSFM_MAX_CTAS];  // owning cut of the i-th split token
+  __shared__ int s_nowned;
   const int32_t* meta = p.metadata;
   if (meta[0] != kMetaMagic || meta[2] != T) return;
   const int G = meta[1];
-  if (G < 0 || G > int(gridDim.x) || G > QSFM_MAX_CTAS) return;
-  const int cb = blockIdx.x;
-  if (cb < 1 || cb >= G) return;
-  const Pair here{meta[kMetaHeader + 2 * cb], meta[kMetaHeader + 2 * cb + 1]};
-  if (here.k <= 0 || here.t < 0 || here.t >= T) return;
-  const Pair prev{meta[kMetaHeader + 2 * cb - 2], meta[kMetaHeader + 2 * cb - 1]};
-  if (prev.t == here.t && prev.k > 0) return;  // an earlier cut owns this token
-  const int t = here.t;
-  const int n = token_geom(p, t).n_tiles;
-  const Pair tok_lo{t, 0}, tok_hi{t, n};
-
-  __shared__ int s_slot[QSFM_MAX_CTAS + 1];
-  __shared__ float s_lse[64];    // log-sum-exp over all parts (sink excluded)
-  __shared__ float s_denom[64];  // log of the full denominator (sink included)
-  __shared__ int s_n;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    int m = 0;
-    for (int c = cb - 1; c < G; ++c) {
-      const Pair b0{meta[kMetaHeader + 2 * c], meta[kMetaHeader + 2 * c + 1]};
-      if (b0.t > t) break;
-      const Pair b1{meta[kMetaHeader + 2 * c + 2], meta[kMetaHeader + 2 * c + 3]};
-      const Pair lo = pair_less(b0, tok_lo) ? tok_lo : b0;
-      const Pair hi = pair_less(b1, tok_hi) ? b1 : tok_hi;
-      if (pair_less(lo, hi)) s_slot[m++] = (b0.t == t) ? 2 * c : 2 * c + 1;
-    }
-    s_n = m;
-  }
+  if (G < 0 || G > QSFM_MAX_CTAS) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 2 * (G + 1); i += kCombineThreads) s_cut[i] = meta[kMetaHeader + i];
   __syncthreads();
-  const int m = s_n;
-  if (tid < 64) {
+  // cut c (1 <= c < G) owns its token when it falls inside it and the
+  // previous cut does not fall inside the same token
+  int own = 0;
+  if (tid >= 1 && tid < G) {
+    const int t = s_cut[2 * tid], k = s_cut[2 * tid + 1];
+    own = (k > 0 && t >= 0 && t < T && !(s_cut[2 * tid - 2] == t && s_cut[2 * tid - 1] > 0)) ? 1 : 0;
+  }
+  int pos, total;
+  Scan(scan_tmp).ExclusiveSum(own, pos, total);
+  if (own) s_owner[pos] = tid;
+  if (tid == 0) s_nowned = total;
+  __syncthreads();
+  const int items = s_nowned * 64;
+  const int warps_total = gridDim.x * (kCombineThreads / 32);
+  for (int it = blockIdx.x * (kCombineThreads / 32) + warp; it < items; it += warps_total) {
+    const int cb = s_owner[it >> 6], h = it & 63;
+    const int t = s_cut[2 * cb];
+    // the parts: ranges [cut c, cut c + 1) for c = cb - 1, cb, ... whose end
+    // lies past the token's start (split-mode cuts never start past a
+    // token's last tile, so every such range holds tiles of t)
+    const int c_begin = cb - 1;
+    int c_end = cb;
+    while (c_end < G && s_cut[2 * c_end] <= t) ++c_end;
+    const int m = c_end - c_begin;
+    // lane i takes parts i, i + 32, ...: slot, lse
+    auto part = [&](int i, int& sl, float& li) {
+      const int c = c_begin + i;
+      const int t1 = s_cut[2 * c + 2], k1 = s_cut[2 * c + 3];
+      const bool ov = t1 > t || (t1 == t && k1 > 0);
+      sl = (s_cut[2 * c] == t) ? 2 * c : 2 * c + 1;
+      li = ov ? ws.lse[size_t(sl) * 64 + h] : -INFINITY;
+    };
     float L = -INFINITY;
-    for (int i = 0; i < m; ++i) L = fmaxf(L, ws.lse[size_t(s_slot[i]) * 64 + tid]);
-    float lse_all = -INFINITY;
-    if (L > -INFINITY) {
-      float sum = 0.f;
-      for (int i = 0; i < m; ++i) sum += expf(ws.lse[size_t(s_slot[i]) * 64 + tid] - L);
-      lse_all = L + logf(sum);
+    for (int i0 = 0; i0 < m; i0 += 32) {
+      int sl;
+      float li = -INFINITY;
+      if (i0 + lane < m) part(i0 + lane, sl, li);
+      L = fmaxf(L, li);
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));
+    float sum = 0.f;
+    for (int i0 = 0; i0 < m && L > -INFINITY; i0 += 32) {
+      int sl;
+      float li = -INFINITY;
+      if (i0 + lane < m) part(i0 + lane, sl, li);
+      if (li > -INFINITY) sum += expf(li - L);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float lse_all = L > -INFINITY ? L + logf(sum) : -INFINITY;
     float denom_log = lse_all;
     if (p.sinks != nullptr && lse_all > -INFINITY) {
-      const float sk = __ldg(p.sinks + tid);
+      const float sk = __ldg(p.sinks + h);
       const float mx = fmaxf(lse_all, sk);
       denom_log = mx + logf(expf(lse_all - mx) + expf(sk - mx));
     }
-    s_lse[tid] = lse_all;
-    s_denom[tid] = denom_log;
-  }
-  __syncthreads();
-  if (p.return_lse && tid < 64) p.softmax_lse[size_t(t) * 64 + tid] = s_lse[tid];
-  // 64 heads x 512 outputs; thread -> (head, 128-wide d range)
-  const int h = tid >> 2, d0 = (tid & 3) * 128;
-  const bool live = s_lse[h] > -INFINITY;
-  const float dl = s_denom[h];
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.attn_out) + (size_t(t) * 64 + h) * kDim + d0;
-  for (int d = 0; d < 128; d += 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < m && live; ++i) {
-      const float li = ws.lse[size_t(s_slot[i]) * 64 + h];
-      if (li == -INFINITY) continue;
-      const float w = expf(li - dl);
-      const float4 v = *reinterpret_cast<const float4*>(
-          ws.out + (size_t(s_slot[i]) * 64 + h) * kDim + d0 + d);
-      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    if (p.return_lse && lane == 0) p.softmax_lse[size_t(t) * 64 + h] = lse_all;
+    float4 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < m && lse_all > -INFINITY; i0 += 32) {
+      // weights of this group of parts, one per lane, then broadcast
+      int sl = 0;
+      float li = -INFINITY;
+      if (i0 + lane < m) part(i0 + lane, sl, li);
+      const float w = li > -INFINITY ? expf(li - denom_log) : 0.f;
+      const int mg = min(32, m - i0);
+      for (int i = 0; i < mg; i += 4) {
+        float4 v[4][4];
+        float wi[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int src_lane = min(i + u, mg - 1);
+          wi[u] = (i + u < mg) ? __shfl_sync(0xffffffffu, w, src_lane) : 0.f;
+          const int su = __shfl_sync(0xffffffffu, sl, src_lane);
+          const float* src = ws.out + (size_t(su) * 64 + h) * kDim + 4 * lane;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[u][q] = __ldg(reinterpret_cast<const float4*>(src + 128 * q));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[q].x += wi[u] * v[u][q].x;
+            acc[q].y += wi[u] * v[u][q].y;
+            acc[q].z += wi[u] * v[u][q].z;
+            acc[q].w += wi[u] * v[u][q].w;
+          }
+      }
     }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out + d) = pk;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.attn_out) + (size_t(t) * 64 + h) * kDim + 4 * lane;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[q].x, acc[q].y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[q].z, acc[q].w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(out + 128 * q) = pk;
+    }
   }
 }
 
@@ -251,7 +296,7 @@ cudaError_t launch_plan(const qsfm_params& p, int num_tokens, int num_ctas, int 
 
 cudaError_t launch_combine(const qsfm_params& p, int num_tokens, int num_ctas,
                            const Workspace& ws, int* fault, cudaStream_t s) {
-  combine_kernel<<<num_ctas, 256, 0, s>>>(p, num_tokens, ws, fault);
+  combine_kernel<<<num_ctas, kCombineThreads, 0, s>>>(p, num_tokens, ws, fault);
   return cudaGetLastError();
 }
 
