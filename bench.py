@@ -226,7 +226,10 @@ def run_gpu_arm(args, w, rank, world, local):
     if Q.device_status() != 0:
         raise RuntimeError("device fault during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # Timed steps: events only before and after each step, so that the
+    # kernels of a step follow each other on the stream as in use (the
+    # attention and combine kernels may start while their predecessor ends).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if world > 1:
         torch.distributed.barrier()
@@ -236,15 +239,25 @@ def run_gpu_arm(args, w, rank, world, local):
         time.sleep(0.3)
     for k in range(args.steps):
         flush.zero_()  # L2 flush, outside the timed events
-        step(evs[k])
+        evs[k][0].record(stream)
+        step()
+        evs[k][1].record(stream)
     torch.cuda.synchronize()
     clk = None if args.quick else clocks.stop()
     if world > 1:
         torch.distributed.barrier()
-    t_plan = [e[0].elapsed_time(e[1]) for e in evs]
-    t_attn = [e[1].elapsed_time(e[2]) for e in evs]
-    t_comb = [e[2].elapsed_time(e[3]) for e in evs]
-    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    t_step = [e[0].elapsed_time(e[1]) for e in evs]
+    # Per-kernel times (for the roofline of the attention kernel): a second
+    # pass with events between the kernels.
+    n_split = min(args.steps, 500)
+    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_split)]
+    for k in range(n_split):
+        flush.zero_()
+        step(kevs[k])
+    torch.cuda.synchronize()
+    t_plan = [e[0].elapsed_time(e[1]) for e in kevs]
+    t_attn = [e[1].elapsed_time(e[2]) for e in kevs]
+    t_comb = [e[2].elapsed_time(e[3]) for e in kevs]
     ms = statistics.mean(t_step)
     ms_attn = statistics.mean(t_attn)
     ms, ms_attn = max_over_ranks([ms, ms_attn], dev)

@@ -718,6 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.ptr = smem_raw + (sm.base - raw_addr);
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  grid_dependency_wait();   // the plan (and every input) is written by now
+  grid_launch_dependents();  // the combine kernel may take SMs as CTAs finish
   const int* meta = p.metadata;
   if (meta[0] != kMetaMagic || meta[2] != T) {
     if (tid == 0 && blockIdx.x == 0) atomicOr(fault, QSFM_FAULT_METADATA);
@@ -818,8 +820,8 @@ cudaError_t launch_attention(const qsfm_params& p, int num_tokens, int num_ctas,
   CUtensorMap qmap;
   e = make_q_map(p.q, num_tokens, &qmap);
   if (e != cudaSuccess) return e;
-  attention_kernel<<<num_ctas, kThreads, kSmemAlloc, s>>>(p, num_tokens, ws, fault, qmap);
-  return cudaGetLastError();
+  return launch_after_predecessor(attention_kernel, dim3(num_ctas), dim3(kThreads), kSmemAlloc, s, p,
+                                  num_tokens, ws, fault, qmap);
 }
 
 }  // namespace qsfm

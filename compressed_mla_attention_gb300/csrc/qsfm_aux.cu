@@ -43,6 +43,9 @@ __global__ void __launch_bounds__(kPlanThreads)
   __shared__ typename Scan::TempStorage scan_tmp;
   __shared__ long long s_total[2];
   const int tid = threadIdx.x;
+  // the attention kernel may take its place on the SMs now; it reads the
+  // plan only after this grid has completed
+  grid_launch_dependents();
   const int per = (T + kPlanThreads - 1) / kPlanThreads;
   const int ta = min(T, tid * per), tb = min(T, ta + per);
   // tiles per token, kept for the second pass for the first kKeep tokens
@@ -116,6 +119,7 @@ __global__ void __launch_bounds__(kCombineThreads)
   __shared__ int s_cut[2 * (QSFM_MAX_CTAS + 1)];
   __shared__ int s_owner[QSFM_MAX_CTAS];  // owning cut of the i-th split token
   __shared__ int s_nowned;
+  grid_dependency_wait();  // the attention kernel's partial results
   const int32_t* meta = p.metadata;
   if (meta[0] != kMetaMagic || meta[2] != T) return;
   const int G = meta[1];
@@ -296,8 +300,8 @@ cudaError_t launch_plan(const qsfm_params& p, int num_tokens, int num_ctas, int 
 
 cudaError_t launch_combine(const qsfm_params& p, int num_tokens, int num_ctas,
                            const Workspace& ws, int* fault, cudaStream_t s) {
-  combine_kernel<<<num_ctas, kCombineThreads, 0, s>>>(p, num_tokens, ws, fault);
-  return cudaGetLastError();
+  return launch_after_predecessor(combine_kernel, dim3(num_ctas), dim3(kCombineThreads), 0, s, p,
+                                  num_tokens, ws, fault);
 }
 
 cudaError_t launch_debug_gather(const qsfm_params& p, const int32_t* tokens, int n,

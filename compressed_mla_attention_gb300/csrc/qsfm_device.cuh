@@ -328,6 +328,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched right after another one
+// on the same stream with the programmatic-serialization attribute may start
+// before its predecessor has finished; grid_dependency_wait() blocks until
+// every grid it depends on has completed and its writes are visible (a no-op
+// without such a dependency). grid_launch_dependents() lets the kernel that
+// follows start its own prologue early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over `count` threads.
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "qsfm.h"
 
 namespace qsfm {
@@ -20,6 +22,26 @@ struct Workspace {
 
 size_t workspace_bytes(int num_ctas);
 Workspace workspace_view(void* base, int num_ctas);
+
+// Launches `kernel` so that it may start while the kernel before it on the
+// stream is still running (programmatic stream serialization); the kernel
+// calls grid_dependency_wait() before it reads anything its predecessor
+// writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_after_predecessor(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                            size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_plan(const qsfm_params& p, int num_tokens, int num_ctas, int split,
                         int32_t* metadata, int* fault, cudaStream_t s);
