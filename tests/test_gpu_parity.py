@@ -93,6 +93,9 @@ EDGE = {
     "k2_1024": dict(layout="BSND", q_lens=[1], s2=[20000], cmp_ratio=4, mode="CSA", k2=1024),
     "large_logits": dict(layout="BSND", q_lens=[2], s2=[3000], cmp_ratio=4, mode="CSA", k2=512,
                          q_scale=12.0),
+    # one token of 64 tiles: with the default CTA count it is split into more
+    # than 32 parts, which the combine merges in groups of 32
+    "one_token_many_parts": dict(layout="BSND", q_lens=[1], s2=[250000], cmp_ratio=64, mode="HCA"),
 }
 
 
