@@ -29,9 +29,10 @@
 //               registers and writes its P values with stmatrix. In the
 //               epilogue thread i owns head-dim lane i of O^T.
 //   warps 4-11  producers: take a tile's physical rows from the resolver,
-//               load their fp8 bytes and scales into registers while the
-//               tile's stage drains, then dequantise them chunk by chunk (a
-//               chunk = 64 rows x 128 d = 2 d-blocks) into the stage.
+//               load their fp8 bytes and scales into registers, dequantise
+//               the whole tile into registers, start the next tile's loads,
+//               then store the tile chunk by chunk (a chunk = 64 rows x 128 d
+//               = 2 d-blocks) once its stage is free.
 //   warp 12     QK^T issue (one thread): Q by TMA, QK^T chunk by chunk as the
 //               producers publish the chunks.
 //   warp 14     PV issue (one thread): PV once the softmax has written P, and
@@ -300,15 +301,14 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, int* fault) 
     return true;
   };
 
-  // The next tile's loads are issued only after this tile's last chunk has
-  // been published: each chunk's release waits for the thread's outstanding
-  // loads, so loads issued earlier would serialise every chunk on a memory
-  // round trip. Issued there, they overlap the wait for the next stage.
-  for (uint32_t n = 0; fetch(n); ++n) {
+  // Per tile: dequantise it into registers (this waits for its loads), start
+  // the next tile's loads, then wait for the stage and store. The next
+  // tile's loads are in flight during the stage wait and the stores.
+  bool have = fetch(0);
+  for (uint32_t n = 0; have; ++n) {
     const uint32_t st = n & 1;
-    // Dequantise the whole tile into registers first: this waits for the
-    // loads and runs while the stage is still in use by tile n - 2.
     uint4 D[4][2][2];  // [chunk][row][16-byte half], bf16
+    const int vrow0 = pr[0] >= 0, vrow1 = pr[1] >= 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int src_lane = (lane & ~7) | (2 * c + (j >> 2));
@@ -319,12 +319,13 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, int* fault) 
         dequant16(raw, sc, D[c][u][0], D[c][u][1]);
       }
     }
+    have = fetch(n + 1);
     if (!warp_wait_or_abort(sm, kBarKvEmpty + st, ((n >> 1) & 1) ^ 1, fault)) return;
     const uint32_t stage = sm.base + kSK + st * kStageBytes;
     if (j == 0) {
       int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + st * kTileRows;
-      valid[row_lo] = pr[0] >= 0;
-      valid[row_lo + 32] = pr[1] >= 0;
+      valid[row_lo] = vrow0;
+      valid[row_lo + 32] = vrow1;
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
