@@ -9,6 +9,7 @@
 // ori mask mode 4; cu_seqlens_q required for TND; seqused_ori_kv and the
 // block table required for paged KV; metadata required.
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 #include <cuda_runtime.h>
 
@@ -51,6 +52,11 @@ qsfm_status resolve_ctas(const qsfm_params& p, int* out) {
 }
 
 // Shape / attribute / pointer checks shared by every entry point.
+// True for a null pointer or one aligned to `bytes`.
+bool aligned(const void* ptr, uintptr_t bytes) {
+  return (reinterpret_cast<uintptr_t>(ptr) & (bytes - 1)) == 0;
+}
+
 qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   if (pp == nullptr) return QSFM_ERR_INVALID_ARG;
   const qsfm_params& p = *pp;
@@ -94,6 +100,18 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
     if (p.q == nullptr || p.attn_out == nullptr) return QSFM_ERR_INVALID_ARG;
     if (p.return_lse && p.softmax_lse == nullptr) return QSFM_ERR_INVALID_ARG;
   }
+  // Alignment the kernels rely on: 16-byte vector, tensor-map and bulk-copy
+  // accesses to q, the KV pools and attn_out; 4-byte element accesses to the
+  // rest.
+  if (!aligned(p.q, 16) || !aligned(p.ori_kv, 16) || !aligned(p.cmp_kv, 16) ||
+      !aligned(p.attn_out, 16))
+    return QSFM_ERR_INVALID_ARG;
+  const void* words[] = {p.ori_scale, p.cmp_scale, p.cmp_sparse_indices, p.ori_block_table,
+                         p.cmp_block_table, p.cu_seqlens_q, p.seqused_q, p.seqused_ori_kv,
+                         p.seqused_cmp_kv, p.cmp_residual_kv, p.cmp_topk_length, p.sinks,
+                         p.metadata, p.softmax_lse};
+  for (const void* w : words)
+    if (!aligned(w, 4)) return QSFM_ERR_INVALID_ARG;
   return QSFM_OK;
 }
 
@@ -145,7 +163,7 @@ void qsfm_params_init(qsfm_params* p) {
 qsfm_status qsfm_metadata(const qsfm_params* p, int32_t* metadata_out, void* stream) {
   qsfm_status st = validate(p, false);
   if (st != QSFM_OK) return st;
-  if (metadata_out == nullptr) return QSFM_ERR_INVALID_ARG;
+  if (metadata_out == nullptr || !aligned(metadata_out, 4)) return QSFM_ERR_INVALID_ARG;
   int ctas = 0;
   st = resolve_ctas(*p, &ctas);
   if (st != QSFM_OK) return st;

@@ -487,12 +487,16 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
   float* alpha = sm.f(kSAlpha);
   float* inv = sm.f(kSInv);
   float* red = sm.f(kSRed);
+  // this thread's head sink (log2 units), read once
+  const float sink2 = (tid < 64 && p.sinks != nullptr) ? __ldg(p.sinks + tid) * kLog2e : -INFINITY;
   PieceIter pieces(&p, rg, T);
   uint32_t n = 0, pieces_live = 0;
   int t, lo, hi;
   TokenGeom g;
-  while (pieces.next(t, g, lo, hi)) {
-    const bool whole = (lo == 0 && hi == g.n_tiles);
+  bool have = pieces.next(t, g, lo, hi);
+  int n_tiles = g.n_tiles;
+  while (have) {
+    const bool whole = (lo == 0 && hi == n_tiles);
     const int slot = (t == rg.t0) ? 2 * c_idx : 2 * c_idx + 1;
     const bool writable = whole || slot < ws.slots;  // split pieces need the workspace
     if (!writable && tid == 0) atomicOr(fault, QSFM_FAULT_METADATA);
@@ -629,6 +633,11 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(kBarPFull + st));
     }
+    // The next piece's geometry, read now: its loads overlap the wait for
+    // this piece's last PV product.
+    int t_next = 0, lo_next = 0, hi_next = 0;
+    const bool have_next = pieces.next(t_next, g, lo_next, hi_next);
+    const int n_tiles_next = g.n_tiles;
     // ---------------- epilogue of the piece
     const bool any = lo < hi;
     if (any) {
@@ -643,7 +652,7 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
       const float lse2 = lt > 0.f ? mu + log2f(lt) : -INFINITY;
       if (whole) {
         float den = lt;
-        if (p.sinks != nullptr && lt > 0.f) den += exp2f(__ldg(p.sinks + tid) * kLog2e - mu);
+        if (p.sinks != nullptr && lt > 0.f) den += exp2f(sink2 - mu);
         inv[tid] = lt > 0.f ? 1.f / den : 0.f;
         if (p.return_lse) p.softmax_lse[size_t(t) * 64 + tid] = lse2 * kLn2;
       } else {
@@ -656,15 +665,19 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
       warp_wait_or_abort(sm, kBarODone, pieces_live & 1, fault);
       tc_fence_after();
     }
-    // O^T chunk by chunk: lane = head-dim element, columns = heads. For each
-    // head the 32 lanes of a warp write 32 consecutive outputs (64 bytes of
-    // bf16, 128 bytes of fp32 for split pieces), so the stores coalesce
-    // without staging.
+    // O^T in blocks of 128 d x 32 heads: lane = head-dim element, columns =
+    // heads. Whole tokens go out through the P buffers, idle now: each block
+    // is written there as 32 rows of 256 bytes ([head][d], bf16), then read
+    // back 16 bytes per thread and stored with 16-byte stores (a warp writes
+    // two 256-byte output rows per store); the two buffers alternate, so one
+    // barrier per block suffices. Split pieces store fp32 rows directly (the
+    // 32 lanes of a warp write 128 consecutive bytes per head).
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         const int h0 = 32 * half;
+        const int blk = 2 * c + half;
         float o[32];
         if (any) {
           tmem_ld32(tmem + kTmemO + 64 * c + 32 * half + lane_base, o);
@@ -687,10 +700,20 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
         }
         if (whole) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.attn_out) +
-                               (size_t(t) * 64 + h0) * kDim + 128 * c + row;
+          // every thread has read block blk - 2 back from this buffer before
+          // the barrier of block blk - 1
+          const uint32_t box = sm.base + kSP + uint32_t(blk & 1) * kPBytes;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) out[size_t(i) * kDim] = __float2bfloat16_rn(o[i]);
+          for (int i = 0; i < 32; ++i) sts_b16(box + uint32_t(i * 256 + 2 * row), __float2bfloat16_rn(o[i]));
+          named_sync(kBarSoft, kSoftThreads);
+          uint8_t* out = static_cast<uint8_t*>(p.attn_out) +
+                         ((size_t(t) * 64 + h0) * kDim + 128 * c) * 2;
+#pragma unroll
+          for (int q = tid; q < 512; q += kSoftThreads) {  // q = 16-byte piece: head q / 16
+            const uint32_t off = uint32_t(q >> 4) * 256 + uint32_t(q & 15) * 16;
+            const uint4 v = lds_v4(box + off);
+            *reinterpret_cast<uint4*>(out + size_t(q >> 4) * kDim * 2 + (q & 15) * 16) = v;
+          }
         } else if (writable) {
           float* out = ws.out + (size_t(slot) * 64 + h0) * kDim + 128 * c + row;
 #pragma unroll
@@ -706,6 +729,11 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
     }
     named_sync(kBarSoft, kSoftThreads);  // m_used / inv / red are reused by the next piece
     if (*sm.abort_flag()) break;         // uniform: read after the barrier
+    have = have_next;
+    t = t_next;
+    lo = lo_next;
+    hi = hi_next;
+    n_tiles = n_tiles_next;
   }
 }
 

@@ -25,13 +25,6 @@ constexpr int kPlanThreads = 1024;
 __device__ __forceinline__ long long lmin(long long a, long long b) { return a < b ? a : b; }
 __device__ __forceinline__ long long lmax(long long a, long long b) { return a > b ? a : b; }
 
-struct Pair {
-  int t, k;
-};
-__device__ __forceinline__ bool pair_less(Pair a, Pair b) {
-  return a.t < b.t || (a.t == b.t && a.k < b.k);
-}
-
 // One CTA. Cost of a token = its KV tiles + 1 (loading Q, writing O). The
 // total cost W is cut into G equal ranges. In split mode a cut may fall
 // inside a token at a tile boundary; otherwise cuts snap to the start of the

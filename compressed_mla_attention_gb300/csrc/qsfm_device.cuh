@@ -571,6 +571,20 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* ptr) {
   return v;
 }
 
+__device__ __forceinline__ void sts_b16(uint32_t saddr, __nv_bfloat16 v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(saddr), "h"(*reinterpret_cast<const uint16_t*>(&v))
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(saddr)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void sts_v4(uint32_t saddr, const uint4& v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)

@@ -108,8 +108,10 @@ typedef enum { QSFM_LAYOUT_BSND = 0, QSFM_LAYOUT_TND = 1 } qsfm_q_layout;
 
 /*
  * All inputs, attributes and outputs of one forward call. Pointers are
- * device pointers; NULL marks an absent optional input. The parameter names
- * follow QuantSparseFlashMla, "参数说明" (parameter table).
+ * device pointers; NULL marks an absent optional input. q, ori_kv, cmp_kv and
+ * attn_out must be 16-byte aligned and every other pointer 4-byte aligned
+ * (QSFM_ERR_INVALID_ARG otherwise). The parameter names follow
+ * QuantSparseFlashMla, "参数说明" (parameter table).
  */
 typedef struct qsfm_params {
   /* shapes */

@@ -115,6 +115,12 @@ INVALID = [
     ("no metadata", dict(metadata=None), 1),
     ("too many CTAs", dict(num_ctas=100000), 1),
     ("nan scale", dict(softmax_scale=float("nan")), 1),
+    ("q not 16-byte aligned", dict(q=0x1008), 1),
+    ("ori_kv not 16-byte aligned", dict(ori_kv=0x1004), 1),
+    ("attn_out not 16-byte aligned", dict(attn_out=0x1002), 1),
+    ("ori_scale not 4-byte aligned", dict(ori_scale=0x1002), 1),
+    ("block table not 4-byte aligned", dict(ori_block_table=0x1001), 1),
+    ("metadata not 4-byte aligned", dict(metadata=0x1003), 1),
 ]
 
 
@@ -153,6 +159,16 @@ def test_workspace_size_depends_on_split(lib):
     p.batch, p.max_s1 = 64, 1  # 64 tokens >= 8 CTAs: no split, no workspace
     assert lib.qsfm_forward_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
     assert n.value == 0
+
+
+def test_word_aligned_pointers_pass_validation(lib):
+    # 4-byte alignment is enough for scales, tables and lengths: validation
+    # passes and the call stops at the missing workspace instead
+    p = _valid(lib)
+    p.ori_scale, p.ori_block_table, p.seqused_ori_kv, p.metadata = 0x1004, 0x1008, 0x100C, 0x1004
+    assert _status(lib, p) == 4
+    plan = ctypes.c_void_p(0x1002)
+    assert lib.qsfm_metadata(ctypes.byref(_valid(lib)), plan, None) == 1
 
 
 def test_forward_needs_workspace_when_splitting(lib):
