@@ -737,6 +737,45 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
   }
 }
 
+// Runs before the plan is readable, while the plan kernel still runs: warms
+// L2 with the inputs of the token this CTA most likely starts with (the plan
+// cuts equal-cost tokens evenly, so CTA c of G starts near token c T / G):
+// its Q, its index list, its first two ori tiles and its first four cmp
+// tiles. Only prefetches, so a wrong guess costs bandwidth, never results;
+// each address is checked against its buffer first. Thread i of the
+// producer warps takes ori slot i (i < 128) or cmp slot i - 128.
+__device__ __noinline__ void warm_first_token(const qsfm_params& p, int T, int c, int G, int i) {
+  const int t = int((long long)c * T / G);
+  if (t >= T) return;
+  if (i == 0)
+    bulk_prefetch_l2(static_cast<const uint8_t*>(p.q) + size_t(t) * kHeads * kDim * 2,
+                     kHeads * kDim * 2);
+  if (p.cmp_sparse_indices != nullptr && i < 32 && 32 * i < p.k2)
+    prefetch_l2(p.cmp_sparse_indices + size_t(t) * p.k2 + 32 * i);
+  const TokenGeom g = token_geom(p, t);
+  int pos = -1;
+  bool cmp = false;
+  if (i < 2 * kTileRows) {
+    if (i < g.n_ori) pos = g.ori_lo + i;
+  } else {
+    const int k = i - 2 * kTileRows;
+    if (k < g.n_cmp) {
+      cmp = true;
+      pos = p.cmp_sparse_indices != nullptr ? __ldg(p.cmp_sparse_indices + size_t(t) * p.k2 + k) : k;
+      if (pos >= g.cmp_vis) pos = -1;
+    }
+  }
+  if (pos < 0) return;
+  const int col = pos / kBlock;
+  const int width = cmp ? p.cmp_max_blocks : p.ori_max_blocks;
+  if (col >= width) return;
+  const int blk = __ldg((cmp ? p.cmp_block_table : p.ori_block_table) + size_t(g.b) * width + col);
+  if (blk < 0 || blk >= (cmp ? p.cmp_num_blocks : p.ori_num_blocks)) return;
+  const size_t row = size_t(blk) * kBlock + pos % kBlock;
+  bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * kDim, kDim);
+  prefetch_l2((cmp ? p.cmp_scale : p.ori_scale) + row * kScales);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const qsfm_params p, const int T, const Workspace ws, int* fault,
                      const __grid_constant__ CUtensorMap qmap) {
@@ -747,6 +786,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.ptr = smem_raw + (sm.base - raw_addr);
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp >= kSoftWarps && warp < kSoftWarps + kProdWarps)
+    warm_first_token(p, T, blockIdx.x, gridDim.x, tid - kSoftThreads);
   grid_dependency_wait();   // the plan (and every input) is written by now
   grid_launch_dependents();  // the combine kernel may take SMs as CTAs finish
   const int* meta = p.metadata;

@@ -283,6 +283,12 @@ __device__ __forceinline__ bool mbar_ready(uint32_t addr, uint32_t parity) {
   return done != 0;
 }
 
+// Hint: bring `bytes` bytes at `ptr` into L2 (ptr 16-byte aligned, bytes a
+// multiple of 16); nothing is written to shared memory.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 // Hint: bring the 128-byte line holding `ptr` into L2.
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
@@ -292,10 +298,10 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
 // `timeout_ns` or as soon as *abort becomes non-zero. try_wait suspends the
 // thread in hardware until the phase completes or a short time limit passes,
 // so the loop polls rarely; only long waits back off further with sleeps.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort, uint64_t timeout_ns) {
-  const uint32_t addr = smem_u32(bar);
-  if (mbar_test(addr, parity)) return true;
+// The polling loop is out of line, so each call site adds one test and a
+// call: the many waits of a kernel then share one copy of the loop.
+static __device__ __noinline__ bool mbar_wait_poll(uint32_t addr, uint32_t parity, volatile int* abort,
+                                            uint64_t timeout_ns) {
   const uint64_t start = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (it > 256) __nanosleep(64);
@@ -305,6 +311,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
       if (globaltimer_ns() - start > timeout_ns) return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, uint64_t timeout_ns) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_test(addr, parity)) return true;
+  return mbar_wait_poll(addr, parity, abort, timeout_ns);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
