@@ -45,7 +45,8 @@ UNIT = "query-tokens/s"
 FLUSH_BYTES = 512 << 20  # > 129 MB L2
 KV_ROW_BYTES = 512 + 8 * 4
 FLOPS_PER_ROW = 4 * 64 * 512
-KERNEL_SRC = os.path.join(ROOT, "compressed_mla_attention_gb300", "csrc", "qsfm_attention.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "compressed_mla_attention_gb300", "csrc", f)
+               for f in ("qsfm_attention.cu", "qsfm_device.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_traffic.txt")
 
 
@@ -83,7 +84,12 @@ def measured_peaks():
 
 
 def kernel_sha() -> str:
-    return hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    """Hash of the attention kernel's sources (its file and the device header
+    it inlines): a recorded traffic figure holds only for this hash."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: int):
@@ -264,7 +270,8 @@ def run_gpu_arm(args, w, rank, world, local):
     if Q.device_status() != 0:
         raise RuntimeError("device fault during the timed steps")
 
-    res = dict(ms=ms, ms_attn=ms_attn, ms_plan=statistics.mean(t_plan), ms_comb=statistics.mean(t_comb),
+    res = dict(ms=ms, ms_attn=ms_attn, ms_plan=statistics.mean(t_plan),
+               ms_comb=statistics.mean(t_comb) if split else None,  # no combine launch
                launches=args.steps * (3 if split else 2), split=split, clocks=clk,
                ctas=int(plan[1].item()))
 
