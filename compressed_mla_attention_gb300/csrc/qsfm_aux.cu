@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 // warp holds head-dim elements 4l..4l+3 of each 128-wide quarter, so each
 // part's partial row is read with coalesced 512-byte loads.
 constexpr int kCombineThreads = 256;
+constexpr int kCombineBlocksPerCta = 4;
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const qsfm_params p, const int T, const Workspace ws, int* fault) {
   using Scan = cub::BlockScan<int, kCombineThreads>;
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     // the parts: ranges [cut c, cut c + 1) for c = cb - 1, cb, ... whose end
     // lies past the token's start (split-mode cuts never start past a
     // token's last tile, so every such range holds tiles of t)
+    const float sk = p.sinks != nullptr ? __ldg(p.sinks + h) : -INFINITY;  // in flight with the lse loads
     const int c_begin = cb - 1;
     int c_end = cb;
     while (c_end < G && s_cut[2 * c_end] <= t) ++c_end;
@@ -173,7 +175,6 @@ __global__ void __launch_bounds__(kCombineThreads)
     const float lse_all = L > -INFINITY ? L + logf(sum) : -INFINITY;
     float denom_log = lse_all;
     if (p.sinks != nullptr && lse_all > -INFINITY) {
-      const float sk = __ldg(p.sinks + h);
       const float mx = fmaxf(lse_all, sk);
       denom_log = mx + logf(expf(lse_all - mx) + expf(sk - mx));
     }
@@ -293,8 +294,11 @@ cudaError_t launch_plan(const qsfm_params& p, int num_tokens, int num_ctas, int 
 
 cudaError_t launch_combine(const qsfm_params& p, int num_tokens, int num_ctas,
                            const Workspace& ws, int* fault, cudaStream_t s) {
-  return launch_after_predecessor(combine_kernel, dim3(num_ctas), dim3(kCombineThreads), 0, s, p,
-                                  num_tokens, ws, fault);
+  // Four blocks per planned CTA: every (split token, head) item of a full
+  // decode batch gets a warp of its own, so the few dependent L2 round trips
+  // of the items overlap instead of queueing in a warp.
+  return launch_after_predecessor(combine_kernel, dim3(kCombineBlocksPerCta * num_ctas),
+                                  dim3(kCombineThreads), 0, s, p, num_tokens, ws, fault);
 }
 
 cudaError_t launch_debug_gather(const qsfm_params& p, const int32_t* tokens, int n,
