@@ -38,25 +38,36 @@ int num_tokens(const qsfm_params& p) {
   return p.layout_q == QSFM_LAYOUT_BSND ? p.batch * p.max_s1 : p.total_t;
 }
 
+// CTAs the work is planned over: p.num_ctas, or the SM count when 0. With at
+// least as many tokens as CTAs the plan cuts at token starts, so some CTAs
+// get ceil(T / n) tokens; the fewest CTAs that keep that maximum take their
+// place (256 tokens on 152 SMs: 128 CTAs of 2 tokens instead of 104 CTAs of
+// 2 and 48 of 1). The longest CTA does as much work as before while fewer
+// CTAs compete for memory and L2.
 qsfm_status resolve_ctas(const qsfm_params& p, int* out) {
-  if (p.num_ctas > 0) {
-    *out = p.num_ctas;
-    return QSFM_OK;
+  int n = p.num_ctas;
+  if (n <= 0) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QSFM_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return QSFM_ERR_CUDA;
+    n = sms < QSFM_MAX_CTAS ? sms : QSFM_MAX_CTAS;
   }
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return QSFM_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return QSFM_ERR_CUDA;
-  *out = sms < QSFM_MAX_CTAS ? sms : QSFM_MAX_CTAS;
+  const long long T = num_tokens(p);
+  if (T >= n) {
+    const long long per = (T + n - 1) / n;
+    n = int((T + per - 1) / per);
+  }
+  *out = n;
   return QSFM_OK;
 }
 
-// Shape / attribute / pointer checks shared by every entry point.
 // True for a null pointer or one aligned to `bytes`.
 bool aligned(const void* ptr, uintptr_t bytes) {
   return (reinterpret_cast<uintptr_t>(ptr) & (bytes - 1)) == 0;
 }
 
+// Shape / attribute / pointer checks shared by every entry point.
 qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   if (pp == nullptr) return QSFM_ERR_INVALID_ARG;
   const qsfm_params& p = *pp;

@@ -127,7 +127,10 @@ typedef struct qsfm_params {
   int32_t cmp_max_blocks; /* cmp_block_table row width                       */
   int32_t ori_num_blocks; /* physical blocks in the ori pool                 */
   int32_t cmp_num_blocks; /* physical blocks in the cmp pool                 */
-  int32_t num_ctas;       /* CTAs the work is planned over; 0 = SM count    */
+  int32_t num_ctas;       /* most CTAs the work is planned over; 0 = SM
+                             count. With T >= num_ctas tokens the plan uses
+                             ceil(T / ceil(T / num_ctas)) CTAs, the fewest
+                             that keep the same tokens per CTA              */
   /* inputs (device) */
   const void* q;
   const void* ori_kv;

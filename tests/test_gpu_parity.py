@@ -69,6 +69,24 @@ def test_config2_all_ctas_variants(cuda_device):
         assert_parity(out, lse, w, toks, o_ref, l_ref)
 
 
+def test_plan_uses_fewest_ctas_with_same_tokens_per_cta(cuda_device):
+    """256 equal-cost tokens on at most n CTAs: the plan keeps ceil(256 / n)
+    tokens per CTA on the fewest CTAs that need (152 -> 128 CTAs of 2)."""
+    w = W.build("equal tokens", layout="BSND", q_lens=[2] * 128, s2=[300] * 128, mode="SWA", seed=3)
+    a = {k: v for k, v in W.device_inputs(w, cuda_device).items() if k != "return_softmax_lse"}
+    plan = torch.empty(1024, dtype=torch.int32, device=cuda_device)
+    for n, g in ((152, 128), (100, 86), (37, 37)):
+        p = Q.make_params(attn_out=torch.empty_like(a["q"]), metadata=plan, num_ctas=n, **a)
+        Q.metadata(p, plan)
+        m = plan.cpu().numpy()
+        assert m[1] == g
+        starts = [int(m[8 + 2 * c]) for c in range(g + 1)]
+        per = -(-256 // n)
+        assert max(b - a_ for a_, b in zip(starts, starts[1:])) == per
+        out, _ = run_gpu(w, cuda_device, num_ctas=n)
+        assert_parity(out, None, w, range(0, w.total_t, 17))
+
+
 # ----------------------------------------------------------- edge cases
 EDGE = {
     "short_seq_decode": dict(layout="BSND", q_lens=[1, 1, 1], s2=[1, 50, 127], cmp_ratio=4, mode="CSA",
