@@ -350,8 +350,11 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, int* fault) 
 // k-step s of d-block db: A (K~) at +db*8 KB + s*32 B, B (Q) at +db*8 KB + s*32 B.
 template <int kDb, int kS>
 __device__ __forceinline__ void qk_mma(uint32_t d, uint64_t a0, uint64_t b0) {
-  mma_bf16_at<uint32_t((kDb * 8192 + kS * 32) >> 4), uint32_t((kDb * 8192 + kS * 32) >> 4)>(
-      d, a0, b0, kIdescQK, (kDb | kS) != 0);
+  constexpr uint32_t off = uint32_t((kDb * 8192 + kS * 32) >> 4);
+  if constexpr ((kDb | kS) == 0)
+    mma_bf16_at<off, off>(d, a0, b0, kIdescQK, 0u);
+  else
+    mma_bf16_acc_at<off, off>(d, a0, b0, kIdescQK);
 }
 
 // PV for head-dim chunk kC: A (V~^T, MN-major) at +kC*16 KB + ks*2 KB,
@@ -360,9 +363,9 @@ template <int kC>
 __device__ __forceinline__ void pv_chunk(uint32_t tmem, uint64_t a0, uint64_t b0, uint32_t acc0) {
   const uint32_t d = tmem + kTmemO + kC * 64;
   mma_bf16_at<uint32_t((kC * 16384 + 0 * 2048) >> 4), uint32_t((0 * 2048) >> 4)>(d, a0, b0, kIdescPV, acc0);
-  mma_bf16_at<uint32_t((kC * 16384 + 1 * 2048) >> 4), uint32_t((1 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
-  mma_bf16_at<uint32_t((kC * 16384 + 2 * 2048) >> 4), uint32_t((2 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
-  mma_bf16_at<uint32_t((kC * 16384 + 3 * 2048) >> 4), uint32_t((3 * 2048) >> 4)>(d, a0, b0, kIdescPV, 1u);
+  mma_bf16_acc_at<uint32_t((kC * 16384 + 1 * 2048) >> 4), uint32_t((1 * 2048) >> 4)>(d, a0, b0, kIdescPV);
+  mma_bf16_acc_at<uint32_t((kC * 16384 + 2 * 2048) >> 4), uint32_t((2 * 2048) >> 4)>(d, a0, b0, kIdescPV);
+  mma_bf16_acc_at<uint32_t((kC * 16384 + 3 * 2048) >> 4), uint32_t((3 * 2048) >> 4)>(d, a0, b0, kIdescPV);
 }
 
 template <int kC>
