@@ -82,6 +82,7 @@ EXPORTS = {
     "qsfm_combine": (_i32, [ctypes.POINTER(QsfmParams), _ptr, ctypes.c_size_t, _ptr]),
     "qsfm_forward_noalloc": (_i32, [ctypes.POINTER(QsfmParams), _ptr]),
     "qsfm_debug_gather": (_i32, [ctypes.POINTER(QsfmParams), _ptr, _i32, _i32, _ptr, _ptr, _ptr, _ptr, _ptr]),
+    "qsfm_debug_bounded_wait": (_i32, [ctypes.c_uint64, _ptr, _ptr]),
     "qsfm_get_device_status": (_i32, [ctypes.POINTER(_i32)]),
     "qsfm_status_string": (ctypes.c_char_p, [_i32]),
     "qsfm_abi_version": (_i32, []),
@@ -259,6 +260,13 @@ def debug_gather(params: QsfmParams, tokens, max_rows: int, rows_out, scales_out
     _check("qsfm_debug_gather", lib().qsfm_debug_gather(
         ctypes.byref(params), _dptr(tokens), int(tokens.numel()), int(max_rows), _dptr(rows_out),
         _dptr(scales_out), _dptr(row_ids_out), _dptr(counts_out), _stream_ptr(stream)))
+
+
+def debug_bounded_wait(timeout_ns: int, elapsed_out, stream=None) -> None:
+    """qsfm_debug_bounded_wait(): runs out a bounded wait on purpose (sets
+    the timeout bit of the fault word; the device stays usable)."""
+    _check("qsfm_debug_bounded_wait", lib().qsfm_debug_bounded_wait(
+        int(timeout_ns), _dptr(elapsed_out), _stream_ptr(stream)))
 
 
 def device_status() -> int:

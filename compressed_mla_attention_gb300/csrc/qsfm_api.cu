@@ -246,6 +246,16 @@ qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens, int32
                                                static_cast<cudaStream_t>(stream)));
 }
 
+qsfm_status qsfm_debug_bounded_wait(uint64_t timeout_ns, uint64_t* elapsed_ns_out, void* stream) {
+  if (elapsed_ns_out == nullptr || !aligned(elapsed_ns_out, 8)) return QSFM_ERR_INVALID_ARG;
+  if (timeout_ns == 0 || timeout_ns > 1000000000ull) return QSFM_ERR_INVALID_ARG;
+  int* fault = fault_ptr();
+  if (fault == nullptr) return QSFM_ERR_CUDA;
+  return cuda_status(qsfm::launch_bounded_wait(
+      timeout_ns, reinterpret_cast<unsigned long long*>(elapsed_ns_out), fault,
+      static_cast<cudaStream_t>(stream)));
+}
+
 qsfm_status qsfm_get_device_status(int32_t* fault_word) {
   if (fault_word == nullptr) return QSFM_ERR_INVALID_ARG;
   int v = 0;

@@ -285,6 +285,39 @@ Workspace workspace_view(void* base, int num_ctas) {
   return w;
 }
 
+// The bounded wait of the kernels against barriers nothing arrives on: the
+// first wait runs out after timeout_ns and raises the abort flag, which ends
+// the second (1000 times longer) wait early.
+__global__ void bounded_wait_kernel(uint64_t timeout_ns, unsigned long long* elapsed, int* fault) {
+  __shared__ uint64_t bars[2];
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int* abort = &abort_flag;
+  const uint64_t t0 = globaltimer_ns();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait_bounded(&bars[0], 0, abort, timeout_ns)) {
+      *abort = 1;
+      atomicOr(fault, QSFM_FAULT_TIMEOUT);
+    }
+    elapsed[0] = globaltimer_ns() - t0;
+  } else if (threadIdx.x == 32) {
+    mbar_wait_bounded(&bars[1], 0, abort, 1000 * timeout_ns);
+    elapsed[1] = globaltimer_ns() - t0;
+  }
+}
+
+cudaError_t launch_bounded_wait(uint64_t timeout_ns, unsigned long long* elapsed, int* fault,
+                                cudaStream_t s) {
+  bounded_wait_kernel<<<1, 64, 0, s>>>(timeout_ns, elapsed, fault);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_plan(const qsfm_params& p, int num_tokens, int num_ctas, int split,
                         int32_t* metadata, int* fault, cudaStream_t s) {
   (void)fault;

@@ -49,6 +49,8 @@ cudaError_t launch_attention(const qsfm_params& p, int num_tokens, int num_ctas,
                              const Workspace& ws, int* fault, cudaStream_t s);
 cudaError_t launch_combine(const qsfm_params& p, int num_tokens, int num_ctas,
                            const Workspace& ws, int* fault, cudaStream_t s);
+cudaError_t launch_bounded_wait(uint64_t timeout_ns, unsigned long long* elapsed, int* fault,
+                                cudaStream_t s);
 cudaError_t launch_debug_gather(const qsfm_params& p, const int32_t* tokens, int n,
                                 int max_rows, uint8_t* rows_out, float* scales_out,
                                 int32_t* row_ids_out, int32_t* counts_out, int* fault,

@@ -245,6 +245,19 @@ qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens,
                               float* scales_out, int32_t* row_ids_out,
                               int32_t* counts_out, void* stream);
 
+/*
+ * Debug check of the bounded waits every kernel of the library uses (no GPU
+ * fault, no hang). One block: a thread waits with a limit of timeout_ns on
+ * an mbarrier that nothing arrives on; when the limit runs out it raises the
+ * block's abort flag and sets QSFM_FAULT_TIMEOUT in the fault word. A thread
+ * of another warp waits on a second such barrier with a limit 1000 times as
+ * long and gives up as soon as it sees the abort flag. Writes the two waits'
+ * durations in ns to elapsed_ns_out[0..1] (device memory, caller-owned).
+ * Errors: QSFM_ERR_INVALID_ARG for a NULL output, or timeout_ns of 0 or
+ * above one second.
+ */
+qsfm_status qsfm_debug_bounded_wait(uint64_t timeout_ns, uint64_t* elapsed_ns_out, void* stream);
+
 /* Synchronously read and clear the device fault word of the current
  * device (QSFM_FAULT_* bits). Returns QSFM_ERR_DEVICE_FAULT when non-zero. */
 qsfm_status qsfm_get_device_status(int32_t* fault_word);

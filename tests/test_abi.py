@@ -176,6 +176,13 @@ def test_forward_needs_workspace_when_splitting(lib):
     assert lib.qsfm_forward(ctypes.byref(p), None, 0, None) == 4
 
 
+def test_debug_bounded_wait_rejects_bad_arguments(lib):
+    assert lib.qsfm_debug_bounded_wait(1000, None, None) == 1          # no output
+    assert lib.qsfm_debug_bounded_wait(0, 0x1000, None) == 1           # no limit
+    assert lib.qsfm_debug_bounded_wait(2_000_000_000, 0x1000, None) == 1  # over one second
+    assert lib.qsfm_debug_bounded_wait(1000, 0x1004, None) == 1        # misaligned output
+
+
 def test_status_strings(lib):
     for code in range(7):
         assert Q.status_string(code)

@@ -237,6 +237,25 @@ def test_bad_block_id_is_reported_not_read(cuda_device):
     assert Q.device_status() == 0  # reading clears the word
 
 
+def test_bounded_wait_runs_out_without_faulting(cuda_device):
+    """A wait on a barrier nothing arrives on ends at its limit with the
+    timeout bit set, a second wait ends on the abort flag, and the device
+    keeps working."""
+    Q.device_status()  # clear
+    elapsed = torch.zeros(2, dtype=torch.int64, device=cuda_device)
+    Q.debug_bounded_wait(2_000_000, elapsed)  # 2 ms
+    torch.cuda.synchronize()
+    assert Q.device_status() & Q.FAULT_TIMEOUT
+    first, second = elapsed.cpu().tolist()
+    assert 2_000_000 <= first < 200_000_000
+    assert first <= second < first + 1_000_000  # well before its own 2 s limit
+    w = W.build("after timeout", layout="BSND", q_lens=[1] * 3, s2=[300, 700, 1200], cmp_ratio=4,
+                mode="CSA", k2=64, seed=11)
+    out, lse = run_gpu(w, cuda_device)
+    assert_parity(out, lse, w, range(w.total_t), derived=True)
+    assert Q.device_status() == 0
+
+
 def test_stale_metadata_is_rejected(cuda_device):
     """A plan made for other lengths is detected; nothing is written."""
     w1 = W.build("m1", layout="BSND", q_lens=[1] * 4, s2=[300] * 4, mode="SWA", seed=1)
