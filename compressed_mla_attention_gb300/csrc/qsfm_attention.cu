@@ -19,8 +19,12 @@
 //
 // Pipeline. Two tile stages in shared memory: while the tensor cores and the
 // softmax work on tile n, the producers fill the other stage with tile n+1.
-// The issue thread runs QK^T(n) before PV(n-1), so the softmax of tile n
-// overlaps the PV product of tile n-1 and the dequantisation of tile n+1.
+// Two threads issue the tensor-core work, each in its own order: QK^T of a
+// tile chunk by chunk as the producers publish it, PV of a tile once the
+// softmax has written P. So QK^T(n+1) runs while the softmax works on tile
+// n, and PV(n) while the producers fill tile n+2's stage. Before the plan is
+// readable (the plan kernel may still run), the producer warps warm L2 with
+// the inputs of the token the CTA most likely starts with.
 //
 // Warp roles (15 warps; at most 4 per SM sub-partition, so 128 registers):
 //   warps 0-3   softmax + epilogue. Warp q owns tile rows 16q..16q+15; each
