@@ -160,7 +160,7 @@ def make_params(
 ) -> QsfmParams:
     """Fill a QsfmParams from device tensors (shapes as in include/qsfm.h).
 
-    q / attn_out: BSND [B, S1, 64, 512] or TND [T1, 64, 512] bf16.
+    q / attn_out: BSND [B, S1, N1, 512] or TND [T1, N1, 512] bf16, N1 = 64 or 128.
     Paged KV: [blocks, 128, 1, 512] uint8 (fp8 e4m3fn bytes) with fp32 scales
     [blocks, 128, 1, 8]; block tables int32 [B, width].
     """
@@ -327,7 +327,7 @@ def quant_sparse_flash_mla(
     lse = None
     if return_softmax_lse:
         T = int(q.shape[0] * q.shape[1]) if (layout == "BSND" and q.dim() == 4) else int(q.shape[0])
-        lse = torch.empty(T, NUM_HEADS, dtype=torch.float32, device=dev)
+        lse = torch.empty(T, int(q.shape[-2]), dtype=torch.float32, device=dev)
     plan = metadata if metadata is not None else torch.empty(METADATA_INTS, dtype=torch.int32, device=dev)
     p = make_params(
         q=q, attn_out=attn_out, ori_kv=ori_kv, ori_scale=ori_scale, ori_block_table=ori_block_table,

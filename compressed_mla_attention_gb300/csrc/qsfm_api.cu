@@ -38,6 +38,10 @@ int num_tokens(const qsfm_params& p) {
   return p.layout_q == QSFM_LAYOUT_BSND ? p.batch * p.max_s1 : p.total_t;
 }
 
+// Work units the kernels plan over: one per 64-head group of each token
+// (N1 = 64: the tokens; N1 = 128: two per token).
+int num_units(const qsfm_params& p) { return num_tokens(p) * (p.n1 / QSFM_NUM_HEADS); }
+
 // CTAs the work is planned over: p.num_ctas, or the SM count when 0. With at
 // least as many tokens as CTAs the plan cuts at token starts, so some CTAs
 // get ceil(T / n) tokens; the fewest CTAs that keep that maximum take their
@@ -53,7 +57,7 @@ qsfm_status resolve_ctas(const qsfm_params& p, int* out) {
       return QSFM_ERR_CUDA;
     n = sms < QSFM_MAX_CTAS ? sms : QSFM_MAX_CTAS;
   }
-  const long long T = num_tokens(p);
+  const long long T = num_units(p);
   if (T >= n) {
     const long long per = (T + n - 1) / n;
     n = int((T + per - 1) / per);
@@ -73,7 +77,7 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   const qsfm_params& p = *pp;
   if (p.n1 <= 0 || p.d <= 0) return QSFM_ERR_INVALID_ARG;
   if (p.d != QSFM_HEAD_DIM) return QSFM_ERR_INVALID_ARG;  // "D only supports 512"
-  if (p.n1 != QSFM_NUM_HEADS) return QSFM_ERR_UNSUPPORTED;
+  if (p.n1 != QSFM_NUM_HEADS && p.n1 != 2 * QSFM_NUM_HEADS) return QSFM_ERR_UNSUPPORTED;
   if (p.batch < 0) return QSFM_ERR_INVALID_ARG;
   if (p.layout_q != QSFM_LAYOUT_BSND && p.layout_q != QSFM_LAYOUT_TND) return QSFM_ERR_INVALID_ARG;
   if (p.layout_q == QSFM_LAYOUT_BSND && p.max_s1 < 0) return QSFM_ERR_INVALID_ARG;
@@ -139,7 +143,7 @@ qsfm_status prepare_forward(const qsfm_params* p, void* workspace, size_t ws_byt
   if (p->metadata == nullptr) return QSFM_ERR_INVALID_ARG;
   st = resolve_ctas(*p, ctas);
   if (st != QSFM_OK) return st;
-  const int T = num_tokens(*p);
+  const int T = num_units(*p);
   if (split_mode(T, *ctas)) {
     if (workspace == nullptr || ws_bytes < qsfm::workspace_bytes(*ctas)) return QSFM_ERR_WORKSPACE;
     *ws = qsfm::workspace_view(workspace, *ctas);
@@ -180,7 +184,7 @@ qsfm_status qsfm_metadata(const qsfm_params* p, int32_t* metadata_out, void* str
   if (st != QSFM_OK) return st;
   int* fault = fault_ptr();
   if (fault == nullptr) return QSFM_ERR_CUDA;
-  const int T = num_tokens(*p);
+  const int T = num_units(*p);
   return cuda_status(qsfm::launch_plan(*p, T, ctas, split_mode(T, ctas), metadata_out, fault,
                                        static_cast<cudaStream_t>(stream)));
 }
@@ -192,7 +196,7 @@ qsfm_status qsfm_forward_workspace_size(const qsfm_params* p, size_t* bytes) {
   int ctas = 0;
   st = resolve_ctas(*p, &ctas);
   if (st != QSFM_OK) return st;
-  *bytes = split_mode(num_tokens(*p), ctas) ? qsfm::workspace_bytes(ctas) : 0;
+  *bytes = split_mode(num_units(*p), ctas) ? qsfm::workspace_bytes(ctas) : 0;
   return QSFM_OK;
 }
 
@@ -203,7 +207,7 @@ qsfm_status qsfm_attention(const qsfm_params* p, void* workspace, size_t workspa
   int* fault = nullptr;
   qsfm_status st = prepare_forward(p, workspace, workspace_bytes, &ctas, &ws, &fault);
   if (st != QSFM_OK) return st;
-  const int T = num_tokens(*p);
+  const int T = num_units(*p);
   if (T == 0) return QSFM_OK;
   return cuda_status(
       qsfm::launch_attention(*p, T, ctas, ws, fault, static_cast<cudaStream_t>(stream)));
@@ -216,7 +220,7 @@ qsfm_status qsfm_combine(const qsfm_params* p, void* workspace, size_t workspace
   int* fault = nullptr;
   qsfm_status st = prepare_forward(p, workspace, workspace_bytes, &ctas, &ws, &fault);
   if (st != QSFM_OK) return st;
-  const int T = num_tokens(*p);
+  const int T = num_units(*p);
   if (T == 0 || !split_mode(T, ctas)) return QSFM_OK;  // no token can be split
   return cuda_status(
       qsfm::launch_combine(*p, T, ctas, ws, fault, static_cast<cudaStream_t>(stream)));

@@ -234,17 +234,17 @@ __device__ void resolver_role(const qsfm_params& p, const Smem& sm, Range rg, in
       if (lane == 0) mbar_arrive(sm.bar(kBarRowsFull + slot));
       return;
     }
-    if (tok != last_tok) {
+    if (g.tok != last_tok) {
       // the next token's index list goes to L2 while this token is resolved
-      if (p.cmp_sparse_indices != nullptr && tok + 1 < T) {
-        const uint8_t* ix = reinterpret_cast<const uint8_t*>(p.cmp_sparse_indices + (size_t)(tok + 1) * p.k2);
+      if (p.cmp_sparse_indices != nullptr && g.tok + 1 < (T >> unit_shift(p))) {
+        const uint8_t* ix = reinterpret_cast<const uint8_t*>(p.cmp_sparse_indices + (size_t)(g.tok + 1) * p.k2);
         for (int off = 128 * lane; off < 4 * p.k2; off += 32 * 128) prefetch_l2(ix + off);
       }
-      last_tok = tok;
+      last_tok = g.tok;
     }
     const int cmp = k >= g.ori_tiles ? 1 : 0;
     int pr[2];
-    resolve_two(p, g, tok, k, lane, fault, pr);
+    resolve_two(p, g, k, lane, fault, pr);
     const uint8_t* pool = static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv);
     const float* spool = cmp ? p.cmp_scale : p.ori_scale;
 #pragma unroll
@@ -494,8 +494,6 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
   float* alpha = sm.f(kSAlpha);
   float* inv = sm.f(kSInv);
   float* red = sm.f(kSRed);
-  // this thread's head sink (log2 units), read once
-  const float sink2 = (tid < 64 && p.sinks != nullptr) ? __ldg(p.sinks + tid) * kLog2e : -INFINITY;
   PieceIter pieces(&p, rg, T);
   uint32_t n = 0, pieces_live = 0;
   int t, lo, hi;
@@ -504,6 +502,9 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
   int n_tiles = g.n_tiles;
   while (have) {
     const bool whole = (lo == 0 && hi == n_tiles);
+    // this thread's head sink (log2 units); the unit's heads start at unit_head0
+    const float sink2 =
+        (tid < 64 && p.sinks != nullptr) ? __ldg(p.sinks + unit_head0(p, t) + tid) * kLog2e : -INFINITY;
     const int slot = (t == rg.t0) ? 2 * c_idx : 2 * c_idx + 1;
     const bool writable = whole || slot < ws.slots;  // split pieces need the workspace
     if (!writable && tid == 0) atomicOr(fault, QSFM_FAULT_METADATA);
@@ -758,7 +759,7 @@ __device__ __noinline__ void warm_first_token(const qsfm_params& p, int T, int c
     bulk_prefetch_l2(static_cast<const uint8_t*>(p.q) + size_t(t) * kHeads * kDim * 2,
                      kHeads * kDim * 2);
   if (p.cmp_sparse_indices != nullptr && i < 32 && 32 * i < p.k2)
-    prefetch_l2(p.cmp_sparse_indices + size_t(t) * p.k2 + 32 * i);
+    prefetch_l2(p.cmp_sparse_indices + size_t(t >> unit_shift(p)) * p.k2 + 32 * i);
   const TokenGeom g = token_geom(p, t);
   int pos = -1;
   bool cmp = false;
@@ -768,7 +769,7 @@ __device__ __noinline__ void warm_first_token(const qsfm_params& p, int T, int c
     const int k = i - 2 * kTileRows;
     if (k < g.n_cmp) {
       cmp = true;
-      pos = p.cmp_sparse_indices != nullptr ? __ldg(p.cmp_sparse_indices + size_t(t) * p.k2 + k) : k;
+      pos = p.cmp_sparse_indices != nullptr ? __ldg(p.cmp_sparse_indices + size_t(g.tok) * p.k2 + k) : k;
       if (pos >= g.cmp_vis) pos = -1;
     }
   }

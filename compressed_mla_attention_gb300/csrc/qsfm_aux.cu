@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(kCombineThreads)
     // the parts: ranges [cut c, cut c + 1) for c = cb - 1, cb, ... whose end
     // lies past the token's start (split-mode cuts never start past a
     // token's last tile, so every such range holds tiles of t)
-    const float sk = p.sinks != nullptr ? __ldg(p.sinks + h) : -INFINITY;  // in flight with the lse loads
+    // in flight with the lse loads; t is a work unit (see unit_shift)
+    const float sk = p.sinks != nullptr ? __ldg(p.sinks + unit_head0(p, t) + h) : -INFINITY;
     const int c_begin = cb - 1;
     int c_end = cb;
     while (c_end < G && s_cut[2 * c_end] <= t) ++c_end;
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(128)
     if (threadIdx.x == 0) counts_out[i] = 0;
     return;
   }
-  const TokenGeom g = token_geom(p, t);
+  const TokenGeom g = token_geom(p, t << unit_shift(p));  // the token's first unit
   const int n_slots = g.n_ori + g.n_cmp;
   if (threadIdx.x == 0) counts_out[i] = n_slots;
   const int lim = min(n_slots, max_rows);
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(128)
       k = g.ori_tiles + cs / kTileRows;
       r = cs % kTileRows;
     }
-    const RowRef ref = resolve_slot(p, g, t, k, r, fault);
+    const RowRef ref = resolve_slot(p, g, k, r, fault);
     uint4* dst = reinterpret_cast<uint4*>(rows_out + (size_t(i) * max_rows + s) * kDim);
     float* dsc = scales_out + (size_t(i) * max_rows + s) * kScales;
     if (ref.row >= 0) {

@@ -37,6 +37,7 @@ constexpr int kMetaHeader = 8;
 struct TokenGeom {
   int b;          // batch of the token
   int s2;         // ori length S2 of the batch
+  int tok;        // query token of the unit
   int ori_lo;     // first ori row attended
   int n_ori;      // ori rows attended (contiguous from ori_lo)
   int n_cmp;      // cmp slots: CSA index entries scanned, HCA visible rows
@@ -48,6 +49,15 @@ struct TokenGeom {
 __device__ __forceinline__ int div_floor(int a, int b) {  // b > 0
   int q = a / b;
   return (a % b != 0 && a < 0) ? q - 1 : q;
+}
+
+// Work units: the 64-head groups of the query tokens (one per token for
+// N1 = 64, two for N1 = 128; the pages' N1 is 64 or 128). Unit u is token
+// u >> unit_shift, heads 64 (u & 1) .. + 63 for N1 = 128, and the flat head
+// rows of q, attn_out and softmax_lse of the unit are 64 u .. 64 u + 63.
+__device__ __forceinline__ int unit_shift(const qsfm_params& p) { return p.n1 == 128 ? 1 : 0; }
+__device__ __forceinline__ int unit_head0(const qsfm_params& p, int u) {
+  return p.n1 == 128 ? 64 * (u & 1) : 0;
 }
 
 // Batch, position in the batch's chunk and chunk length of query token t.
@@ -72,8 +82,11 @@ __device__ __forceinline__ void token_batch(const qsfm_params& p, int t, int& b,
 
 // Not inlined: called once per token / tile, and every inlined copy would
 // grow the instruction footprint of the hot loops around it.
-static __device__ __noinline__ TokenGeom token_geom(const qsfm_params& p, int t) {
+// Geometry of work unit u (its token's rows; see unit_shift).
+static __device__ __noinline__ TokenGeom token_geom(const qsfm_params& p, int u) {
   TokenGeom g;
+  const int t = u >> unit_shift(p);
+  g.tok = t;
   int s, s1;
   token_batch(p, t, g.b, s, s1);
   // every per-batch / per-token length this token may need, loaded together
@@ -129,8 +142,8 @@ struct RowRef {
 // Row for slot `i` of tile `k` of token t. Slots past the token's rows, -1
 // or invisible CSA entries resolve to row = -1. Bad block ids set a fault
 // bit and also resolve to -1 (the row is skipped, never read).
-static __device__ __noinline__ RowRef resolve_slot(const qsfm_params& p, const TokenGeom& g, int t,
-                                            int k, int i, int* fault) {
+static __device__ __noinline__ RowRef resolve_slot(const qsfm_params& p, const TokenGeom& g, int k,
+                                                   int i, int* fault) {
   RowRef r{nullptr, nullptr, -1, 0};
   int row;
   const uint8_t* pool;
@@ -147,7 +160,7 @@ static __device__ __noinline__ RowRef resolve_slot(const qsfm_params& p, const T
     const int slot = (k - g.ori_tiles) * kTileRows + i;
     if (slot >= g.n_cmp) return r;
     if (p.cmp_sparse_indices != nullptr) {
-      row = __ldg(p.cmp_sparse_indices + (size_t)t * p.k2 + slot);
+      row = __ldg(p.cmp_sparse_indices + (size_t)g.tok * p.k2 + slot);
       if (row < 0 || row >= g.cmp_vis) return r;
     } else {
       row = slot;
@@ -174,10 +187,11 @@ static __device__ __noinline__ RowRef resolve_slot(const qsfm_params& p, const T
 }
 
 // Physical rows (block * kBlock + offset; -1 when masked) of slots i0 and
-// i0 + 32 of tile k of token t, by the rules of resolve_slot, with the index
-// loads of both slots in flight together and then their block-table loads.
-__device__ __forceinline__ void resolve_two(const qsfm_params& p, const TokenGeom& g, int t, int k,
-                                            int i0, int* fault, int (&prow)[2]) {
+// i0 + 32 of tile k of the unit g, by the rules of resolve_slot, with the
+// index loads of both slots in flight together and then their block-table
+// loads.
+__device__ __forceinline__ void resolve_two(const qsfm_params& p, const TokenGeom& g, int k, int i0,
+                                            int* fault, int (&prow)[2]) {
   const bool ori = k < g.ori_tiles;
   const int base = (ori ? k : k - g.ori_tiles) * kTileRows + i0;
   const int n = ori ? g.n_ori : g.n_cmp;
@@ -192,7 +206,7 @@ __device__ __forceinline__ void resolve_two(const qsfm_params& p, const TokenGeo
   if (!ori && p.cmp_sparse_indices != nullptr) {
 #pragma unroll
     for (int u = 0; u < 2; ++u)
-      if (ok[u]) row[u] = __ldg(p.cmp_sparse_indices + (size_t)t * p.k2 + base + 32 * u);
+      if (ok[u]) row[u] = __ldg(p.cmp_sparse_indices + (size_t)g.tok * p.k2 + base + 32 * u);
 #pragma unroll
     for (int u = 0; u < 2; ++u) ok[u] = ok[u] && row[u] >= 0 && row[u] < g.cmp_vis;
   }

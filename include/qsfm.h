@@ -89,7 +89,7 @@ extern "C" {
 typedef enum {
   QSFM_OK = 0,
   QSFM_ERR_INVALID_ARG = 1,  /* a constraint of the op is violated        */
-  QSFM_ERR_UNSUPPORTED = 2,  /* valid for the op but not built (n1 != 64) */
+  QSFM_ERR_UNSUPPORTED = 2,  /* valid for the op but not built             */
   QSFM_ERR_CUDA = 3,         /* a CUDA runtime call failed                */
   QSFM_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than required   */
   QSFM_ERR_DEVICE_FAULT = 5, /* the device fault word is non-zero         */
@@ -118,7 +118,7 @@ typedef struct qsfm_params {
   int32_t batch;          /* B                                               */
   int32_t max_s1;         /* BSND: S1. TND: unused                           */
   int32_t total_t;        /* TND: T1 (= q.shape[0]). BSND: unused            */
-  int32_t n1;             /* query heads; only 64 is built                   */
+  int32_t n1;             /* query heads: 64 or 128 (the pages allow both)   */
   int32_t d;              /* head dim; must be 512                           */
   int32_t k2;             /* index row length K2 (CSA); 0 otherwise          */
   int32_t ori_block_size; /* tokens per ori block; only 128 is built         */
@@ -128,9 +128,11 @@ typedef struct qsfm_params {
   int32_t ori_num_blocks; /* physical blocks in the ori pool                 */
   int32_t cmp_num_blocks; /* physical blocks in the cmp pool                 */
   int32_t num_ctas;       /* most CTAs the work is planned over; 0 = SM
-                             count. With T >= num_ctas tokens the plan uses
-                             ceil(T / ceil(T / num_ctas)) CTAs, the fewest
-                             that keep the same tokens per CTA              */
+                             count. The plan's units are the 64-head groups
+                             of the tokens (U = T * n1 / 64). With U >=
+                             num_ctas the plan uses ceil(U / ceil(U /
+                             num_ctas)) CTAs, the fewest that keep the same
+                             units per CTA                                  */
   /* inputs (device) */
   const void* q;
   const void* ori_kv;

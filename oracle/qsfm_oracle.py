@@ -177,7 +177,7 @@ def gather_paged(kv_pool, scale_pool, table_row, rows):
 # KvQuantSparseAttnSharedKv parameter table row softmax_lse).
 # --------------------------------------------------------------------------
 def attend(q: np.ndarray, k: np.ndarray, softmax_scale: float, sinks):
-    """O[64, 512] and lse[64] of one token over its rows k [n, 512] (fp64).
+    """O[N1, 512] and lse[N1] of one token over its rows k [n, 512] (fp64).
 
     x = softmax_scale * q k^T; m = max(max_j x_j, sink_h);
     O = sum_j e^{x_j - m} k_j / (sum_j e^{x_j - m} + e^{sink_h - m});
@@ -214,20 +214,21 @@ def token_kv(w, t: int, b: int, s: int):
 
 
 def q_fp64(w, t: int) -> np.ndarray:
-    """Query of token t as fp64 [64, 512] (bf16 -> fp32 -> fp64 is exact)."""
+    """Query of token t as fp64 [N1, 512] (bf16 -> fp32 -> fp64 is exact)."""
     return w.q[t].float().numpy().astype(np.float64)
 
 
 def reference(w, tokens=None):
-    """O (fp64 [n, 64, 512]) and lse (fp64 [n, 64]) for the given tokens.
+    """O (fp64 [n, N1, 512]) and lse (fp64 [n, N1]) for the given tokens.
 
     tokens: iterable of query-token indices; default all tokens.
     """
     tokens = range(w.total_t) if tokens is None else tokens
     tokens = list(tokens)
     tb, tp = w.token_batch(), w.token_pos()
-    out = np.zeros((len(tokens), NUM_HEADS, HEAD_DIM))
-    lse = np.full((len(tokens), NUM_HEADS), -np.inf)
+    nh = int(w.q.shape[1])  # N1: 64 or 128
+    out = np.zeros((len(tokens), nh, HEAD_DIM))
+    lse = np.full((len(tokens), nh), -np.inf)
     sinks = None if w.sinks is None else np.asarray(w.sinks, dtype=np.float64)
     for i, t in enumerate(tokens):
         k = token_kv(w, t, int(tb[t]), int(tp[t]))
@@ -277,8 +278,9 @@ def reference_parallel(w, tokens, processes: int):
             res = pool.map(_reference_chunk, chunks)
     finally:
         _FORK_WORKLOAD = None
-    out = np.zeros((len(tokens), NUM_HEADS, HEAD_DIM))
-    lse = np.zeros((len(tokens), NUM_HEADS))
+    nh = int(w.q.shape[1])
+    out = np.zeros((len(tokens), nh, HEAD_DIM))
+    lse = np.zeros((len(tokens), nh))
     for i, (o, l) in enumerate(res):
         out[i::processes] = o
         lse[i::processes] = l

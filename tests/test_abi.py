@@ -91,7 +91,7 @@ def _status(lib, p, fn="qsfm_forward"):
 
 INVALID = [
     ("d != 512", dict(d=256), 1),
-    ("n1 = 128 is valid but not built", dict(n1=128), 2),
+    ("n1 = 96 is not built (the pages allow 64 and 128)", dict(n1=96), 2),
     ("n1 = 0", dict(n1=0), 1),
     ("block size 64 not built", dict(ori_block_size=64), 2),
     ("block size 2048 invalid", dict(ori_block_size=2048), 1),
@@ -159,6 +159,12 @@ def test_workspace_size_depends_on_split(lib):
     p.batch, p.max_s1 = 64, 1  # 64 tokens >= 8 CTAs: no split, no workspace
     assert lib.qsfm_forward_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
     assert n.value == 0
+
+
+def test_n1_128_passes_validation(lib):
+    p = _valid(lib)
+    p.n1 = 128
+    assert _status(lib, p) == 4  # valid; stops at the missing workspace (4 units < 8 CTAs split)
 
 
 def test_word_aligned_pointers_pass_validation(lib):

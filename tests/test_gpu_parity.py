@@ -117,6 +117,29 @@ EDGE = {
 }
 
 
+# the pages' other shapes: N1 = 128 heads (two 64-head units per token) and
+# K2 = 1024 index entries
+WIDE = {
+    "n1_128_csa_decode": dict(layout="BSND", q_lens=[2] * 6, s2=[5000, 9000, 700, 20000, 4096, 3000],
+                              cmp_ratio=4, mode="CSA", k2=512, n1=128),
+    "n1_128_split": dict(layout="BSND", q_lens=[1], s2=[9000], cmp_ratio=4, mode="CSA", k2=512, n1=128),
+    "n1_128_hca_tnd": dict(layout="TND", q_lens=[3, 5], s2=[3000, 40000], cmp_ratio=128, mode="HCA", n1=128),
+    "k2_1024": dict(layout="BSND", q_lens=[2] * 4, s2=[8000, 30000, 5000, 12000], cmp_ratio=4, mode="CSA",
+                    k2=1024),
+    "n1_128_k2_1024": dict(layout="BSND", q_lens=[2, 2], s2=[20000, 9000], cmp_ratio=4, mode="CSA", k2=1024,
+                           n1=128),
+}
+
+
+@pytest.mark.parametrize("name", sorted(WIDE))
+@pytest.mark.parametrize("ctas", [0, 5])
+def test_wide_shape_parity(cuda_device, name, ctas):
+    w = W.build(name, seed=zlib.crc32(name.encode()) % 1000, return_lse=True, **WIDE[name])
+    out, lse = run_gpu(w, cuda_device, num_ctas=ctas)
+    assert out.shape[1] == w.q.shape[1]
+    assert_parity(out, lse, w, range(w.total_t))
+
+
 @pytest.mark.parametrize("name", sorted(EDGE))
 @pytest.mark.parametrize("ctas", [0, 3])
 def test_edge_case_parity(cuda_device, name, ctas):

@@ -127,6 +127,18 @@ def test_oracle_matches_brute_force(i):
     assert np.all(l_ref[~fin] == -np.inf)
 
 
+def test_oracle_matches_brute_force_128_heads():
+    """N1 = 128 (the pages allow 64 and 128): same definition per head."""
+    w = W.build("h128", layout="BSND", q_lens=[2, 2], s2=[80, 150], cmp_ratio=4, mode="CSA", k2=16,
+                block_size=16, ori_win_left=20, n1=128, seed=31)
+    assert tuple(w.q.shape[1:]) == (128, 512) and tuple(w.sinks.shape) == (128,)
+    o_ref, l_ref = O.reference(w)
+    o_bf, l_bf = brute_force(w)
+    assert o_ref.shape == (4, 128, 512)
+    assert np.allclose(o_ref, o_bf.numpy(), rtol=1e-12, atol=1e-13)
+    assert np.allclose(l_ref, l_bf.numpy(), rtol=1e-12)
+
+
 def test_brute_force_sees_duplicate_indices_as_multiset():
     w = W.build("dup", layout="BSND", q_lens=[1], s2=[64], cmp_ratio=4, mode="CSA", k2=8,
                 block_size=16, seed=7)

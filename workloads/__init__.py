@@ -59,7 +59,7 @@ class Workload:
     max_s1: int  # BSND: S1; TND: max chunk length
     q_lens: np.ndarray  # int64 [B]: query tokens per batch
     cu_seqlens_q: Optional[torch.Tensor]  # int32 [B+1] (TND)
-    q: torch.Tensor  # bf16 [T, 64, 512] (BSND memory is identical)
+    q: torch.Tensor  # bf16 [T, N1, 512], N1 = 64 or 128 (BSND memory is identical)
     ori_kv: torch.Tensor  # uint8 [nb, 128, 1, 512]
     ori_scale: torch.Tensor  # fp32 [nb, 128, 1, 8]
     ori_block_table: torch.Tensor  # int32 [B, wo]
@@ -180,6 +180,7 @@ def build(
     seqused_q: Optional[list] = None,
     q_scale: float = 1.0,
     block_size: int = BLOCK,
+    n1: int = NUM_HEADS,
 ) -> Workload:
     """Build one workload. q_lens / s2 are per-batch query and ori lengths."""
     gen = torch.Generator().manual_seed(seed)
@@ -188,9 +189,9 @@ def build(
     B = len(q_lens)
     assert len(s2) == B
     T = int(q_lens.sum())
-    q = (torch.randn(T, NUM_HEADS, HEAD_DIM, generator=gen) * q_scale).to(torch.bfloat16)
+    q = (torch.randn(T, n1, HEAD_DIM, generator=gen) * q_scale).to(torch.bfloat16)
     ori_kv, ori_scale, ori_table = _paged_pool(s2, gen, block=block_size)
-    sink = torch.randn(NUM_HEADS, generator=gen, dtype=torch.float32) if sinks else None
+    sink = torch.randn(n1, generator=gen, dtype=torch.float32) if sinks else None
     cu = None
     if layout == "TND":
         cu = torch.zeros(B + 1, dtype=torch.int32)
