@@ -24,6 +24,9 @@ METADATA_INTS = 1024
 MAX_CTAS = 256
 LAYOUT_BSND = 0
 LAYOUT_TND = 1
+KV_FP8_FP32_SCALES = 0
+KV_PACKED640 = 1
+PACKED_ROW_BYTES = 640
 
 STATUS = {
     0: "QSFM_OK",
@@ -62,6 +65,7 @@ class QsfmParams(ctypes.Structure):
         ("cmp_mask_mode", _i32), ("ori_win_left", _i32), ("ori_win_right", _i32),
         ("layout_q", _i32), ("return_lse", _i32),
         ("attn_out", _ptr), ("softmax_lse", _ptr),
+        ("kv_layout", _i32),
     ]
 
 
@@ -162,7 +166,8 @@ def make_params(
 
     q / attn_out: BSND [B, S1, N1, 512] or TND [T1, N1, 512] bf16, N1 = 64 or 128.
     Paged KV: [blocks, 128, 1, 512] uint8 (fp8 e4m3fn bytes) with fp32 scales
-    [blocks, 128, 1, 8]; block tables int32 [B, width].
+    [blocks, 128, 1, 8], or packed [blocks, 128, 1, 640] uint8 rows (bf16 rope,
+    e4m3fn nope, e8m0 scales; scales None); block tables int32 [B, width].
     """
     p = QsfmParams()
     lib().qsfm_params_init(ctypes.byref(p))
@@ -185,6 +190,8 @@ def make_params(
         raise ValueError(layout)
     p.n1, p.d = int(q.shape[-2]), int(q.shape[-1])
     p.k2 = int(cmp_sparse_indices.shape[-1]) if cmp_sparse_indices is not None else 0
+    # packed 640-byte rows (bf16 rope, e4m3 nope, e8m0 scales) or fp8 rows + fp32 scales
+    p.kv_layout = KV_PACKED640 if int(ori_kv.shape[-1]) == PACKED_ROW_BYTES else KV_FP8_FP32_SCALES
     p.ori_block_size = int(ori_kv.shape[1])
     p.ori_max_blocks = int(ori_block_table.shape[-1])
     p.ori_num_blocks = int(ori_kv.shape[0])

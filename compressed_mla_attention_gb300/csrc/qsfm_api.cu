@@ -89,7 +89,12 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   // paged ori KV is always present
   if (p.ori_block_size < 1 || p.ori_block_size > 1024) return QSFM_ERR_INVALID_ARG;
   if (p.ori_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
-  if (p.ori_kv == nullptr || p.ori_scale == nullptr || p.ori_block_table == nullptr ||
+  if (p.kv_layout != QSFM_KV_FP8_FP32_SCALES && p.kv_layout != QSFM_KV_PACKED640)
+    return QSFM_ERR_INVALID_ARG;
+  const bool packed = p.kv_layout == QSFM_KV_PACKED640;
+  // scales are in the packed rows; separate scale tensors with them are a mistake
+  if (packed && (p.ori_scale != nullptr || p.cmp_scale != nullptr)) return QSFM_ERR_INVALID_ARG;
+  if (p.ori_kv == nullptr || (!packed && p.ori_scale == nullptr) || p.ori_block_table == nullptr ||
       p.seqused_ori_kv == nullptr)
     return QSFM_ERR_INVALID_ARG;
   if (p.ori_max_blocks < 1 || p.ori_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
@@ -100,7 +105,7 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   } else {
     if (p.cmp_block_size < 1 || p.cmp_block_size > 1024) return QSFM_ERR_INVALID_ARG;
     if (p.cmp_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
-    if (p.cmp_scale == nullptr || p.cmp_block_table == nullptr) return QSFM_ERR_INVALID_ARG;
+    if ((!packed && p.cmp_scale == nullptr) || p.cmp_block_table == nullptr) return QSFM_ERR_INVALID_ARG;
     if (p.cmp_max_blocks < 1 || p.cmp_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
     if (p.cmp_sparse_indices != nullptr && p.k2 < 1) return QSFM_ERR_INVALID_ARG;
   }
@@ -238,6 +243,7 @@ qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens, int32
                               int32_t* row_ids_out, int32_t* counts_out, void* stream) {
   qsfm_status st = validate(p, false);
   if (st != QSFM_OK) return st;
+  if (p->kv_layout != QSFM_KV_FP8_FP32_SCALES) return QSFM_ERR_UNSUPPORTED;  // exports 512-B rows + scales
   if (n < 0 || max_rows < 0) return QSFM_ERR_INVALID_ARG;
   if (n == 0) return QSFM_OK;
   if (tokens == nullptr || counts_out == nullptr) return QSFM_ERR_INVALID_ARG;

@@ -217,6 +217,7 @@ __device__ __forceinline__ bool warp_wait_or_abort(const Smem& sm, int bar, uint
 // Tile n's rows go to ring slot n % kRing: 64 physical rows (block * 128 +
 // offset, -1 = masked) and the pool they come from. After the CTA's last tile
 // the resolver writes an end mark (-1) in the next slot.
+template <int kFmt>
 __device__ void resolver_role(const qsfm_params& p, const Smem& sm, Range rg, int T, int* fault) {
   const int lane = threadIdx.x & 31;
   int* rows = reinterpret_cast<int*>(sm.ptr + kSRows);
@@ -251,10 +252,16 @@ __device__ void resolver_role(const qsfm_params& p, const Smem& sm, Range rg, in
     for (int u = 0; u < 2; ++u) {
       rows[slot * kTileRows + lane + 32 * u] = pr[u];
       if (pr[u] >= 0) {
-        const uint8_t* src = pool + size_t(pr[u]) * kDim;
+        if constexpr (kFmt == QSFM_KV_PACKED640) {
+          const uint8_t* src = pool + size_t(pr[u]) * QSFM_PACKED_ROW_BYTES;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) prefetch_l2(src + 128 * c);
-        prefetch_l2(spool + size_t(pr[u]) * kScales);
+          for (int c = 0; c < 5; ++c) prefetch_l2(src + 128 * c);
+        } else {
+          const uint8_t* src = pool + size_t(pr[u]) * kDim;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) prefetch_l2(src + 128 * c);
+          prefetch_l2(spool + size_t(pr[u]) * kScales);
+        }
       }
     }
     if (lane == 0) kind[slot] = cmp;
@@ -342,6 +349,109 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, int* fault) 
         const uint32_t c0 = 2 * (j & 3);
         sts_v4(rowb + (((c0 + odd_first) ^ sw) << 4), odd_first ? D[c][u][1] : D[c][u][0]);
         sts_v4(rowb + (((c0 + 1 - odd_first) ^ sw) << 4), odd_first ? D[c][u][0] : D[c][u][1]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(kBarKvFull + 4 * st + c));
+    }
+  }
+}
+
+// Producers for packed 640-byte rows (bf16 rope, bytes 0..127 | e4m3fn nope,
+// bytes 128..575 | e8m0 scales, bytes 576..582 | pad; KvQuantSparseAttnSharedKv
+// constraints). The tile in shared memory is the same as for fp8 rows: d 0..63
+// (d-block 0) is the rope, d 64..511 the nope. Thread (row_lo, j): rows
+// row_lo and row_lo + 32; of each row the 16-byte pieces j (rope elements
+// 8j .. 8j + 7, copied as they are) and 8 + m for m = 8i + j, i = 0..3
+// (nope elements 16m .. 16m + 15 of d-block 1 + m / 4 with scale m / 4;
+// i = 3 only for j < 4). Lane j = 4 of each row also loads the piece with
+// the seven scale bytes. Nope piece m lands in chunk (1 + 2i + j / 4) / 2:
+// chunk i for j < 4, chunk i + 1 for j >= 4. The loads of a tile are issued
+// after the previous tile is stored (the registers hold one tile).
+__device__ __forceinline__ float e8m0_value(uint32_t e) {
+  // 2^(e - 127): the fp32 with biased exponent e (e = 0: the subnormal 2^-127)
+  return e == 0xFFu ? __uint_as_float(0x7FC00000u) : e == 0u ? __uint_as_float(0x00400000u)
+                                                             : __uint_as_float(e << 23);
+}
+
+__device__ void producer_role_packed(const qsfm_params& p, const Smem& sm, int* fault) {
+  const int ptid = threadIdx.x - kSoftThreads;  // 0..255 (8 producer warps)
+  const int lane = threadIdx.x & 31;
+  const int row_lo = ptid >> 3;  // 0..31
+  const int j = ptid & 7;
+  const int odd_first = j >> 2;  // j >= 4 stores its odd 16-B unit first (no bank conflicts)
+  const int* rows = reinterpret_cast<const int*>(sm.ptr + kSRows);
+  const int* kind = reinterpret_cast<const int*>(sm.ptr + kSRowKind);
+  constexpr int kRow = QSFM_PACKED_ROW_BYTES;
+
+  int pr[2];
+  uint4 Rr[2];     // rope piece j of each row (bf16)
+  uint4 Rn[4][2];  // nope pieces m = 8i + j (e4m3fn)
+  uint4 Rs[2];     // scale piece (lane j = 4 only)
+
+  auto fetch = [&](uint32_t n) -> bool {
+    const uint32_t slot = n % kRing;
+    if (!warp_wait_or_abort(sm, kBarRowsFull + slot, (n / kRing) & 1, fault)) return false;
+    const int kd = kind[slot];
+    pr[0] = rows[slot * kTileRows + row_lo];
+    pr[1] = rows[slot * kTileRows + row_lo + 32];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(kBarRowsEmpty + slot));
+    if (kd < 0) return false;
+    const uint8_t* pool = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv);
+    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const bool v = pr[u] >= 0;
+      const uint8_t* base = pool + size_t(v ? pr[u] : 0) * kRow;
+      Rr[u] = v ? ldg_stream_v4(base + 16 * j) : z;
+#pragma unroll
+      for (int i = 0; i < 3; ++i) Rn[i][u] = v ? ldg_stream_v4(base + 128 + 16 * (8 * i + j)) : z;
+      Rn[3][u] = (v && j < 4) ? ldg_stream_v4(base + 128 + 16 * (24 + j)) : z;
+      Rs[u] = (v && j == 4) ? ldg_stream_v4(base + 576) : z;
+    }
+    return true;
+  };
+
+  for (uint32_t n = 0; fetch(n); ++n) {
+    const uint32_t st = n & 1;
+    uint4 D[4][2][2];  // [i][row][16-byte half] of nope piece 8i + j, bf16
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t w0 = __shfl_sync(0xffffffffu, Rs[u].x, (lane & ~7) | 4);  // scale bytes 0..3
+      const uint32_t w1 = __shfl_sync(0xffffffffu, Rs[u].y, (lane & ~7) | 4);  // scale bytes 4..6
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int sidx = 2 * i + (j >> 2);  // scale of nope piece 8i + j
+        const uint32_t e = (sidx < 4 ? w0 >> (8 * sidx) : w1 >> (8 * (sidx - 4))) & 0xFFu;
+        dequant16(Rn[i][u], e8m0_value(e), D[i][u][0], D[i][u][1]);
+      }
+    }
+    if (!warp_wait_or_abort(sm, kBarKvEmpty + st, ((n >> 1) & 1) ^ 1, fault)) return;
+    const uint32_t stage = sm.base + kSK + st * kStageBytes;
+    if (j == 0) {
+      int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + st * kTileRows;
+      valid[row_lo] = pr[0] >= 0;
+      valid[row_lo + 32] = pr[1] >= 0;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int r = row_lo + 32 * u;
+        const uint32_t sw = uint32_t(r & 7);
+        if (c == 0) sts_v4(stage + r * 128 + ((uint32_t(j) ^ sw) << 4), Rr[u]);  // rope: d-block 0
+        // nope piece of this chunk: i = c (j < 4) or i = c - 1 (j >= 4)
+        const bool has = j < 4 || (c >= 1);
+        if (has) {
+          const uint4 lo = (j < 4) ? D[c][u][0] : D[c > 0 ? c - 1 : 0][u][0];
+          const uint4 hi = (j < 4) ? D[c][u][1] : D[c > 0 ? c - 1 : 0][u][1];
+          const int db = 1 + 2 * ((j < 4) ? c : c - 1) + (j >> 2);
+          const uint32_t rowb = stage + db * kDBlockBytes + r * 128;
+          const uint32_t c0 = 2 * (j & 3);
+          sts_v4(rowb + (((c0 + odd_first) ^ sw) << 4), odd_first ? hi : lo);
+          sts_v4(rowb + (((c0 + 1 - odd_first) ^ sw) << 4), odd_first ? lo : hi);
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -752,6 +862,7 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
 // tiles. Only prefetches, so a wrong guess costs bandwidth, never results;
 // each address is checked against its buffer first. Thread i of the
 // producer warps takes ori slot i (i < 128) or cmp slot i - 128.
+template <int kFmt>
 __device__ __noinline__ void warm_first_token(const qsfm_params& p, int T, int c, int G, int i) {
   const int t = int((long long)c * T / G);
   if (t >= T) return;
@@ -780,10 +891,16 @@ __device__ __noinline__ void warm_first_token(const qsfm_params& p, int T, int c
   const int blk = __ldg((cmp ? p.cmp_block_table : p.ori_block_table) + size_t(g.b) * width + col);
   if (blk < 0 || blk >= (cmp ? p.cmp_num_blocks : p.ori_num_blocks)) return;
   const size_t row = size_t(blk) * kBlock + pos % kBlock;
-  bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * kDim, kDim);
-  prefetch_l2((cmp ? p.cmp_scale : p.ori_scale) + row * kScales);
+  if constexpr (kFmt == QSFM_KV_PACKED640) {
+    bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * QSFM_PACKED_ROW_BYTES,
+                     QSFM_PACKED_ROW_BYTES);
+  } else {
+    bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * kDim, kDim);
+    prefetch_l2((cmp ? p.cmp_scale : p.ori_scale) + row * kScales);
+  }
 }
 
+template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const qsfm_params p, const int T, const Workspace ws, int* fault,
                      const __grid_constant__ CUtensorMap qmap) {
@@ -795,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp >= kSoftWarps && warp < kSoftWarps + kProdWarps)
-    warm_first_token(p, T, blockIdx.x, gridDim.x, tid - kSoftThreads);
+    warm_first_token<kFmt>(p, T, blockIdx.x, gridDim.x, tid - kSoftThreads);
   grid_dependency_wait();   // the plan (and every input) is written by now
   grid_launch_dependents();  // the combine kernel may take SMs as CTAs finish
   const int* meta = p.metadata;
@@ -846,13 +963,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kSoftWarps) {
     softmax_role(p, sm, rg, T, tmem, ws, c, fault);
   } else if (warp < kMmaWarp) {
-    producer_role(p, sm, fault);
+    if constexpr (kFmt == QSFM_KV_PACKED640)
+      producer_role_packed(p, sm, fault);
+    else
+      producer_role(p, sm, fault);
   } else if (warp == kMmaWarp) {
     qk_role(p, sm, rg, T, tmem, &qmap, fault);
   } else if (warp == kPvWarp) {
     pv_role(p, sm, rg, T, tmem, fault);
   } else {
-    resolver_role(p, sm, rg, T, fault);
+    resolver_role<kFmt>(p, sm, rg, T, fault);
   }
 
   tc_fence_before();
@@ -892,14 +1012,16 @@ cudaError_t make_q_map(const void* q, int T, CUtensorMap* map) {
 
 cudaError_t launch_attention(const qsfm_params& p, int num_tokens, int num_ctas,
                              const Workspace& ws, int* fault, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(attention_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  // one instantiation per KV row format, so neither pays for the other
+  const bool packed = p.kv_layout == QSFM_KV_PACKED640;
+  auto* kernel = packed ? attention_kernel<QSFM_KV_PACKED640> : attention_kernel<QSFM_KV_FP8_FP32_SCALES>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e != cudaSuccess) return e;
   CUtensorMap qmap;
   e = make_q_map(p.q, num_tokens, &qmap);
   if (e != cudaSuccess) return e;
-  return launch_after_predecessor(attention_kernel, dim3(num_ctas), dim3(kThreads), kSmemAlloc, s, p,
-                                  num_tokens, ws, fault, qmap);
+  return launch_after_predecessor(kernel, dim3(num_ctas), dim3(kThreads), kSmemAlloc, s, p, num_tokens,
+                                  ws, fault, qmap);
 }
 
 }  // namespace qsfm

@@ -78,13 +78,27 @@
 extern "C" {
 #endif
 
-#define QSFM_ABI_VERSION 1
+#define QSFM_ABI_VERSION 2
 #define QSFM_NUM_HEADS 64
 #define QSFM_HEAD_DIM 512
 #define QSFM_BLOCK_SIZE 128
 #define QSFM_SCALES_PER_ROW 8
 #define QSFM_METADATA_INTS 1024
 #define QSFM_MAX_CTAS 256
+#define QSFM_PACKED_ROW_BYTES 640
+
+/* KV row formats (qsfm_params.kv_layout). */
+typedef enum {
+  /* fp8 e4m3fn rows [blocks, 128, 1, 512] with fp32 scale tensors
+   * [blocks, 128, 1, 8], one scale per 64 elements (the default). */
+  QSFM_KV_FP8_FP32_SCALES = 0,
+  /* Packed 640-byte rows [blocks, 128, 1, 640] (KvQuantSparseAttnSharedKv
+   * constraints): bf16 rope (64 elements, bytes 0..127), e4m3fn nope (448
+   * elements, bytes 128..575), e8m0 scales (7, one per 64 nope elements,
+   * bytes 576..582), zero padding to 640. The 512 elements of a row are
+   * rope then nope; ori_scale and cmp_scale must be NULL. */
+  QSFM_KV_PACKED640 = 1
+} qsfm_kv_layout;
 
 typedef enum {
   QSFM_OK = 0,
@@ -162,6 +176,8 @@ typedef struct qsfm_params {
   /* outputs (device) */
   void* attn_out;
   float* softmax_lse;
+  /* appended in ABI version 2 */
+  int32_t kv_layout;      /* qsfm_kv_layout of ori_kv and cmp_kv (both)      */
 } qsfm_params;
 
 /* Fill *p with the defaults of the op: n1 64, d 512, block size 128,
@@ -241,6 +257,7 @@ qsfm_status qsfm_forward_noalloc(const qsfm_params* p, void* stream);
  *                                         slot that is masked out
  *   counts_out  int32 [n]                 number of slots of the token
  * Masked slots get zero bytes and zero scales. All buffers are device memory.
+ * Only for kv_layout QSFM_KV_FP8_FP32_SCALES (QSFM_ERR_UNSUPPORTED otherwise).
  */
 qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens,
                               int32_t n, int32_t max_rows, uint8_t* rows_out,

@@ -78,6 +78,34 @@ def decode_e4m3fn_code(code: int) -> float:
 E4M3FN_TABLE = np.array([decode_e4m3fn_code(c) for c in range(256)], dtype=np.float64)
 
 
+def decode_e8m0_code(code: int) -> float:
+    """Value of one e8m0 (float8_e8m0fnu) byte: 2^(code - 127); 0xFF is NaN."""
+    return math.nan if code == 0xFF else 2.0 ** (code - 127)
+
+
+E8M0_TABLE = np.array([decode_e8m0_code(c) for c in range(256)], dtype=np.float64)
+ROPE_DIM = 64
+PACKED_ROW = 640
+
+
+def dequant_packed_rows(rows: np.ndarray) -> np.ndarray:
+    """K~ of packed 640-byte rows [n, 640] -> fp64 [n, 512], exactly.
+
+    KvQuantSparseAttnSharedKv constraints: a row is kv_rope (64 bf16,
+    bytes 0..127), kv_nope (448 e4m3fn, bytes 128..575) and the nope scales
+    (7 e8m0, bytes 576..582, one per 64 nope elements), padded to 640 bytes.
+    The 512 elements are rope then nope (R12).
+    """
+    rows = np.ascontiguousarray(rows)
+    n = rows.shape[0]
+    bits = rows[:, :2 * ROPE_DIM].copy().view("<u2").astype(np.uint32) << 16
+    rope = bits.view(np.float32).astype(np.float64)
+    nope_end = 2 * ROPE_DIM + (HEAD_DIM - ROPE_DIM)
+    nope = E4M3FN_TABLE[rows[:, 2 * ROPE_DIM:nope_end].astype(np.int64)]
+    scales = E8M0_TABLE[rows[:, nope_end:nope_end + (HEAD_DIM - ROPE_DIM) // TILE].astype(np.int64)]
+    return np.concatenate([rope, nope * np.repeat(scales, TILE, axis=1)], axis=1).reshape(n, HEAD_DIM)
+
+
 def dequant_rows(kv_bytes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     """K~[j, d] = e4m3fn(kv[j, d]) * scale[j, d // 64], exactly, in fp64.
 
@@ -162,13 +190,22 @@ def gather_paged(kv_pool, scale_pool, table_row, rows):
     """
     bs = kv_pool.shape[1]
     n = len(rows)
-    out_b = np.zeros((n, HEAD_DIM), dtype=np.uint8)
-    out_s = np.zeros((n, HEAD_DIM // TILE), dtype=np.float32)
+    out_b = np.zeros((n, kv_pool.shape[-1]), dtype=np.uint8)
+    out_s = None if scale_pool is None else np.zeros((n, HEAD_DIM // TILE), dtype=np.float32)
     for i, j in enumerate(rows):
         blk = int(table_row[j // bs])
         out_b[i] = kv_pool[blk, j % bs, 0]
-        out_s[i] = scale_pool[blk, j % bs, 0]
+        if out_s is not None:
+            out_s[i] = scale_pool[blk, j % bs, 0]
     return out_b, out_s
+
+
+def decode_rows(kv_bytes: np.ndarray, scales) -> np.ndarray:
+    """K~ of gathered rows: packed 640-byte rows carry their scales; 512-byte
+    fp8 rows come with a separate fp32 scale row."""
+    if kv_bytes.shape[-1] == PACKED_ROW:
+        return dequant_packed_rows(kv_bytes)
+    return dequant_rows(kv_bytes, scales)
 
 
 # --------------------------------------------------------------------------
@@ -203,13 +240,13 @@ def token_kv(w, t: int, b: int, s: int):
     if ori is None:
         return None
     parts = []
-    ob, os_ = gather_paged(np.asarray(w.ori_kv), np.asarray(w.ori_scale),
+    ob, os_ = gather_paged(np.asarray(w.ori_kv), None if w.ori_scale is None else np.asarray(w.ori_scale),
                            np.asarray(w.ori_block_table[b]), ori)
-    parts.append(dequant_rows(ob, os_))
+    parts.append(decode_rows(ob, os_))
     if cmp_rows:
-        cb, cs = gather_paged(np.asarray(w.cmp_kv), np.asarray(w.cmp_scale),
+        cb, cs = gather_paged(np.asarray(w.cmp_kv), None if w.cmp_scale is None else np.asarray(w.cmp_scale),
                               np.asarray(w.cmp_block_table[b]), cmp_rows)
-        parts.append(dequant_rows(cb, cs))
+        parts.append(decode_rows(cb, cs))
     return np.concatenate(parts, axis=0)
 
 

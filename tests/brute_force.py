@@ -24,11 +24,16 @@ import torch
 def _logical_cache(pool, scale_pool, table_row, length):
     """Decoded logical rows 0..length-1 of one batch, fp64 [length, 512]."""
     if length == 0:
-        return torch.zeros(0, pool.shape[-1], dtype=torch.float64)
+        return torch.zeros(0, 512, dtype=torch.float64)
     bs = pool.shape[1]
     nblk = (length + bs - 1) // bs
     blocks = table_row[:nblk].long()
     raw = pool[blocks].reshape(-1, pool.shape[-1])[:length]
+    if scale_pool is None:  # packed 640-byte rows: bf16 rope | e4m3fn nope | e8m0 scales | pad
+        rope = raw[:, :128].contiguous().view(torch.bfloat16).to(torch.float64)
+        nope = raw[:, 128:576].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+        sc = raw[:, 576:583].contiguous().view(torch.float8_e8m0fnu).to(torch.float64)
+        return torch.cat([rope, nope * sc.repeat_interleave(64, dim=1)], dim=1)
     sc = scale_pool[blocks].reshape(-1, scale_pool.shape[-1])[:length]
     vals = raw.contiguous().view(torch.float8_e4m3fn).to(torch.float64)
     tile = pool.shape[-1] // sc.shape[-1]

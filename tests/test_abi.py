@@ -37,7 +37,7 @@ def test_every_declared_function_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) <= set(Q.EXPORTS)
-    assert lib.qsfm_abi_version() == 1
+    assert lib.qsfm_abi_version() == 2  # version 2 appended qsfm_params.kv_layout
 
 
 def test_exports_are_c_symbols(lib):
@@ -159,6 +159,22 @@ def test_workspace_size_depends_on_split(lib):
     p.batch, p.max_s1 = 64, 1  # 64 tokens >= 8 CTAs: no split, no workspace
     assert lib.qsfm_forward_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
     assert n.value == 0
+
+
+def test_kv_layout_checks(lib):
+    p = _valid(lib)
+    p.kv_layout = 1  # packed rows carry their scales: a separate scale tensor is an error
+    assert _status(lib, p) == 1
+    p.ori_scale = None
+    assert _status(lib, p) == 4  # valid; stops at the missing workspace
+    p.kv_layout = 7
+    assert _status(lib, p) == 1
+
+
+def test_debug_gather_is_for_fp8_rows_only(lib):
+    p = _valid(lib)
+    p.kv_layout, p.ori_scale = 1, None
+    assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, 0x1000, 0x1000, 0x1000, 0x1000, None) == 2
 
 
 def test_n1_128_passes_validation(lib):

@@ -128,6 +128,15 @@ WIDE = {
                     k2=1024),
     "n1_128_k2_1024": dict(layout="BSND", q_lens=[2, 2], s2=[20000, 9000], cmp_ratio=4, mode="CSA", k2=1024,
                            n1=128),
+    # packed 640-byte KV rows (bf16 rope | e4m3fn nope | e8m0 scales)
+    "packed_csa_decode": dict(layout="BSND", q_lens=[2] * 6, s2=[5000, 9000, 700, 20000, 4096, 3000],
+                              cmp_ratio=4, mode="CSA", k2=512, kv_format="packed640"),
+    "packed_hca_tnd": dict(layout="TND", q_lens=[3, 5], s2=[3000, 40000], cmp_ratio=128, mode="HCA",
+                           kv_format="packed640"),
+    "packed_split": dict(layout="BSND", q_lens=[1], s2=[9000], cmp_ratio=4, mode="CSA", k2=512,
+                         kv_format="packed640"),
+    "packed_n1_128_swa": dict(layout="TND", q_lens=[40, 9], s2=[300, 9], mode="SWA", n1=128,
+                              kv_format="packed640"),
 }
 
 

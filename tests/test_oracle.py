@@ -58,6 +58,54 @@ def test_dequant_uses_tile_of_column():
         assert k[0, d] == float(d // 64 + 1)
 
 
+def test_e8m0_all_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = O.E8M0_TABLE
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+
+
+def test_packed_row_by_hand():
+    """A 640-byte row built by hand: rope bf16 bit patterns, nope e4m3fn
+    codes and e8m0 scales written from the format definitions."""
+    row = np.zeros((1, 640), dtype=np.uint8)
+    # rope element 0 = 1.5 (bf16 0x3FC0), element 63 = -2.0 (0xC000), little-endian
+    row[0, 0:2] = [0xC0, 0x3F]
+    row[0, 126:128] = [0x00, 0xC0]
+    # nope element 0 (output 64) = 0x38 = 1.0, scale byte 126 = 2^-1 -> 0.5
+    row[0, 128] = 0x38
+    # nope element 447 (output 511) = 0xC4 (sign 1, exponent 1000b -> 2^1,
+    # mantissa 100b -> 1.5) = -3.0, scale byte 6 = 130 = 2^3 -> -24
+    row[0, 128 + 447] = 0xC4
+    row[0, 576 + 0] = 126
+    row[0, 576 + 6] = 130
+    k = O.dequant_packed_rows(row)
+    assert k.shape == (1, 512)
+    assert k[0, 0] == 1.5 and k[0, 63] == -2.0
+    assert k[0, 64] == 0.5 and k[0, 511] == -24.0
+    assert np.count_nonzero(k) == 4
+
+
+PACKED_CASES = [
+    dict(layout="BSND", q_lens=[2, 2], s2=[100, 300], cmp_ratio=4, mode="CSA", k2=16, block_size=16,
+         ori_win_left=40),
+    dict(layout="TND", q_lens=[3, 4], s2=[60, 200], cmp_ratio=3, mode="HCA", block_size=16),
+]
+
+
+@pytest.mark.parametrize("i", range(len(PACKED_CASES)))
+def test_oracle_matches_brute_force_packed_rows(i):
+    w = W.build(f"packed{i}", seed=200 + i, kv_format="packed640", **PACKED_CASES[i])
+    assert w.ori_kv.shape[-1] == 640 and w.ori_scale is None
+    o_ref, l_ref = O.reference(w)
+    o_bf, l_bf = brute_force(w)
+    assert np.allclose(o_ref, o_bf.numpy(), rtol=1e-12, atol=1e-13)
+    fin = np.isfinite(l_ref)
+    assert np.allclose(l_ref[fin], l_bf.numpy()[fin], rtol=1e-12)
+
+
 # -------------------------------------------------------------- mask fixtures
 def _fake(S2, S1, mode=4, wl=127, wr=0, r=1, cmp_len=None, res=None, cmp_mode=3, cmp=False):
     return types.SimpleNamespace(

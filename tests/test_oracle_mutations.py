@@ -155,3 +155,22 @@ def test_dropped_invalid_index_filter_is_caught(monkeypatch):
     pins only: an unbounded visible count would make HCA rows endless)."""
     monkeypatch.setattr(O, "cmp_visible_count", lambda p_c, cmp_len, ratio, mode: 10 ** 9)
     assert _fails([P.test_invisible_indices_are_dropped])
+
+
+def test_e8m0_bias_mistake_is_caught(monkeypatch):
+    """e8m0 as 2^(e - 126) instead of 2^(e - 127)."""
+    monkeypatch.setattr(O, "E8M0_TABLE", O.E8M0_TABLE * 2.0)
+    assert _fails([P.test_e8m0_all_codes_match_torch, P.test_packed_row_by_hand])
+
+
+def test_nope_before_rope_is_caught(monkeypatch):
+    """The 512 elements of a packed row taken as nope then rope."""
+    orig = O.dequant_packed_rows
+
+    def dequant_packed_rows(rows):
+        k = orig(rows)
+        return np.concatenate([k[:, 64:], k[:, :64]], axis=1)
+
+    monkeypatch.setattr(O, "dequant_packed_rows", dequant_packed_rows)
+    assert _fails([P.test_packed_row_by_hand] + [lambda i=i: P.test_oracle_matches_brute_force_packed_rows(i)
+                                                 for i in range(len(P.PACKED_CASES))])

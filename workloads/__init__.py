@@ -60,8 +60,8 @@ class Workload:
     q_lens: np.ndarray  # int64 [B]: query tokens per batch
     cu_seqlens_q: Optional[torch.Tensor]  # int32 [B+1] (TND)
     q: torch.Tensor  # bf16 [T, N1, 512], N1 = 64 or 128 (BSND memory is identical)
-    ori_kv: torch.Tensor  # uint8 [nb, 128, 1, 512]
-    ori_scale: torch.Tensor  # fp32 [nb, 128, 1, 8]
+    ori_kv: torch.Tensor  # uint8 [nb, 128, 1, 512], or [nb, 128, 1, 640] packed rows
+    ori_scale: Optional[torch.Tensor]  # fp32 [nb, 128, 1, 8]; None for packed rows
     ori_block_table: torch.Tensor  # int32 [B, wo]
     seqused_ori_kv: torch.Tensor  # int32 [B]
     cmp_kv: Optional[torch.Tensor]
@@ -115,6 +115,38 @@ def _quantize_rows(x: torch.Tensor):
     return q8.view(torch.uint8).view(n, HEAD_DIM), scale.to(torch.float32)
 
 
+PACKED_ROW = 640     # bf16 rope 64 (128 B) + e4m3fn nope 448 + e8m0 scales 7 + pad
+ROPE_DIM = 64
+NOPE_DIM = HEAD_DIM - ROPE_DIM
+
+
+def _quantize_packed_rows(x: torch.Tensor):
+    """fp32 rows [n, 512] as packed 640-byte rows: the first 64 elements in
+    bf16, the other 448 per 64-tile as e4m3fn with a power-of-two scale
+    (e8m0: 2^(e - 127)), the smallest that keeps the tile within the e4m3fn
+    range."""
+    n = x.shape[0]
+    rope = x[:, :ROPE_DIM].to(torch.bfloat16)
+    t = x[:, ROPE_DIM:].reshape(n, NOPE_DIM // TILE, TILE)
+    amax = torch.clamp(t.abs().amax(dim=-1), min=1e-30)
+    e = torch.ceil(torch.log2(amax / FP8_MAX)).clamp(-127, 127)
+    scale = torch.pow(2.0, e)
+    q8 = (t / scale.unsqueeze(-1)).to(torch.float8_e4m3fn)
+    out = torch.zeros(n, PACKED_ROW, dtype=torch.uint8)
+    out[:, :2 * ROPE_DIM] = rope.view(torch.uint8).view(n, 2 * ROPE_DIM)
+    out[:, 2 * ROPE_DIM:2 * ROPE_DIM + NOPE_DIM] = q8.view(torch.uint8).reshape(n, NOPE_DIM)
+    out[:, 2 * ROPE_DIM + NOPE_DIM:2 * ROPE_DIM + NOPE_DIM + NOPE_DIM // TILE] = (e + 127).to(torch.uint8)
+    return out
+
+
+def _random_packed_rows(n: int, gen: torch.Generator, chunk: int = 1 << 16):
+    rows = torch.empty(n, PACKED_ROW, dtype=torch.uint8)
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        rows[lo:hi] = _quantize_packed_rows(torch.randn(hi - lo, HEAD_DIM, generator=gen, dtype=torch.float32))
+    return rows
+
+
 def _random_rows(n: int, gen: torch.Generator, chunk: int = 1 << 16):
     rows = torch.empty(n, HEAD_DIM, dtype=torch.uint8)
     scales = torch.empty(n, SCALES_PER_ROW, dtype=torch.float32)
@@ -128,8 +160,9 @@ def _random_rows(n: int, gen: torch.Generator, chunk: int = 1 << 16):
 
 
 def _paged_pool(lengths: np.ndarray, gen: torch.Generator, min_width: int = 0,
-                block: int = BLOCK):
-    """Pool + shuffled block table holding lengths[b] rows for each batch."""
+                block: int = BLOCK, packed: bool = False):
+    """Pool + shuffled block table holding lengths[b] rows for each batch
+    (packed: 640-byte rows and no scale tensor)."""
     nblk = [(int(l) + block - 1) // block for l in lengths]
     total = sum(nblk)
     width = max([min_width] + nblk + [1])
@@ -140,6 +173,13 @@ def _paged_pool(lengths: np.ndarray, gen: torch.Generator, min_width: int = 0,
         table[b, :k] = perm[off:off + k]
         off += k
     nrows = max(total, 1) * block
+    if packed:
+        if nrows <= BANK_ROWS:
+            rows = _random_packed_rows(nrows, gen)
+        else:
+            bank = _random_packed_rows(BANK_ROWS, gen)
+            rows = bank[torch.randint(0, BANK_ROWS, (nrows,), generator=gen)]
+        return rows.view(max(total, 1), block, 1, PACKED_ROW), None, table
     if nrows <= BANK_ROWS:
         rows, scales = _random_rows(nrows, gen)
     else:
@@ -181,6 +221,7 @@ def build(
     q_scale: float = 1.0,
     block_size: int = BLOCK,
     n1: int = NUM_HEADS,
+    kv_format: str = "fp8_fp32_scales",
 ) -> Workload:
     """Build one workload. q_lens / s2 are per-batch query and ori lengths."""
     gen = torch.Generator().manual_seed(seed)
@@ -190,7 +231,9 @@ def build(
     assert len(s2) == B
     T = int(q_lens.sum())
     q = (torch.randn(T, n1, HEAD_DIM, generator=gen) * q_scale).to(torch.bfloat16)
-    ori_kv, ori_scale, ori_table = _paged_pool(s2, gen, block=block_size)
+    assert kv_format in ("fp8_fp32_scales", "packed640")
+    packed = kv_format == "packed640"
+    ori_kv, ori_scale, ori_table = _paged_pool(s2, gen, block=block_size, packed=packed)
     sink = torch.randn(n1, generator=gen, dtype=torch.float32) if sinks else None
     cu = None
     if layout == "TND":
@@ -204,7 +247,7 @@ def build(
         res = (s2 % cmp_ratio) if with_residual else np.zeros_like(s2)
         cmp_w = (int(s2.max()) // cmp_ratio + block_size - 1) // block_size if B else 1
         cmp_kv, cmp_scale, cmp_table = _paged_pool(cmp_len, gen, min_width=cmp_w,
-                                                   block=block_size)
+                                                   block=block_size, packed=packed)
         resid = torch.from_numpy(res.astype(np.int32))
         if mode == "CSA":
             idx = torch.full((T, 1, k2), -1, dtype=torch.int32)
