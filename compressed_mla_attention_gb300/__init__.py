@@ -26,6 +26,7 @@ LAYOUT_BSND = 0
 LAYOUT_TND = 1
 KV_FP8_FP32_SCALES = 0
 KV_PACKED640 = 1
+KV_BF16 = 2
 PACKED_ROW_BYTES = 640
 
 STATUS = {
@@ -167,7 +168,8 @@ def make_params(
     q / attn_out: BSND [B, S1, N1, 512] or TND [T1, N1, 512] bf16, N1 = 64 or 128.
     Paged KV: [blocks, 128, 1, 512] uint8 (fp8 e4m3fn bytes) with fp32 scales
     [blocks, 128, 1, 8], or packed [blocks, 128, 1, 640] uint8 rows (bf16 rope,
-    e4m3fn nope, e8m0 scales; scales None); block tables int32 [B, width].
+    e4m3fn nope, e8m0 scales; scales None), or bf16 rows [blocks, 128, 1, 512]
+    (scales None); block tables int32 [B, width].
     """
     p = QsfmParams()
     lib().qsfm_params_init(ctypes.byref(p))
@@ -190,8 +192,15 @@ def make_params(
         raise ValueError(layout)
     p.n1, p.d = int(q.shape[-2]), int(q.shape[-1])
     p.k2 = int(cmp_sparse_indices.shape[-1]) if cmp_sparse_indices is not None else 0
-    # packed 640-byte rows (bf16 rope, e4m3 nope, e8m0 scales) or fp8 rows + fp32 scales
-    p.kv_layout = KV_PACKED640 if int(ori_kv.shape[-1]) == PACKED_ROW_BYTES else KV_FP8_FP32_SCALES
+    # bf16 rows, packed 640-byte rows (bf16 rope, e4m3 nope, e8m0 scales) or fp8 rows + fp32 scales
+    if cmp_kv is not None and (cmp_kv.dtype != ori_kv.dtype or cmp_kv.shape[-1] != ori_kv.shape[-1]):
+        raise ValueError("ori_kv and cmp_kv must have the same row format")
+    if str(ori_kv.dtype) == "torch.bfloat16":
+        p.kv_layout = KV_BF16
+    elif int(ori_kv.shape[-1]) == PACKED_ROW_BYTES:
+        p.kv_layout = KV_PACKED640
+    else:
+        p.kv_layout = KV_FP8_FP32_SCALES
     p.ori_block_size = int(ori_kv.shape[1])
     p.ori_max_blocks = int(ori_block_table.shape[-1])
     p.ori_num_blocks = int(ori_kv.shape[0])

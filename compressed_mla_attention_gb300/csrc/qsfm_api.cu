@@ -89,12 +89,14 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   // paged ori KV is always present
   if (p.ori_block_size < 1 || p.ori_block_size > 1024) return QSFM_ERR_INVALID_ARG;
   if (p.ori_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
-  if (p.kv_layout != QSFM_KV_FP8_FP32_SCALES && p.kv_layout != QSFM_KV_PACKED640)
+  if (p.kv_layout != QSFM_KV_FP8_FP32_SCALES && p.kv_layout != QSFM_KV_PACKED640 &&
+      p.kv_layout != QSFM_KV_BF16)
     return QSFM_ERR_INVALID_ARG;
-  const bool packed = p.kv_layout == QSFM_KV_PACKED640;
-  // scales are in the packed rows; separate scale tensors with them are a mistake
-  if (packed && (p.ori_scale != nullptr || p.cmp_scale != nullptr)) return QSFM_ERR_INVALID_ARG;
-  if (p.ori_kv == nullptr || (!packed && p.ori_scale == nullptr) || p.ori_block_table == nullptr ||
+  const bool no_scales = p.kv_layout != QSFM_KV_FP8_FP32_SCALES;
+  // packed rows carry their scales and bf16 rows need none: a separate scale
+  // tensor with them is a mistake
+  if (no_scales && (p.ori_scale != nullptr || p.cmp_scale != nullptr)) return QSFM_ERR_INVALID_ARG;
+  if (p.ori_kv == nullptr || (!no_scales && p.ori_scale == nullptr) || p.ori_block_table == nullptr ||
       p.seqused_ori_kv == nullptr)
     return QSFM_ERR_INVALID_ARG;
   if (p.ori_max_blocks < 1 || p.ori_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
@@ -105,7 +107,7 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   } else {
     if (p.cmp_block_size < 1 || p.cmp_block_size > 1024) return QSFM_ERR_INVALID_ARG;
     if (p.cmp_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
-    if ((!packed && p.cmp_scale == nullptr) || p.cmp_block_table == nullptr) return QSFM_ERR_INVALID_ARG;
+    if ((!no_scales && p.cmp_scale == nullptr) || p.cmp_block_table == nullptr) return QSFM_ERR_INVALID_ARG;
     if (p.cmp_max_blocks < 1 || p.cmp_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
     if (p.cmp_sparse_indices != nullptr && p.k2 < 1) return QSFM_ERR_INVALID_ARG;
   }

@@ -36,7 +36,10 @@
 //               load their fp8 bytes and scales into registers, dequantise
 //               the whole tile into registers, start the next tile's loads,
 //               then store the tile chunk by chunk (a chunk = 64 rows x 128 d
-//               = 2 d-blocks) once its stage is free.
+//               = 2 d-blocks) once its stage is free. Packed 640-byte rows
+//               and bf16 rows have producers of their own (one kernel
+//               instantiation per row format); the tile they store is the
+//               same.
 //   warp 12     QK^T issue (one thread): Q by TMA, QK^T chunk by chunk as the
 //               producers publish the chunks.
 //   warp 14     PV issue (one thread): PV once the softmax has written P, and
@@ -256,6 +259,10 @@ __device__ void resolver_role(const qsfm_params& p, const Smem& sm, Range rg, in
           const uint8_t* src = pool + size_t(pr[u]) * QSFM_PACKED_ROW_BYTES;
 #pragma unroll
           for (int c = 0; c < 5; ++c) prefetch_l2(src + 128 * c);
+        } else if constexpr (kFmt == QSFM_KV_BF16) {
+          const uint8_t* src = pool + size_t(pr[u]) * QSFM_BF16_ROW_BYTES;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) prefetch_l2(src + 128 * c);
         } else {
           const uint8_t* src = pool + size_t(pr[u]) * kDim;
 #pragma unroll
@@ -452,6 +459,72 @@ __device__ void producer_role_packed(const qsfm_params& p, const Smem& sm, int* 
           sts_v4(rowb + (((c0 + odd_first) ^ sw) << 4), odd_first ? hi : lo);
           sts_v4(rowb + (((c0 + 1 - odd_first) ^ sw) << 4), odd_first ? lo : hi);
         }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(kBarKvFull + 4 * st + c));
+    }
+  }
+}
+
+// Producers for bf16 rows (1024 bytes, no quantisation): the row's 16-byte
+// piece q holds elements 8q .. 8q + 7, i.e. unit q % 8 of d-block q / 8.
+// Thread (row_lo, j): rows row_lo and row_lo + 32, pieces 16c + j and
+// 16c + 8 + j of chunk c (unit j of d-blocks 2c and 2c + 1), copied as they
+// are. The loads of a tile are issued after the previous tile is stored.
+__device__ void producer_role_bf16(const qsfm_params& p, const Smem& sm, int* fault) {
+  const int ptid = threadIdx.x - kSoftThreads;  // 0..255 (8 producer warps)
+  const int lane = threadIdx.x & 31;
+  const int row_lo = ptid >> 3;  // 0..31
+  const int j = ptid & 7;
+  const int* rows = reinterpret_cast<const int*>(sm.ptr + kSRows);
+  const int* kind = reinterpret_cast<const int*>(sm.ptr + kSRowKind);
+  constexpr int kRow = QSFM_BF16_ROW_BYTES;
+
+  int pr[2];
+  uint4 R[4][2][2];  // [chunk][row][d-block of the chunk]
+
+  auto fetch = [&](uint32_t n) -> bool {
+    const uint32_t slot = n % kRing;
+    if (!warp_wait_or_abort(sm, kBarRowsFull + slot, (n / kRing) & 1, fault)) return false;
+    const int kd = kind[slot];
+    pr[0] = rows[slot * kTileRows + row_lo];
+    pr[1] = rows[slot * kTileRows + row_lo + 32];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(kBarRowsEmpty + slot));
+    if (kd < 0) return false;
+    const uint8_t* pool = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv);
+    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const bool v = pr[u] >= 0;
+      const uint8_t* base = pool + size_t(v ? pr[u] : 0) * kRow + 16 * j;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        R[c][u][0] = v ? ldg_stream_v4(base + 256 * c) : z;
+        R[c][u][1] = v ? ldg_stream_v4(base + 256 * c + 128) : z;
+      }
+    }
+    return true;
+  };
+
+  for (uint32_t n = 0; fetch(n); ++n) {
+    const uint32_t st = n & 1;
+    if (!warp_wait_or_abort(sm, kBarKvEmpty + st, ((n >> 1) & 1) ^ 1, fault)) return;
+    const uint32_t stage = sm.base + kSK + st * kStageBytes;
+    if (j == 0) {
+      int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + st * kTileRows;
+      valid[row_lo] = pr[0] >= 0;
+      valid[row_lo + 32] = pr[1] >= 0;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int r = row_lo + 32 * u;
+        const uint32_t unit = (uint32_t(j) ^ uint32_t(r & 7)) << 4;
+        sts_v4(stage + (2 * c) * kDBlockBytes + r * 128 + unit, R[c][u][0]);
+        sts_v4(stage + (2 * c + 1) * kDBlockBytes + r * 128 + unit, R[c][u][1]);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -894,6 +967,9 @@ __device__ __noinline__ void warm_first_token(const qsfm_params& p, int T, int c
   if constexpr (kFmt == QSFM_KV_PACKED640) {
     bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * QSFM_PACKED_ROW_BYTES,
                      QSFM_PACKED_ROW_BYTES);
+  } else if constexpr (kFmt == QSFM_KV_BF16) {
+    bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * QSFM_BF16_ROW_BYTES,
+                     QSFM_BF16_ROW_BYTES);
   } else {
     bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * kDim, kDim);
     prefetch_l2((cmp ? p.cmp_scale : p.ori_scale) + row * kScales);
@@ -965,6 +1041,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kMmaWarp) {
     if constexpr (kFmt == QSFM_KV_PACKED640)
       producer_role_packed(p, sm, fault);
+    else if constexpr (kFmt == QSFM_KV_BF16)
+      producer_role_bf16(p, sm, fault);
     else
       producer_role(p, sm, fault);
   } else if (warp == kMmaWarp) {
@@ -1012,9 +1090,10 @@ cudaError_t make_q_map(const void* q, int T, CUtensorMap* map) {
 
 cudaError_t launch_attention(const qsfm_params& p, int num_tokens, int num_ctas,
                              const Workspace& ws, int* fault, cudaStream_t s) {
-  // one instantiation per KV row format, so neither pays for the other
-  const bool packed = p.kv_layout == QSFM_KV_PACKED640;
-  auto* kernel = packed ? attention_kernel<QSFM_KV_PACKED640> : attention_kernel<QSFM_KV_FP8_FP32_SCALES>;
+  // one instantiation per KV row format, so none pays for the others
+  auto* kernel = p.kv_layout == QSFM_KV_PACKED640 ? attention_kernel<QSFM_KV_PACKED640>
+                 : p.kv_layout == QSFM_KV_BF16    ? attention_kernel<QSFM_KV_BF16>
+                                                  : attention_kernel<QSFM_KV_FP8_FP32_SCALES>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e != cudaSuccess) return e;
   CUtensorMap qmap;

@@ -86,6 +86,7 @@ extern "C" {
 #define QSFM_METADATA_INTS 1024
 #define QSFM_MAX_CTAS 256
 #define QSFM_PACKED_ROW_BYTES 640
+#define QSFM_BF16_ROW_BYTES 1024
 
 /* KV row formats (qsfm_params.kv_layout). */
 typedef enum {
@@ -97,7 +98,10 @@ typedef enum {
    * elements, bytes 128..575), e8m0 scales (7, one per 64 nope elements,
    * bytes 576..582), zero padding to 640. The 512 elements of a row are
    * rope then nope; ori_scale and cmp_scale must be NULL. */
-  QSFM_KV_PACKED640 = 1
+  QSFM_KV_PACKED640 = 1,
+  /* bf16 rows [blocks, 128, 1, 512] without quantisation (the KV of
+   * SparseCompressedFlashAttention); ori_scale and cmp_scale must be NULL. */
+  QSFM_KV_BF16 = 2
 } qsfm_kv_layout;
 
 typedef enum {

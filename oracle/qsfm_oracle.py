@@ -22,6 +22,8 @@ Sources (page title, section):
     ori_win_left/right (-1 = unbounded).
   * QuantSparseFlashMla, "约束说明" (constraints): PageAttention layout, the
     cmp length default and cmp_len * cmp_ratio + residual.
+  * SparseCompressedFlashAttention, parameter table: the same attention over
+    unquantised bf16 KV rows.
   * KvQuantSparseAttnSharedKv, parameter table: fp8 e4m3fn KV with per-tile
     quantisation (tile 64), softmax_lse definition; its constraints: indices
     valid-first, -1 after.
@@ -104,6 +106,23 @@ def dequant_packed_rows(rows: np.ndarray) -> np.ndarray:
     nope = E4M3FN_TABLE[rows[:, 2 * ROPE_DIM:nope_end].astype(np.int64)]
     scales = E8M0_TABLE[rows[:, nope_end:nope_end + (HEAD_DIM - ROPE_DIM) // TILE].astype(np.int64)]
     return np.concatenate([rope, nope * np.repeat(scales, TILE, axis=1)], axis=1).reshape(n, HEAD_DIM)
+
+
+BF16_ROW = 2 * HEAD_DIM
+
+
+def decode_bf16_rows(rows: np.ndarray) -> np.ndarray:
+    """K~ of unquantised bf16 rows given as little-endian bytes [n, 1024] ->
+    fp64 [n, 512], exactly.
+
+    SparseCompressedFlashAttention, parameter table rows ori_kv / cmp_kv:
+    bf16 [block_num, block_size, 1, 512]. A bf16 value is the top half of
+    the fp32 with the same sign, exponent and leading mantissa bits, so its
+    16 bits shifted up by 16 are that fp32 exactly.
+    """
+    rows = np.ascontiguousarray(rows)
+    bits = rows.view("<u2").astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64).reshape(rows.shape[0], HEAD_DIM)
 
 
 def dequant_rows(kv_bytes: np.ndarray, scales: np.ndarray) -> np.ndarray:
@@ -201,10 +220,13 @@ def gather_paged(kv_pool, scale_pool, table_row, rows):
 
 
 def decode_rows(kv_bytes: np.ndarray, scales) -> np.ndarray:
-    """K~ of gathered rows: packed 640-byte rows carry their scales; 512-byte
-    fp8 rows come with a separate fp32 scale row."""
+    """K~ of gathered rows: packed 640-byte rows carry their scales, bf16
+    rows (1024 bytes) need none; 512-byte fp8 rows come with a separate fp32
+    scale row."""
     if kv_bytes.shape[-1] == PACKED_ROW:
         return dequant_packed_rows(kv_bytes)
+    if kv_bytes.shape[-1] == BF16_ROW:
+        return decode_bf16_rows(kv_bytes)
     return dequant_rows(kv_bytes, scales)
 
 
@@ -234,17 +256,27 @@ def attend(q: np.ndarray, k: np.ndarray, softmax_scale: float, sinks):
     return o, lse
 
 
+def pool_bytes(pool) -> np.ndarray:
+    """A KV pool as a byte array [blocks, block_size, 1, row bytes] (bf16
+    rows are taken as their 1024 little-endian bytes)."""
+    if str(getattr(pool, "dtype", "")) == "torch.bfloat16":
+        import torch  # the workload's tensors are torch tensors; numpy has no bf16
+
+        pool = pool.contiguous().view(torch.uint8)  # last dim 512 -> 1024 bytes
+    return np.asarray(pool)
+
+
 def token_kv(w, t: int, b: int, s: int):
     """Dequantised K~ = V~ rows [n, 512] of token t: ori rows, then cmp rows."""
     ori, cmp_rows = token_rows(w, t, b, s)
     if ori is None:
         return None
     parts = []
-    ob, os_ = gather_paged(np.asarray(w.ori_kv), None if w.ori_scale is None else np.asarray(w.ori_scale),
+    ob, os_ = gather_paged(pool_bytes(w.ori_kv), None if w.ori_scale is None else np.asarray(w.ori_scale),
                            np.asarray(w.ori_block_table[b]), ori)
     parts.append(decode_rows(ob, os_))
     if cmp_rows:
-        cb, cs = gather_paged(np.asarray(w.cmp_kv), None if w.cmp_scale is None else np.asarray(w.cmp_scale),
+        cb, cs = gather_paged(pool_bytes(w.cmp_kv), None if w.cmp_scale is None else np.asarray(w.cmp_scale),
                               np.asarray(w.cmp_block_table[b]), cmp_rows)
         parts.append(decode_rows(cb, cs))
     return np.concatenate(parts, axis=0)

@@ -4,7 +4,8 @@ Used only to pin the oracle on tiny inputs. It shares no code with
 ``oracle/`` and takes a different route to the same definition:
 
 * the whole logical KV cache of a batch is materialised by indexing the pool
-  with the block table, and decoded with torch's own float8_e4m3fn type;
+  with the block table, and decoded with torch's own float8_e4m3fn,
+  float8_e8m0fnu and bfloat16 types;
 * every query token is scored against *every* key of both caches, and a
   per-key weight (0 = masked, k = the key occurs k times among the CSA
   indices) is built from predicates written per key;
@@ -29,6 +30,8 @@ def _logical_cache(pool, scale_pool, table_row, length):
     nblk = (length + bs - 1) // bs
     blocks = table_row[:nblk].long()
     raw = pool[blocks].reshape(-1, pool.shape[-1])[:length]
+    if raw.dtype == torch.bfloat16:  # unquantised bf16 rows
+        return raw.to(torch.float64)
     if scale_pool is None:  # packed 640-byte rows: bf16 rope | e4m3fn nope | e8m0 scales | pad
         rope = raw[:, :128].contiguous().view(torch.bfloat16).to(torch.float64)
         nope = raw[:, 128:576].contiguous().view(torch.float8_e4m3fn).to(torch.float64)

@@ -167,14 +167,20 @@ def test_kv_layout_checks(lib):
     assert _status(lib, p) == 1
     p.ori_scale = None
     assert _status(lib, p) == 4  # valid; stops at the missing workspace
+    p.kv_layout = 2  # bf16 rows: no scales either
+    assert _status(lib, p) == 4
+    p.ori_scale = 0x2000
+    assert _status(lib, p) == 1
+    p.ori_scale = None
     p.kv_layout = 7
     assert _status(lib, p) == 1
 
 
 def test_debug_gather_is_for_fp8_rows_only(lib):
     p = _valid(lib)
-    p.kv_layout, p.ori_scale = 1, None
-    assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, 0x1000, 0x1000, 0x1000, 0x1000, None) == 2
+    for layout in (1, 2):
+        p.kv_layout, p.ori_scale = layout, None
+        assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, 0x1000, 0x1000, 0x1000, 0x1000, None) == 2
 
 
 def test_n1_128_passes_validation(lib):

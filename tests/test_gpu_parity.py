@@ -137,6 +137,14 @@ WIDE = {
                          kv_format="packed640"),
     "packed_n1_128_swa": dict(layout="TND", q_lens=[40, 9], s2=[300, 9], mode="SWA", n1=128,
                               kv_format="packed640"),
+    # unquantised bf16 KV rows (SparseCompressedFlashAttention: TND, K2 = 512,
+    # window 128, cmp_ratio 4)
+    "bf16_csa_tnd": dict(layout="TND", q_lens=[3, 1, 4, 2], s2=[5000, 700, 20000, 130], cmp_ratio=4,
+                         mode="CSA", k2=512, kv_format="bf16"),
+    "bf16_split": dict(layout="TND", q_lens=[1], s2=[9000], cmp_ratio=4, mode="CSA", k2=512,
+                       kv_format="bf16"),
+    "bf16_n1_128_hca": dict(layout="TND", q_lens=[3, 5], s2=[3000, 40000], cmp_ratio=128, mode="HCA",
+                            n1=128, kv_format="bf16"),
 }
 
 

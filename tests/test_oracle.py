@@ -106,6 +106,39 @@ def test_oracle_matches_brute_force_packed_rows(i):
     assert np.allclose(l_ref[fin], l_bf.numpy()[fin], rtol=1e-12)
 
 
+def test_bf16_row_by_hand():
+    """A bf16 row (1024 little-endian bytes) built from the bf16 format
+    definition: 1 sign bit, 8 exponent bits with bias 127, 7 mantissa bits."""
+    row = np.zeros((1, 1024), dtype=np.uint8)
+    row[0, 0:2] = [0xC0, 0x3F]      # element 0: 0x3FC0 = +2^0 * 1.5
+    row[0, 2:4] = [0x80, 0xC0]      # element 1: 0xC080 = -2^(129-127) * 1.0
+    row[0, 1022:1024] = [0x01, 0x00]  # element 511: 0x0001, the smallest subnormal 2^-133
+    row[0, 600:602] = [0x49, 0x42]  # element 300: 0x4249 = 2^5 * (1 + 73/128) = 50.25
+    k = O.decode_bf16_rows(row)
+    assert k.shape == (1, 512)
+    assert k[0, 0] == 1.5 and k[0, 1] == -4.0 and k[0, 300] == 50.25
+    assert k[0, 511] == 2.0 ** -133
+    assert np.count_nonzero(k) == 4
+
+
+BF16_CASES = [
+    dict(layout="TND", q_lens=[3, 2], s2=[90, 260], cmp_ratio=4, mode="CSA", k2=16, block_size=16,
+         ori_win_left=31),
+    dict(layout="TND", q_lens=[2, 3], s2=[70, 150], cmp_ratio=4, mode="HCA", block_size=16),
+]
+
+
+@pytest.mark.parametrize("i", range(len(BF16_CASES)))
+def test_oracle_matches_brute_force_bf16_rows(i):
+    w = W.build(f"bf16_{i}", seed=300 + i, kv_format="bf16", **BF16_CASES[i])
+    assert str(w.ori_kv.dtype) == "torch.bfloat16" and w.ori_scale is None
+    o_ref, l_ref = O.reference(w)
+    o_bf, l_bf = brute_force(w)
+    assert np.allclose(o_ref, o_bf.numpy(), rtol=1e-12, atol=1e-13)
+    fin = np.isfinite(l_ref)
+    assert np.allclose(l_ref[fin], l_bf.numpy()[fin], rtol=1e-12)
+
+
 # -------------------------------------------------------------- mask fixtures
 def _fake(S2, S1, mode=4, wl=127, wr=0, r=1, cmp_len=None, res=None, cmp_mode=3, cmp=False):
     return types.SimpleNamespace(

@@ -174,3 +174,15 @@ def test_nope_before_rope_is_caught(monkeypatch):
     monkeypatch.setattr(O, "dequant_packed_rows", dequant_packed_rows)
     assert _fails([P.test_packed_row_by_hand] + [lambda i=i: P.test_oracle_matches_brute_force_packed_rows(i)
                                                  for i in range(len(P.PACKED_CASES))])
+
+
+def test_big_endian_bf16_is_caught(monkeypatch):
+    """bf16 rows read with the two bytes of an element swapped."""
+    def decode_bf16_rows(rows):
+        rows = np.ascontiguousarray(rows)
+        bits = rows.view(">u2").astype(np.uint32) << 16
+        return bits.view(np.float32).astype(np.float64).reshape(rows.shape[0], O.HEAD_DIM)
+
+    monkeypatch.setattr(O, "decode_bf16_rows", decode_bf16_rows)
+    assert _fails([P.test_bf16_row_by_hand] + [lambda i=i: P.test_oracle_matches_brute_force_bf16_rows(i)
+                                               for i in range(len(P.BF16_CASES))])

@@ -60,8 +60,8 @@ class Workload:
     q_lens: np.ndarray  # int64 [B]: query tokens per batch
     cu_seqlens_q: Optional[torch.Tensor]  # int32 [B+1] (TND)
     q: torch.Tensor  # bf16 [T, N1, 512], N1 = 64 or 128 (BSND memory is identical)
-    ori_kv: torch.Tensor  # uint8 [nb, 128, 1, 512], or [nb, 128, 1, 640] packed rows
-    ori_scale: Optional[torch.Tensor]  # fp32 [nb, 128, 1, 8]; None for packed rows
+    ori_kv: torch.Tensor  # uint8 [nb, 128, 1, 512], uint8 [nb, 128, 1, 640] packed rows, or bf16 [nb, 128, 1, 512]
+    ori_scale: Optional[torch.Tensor]  # fp32 [nb, 128, 1, 8]; None for packed and bf16 rows
     ori_block_table: torch.Tensor  # int32 [B, wo]
     seqused_ori_kv: torch.Tensor  # int32 [B]
     cmp_kv: Optional[torch.Tensor]
@@ -147,6 +147,15 @@ def _random_packed_rows(n: int, gen: torch.Generator, chunk: int = 1 << 16):
     return rows
 
 
+def _random_bf16_rows(n: int, gen: torch.Generator, chunk: int = 1 << 16):
+    """Unquantised rows: N(0, 1) draws rounded to bf16."""
+    rows = torch.empty(n, HEAD_DIM, dtype=torch.bfloat16)
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        rows[lo:hi] = torch.randn(hi - lo, HEAD_DIM, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    return rows
+
+
 def _random_rows(n: int, gen: torch.Generator, chunk: int = 1 << 16):
     rows = torch.empty(n, HEAD_DIM, dtype=torch.uint8)
     scales = torch.empty(n, SCALES_PER_ROW, dtype=torch.float32)
@@ -160,9 +169,10 @@ def _random_rows(n: int, gen: torch.Generator, chunk: int = 1 << 16):
 
 
 def _paged_pool(lengths: np.ndarray, gen: torch.Generator, min_width: int = 0,
-                block: int = BLOCK, packed: bool = False):
+                block: int = BLOCK, fmt: str = "fp8_fp32_scales"):
     """Pool + shuffled block table holding lengths[b] rows for each batch
-    (packed: 640-byte rows and no scale tensor)."""
+    (fmt packed640: 640-byte rows, bf16: bf16 rows; neither has a scale
+    tensor)."""
     nblk = [(int(l) + block - 1) // block for l in lengths]
     total = sum(nblk)
     width = max([min_width] + nblk + [1])
@@ -173,13 +183,14 @@ def _paged_pool(lengths: np.ndarray, gen: torch.Generator, min_width: int = 0,
         table[b, :k] = perm[off:off + k]
         off += k
     nrows = max(total, 1) * block
-    if packed:
+    if fmt in ("packed640", "bf16"):
+        make, width_b = (_random_packed_rows, PACKED_ROW) if fmt == "packed640" else (_random_bf16_rows, HEAD_DIM)
         if nrows <= BANK_ROWS:
-            rows = _random_packed_rows(nrows, gen)
+            rows = make(nrows, gen)
         else:
-            bank = _random_packed_rows(BANK_ROWS, gen)
+            bank = make(BANK_ROWS, gen)
             rows = bank[torch.randint(0, BANK_ROWS, (nrows,), generator=gen)]
-        return rows.view(max(total, 1), block, 1, PACKED_ROW), None, table
+        return rows.view(max(total, 1), block, 1, width_b), None, table
     if nrows <= BANK_ROWS:
         rows, scales = _random_rows(nrows, gen)
     else:
@@ -231,9 +242,8 @@ def build(
     assert len(s2) == B
     T = int(q_lens.sum())
     q = (torch.randn(T, n1, HEAD_DIM, generator=gen) * q_scale).to(torch.bfloat16)
-    assert kv_format in ("fp8_fp32_scales", "packed640")
-    packed = kv_format == "packed640"
-    ori_kv, ori_scale, ori_table = _paged_pool(s2, gen, block=block_size, packed=packed)
+    assert kv_format in ("fp8_fp32_scales", "packed640", "bf16")
+    ori_kv, ori_scale, ori_table = _paged_pool(s2, gen, block=block_size, fmt=kv_format)
     sink = torch.randn(n1, generator=gen, dtype=torch.float32) if sinks else None
     cu = None
     if layout == "TND":
@@ -247,7 +257,7 @@ def build(
         res = (s2 % cmp_ratio) if with_residual else np.zeros_like(s2)
         cmp_w = (int(s2.max()) // cmp_ratio + block_size - 1) // block_size if B else 1
         cmp_kv, cmp_scale, cmp_table = _paged_pool(cmp_len, gen, min_width=cmp_w,
-                                                   block=block_size, packed=packed)
+                                                   block=block_size, fmt=kv_format)
         resid = torch.from_numpy(res.astype(np.int32))
         if mode == "CSA":
             idx = torch.full((T, 1, k2), -1, dtype=torch.int32)
@@ -333,7 +343,7 @@ def subset_tokens(w: Workload, n: int, seed: int = 0) -> np.ndarray:
 def device_inputs(w: Workload, device) -> dict:
     """The workload's tensors on `device`, keyed by the op's argument names.
 
-    Pure data movement (no arithmetic): uint8 fp8 bytes, fp32 scales, int32
+    Pure data movement (no arithmetic): uint8 fp8 bytes, bf16 rows, fp32 scales, int32
     tables / lengths / indices and the bf16 query are copied as they are.
     """
     def mv(t):
