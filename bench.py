@@ -43,8 +43,10 @@ import workloads as W  # noqa: E402
 METRIC = "query-tokens/s (64 heads, D=512) and % of roofline (HBM GB/s, TC util)"
 UNIT = "query-tokens/s"
 FLUSH_BYTES = 512 << 20  # > 129 MB L2
-KV_ROW_BYTES = 512 + 8 * 4
-FLOPS_PER_ROW = 4 * 64 * 512
+# bytes one KV row takes in each row format: 512 fp8 + 8 fp32 scales; a
+# packed 640-byte row; 512 bf16
+KV_ROW_BYTES = {"fp8_fp32_scales": 512 + 8 * 4, "packed640": 640, "bf16": 1024}
+FLOPS_PER_ROW_HEAD = 4 * 512  # QK^T + PV per attended (token, row) and head
 KERNEL_SRCS = [os.path.join(ROOT, "compressed_mla_attention_gb300", "csrc", f)
                for f in ("qsfm_attention.cu", "qsfm_device.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_traffic.txt")
@@ -177,11 +179,9 @@ def algorithmic_work(Q, p, w, dev):
     for lo in range(0, T, chunk):
         toks = torch.arange(lo, min(T, lo + chunk), dtype=torch.int32, device=dev)
         n = toks.numel()
-        rows = torch.empty(n, max_rows, 512, dtype=torch.uint8, device=dev)
-        scales = torch.empty(n, max_rows, 8, dtype=torch.float32, device=dev)
         ids = torch.empty(n, max_rows, dtype=torch.int32, device=dev)
         counts = torch.empty(n, dtype=torch.int32, device=dev)
-        Q.debug_gather(p, toks, max_rows, rows, scales, ids, counts)
+        Q.debug_gather(p, toks, max_rows, None, None, ids, counts)  # row ids only
         torch.cuda.synchronize()
         ids, counts = ids.cpu().numpy(), counts.cpu().numpy()
         for i in range(n):
@@ -201,7 +201,7 @@ def run_gpu_arm(args, w, rank, world, local):
     a = W.device_inputs(w, dev)
     lse_wanted = a.pop("return_softmax_lse")
     out = torch.empty_like(a["q"])
-    lse = torch.empty(w.total_t, 64, dtype=torch.float32, device=dev) if lse_wanted else None
+    lse = torch.empty(w.total_t, w.n1, dtype=torch.float32, device=dev) if lse_wanted else None
     plan = torch.empty(1024, dtype=torch.int32, device=dev)
     p = Q.make_params(attn_out=out, softmax_lse=lse, metadata=plan, return_lse=lse_wanted,
                       num_ctas=args.ctas, **a)
@@ -334,7 +334,7 @@ def run_gpu_arm(args, w, rank, world, local):
         e2e_ms = graph_ms if graph_ms is not None else eager_ms
         e2e_ms, eager_ms = max_over_ranks([e2e_ms, eager_ms], dev)
         res["e2e"] = dict(ms=e2e_ms, eager_ms=eager_ms, graph=graph_ms is not None, h2d=h2d, d2h=d2h)
-        res["work"] = algorithmic_work(Q, p, w, dev)
+    res["work"] = algorithmic_work(Q, p, w, dev)
     return res
 
 
@@ -345,6 +345,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="qsfm", choices=["qsfm", "reference"])
     ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--kv-format", default="fp8_fp32_scales", choices=sorted(KV_ROW_BYTES),
+                    help="KV row format of the workload (default: fp8 rows + fp32 scales)")
+    ap.add_argument("--n1", type=int, default=64, choices=[64, 128], help="query heads")
     ap.add_argument("--ctas", type=int, default=0, help="planned CTAs (0 = SM count)")
     ap.add_argument("--quick", action="store_true", help="kernels only: no e2e, clocks, baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -360,7 +363,8 @@ def main():
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
 
-    w = W.profile_case() if args.profile_size else W.config(args.workload)
+    w = W.profile_case() if args.profile_size else W.config(args.workload, kv_format=args.kv_format,
+                                                             n1=args.n1)
     T = w.total_t
     cores = os.cpu_count() or 1
 
@@ -426,18 +430,23 @@ def main():
     }
     if "work" in res:
         uniq, pairs = res["work"]
-        q_bytes = T * 64 * 512 * 2
-        o_bytes = T * 64 * 512 * 2
+        n1 = w.n1
+        q_bytes = T * n1 * 512 * 2
+        o_bytes = T * n1 * 512 * 2
         idx_bytes = T * w.k2 * 4
-        lse_bytes = T * 64 * 4 if w.return_lse else 0
-        alg_bytes = uniq * KV_ROW_BYTES + q_bytes + o_bytes + idx_bytes + lse_bytes
-        flops = pairs * FLOPS_PER_ROW
+        lse_bytes = T * n1 * 4 if w.return_lse else 0
+        alg_bytes = uniq * KV_ROW_BYTES[args.kv_format] + q_bytes + o_bytes + idx_bytes + lse_bytes
+        flops = pairs * FLOPS_PER_ROW_HEAD * n1
         achieved = alg_bytes / (res["ms_attn"] / 1e3) / 1e9
+        # the recorded ncu traffic is for the default format and head count
+        default_shape = args.kv_format == "fp8_fp32_scales" and n1 == 64 and not args.profile_size
         line["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                            "frac": achieved / hbm, "traffic": recorded_traffic(args.workload),
+                            "frac": achieved / hbm,
+                            "traffic": recorded_traffic(args.workload) if default_shape else None,
                             "peak_kind": kind, "algorithmic_bytes": alg_bytes,
                             "tensor_tflops": flops / (res["ms_attn"] / 1e3) / 1e12,
                             "tensor_frac": flops / (res["ms_attn"] / 1e3) / 1e12 / tf}
+    if "e2e" in res:  # not in --quick runs
         e = res["e2e"]
         line["e2e"] = {"value": job_throughput(world, T, e["ms"]), "unit": UNIT,
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],

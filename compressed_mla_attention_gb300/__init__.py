@@ -272,7 +272,8 @@ def forward_noalloc(params: QsfmParams, stream=None) -> None:
 
 def debug_gather(params: QsfmParams, tokens, max_rows: int, rows_out, scales_out, row_ids_out,
                  counts_out, stream=None) -> None:
-    """qsfm_debug_gather(): the rows the attention kernel resolves per token."""
+    """qsfm_debug_gather(): the rows the attention kernel resolves per token
+    (rows_out = scales_out = None: row ids and counts only, any row format)."""
     _check("qsfm_debug_gather", lib().qsfm_debug_gather(
         ctypes.byref(params), _dptr(tokens), int(tokens.numel()), int(max_rows), _dptr(rows_out),
         _dptr(scales_out), _dptr(row_ids_out), _dptr(counts_out), _stream_ptr(stream)))

@@ -245,11 +245,14 @@ qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens, int32
                               int32_t* row_ids_out, int32_t* counts_out, void* stream) {
   qsfm_status st = validate(p, false);
   if (st != QSFM_OK) return st;
-  if (p->kv_layout != QSFM_KV_FP8_FP32_SCALES) return QSFM_ERR_UNSUPPORTED;  // exports 512-B rows + scales
+  // row bytes + scales are exported as 512-B fp8 rows and 8 fp32 scales;
+  // the row ids alone (rows_out = scales_out = NULL) are format-independent
+  const bool ids_only = rows_out == nullptr && scales_out == nullptr;
+  if (!ids_only && p->kv_layout != QSFM_KV_FP8_FP32_SCALES) return QSFM_ERR_UNSUPPORTED;
   if (n < 0 || max_rows < 0) return QSFM_ERR_INVALID_ARG;
   if (n == 0) return QSFM_OK;
   if (tokens == nullptr || counts_out == nullptr) return QSFM_ERR_INVALID_ARG;
-  if (max_rows > 0 && (rows_out == nullptr || scales_out == nullptr || row_ids_out == nullptr))
+  if (max_rows > 0 && (row_ids_out == nullptr || (!ids_only && (rows_out == nullptr || scales_out == nullptr))))
     return QSFM_ERR_INVALID_ARG;
   int* fault = fault_ptr();
   if (fault == nullptr) return QSFM_ERR_CUDA;

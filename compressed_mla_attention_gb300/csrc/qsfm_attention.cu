@@ -334,7 +334,9 @@ __device__ void producer_role(const qsfm_params& p, const Smem& sm, int* fault) 
       for (int u = 0; u < 2; ++u) {
         const float sc = __shfl_sync(0xffffffffu, csc[u], src_lane);
         const uint4 raw = c == 0 ? R0[u] : c == 1 ? R1[u] : c == 2 ? R2[u] : R3[u];
-        dequant16(raw, sc, D[c][u][0], D[c][u][1]);
+        // packed fp32 multiplies: 3 % faster here (the packed-row producer
+        // keeps dequant16: there they were 2.5 % slower)
+        dequant16_x2(raw, sc, D[c][u][0], D[c][u][1]);
       }
     }
     have = fetch(n + 1);

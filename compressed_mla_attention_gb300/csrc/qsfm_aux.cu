@@ -254,17 +254,17 @@ __global__ void __launch_bounds__(128)
       r = cs % kTileRows;
     }
     const RowRef ref = resolve_slot(p, g, k, r, fault);
+    row_ids_out[size_t(i) * max_rows + s] = ref.row >= 0 ? (ref.source << 30) | ref.row : -1;
+    if (rows_out == nullptr) continue;  // row ids only (any row format)
     uint4* dst = reinterpret_cast<uint4*>(rows_out + (size_t(i) * max_rows + s) * kDim);
     float* dsc = scales_out + (size_t(i) * max_rows + s) * kScales;
     if (ref.row >= 0) {
       const uint4* src = reinterpret_cast<const uint4*>(ref.kv);
       for (int j = 0; j < kDim / 16; ++j) dst[j] = src[j];
       for (int j = 0; j < kScales; ++j) dsc[j] = ref.sc[j];
-      row_ids_out[size_t(i) * max_rows + s] = (ref.source << 30) | ref.row;
     } else {
       for (int j = 0; j < kDim / 16; ++j) dst[j] = make_uint4(0, 0, 0, 0);
       for (int j = 0; j < kScales; ++j) dsc[j] = 0.f;
-      row_ids_out[size_t(i) * max_rows + s] = -1;
     }
   }
 }

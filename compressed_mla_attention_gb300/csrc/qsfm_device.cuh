@@ -588,6 +588,32 @@ __device__ __forceinline__ uint32_t dequant2(uint16_t two, float scale) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
+// The same with both products of a pair in one packed fp32 multiply
+// (mul.rn.f32x2: each lane rounds like mul.rn.f32, subnormals kept), so the
+// result is bit-identical to dequant2.
+__device__ __forceinline__ uint32_t dequant2_x2(uint16_t two, uint64_t scale2) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  const uint64_t in = (uint64_t(__float_as_uint(f.y)) << 32) | __float_as_uint(f.x);
+  uint64_t out;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(out) : "l"(in), "l"(scale2));
+  __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(uint32_t(out)), __uint_as_float(uint32_t(out >> 32)));
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// 16 fp8 bytes -> 16 bf16 (two 16-byte chunks), packed multiplies.
+__device__ __forceinline__ void dequant16_x2(const uint4& in, float scale, uint4& lo, uint4& hi) {
+  const uint64_t s2 = (uint64_t(__float_as_uint(scale)) << 32) | __float_as_uint(scale);
+  lo.x = dequant2_x2(uint16_t(in.x & 0xFFFF), s2);
+  lo.y = dequant2_x2(uint16_t(in.x >> 16), s2);
+  lo.z = dequant2_x2(uint16_t(in.y & 0xFFFF), s2);
+  lo.w = dequant2_x2(uint16_t(in.y >> 16), s2);
+  hi.x = dequant2_x2(uint16_t(in.z & 0xFFFF), s2);
+  hi.y = dequant2_x2(uint16_t(in.z >> 16), s2);
+  hi.z = dequant2_x2(uint16_t(in.w & 0xFFFF), s2);
+  hi.w = dequant2_x2(uint16_t(in.w >> 16), s2);
+}
+
 // 16 fp8 bytes -> 16 bf16 (two 16-byte chunks).
 __device__ __forceinline__ void dequant16(const uint4& in, float scale, uint4& lo, uint4& hi) {
   lo.x = dequant2(uint16_t(in.x & 0xFFFF), scale);

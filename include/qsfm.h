@@ -261,7 +261,10 @@ qsfm_status qsfm_forward_noalloc(const qsfm_params* p, void* stream);
  *                                         slot that is masked out
  *   counts_out  int32 [n]                 number of slots of the token
  * Masked slots get zero bytes and zero scales. All buffers are device memory.
- * Only for kv_layout QSFM_KV_FP8_FP32_SCALES (QSFM_ERR_UNSUPPORTED otherwise).
+ * rows_out and scales_out may both be NULL: then only the row ids and counts
+ * are written, for any kv_layout. Row bytes and scales are exported only for
+ * kv_layout QSFM_KV_FP8_FP32_SCALES (QSFM_ERR_UNSUPPORTED for the others
+ * when rows_out or scales_out is given).
  */
 qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens,
                               int32_t n, int32_t max_rows, uint8_t* rows_out,

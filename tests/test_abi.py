@@ -176,11 +176,13 @@ def test_kv_layout_checks(lib):
     assert _status(lib, p) == 1
 
 
-def test_debug_gather_is_for_fp8_rows_only(lib):
+def test_debug_gather_exports_bytes_for_fp8_rows_only(lib):
     p = _valid(lib)
     for layout in (1, 2):
         p.kv_layout, p.ori_scale = layout, None
         assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, 0x1000, 0x1000, 0x1000, 0x1000, None) == 2
+        # row ids only (rows and scales NULL) are allowed for every format, but need the id buffer
+        assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, None, None, None, 0x1000, None) == 1
 
 
 def test_n1_128_passes_validation(lib):

@@ -203,16 +203,20 @@ def test_index_permutation_invariance(cuda_device):
 
 
 # ------------------------------------------------------ row resolution
-def _expected_slots(w, t):
-    """(row ids, bytes, scales) of token t's slots, gathered in Python."""
+def _expected_slots(w, t, with_bytes=True):
+    """(row ids, bytes, scales) of token t's slots, gathered in Python
+    (with_bytes=False: row ids only, bytes and scales left empty)."""
     b, s = int(w.token_batch()[t]), int(w.token_pos()[t])
     ori, _ = O.token_rows(w, t, b, s)
     ids, rows_b, rows_s = [], [], []
-    kv, sc, tab = w.ori_kv.numpy(), w.ori_scale.numpy(), w.ori_block_table[b].numpy()
+    tab = w.ori_block_table[b].numpy()
+    if with_bytes:
+        kv, sc = w.ori_kv.numpy(), w.ori_scale.numpy()
     for r in ori or []:
         ids.append(r)
-        rows_b.append(kv[tab[r // 128], r % 128, 0])
-        rows_s.append(sc[tab[r // 128], r % 128, 0])
+        if with_bytes:
+            rows_b.append(kv[tab[r // 128], r % 128, 0])
+            rows_s.append(sc[tab[r // 128], r % 128, 0])
     if w.cmp_kv is not None and ori is not None:
         s1, s2 = int(w.q_lens[b]), int(w.seqused_ori_kv[b])
         cmp_len = s2 // w.cmp_ratio
@@ -223,16 +227,15 @@ def _expected_slots(w, t):
                    else list(range(v)))
         if w.cmp_topk_length is not None:
             entries = entries[:int(w.cmp_topk_length[t])]
-        ckv, csc, ctab = w.cmp_kv.numpy(), w.cmp_scale.numpy(), w.cmp_block_table[b].numpy()
+        ctab = w.cmp_block_table[b].numpy()
+        if with_bytes:
+            ckv, csc = w.cmp_kv.numpy(), w.cmp_scale.numpy()
         for e in entries:
-            if 0 <= e < v:
-                ids.append((1 << 30) | e)
-                rows_b.append(ckv[ctab[e // 128], e % 128, 0])
-                rows_s.append(csc[ctab[e // 128], e % 128, 0])
-            else:
-                ids.append(-1)
-                rows_b.append(np.zeros(512, np.uint8))
-                rows_s.append(np.zeros(8, np.float32))
+            ok = 0 <= e < v
+            ids.append((1 << 30) | e if ok else -1)
+            if with_bytes:
+                rows_b.append(ckv[ctab[e // 128], e % 128, 0] if ok else np.zeros(512, np.uint8))
+                rows_s.append(csc[ctab[e // 128], e % 128, 0] if ok else np.zeros(8, np.float32))
     return ids, rows_b, rows_s
 
 
@@ -261,6 +264,44 @@ def test_debug_gather_bit_exact(cuda_device, i):
         assert np.array_equal(ids[j, :m], np.array(e_ids[:m], dtype=np.int32))
         assert np.array_equal(rows[j, :m], np.stack(e_b[:m]))
         assert np.array_equal(scales[j, :m].view(np.uint32), np.stack(e_s[:m]).view(np.uint32))
+
+
+GATHER_ID_CASES = {
+    "tiny_csa_decode": lambda f: W.config(0, kv_format=f),
+    "csa_chunked_prefill": lambda f: W.config(4, kv_format=f),
+    "hca_tnd": lambda f: W.build("hca", layout="TND", q_lens=[3, 5], s2=[3000, 40000], cmp_ratio=128,
+                                 mode="HCA", kv_format=f, seed=5),
+}
+
+
+@pytest.mark.parametrize("kv_format", ["packed640", "bf16"])
+@pytest.mark.parametrize("case", sorted(GATHER_ID_CASES))
+def test_debug_gather_row_ids_of_other_formats(cuda_device, kv_format, case):
+    """Row ids only (no row bytes), which every row format supports."""
+    w = GATHER_ID_CASES[case](kv_format)
+    toks = W.subset_tokens(w, 12, seed=len(case)).tolist()
+    args = W.device_inputs(w, cuda_device)
+    out = torch.empty_like(args["q"])
+    p = Q.make_params(attn_out=out, **{k: v for k, v in args.items() if k != "return_softmax_lse"})
+    max_rows = 1280
+    n = len(toks)
+    tok = torch.tensor(toks, dtype=torch.int32, device=cuda_device)
+    ids = torch.empty(n, max_rows, dtype=torch.int32, device=cuda_device)
+    counts = torch.empty(n, dtype=torch.int32, device=cuda_device)
+    Q.debug_gather(p, tok, max_rows, None, None, ids, counts)
+    torch.cuda.synchronize()
+    assert Q.device_status() == 0
+    ids, counts = ids.cpu().numpy(), counts.cpu().numpy()
+    for j, t in enumerate(toks):
+        e_ids, _, _ = _expected_slots(w, t, with_bytes=False)
+        assert counts[j] == len(e_ids)
+        m = min(len(e_ids), max_rows)
+        assert np.array_equal(ids[j, :m], np.array(e_ids[:m], dtype=np.int32))
+    rows = torch.empty(n, max_rows, 512, dtype=torch.uint8, device=cuda_device)
+    ids_d = torch.empty(n, max_rows, dtype=torch.int32, device=cuda_device)
+    counts_d = torch.empty(n, dtype=torch.int32, device=cuda_device)
+    with pytest.raises(Q.QsfmError):  # row bytes are exported for fp8 rows only (refused before launch)
+        Q.debug_gather(p, tok, max_rows, rows, None, ids_d, counts_d)
 
 
 # --------------------------------------------------------- fault reporting

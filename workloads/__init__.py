@@ -87,6 +87,10 @@ class Workload:
         return int(self.q.shape[0])
 
     @property
+    def n1(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
     def k2(self) -> int:
         return 0 if self.cmp_sparse_indices is None else int(self.cmp_sparse_indices.shape[-1])
 
@@ -288,15 +292,29 @@ def build(
     )
 
 
+_build = build
+
+
 def _uniform_int(gen: torch.Generator, lo: int, hi: int, n: int) -> np.ndarray:
     """n integers uniform on the inclusive range [lo, hi]."""
     return torch.randint(lo, hi + 1, (n,), generator=gen).numpy().astype(np.int64)
 
 
-def config(index: int, seed: Optional[int] = None) -> Workload:
-    """The five spec workloads; seed defaults to the workload index."""
+def config(index: int, seed: Optional[int] = None, kv_format: str = "fp8_fp32_scales",
+           n1: int = NUM_HEADS) -> Workload:
+    """The five spec workloads; seed defaults to the workload index.
+
+    kv_format / n1 give the same workload with another KV row format or head
+    count (the indices, lengths and block tables are drawn the same way; the
+    name says what changed)."""
     seed = index if seed is None else seed
     gen = torch.Generator().manual_seed(10_000 + seed)
+    extra = dict(kv_format=kv_format, n1=n1)
+    tag = ("" if kv_format == "fp8_fp32_scales" else f" kv={kv_format}") + ("" if n1 == NUM_HEADS else f" N1={n1}")
+
+    def build(name, **kw):  # the module-level build with the format / head count applied
+        return _build(name + tag, **kw, **extra)
+
     if index == 0:  # tiny CSA decode
         return build("tiny CSA decode B=2 S1=1 S2=4096 r=4 K2=512 (384 valid)",
                      layout="BSND", q_lens=[1, 1], s2=[4096, 4096], cmp_ratio=4,
