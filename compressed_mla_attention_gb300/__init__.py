@@ -363,3 +363,57 @@ def quant_sparse_flash_mla(
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev) if nbytes else None
     forward(p, workspace, stream)
     return attn_out, lse
+
+
+def sparse_compressed_flash_attention(
+    query,
+    q_act_seqs,
+    ori_kv,
+    cmp_kv,
+    ori_block_table,
+    cmp_block_table,
+    atten_sink,
+    seqused_kv,
+    cmp_sparse_indices,
+    softmax_scale: float,
+    win_size: int = 128,
+    cmp_ratio: int = 4,
+    stream=None,
+):
+    """The bf16-KV entry point with SparseCompressedFlashAttention's argument
+    names and shapes (its parameter table; TND only), on the same kernels.
+
+    query [T1 * N1, 512] bf16 (N1 = 64); q_act_seqs int32 [B], the running
+    token totals per batch (no leading zero); ori_kv / cmp_kv bf16
+    [block_num * 128, 512]; block tables int32 [B, width]; atten_sink fp32
+    [N1]; seqused_kv int32 [B]; cmp_sparse_indices int32 [T1, K2].
+    The window of win_size tokens ending at the query is band mode 4 with
+    ori_win_left = win_size - 1 and ori_win_right = 0; the compressed part
+    takes the causal mode 3. Returns attention_out [T1 * N1, 512] bf16.
+    Argument marshalling only: views of the given tensors, and cu_seqlens_q
+    = [0, q_act_seqs...] (one small device concatenation).
+    """
+    import torch
+
+    n1 = int(atten_sink.shape[0])
+    if query.dim() != 2 or int(query.shape[0]) % n1:
+        raise ValueError("query must be [T1 * N1, D] with N1 = atten_sink.shape[0]")
+    if win_size < 1:
+        raise ValueError("win_size must be >= 1")
+    t1 = int(query.shape[0]) // n1
+    d = int(query.shape[1])
+
+    def paged(kv):  # [block_num * 128, D] -> [block_num, 128, 1, D] (a view)
+        if kv.dim() != 2 or int(kv.shape[0]) % BLOCK_SIZE:
+            raise ValueError("ori_kv / cmp_kv must be [block_num * 128, D]")
+        return kv.view(int(kv.shape[0]) // BLOCK_SIZE, BLOCK_SIZE, 1, int(kv.shape[1]))
+
+    cu = torch.cat([torch.zeros(1, dtype=q_act_seqs.dtype, device=q_act_seqs.device), q_act_seqs])
+    out, _ = quant_sparse_flash_mla(
+        query.view(t1, n1, d), paged(ori_kv), None, ori_block_table, seqused_kv,
+        layout="TND", cmp_kv=paged(cmp_kv), cmp_block_table=cmp_block_table,
+        cmp_sparse_indices=cmp_sparse_indices.view(t1, 1, int(cmp_sparse_indices.shape[-1])),
+        cu_seqlens_q=cu, sinks=atten_sink, softmax_scale=float(softmax_scale), cmp_ratio=int(cmp_ratio),
+        ori_mask_mode=4, cmp_mask_mode=3, ori_win_left=int(win_size) - 1, ori_win_right=0,
+        stream=stream)
+    return out.view(t1 * n1, d)

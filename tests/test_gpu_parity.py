@@ -157,6 +157,28 @@ def test_wide_shape_parity(cuda_device, name, ctas):
     assert_parity(out, lse, w, range(w.total_t))
 
 
+def test_sparse_compressed_flash_attention_entry(cuda_device):
+    """The bf16-KV entry point with SparseCompressedFlashAttention's argument
+    layout (flat query and KV, q_act_seqs without the leading zero, win_size)
+    matches the oracle and gives the same bits as the general entry point."""
+    w = W.build("scfa", layout="TND", q_lens=[3, 1, 4], s2=[5000, 700, 20000], cmp_ratio=4, mode="CSA",
+                k2=512, kv_format="bf16", with_residual=False, seed=41)
+    a = W.device_inputs(w, cuda_device)
+    T = w.total_t
+    out = Q.sparse_compressed_flash_attention(
+        a["q"].reshape(T * 64, 512), a["cu_seqlens_q"][1:].contiguous(), a["ori_kv"].reshape(-1, 512),
+        a["cmp_kv"].reshape(-1, 512), a["ori_block_table"], a["cmp_block_table"], a["sinks"],
+        a["seqused_ori_kv"], a["cmp_sparse_indices"].reshape(T, 512), w.softmax_scale,
+        win_size=128, cmp_ratio=4)
+    torch.cuda.synchronize()
+    assert Q.device_status() == 0
+    assert out.shape == (T * 64, 512)
+    got = out.float().cpu().reshape(T, 64, 512).numpy()
+    general, _ = run_gpu(w, cuda_device)
+    assert np.array_equal(got, general)
+    assert_parity(got, None, w, range(T))
+
+
 @pytest.mark.parametrize("name", sorted(EDGE))
 @pytest.mark.parametrize("ctas", [0, 3])
 def test_edge_case_parity(cuda_device, name, ctas):
