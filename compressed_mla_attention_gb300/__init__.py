@@ -1,5 +1,6 @@
 """Python binding of libqsfm, the quantized shared-KV sparse MLA attention
-forward for sm_103a (QuantSparseFlashMla / KvQuantSparseAttnSharedKv).
+forward for sm_103a (QuantSparseFlashMla / KvQuantSparseAttnSharedKv, and the
+bf16-KV SparseCompressedFlashAttention).
 
 This module only marshals arguments: it fills the C ``qsfm_params`` struct
 from torch tensors (device pointers, shapes) and calls the C ABI declared in
