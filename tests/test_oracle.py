@@ -106,6 +106,20 @@ def test_oracle_matches_brute_force_packed_rows(i):
     assert np.allclose(l_ref[fin], l_bf.numpy()[fin], rtol=1e-12)
 
 
+def test_bf16_all_bit_patterns_match_torch():
+    """Every one of the 65,536 bf16 bit patterns, decoded by the oracle, equals
+    torch's own bfloat16 -> float64 conversion (NaNs compared as NaNs)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype("<u2")
+    rows = bits.view(np.uint8).reshape(-1, 1024)  # 64 rows of 512 elements
+    with np.errstate(invalid="ignore"):  # the signalling-NaN patterns
+        got = O.decode_bf16_rows(rows).reshape(-1)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))  # -0.0 kept
+
+
 def test_bf16_row_by_hand():
     """A bf16 row (1024 little-endian bytes) built from the bf16 format
     definition: 1 sign bit, 8 exponent bits with bias 127, 7 mantissa bits."""

@@ -186,3 +186,16 @@ def test_big_endian_bf16_is_caught(monkeypatch):
     monkeypatch.setattr(O, "decode_bf16_rows", decode_bf16_rows)
     assert _fails([P.test_bf16_row_by_hand] + [lambda i=i: P.test_oracle_matches_brute_force_bf16_rows(i)
                                                for i in range(len(P.BF16_CASES))])
+
+
+def test_bf16_subnormal_flush_is_caught(monkeypatch):
+    """bf16 subnormals (and -0.0) flushed to +0.0."""
+    orig = O.decode_bf16_rows
+
+    def decode_bf16_rows(rows):
+        k = orig(rows)
+        k[np.abs(k) < 2.0 ** -126] = 0.0
+        return k
+
+    monkeypatch.setattr(O, "decode_bf16_rows", decode_bf16_rows)
+    assert _fails([P.test_bf16_all_bit_patterns_match_torch, P.test_bf16_row_by_hand])
