@@ -59,6 +59,18 @@ def test_config_parity(cuda_device, i):
     print(f"config {i}: {len(toks)} tokens checked, max |err| {err:.3g}")
 
 
+@pytest.mark.parametrize("kv_format,n1", [("packed640", 64), ("bf16", 64), ("fp8_fp32_scales", 128)])
+def test_config2_other_formats_full_size(cuda_device, kv_format, n1):
+    """The CSA decode batch at full size with the other row formats and head
+    count, in the launch configuration the bench times (default CTA count),
+    on sampled tokens (every output element of each)."""
+    w = W.config(2, kv_format=kv_format, n1=n1)
+    out, lse = run_gpu(w, cuda_device, lse=True)
+    assert np.isfinite(out).all()
+    toks = W.subset_tokens(w, 24, seed=6).tolist()
+    assert_parity(out, lse, w, toks)
+
+
 def test_config2_all_ctas_variants(cuda_device):
     """The decode batch planned over fewer CTAs than SMs gives the same result."""
     w = W.config(2)
