@@ -67,6 +67,13 @@ qsfm_status resolve_ctas(const qsfm_params& p, int* out) {
   return QSFM_OK;
 }
 
+// Limits of the kernels' 32-bit index arithmetic (work units, head rows,
+// index offsets within a row, physical KV rows). Every batch that fits in
+// device memory is far below them; larger shapes are refused, not wrapped.
+constexpr long long kMaxUnits = 1ll << 24;     // units x 64 head rows < 2^31
+constexpr int kMaxK2 = 1 << 16;                // index entries per token
+constexpr long long kMaxPoolRows = (1ll << 31) - 1;
+
 // True for a null pointer or one aligned to `bytes`.
 bool aligned(const void* ptr, uintptr_t bytes) {
   return (reinterpret_cast<uintptr_t>(ptr) & (bytes - 1)) == 0;
@@ -87,6 +94,10 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
     if (p.cu_seqlens_q == nullptr && p.batch > 0) return QSFM_ERR_INVALID_ARG;
   }
   if (p.num_ctas < 0 || p.num_ctas > QSFM_MAX_CTAS) return QSFM_ERR_INVALID_ARG;
+  const long long tokens = p.layout_q == QSFM_LAYOUT_BSND ? (long long)p.batch * p.max_s1 : p.total_t;
+  if (tokens * (p.n1 / QSFM_NUM_HEADS) > kMaxUnits) return QSFM_ERR_UNSUPPORTED;
+  if (p.k2 < 0) return QSFM_ERR_INVALID_ARG;
+  if (p.k2 > kMaxK2) return QSFM_ERR_UNSUPPORTED;
   // paged ori KV is always present
   if (p.ori_block_size < 1 || p.ori_block_size > 1024) return QSFM_ERR_INVALID_ARG;
   if (p.ori_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
@@ -101,6 +112,7 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
       p.seqused_ori_kv == nullptr)
     return QSFM_ERR_INVALID_ARG;
   if (p.ori_max_blocks < 1 || p.ori_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
+  if ((long long)p.ori_num_blocks * p.ori_block_size > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
   if (p.cmp_ratio < 1 || p.cmp_ratio > 128) return QSFM_ERR_INVALID_ARG;
   if (p.cmp_kv == nullptr) {
     if (p.cmp_ratio != 1) return QSFM_ERR_INVALID_ARG;  // SWA keeps the default 1
@@ -110,6 +122,7 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
     if (p.cmp_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
     if ((!no_scales && p.cmp_scale == nullptr) || p.cmp_block_table == nullptr) return QSFM_ERR_INVALID_ARG;
     if (p.cmp_max_blocks < 1 || p.cmp_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
+    if ((long long)p.cmp_num_blocks * p.cmp_block_size > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
     if (p.cmp_sparse_indices != nullptr && p.k2 < 1) return QSFM_ERR_INVALID_ARG;
   }
   if (p.ori_mask_mode != 0 && p.ori_mask_mode != 3 && p.ori_mask_mode != 4)

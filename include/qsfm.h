@@ -130,6 +130,10 @@ typedef enum { QSFM_LAYOUT_BSND = 0, QSFM_LAYOUT_TND = 1 } qsfm_q_layout;
  * attn_out must be 16-byte aligned and every other pointer 4-byte aligned
  * (QSFM_ERR_INVALID_ARG otherwise). The parameter names follow
  * QuantSparseFlashMla, "参数说明" (parameter table).
+ * Size limits of the kernels' 32-bit index arithmetic (QSFM_ERR_UNSUPPORTED
+ * beyond them; every batch that fits in device memory is far below): at
+ * most 2^24 work units (tokens x n1 / 64), k2 <= 65536, and fewer than 2^31
+ * rows in each KV pool (num_blocks x block_size).
  */
 typedef struct qsfm_params {
   /* shapes */

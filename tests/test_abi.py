@@ -185,6 +185,26 @@ def test_debug_gather_exports_bytes_for_fp8_rows_only(lib):
         assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, None, None, None, 0x1000, None) == 1
 
 
+@pytest.mark.parametrize("why,change", [
+    ("2^24 + 1 units", dict(batch=(1 << 24) + 1, max_s1=1)),
+    ("2^23 + 1 tokens of 128 heads", dict(batch=(1 << 23) + 1, max_s1=1, n1=128)),
+    ("k2 above 65536", dict(k2=(1 << 16) + 1)),
+    ("2^31 rows in the ori pool", dict(ori_num_blocks=1 << 24)),
+])
+def test_index_limits_are_refused(lib, why, change):
+    # qsfm_forward_workspace_size validates like qsfm_forward and never launches
+    p = _valid(lib)
+    for k, v in change.items():
+        setattr(p, k, v)
+    assert _status(lib, p, fn="workspace") == 2, why  # QSFM_ERR_UNSUPPORTED
+
+
+def test_index_limits_allow_the_largest_shapes(lib):
+    p = _valid(lib)
+    p.batch, p.max_s1, p.k2, p.ori_num_blocks = 1 << 23, 2, 1 << 16, (1 << 24) - 1
+    assert _status(lib, p, fn="workspace") == 0  # validation only, nothing launched
+
+
 def test_n1_128_passes_validation(lib):
     p = _valid(lib)
     p.n1 = 128
