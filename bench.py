@@ -9,7 +9,11 @@ cmp_ratio 4, K2 = 512 top-k indices, fp8 e4m3 KV with per-64 fp32 scales,
 128-token pages). Metric: query tokens per second.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl qsfm|reference]
-                  [--workload I] [--quick]
+                  [--workload I] [--kv-format fp8_fp32_scales|packed640|bf16]
+                  [--n1 64|128] [--quick]
+
+--kv-format and --n1 time the same workload with another KV row format or
+head count (the default line is fp8 rows with fp32 scales and 64 heads).
 
 Under torchrun each rank runs its own replica of the batch (no collective on
 the data path); the step time is the max over ranks and the value counts the
