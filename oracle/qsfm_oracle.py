@@ -331,14 +331,18 @@ def _reference_chunk(tokens):
 def reference_parallel(w, tokens, processes: int):
     """reference() split over a pool of `processes` forked workers.
 
-    The workers inherit w through fork (no copy of the KV pools), so this
-    must run before the calling process initialises CUDA.
+    The workers inherit w through fork (no copy of the KV pools). A process
+    forked after CUDA is initialised can hang, so once the calling process
+    has initialised CUDA this runs serially instead.
     """
     import multiprocessing as mp
+    import sys
 
     global _FORK_WORKLOAD
     tokens = list(tokens)
-    if processes <= 1 or len(tokens) < 2:
+    torch_mod = sys.modules.get("torch")
+    cuda_up = torch_mod is not None and torch_mod.cuda.is_initialized()
+    if processes <= 1 or len(tokens) < 2 or cuda_up:
         return reference(w, tokens)
     chunks = [tokens[i::processes] for i in range(processes)]
     _FORK_WORKLOAD = w

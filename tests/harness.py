@@ -1,7 +1,7 @@
 """Helpers for the GPU parity tests: run the CUDA path, compare with the oracle.
 
-Tolerances (spec description of the path): each bf16 output element
-within 1e-2 + 2e-2 * |ref| of the fp64 oracle, lse within 1e-3 absolute.
+Tolerances stated for the path: each bf16 output element within
+1e-2 + 2e-2 * |ref| of the fp64 oracle, lse within 1e-3 absolute.
 """
 
 from __future__ import annotations
