@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import re
 from typing import Optional
 
 PKG = os.path.dirname(os.path.abspath(__file__))
@@ -262,7 +263,16 @@ def combine(params: QsfmParams, workspace=None, stream=None) -> None:
     _check("qsfm_combine", lib().qsfm_combine(ctypes.byref(params), w, n, _stream_ptr(stream)))
 
 
-NOALLOC_SCRATCH_BYTES = 8 << 20
+def _header_scratch_bytes() -> int:
+    """QSFM_NOALLOC_SCRATCH_BYTES as the C header defines it."""
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qsfm.h")
+    m = re.search(r"#define QSFM_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", open(path).read())
+    if m is None:
+        raise RuntimeError("QSFM_NOALLOC_SCRATCH_BYTES not found in qsfm.h")
+    return int(m.group(1)) << int(m.group(2))
+
+
+NOALLOC_SCRATCH_BYTES = _header_scratch_bytes()
 
 
 def forward_noalloc(params: QsfmParams, stream=None) -> None:

@@ -11,6 +11,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
@@ -23,10 +24,15 @@ namespace {
 // library. Kernels get its address as an argument.
 __device__ int g_fault_word;
 
+// The address is looked up once per device, under a lock: two host threads
+// making their first call on a device at the same time both see it set.
+std::mutex g_fault_lock;
+
 int* fault_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   static int* ptrs[64] = {nullptr};
+  std::lock_guard<std::mutex> guard(g_fault_lock);
   if (ptrs[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
@@ -272,15 +278,17 @@ qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens, int32
                               int32_t* row_ids_out, int32_t* counts_out, void* stream) {
   qsfm_status st = validate(p, false);
   if (st != QSFM_OK) return st;
-  // row bytes + scales are exported as 512-B fp8 rows and 8 fp32 scales;
-  // the row ids alone (rows_out = scales_out = NULL) are format-independent
-  const bool ids_only = rows_out == nullptr && scales_out == nullptr;
-  if (!ids_only && p->kv_layout != QSFM_KV_FP8_FP32_SCALES) return QSFM_ERR_UNSUPPORTED;
+  // row bytes are exported in the pool's own row format; separate scales
+  // exist for fp8 rows only. With rows_out = scales_out = NULL only the row
+  // ids and counts are written.
+  const bool fp8 = p->kv_layout == QSFM_KV_FP8_FP32_SCALES;
+  if (!fp8 && scales_out != nullptr) return QSFM_ERR_INVALID_ARG;
+  if (fp8 && (rows_out == nullptr) != (scales_out == nullptr)) return QSFM_ERR_INVALID_ARG;
   if (n < 0 || max_rows < 0) return QSFM_ERR_INVALID_ARG;
   if (n == 0) return QSFM_OK;
   if (tokens == nullptr || counts_out == nullptr) return QSFM_ERR_INVALID_ARG;
-  if (max_rows > 0 && (row_ids_out == nullptr || (!ids_only && (rows_out == nullptr || scales_out == nullptr))))
-    return QSFM_ERR_INVALID_ARG;
+  if (max_rows > 0 && row_ids_out == nullptr) return QSFM_ERR_INVALID_ARG;
+  if (!aligned(rows_out, 16)) return QSFM_ERR_INVALID_ARG;
   int* fault = fault_ptr();
   if (fault == nullptr) return QSFM_ERR_CUDA;
   return cuda_status(qsfm::launch_debug_gather(*p, tokens, n, max_rows, rows_out, scales_out,

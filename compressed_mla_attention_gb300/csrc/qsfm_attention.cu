@@ -1,58 +1,61 @@
 // Attention kernel of the quantized shared-KV sparse MLA forward (sm_103a).
 //
-// Computes, for every planned (token, KV-tile range) piece,
+// Computes, for every planned (work unit, KV-tile range) piece,
 //   O = softmax([Q K~^T * softmax_scale, sink]) V~  with K~ = V~
 // (QuantSparseFlashMla, function description formula; sink from its
 // parameter table row "sinks"; lse from KvQuantSparseAttnSharedKv, parameter
 // table row softmax_lse).
 //
 // Orientation. The contractions run transposed so that the KV rows of a tile
-// (64 rows) are the M dimension of the score product and the 64 heads are N:
-//   S^T[j, h]  = sum_d K~[j, d] Q[h, d]      (M = 64 rows, N = 64, K = 512)
+// (128 rows) are the M dimension of the score product and the 64 heads of a
+// unit are N:
+//   S^T[j, h]  = sum_d K~[j, d] Q[h, d]      (M = 128 rows, N = 64, K = 512)
 //   O^T[d, h] += sum_j V~[j, d] P[h, j]      (M = 128 d per chunk, N = 64,
-//                                             K = 64 rows, 4 chunks)
-// Both accumulators live in tensor memory: S^T in two buffers of 64 columns
-// (an M = 64 accumulator fills lanes 0-15 of each 32-lane quarter), O^T in
-// 256 columns. One dequantised bf16 tile (64 rows x 512, 128-B swizzle, 8
-// d-blocks of 8 KB) is the K-major A operand of the first product and, read
-// through an MN-major descriptor, the A operand of the second.
+//                                             K = 128 rows, 4 chunks)
+// Both accumulators live in tensor memory: S^T in 64 columns (lane = tile
+// row), O^T in 256 columns (lane = head-dim element of a 128-wide chunk).
+// The dequantised bf16 tile (128 rows x 512, eight 16 KB slabs of 64 d with
+// the 128-byte swizzle) is the K-major A operand of the first product and,
+// read through an MN-major descriptor, the A operand of the second: each row
+// is dequantised once and read by both products.
 //
-// Pipeline. Two tile stages in shared memory: while the tensor cores and the
-// softmax work on tile n, the producers fill the other stage with tile n+1.
-// Two threads issue the tensor-core work, each in its own order: QK^T of a
-// tile chunk by chunk as the producers publish it, PV of a tile once the
-// softmax has written P. So QK^T(n+1) runs while the softmax works on tile
-// n, and PV(n) while the producers fill tile n+2's stage. Before the plan is
-// readable (the plan kernel may still run), the producer warps warm L2 with
-// the inputs of the token the CTA most likely starts with.
+// Pipeline. One tile buffer, in four chunks of two slabs (128 d each). The
+// single MMA-issuing thread runs, per tile n:
+//   PV(n) chunks 0..3 (a commit after chunks 1 and 3 frees them in pairs),
+//   then QK^T(n + 1) chunks 0..3 as the workers refill them with tile n + 1,
+// so the workers store chunks 0 and 1 of tile n + 1 while the tensor cores
+// run chunks 2 and 3 of PV(n). Only the softmax of a tile (between its last
+// QK^T MMA and its first PV MMA) leaves the tensor pipe idle. Commits are
+// kept few: each one drains the tensor pipe (about 140 cycles).
 //
-// Warp roles (15 warps; at most 4 per SM sub-partition, so 128 registers):
-//   warps 0-3   softmax + epilogue. Warp q owns tile rows 16q..16q+15; each
-//               thread holds two rows x 16 heads of S^T (the accumulator-
-//               fragment layout), keeps the row sums of its 16 heads in
-//               registers and writes its P values with stmatrix. In the
-//               epilogue thread i owns head-dim lane i of O^T.
-//   warps 4-11  producers: take a tile's physical rows from the resolver,
-//               load their fp8 bytes and scales into registers, dequantise
-//               the whole tile into registers, start the next tile's loads,
-//               then store the tile chunk by chunk (a chunk = 64 rows x 128 d
-//               = 2 d-blocks) once its stage is free. Packed 640-byte rows
-//               and bf16 rows have producers of their own (one kernel
-//               instantiation per row format); the tile they store is the
-//               same.
-//   warp 12     QK^T issue (one thread): Q by TMA, QK^T chunk by chunk as the
-//               producers publish the chunks.
-//   warp 14     PV issue (one thread): PV once the softmax has written P, and
-//               the commits that release stages and hand O^T to the epilogue.
-//   warp 13     resolver: runs up to 4 tiles ahead, turns each tile's slots
-//               into physical rows (sparse indices, block tables) in a
-//               shared-memory ring, and asks L2 for those rows' bytes.
+// Warp roles (10 warps, at most 3 per SM sub-partition, so up to 168
+// registers per thread):
+//   warps 0-7   workers: each tile's softmax, the production of the next
+//               tile and each unit's epilogue, in that order.
+//               Softmax / epilogue view: warp w reads tensor-memory lanes
+//               32 (w % 4) .. + 31 (tile rows, or head-dim elements of a
+//               128-wide O^T chunk) and heads 32 (w / 4) .. + 31; each thread
+//               writes its P values (bf16, the MN-major B operand of PV);
+//               lane i keeps the running sum of P for head 32 (w / 4) + i
+//               over the warp's rows.
+//               Producer view: thread (row_lo, j) holds rows row_lo + 32 u
+//               (u < 4) of the next tile, raw, in registers (all four
+//               chunks for fp8 and packed rows; two for bf16 rows); once PV
+//               has read a chunk's slabs it dequantises that chunk (fp8 ->
+//               f16 -> fp32 x scale -> bf16), stores and publishes it; after
+//               the last chunk it loads the tile after next, which then has
+//               a whole tile's time in flight.
+//   warp 8      MMA issue (one thread): Q by TMA, PV and QK^T as above.
+//   warp 9      resolver: turns the tiles' slots into physical rows (sparse
+//               indices, block tables, masks), four tiles per pass with all
+//               their loads in flight together, up to 8 tiles ahead, into a
+//               shared-memory ring, and asks L2 for each new unit's Q.
 // mbarriers carry every hand-off; every wait is bounded in time.
 //
 // Softmax: the running max m_used per head is moved only when a tile's max
 // exceeds it by more than 8 (log2 units); a named-barrier vote detects that
-// case, so most tiles need no cross-thread max reduction. When it moves, O^T
-// and the row sums l are rescaled exactly. P <= 2^8 in bf16.
+// case, so most tiles need no cross-row max reduction. When it moves, O^T
+// and the row sums are rescaled exactly. P <= 2^8 in bf16.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -65,58 +68,58 @@
 namespace qsfm {
 namespace {
 
-static_assert(kTileRows == 64, "the kernel's layouts assume 64-row tiles");
+static_assert(kTileRows == 128, "the kernel's layouts assume 128-row tiles");
 
-constexpr int kSoftWarps = 4;
-constexpr int kProdWarps = 8;
-constexpr int kMmaWarp = kSoftWarps + kProdWarps;
+constexpr int kWorkWarps = 16;
+constexpr int kWorkThreads = kWorkWarps * 32;
+constexpr int kHPT = 256 / kWorkWarps;       // heads per worker thread (softmax, epilogue)
+constexpr int kRPT = 32 / kWorkWarps;        // tile rows per worker thread (producer)
+constexpr int kRowStride = 4 * kWorkWarps;   // between a producer thread's rows
+static_assert(kHPT == 16 || kHPT == 32, "worker warps: 8 or 16");
+constexpr int kMmaWarp = kWorkWarps;
 constexpr int kResolverWarp = kMmaWarp + 1;
-constexpr int kPvWarp = kResolverWarp + 1;
-constexpr int kThreads = (kPvWarp + 1) * 32;
-constexpr int kRing = 4;  // tiles of resolved rows in flight
-constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kBarSoft = 1;  // named barrier id of the softmax warps
-constexpr int kStages = 2;
+constexpr int kThreads = (kResolverWarp + 1) * 32;
+constexpr int kRing = 8;     // tiles of resolved rows in flight
+constexpr int kResolveTiles = 4;  // tiles the resolver resolves per pass (loads in flight together)
+constexpr int kBarWork = 1;  // named barrier id of the worker warps
 
 // shared memory map (byte offsets from a 1024-aligned base)
-constexpr uint32_t kDBlockBytes = kTileRows * 128;           // 64 rows x 64 d (bf16)
-constexpr uint32_t kStageBytes = 8 * kDBlockBytes;           // one tile: 64 KB
-constexpr uint32_t kPBytes = kTileRows * 128;                // P: 64 rows x 64 heads (bf16)
-constexpr uint32_t kSK = 0;                                  // K~ stages
-constexpr uint32_t kSQ = kSK + kStages * kStageBytes;        // Q: 8 d-blocks x 64 heads x 128 B
-constexpr uint32_t kSP = kSQ + 8 * 64 * 128;                 // P stages
-constexpr uint32_t kSRed = kSP + kStages * kPBytes;          // [4][64] f32 per-warp partials
-constexpr uint32_t kSMUsed = kSRed + 1024;                   // [64] f32
-constexpr uint32_t kSAlpha = kSMUsed + 256;                  // [64] f32
-constexpr uint32_t kSInv = kSAlpha + 256;                    // [64] f32
-constexpr uint32_t kSValid = kSInv + 256;                    // [2][64] i32
-constexpr uint32_t kSRows = kSValid + 512;                   // [kRing][64] i32 physical rows
+constexpr uint32_t kSlabBytes = kTileRows * 128;                // 128 rows x 64 d (bf16): 16 KB
+constexpr uint32_t kSK = 0;                                     // K~ tile: 8 slabs
+constexpr uint32_t kSQ = kSK + 8 * kSlabBytes;                  // Q: 8 d-blocks x 64 heads x 128 B
+constexpr uint32_t kSP = kSQ + 8 * 64 * 128;                    // P: 128 rows x 64 heads (bf16)
+constexpr uint32_t kSRows = kSP + kTileRows * 128;              // [kRing][128] i32 physical rows
 constexpr uint32_t kSRowKind = kSRows + kRing * kTileRows * 4;  // [kRing] i32: 0 ori, 1 cmp, -1 end
-constexpr uint32_t kSBar = kSRowKind + 64;                   // mbarriers, tmem base, flags
+constexpr uint32_t kSValid = kSRowKind + 64;                    // [128] i32: row of the tile valid
+constexpr uint32_t kSRed = kSValid + kTileRows * 4;             // [4][64] f32 per-quadrant partials
+constexpr uint32_t kSMUsed = kSRed + 1024;                      // [64] f32
+constexpr uint32_t kSAlpha = kSMUsed + 256;                     // [64] f32
+constexpr uint32_t kSInv = kSAlpha + 256;                       // [64] f32
+constexpr uint32_t kSBar = kSInv + 256;                         // mbarriers, tmem base, flags
 constexpr uint32_t kSmemBytes = kSBar + 256;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+static_assert(kSmemAlloc <= 232448, "more than the 227 KB a CTA may use");
 
 // mbarrier slots
 constexpr int kBarQFull = 0;
-constexpr int kBarKvFull = 1;    // [stage][chunk], one arrive per producer warp
-constexpr int kBarKvEmpty = 9;   // [stage]: the PV product of the stage's tile completed
-constexpr int kBarSFull = 11;    // [stage]
-constexpr int kBarSFree = 13;    // [stage]
-constexpr int kBarPFull = 15;    // [stage]
-constexpr int kBarODone = 17;
-constexpr int kBarOFree = 18;
-constexpr int kBarRowsFull = 19;   // [ring slot]
-constexpr int kBarRowsEmpty = 23;  // [ring slot], one arrive per producer warp
+constexpr int kBarFull = 1;       // [chunk]: stored (one arrive per worker warp)
+constexpr int kBarFree = 5;       // [chunk pair]: PV of chunks 2i, 2i + 1 completed (commit)
+constexpr int kBarSFull = 7;      // S^T of the tile complete (commit)
+constexpr int kBarPFull = 8;      // P of the tile written (one arrive per worker warp)
+constexpr int kBarOFree = 9;      // O^T read by the epilogue (one arrive per worker warp)
+constexpr int kBarDrain = 10;     // every MMA of the CTA completed (commit)
+constexpr int kBarRowsFull = 11;  // [ring slot]
+constexpr int kBarRowsEmpty = 19; // [ring slot], one arrive per worker warp
 constexpr int kNumBars = 27;
 static_assert(kNumBars * 8 <= 224, "barriers overlap the tmem slot");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;  // + 64 * stage
-constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemO = 256;  // + 64 * chunk
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kIdescQK = make_idesc_bf16(64, 64, /*a_mn=*/0, /*b_mn=*/0);
+constexpr uint32_t kIdescQK = make_idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, 64, /*a_mn=*/1, /*b_mn=*/1);
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -124,7 +127,7 @@ struct Range {
   int t0, k0, t1, k1;
 };
 
-// Walks the (token, tile-range) pieces of a CTA's range in order.
+// Walks the (unit, tile-range) pieces of a CTA's range in order.
 struct PieceIter {
   const qsfm_params* p;
   Range r;
@@ -142,7 +145,7 @@ struct PieceIter {
   }
 };
 
-// Walks the (token, tile) jobs of the range, skipping tokens without tiles.
+// Walks the (unit, tile) jobs of the range, skipping units without tiles.
 struct JobIter {
   PieceIter pieces;
   int tok = -1, k = 0, hi = 0;
@@ -166,23 +169,45 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Max (kMax) or sum of 16 values per lane over the 8 lanes of a warp that
-// share lane % 4 (lane bits 2-4). Afterwards lane l holds, in v[0] and v[1],
-// the results for value indices 2 * (l >> 2) and 2 * (l >> 2) + 1.
-template <bool kMax>
-__device__ __forceinline__ void reduce_rows16(float (&v)[16]) {
+// Max (kMax) or sum of kN (16 or 32) values per lane over the 32 lanes of a
+// warp, by halving exchanges (for kN = 16, lanes l and l ^ 16 are combined
+// first): afterwards lane l holds the result for value index l % kN. The
+// array is consumed.
+template <bool kMax, int kN>
+__device__ __forceinline__ float reduce_lanes(float (&v)[kN]) {
   const int lane = threadIdx.x & 31;
+  if constexpr (kN == 16) {
 #pragma unroll
-  for (int w = 16, n = 8; w >= 4; w >>= 1, n >>= 1) {
+    for (int i = 0; i < 16; ++i) {
+      const float got = __shfl_xor_sync(0xffffffffu, v[i], 16);
+      v[i] = kMax ? fmaxf(v[i], got) : v[i] + got;
+    }
+  }
+#pragma unroll
+  for (int w = kN / 2; w >= 1; w >>= 1) {
     const bool up = lane & w;
 #pragma unroll
-    for (int i = 0; i < n; ++i) {
-      const float keep = up ? v[n + i] : v[i];
-      const float send = up ? v[i] : v[n + i];
+    for (int i = 0; i < w; ++i) {
+      const float keep = up ? v[w + i] : v[i];
+      const float send = up ? v[i] : v[w + i];
       const float got = __shfl_xor_sync(0xffffffffu, send, w);
       v[i] = kMax ? fmaxf(keep, got) : keep + got;
     }
   }
+  return v[0];
+}
+
+// kN consecutive tensor-memory columns of the warp's 32 lanes, one lane per
+// thread.
+template <int kN>
+__device__ __forceinline__ void tmem_load(uint32_t taddr, float (&v)[kN]) {
+  if constexpr (kN == 32) tmem_ld32(taddr, v);
+  else tmem_ld16(taddr, v);
+}
+template <int kN>
+__device__ __forceinline__ void tmem_store(uint32_t taddr, const float (&v)[kN]) {
+  if constexpr (kN == 32) tmem_st32(taddr, v);
+  else tmem_st16(taddr, v);
 }
 
 struct Smem {
@@ -216,363 +241,133 @@ __device__ __forceinline__ bool warp_wait_or_abort(const Smem& sm, int bar, uint
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// Asks L2 for the bytes of physical row `prow` of a pool (and its scale row).
+template <int kFmt>
+__device__ __forceinline__ void prefetch_row(const uint8_t* pool, const float* spool, int prow) {
+  constexpr uint32_t kRowB = kv_row_bytes(kFmt);
+  bulk_prefetch_l2(pool + size_t(prow) * kRowB, kRowB);
+  if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) prefetch_l2(spool + size_t(prow) * kScales);
+}
+
 // ------------------------------------------------------------- resolver
-// Tile n's rows go to ring slot n % kRing: 64 physical rows (block * 128 +
+// Tile n's rows go to ring slot n % kRing: 128 physical rows (block * 128 +
 // offset, -1 = masked) and the pool they come from. After the CTA's last tile
-// the resolver writes an end mark (-1) in the next slot.
+// the resolver writes an end mark (-1) in the next slot. Up to kResolveTiles
+// tiles of one unit per pass: all their index loads are in flight together,
+// then all their block-table loads, so a pass costs two memory round trips
+// whatever its tile count.
 template <int kFmt>
 __device__ void resolver_role(const qsfm_params& p, const Smem& sm, Range rg, int T, int* fault) {
+  constexpr int kN = kResolveTiles;
   const int lane = threadIdx.x & 31;
   int* rows = reinterpret_cast<int*>(sm.ptr + kSRows);
   int* kind = reinterpret_cast<int*>(sm.ptr + kSRowKind);
-  JobIter jobs(&p, rg, T);
-  int tok, k, last_tok = -1;
+  const uint8_t* q8 = static_cast<const uint8_t*>(p.q);
+  PieceIter pieces(&p, rg, T);
+  uint32_t n = 0;  // next ring position
+  int unit, lo, hi;
   TokenGeom g;
-  for (uint32_t n = 0;; ++n) {
-    const bool more = jobs.next(tok, k, g);
-    const uint32_t slot = n % kRing;
-    if (!warp_wait_or_abort(sm, kBarRowsEmpty + slot, ((n / kRing) & 1) ^ 1, fault)) return;
-    if (!more) {
-      if (lane == 0) kind[slot] = -1;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(kBarRowsFull + slot));
-      return;
+  while (pieces.next(unit, g, lo, hi)) {
+    if (lo >= hi) continue;
+    // the unit's Q goes to L2 a few tiles before its first product; the next
+    // token's index list while this one is resolved
+    if (lane == 0) bulk_prefetch_l2(q8 + size_t(unit) * kHeads * kDim * 2, kHeads * kDim * 2);
+    if (p.cmp_sparse_indices != nullptr && g.tok + 1 < (T >> unit_shift(p))) {
+      const uint8_t* ix = reinterpret_cast<const uint8_t*>(p.cmp_sparse_indices + (size_t)(g.tok + 1) * p.k2);
+      for (int off = 128 * lane; off < 4 * p.k2; off += 32 * 128) prefetch_l2(ix + off);
     }
-    if (g.tok != last_tok) {
-      // the next token's index list goes to L2 while this token is resolved
-      if (p.cmp_sparse_indices != nullptr && g.tok + 1 < (T >> unit_shift(p))) {
-        const uint8_t* ix = reinterpret_cast<const uint8_t*>(p.cmp_sparse_indices + (size_t)(g.tok + 1) * p.k2);
-        for (int off = 128 * lane; off < 4 * p.k2; off += 32 * 128) prefetch_l2(ix + off);
+    // passes of up to kN tiles of this unit
+    for (int k0 = lo; k0 < hi; k0 += kN) {
+      int k[kN];
+      bool live[kN];
+#pragma unroll
+      for (int t = 0; t < kN; ++t) {
+        k[t] = k0 + t;
+        live[t] = k0 + t < hi;
       }
-      last_tok = g.tok;
-    }
-    const int cmp = k >= g.ori_tiles ? 1 : 0;
-    int pr[2];
-    resolve_two(p, g, k, lane, fault, pr);
-    const uint8_t* pool = static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv);
-    const float* spool = cmp ? p.cmp_scale : p.ori_scale;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      rows[slot * kTileRows + lane + 32 * u] = pr[u];
-      if (pr[u] >= 0) {
-        if constexpr (kFmt == QSFM_KV_PACKED640) {
-          const uint8_t* src = pool + size_t(pr[u]) * QSFM_PACKED_ROW_BYTES;
-#pragma unroll
-          for (int c = 0; c < 5; ++c) prefetch_l2(src + 128 * c);
-        } else if constexpr (kFmt == QSFM_KV_BF16) {
-          const uint8_t* src = pool + size_t(pr[u]) * QSFM_BF16_ROW_BYTES;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) prefetch_l2(src + 128 * c);
-        } else {
-          const uint8_t* src = pool + size_t(pr[u]) * kDim;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) prefetch_l2(src + 128 * c);
-          prefetch_l2(spool + size_t(pr[u]) * kScales);
-        }
+      for (int t = 0; t < kN; ++t) {
+        const uint32_t m = n + t;
+        if (live[t] && !warp_wait_or_abort(sm, kBarRowsEmpty + m % kRing, ((m / kRing) & 1) ^ 1, fault)) return;
       }
-    }
-    if (lane == 0) kind[slot] = cmp;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.bar(kBarRowsFull + slot));
-  }
-}
-
-// ------------------------------------------------------------- producers
-// Thread (row_lo, j) of the 8 producer warps: tile rows row_lo and row_lo +
-// 32, 16-byte slot j of each 128-byte chunk of those rows.
-__device__ void producer_role(const qsfm_params& p, const Smem& sm, int* fault) {
-  const int ptid = threadIdx.x - kSoftThreads;  // 0..255 (8 producer warps)
-  const int lane = threadIdx.x & 31;
-  const int row_lo = ptid >> 3;   // 0..31
-  const int j = ptid & 7;
-  const int odd_first = j >> 2;   // j >= 4 stores its odd 16-B chunk first (no bank conflicts)
-  const int* rows = reinterpret_cast<const int*>(sm.ptr + kSRows);
-  const int* kind = reinterpret_cast<const int*>(sm.ptr + kSRowKind);
-
-  int pr[2];
-  float csc[2];  // scale j of each row (this lane's share of the row's 8 scales)
-  uint4 R0[2], R1[2], R2[2], R3[2];  // fp8 bytes of chunks 0..3 of the two rows
-
-  // Rows of tile n from the ring; their loads start at once. False at the
-  // end mark or on abort.
-  auto fetch = [&](uint32_t n) -> bool {
-    const uint32_t slot = n % kRing;
-    if (!warp_wait_or_abort(sm, kBarRowsFull + slot, (n / kRing) & 1, fault)) return false;
-    const int kd = kind[slot];
-    pr[0] = rows[slot * kTileRows + row_lo];
-    pr[1] = rows[slot * kTileRows + row_lo + 32];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.bar(kBarRowsEmpty + slot));
-    if (kd < 0) return false;
-    const uint8_t* pool = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv);
-    const float* spool = kd ? p.cmp_scale : p.ori_scale;
+      int lg[kN][4], pr[kN][4];
+      bool cmp[kN];
+      resolve_tile_rows<kN>(p, g, k, live, lane, fault, lg, pr, cmp);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const bool v = pr[u] >= 0;
-      const uint8_t* src = pool + size_t(v ? pr[u] : 0) * kDim + 16 * j;
-      R0[u] = v ? ldg_stream_v4(src) : make_uint4(0, 0, 0, 0);
-      R1[u] = v ? ldg_stream_v4(src + 128) : make_uint4(0, 0, 0, 0);
-      R2[u] = v ? ldg_stream_v4(src + 256) : make_uint4(0, 0, 0, 0);
-      R3[u] = v ? ldg_stream_v4(src + 384) : make_uint4(0, 0, 0, 0);
-      csc[u] = v ? __ldg(spool + size_t(pr[u]) * kScales + j) : 0.f;
-    }
-    return true;
-  };
-
-  // Per tile: dequantise it into registers (this waits for its loads), start
-  // the next tile's loads, then wait for the stage and store. The next
-  // tile's loads are in flight during the stage wait and the stores.
-  bool have = fetch(0);
-  for (uint32_t n = 0; have; ++n) {
-    const uint32_t st = n & 1;
-    uint4 D[4][2][2];  // [chunk][row][16-byte half], bf16
-    const int vrow0 = pr[0] >= 0, vrow1 = pr[1] >= 0;
+      for (int t = 0; t < kN; ++t) {
+        if (!live[t]) continue;
+        const uint32_t slot = (n + t) % kRing;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int src_lane = (lane & ~7) | (2 * c + (j >> 2));
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float sc = __shfl_sync(0xffffffffu, csc[u], src_lane);
-        const uint4 raw = c == 0 ? R0[u] : c == 1 ? R1[u] : c == 2 ? R2[u] : R3[u];
-        // packed fp32 multiplies: 3 % faster here (the packed-row producer
-        // keeps dequant16: there they were 2.5 % slower)
-        dequant16_x2(raw, sc, D[c][u][0], D[c][u][1]);
+        for (int u = 0; u < 4; ++u) rows[slot * kTileRows + lane + 32 * u] = pr[t][u];
+        if (lane == 0) kind[slot] = cmp[t] ? 1 : 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.bar(kBarRowsFull + slot));
       }
-    }
-    have = fetch(n + 1);
-    if (!warp_wait_or_abort(sm, kBarKvEmpty + st, ((n >> 1) & 1) ^ 1, fault)) return;
-    const uint32_t stage = sm.base + kSK + st * kStageBytes;
-    if (j == 0) {
-      int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + st * kTileRows;
-      valid[row_lo] = vrow0;
-      valid[row_lo + 32] = vrow1;
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t blk = stage + (2 * c + (j >> 2)) * kDBlockBytes;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int r = row_lo + 32 * u;
-        const uint32_t sw = uint32_t(r & 7);
-        const uint32_t rowb = blk + r * 128;
-        const uint32_t c0 = 2 * (j & 3);
-        sts_v4(rowb + (((c0 + odd_first) ^ sw) << 4), odd_first ? D[c][u][1] : D[c][u][0]);
-        sts_v4(rowb + (((c0 + 1 - odd_first) ^ sw) << 4), odd_first ? D[c][u][0] : D[c][u][1]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(kBarKvFull + 4 * st + c));
+      n += min(kN, hi - k0);
     }
   }
+  // end mark after the CTA's last tile
+  const uint32_t slot = n % kRing;
+  if (!warp_wait_or_abort(sm, kBarRowsEmpty + slot, ((n / kRing) & 1) ^ 1, fault)) return;
+  if (lane == 0) kind[slot] = -1;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sm.bar(kBarRowsFull + slot));
 }
 
-// Producers for packed 640-byte rows (bf16 rope, bytes 0..127 | e4m3fn nope,
-// bytes 128..575 | e8m0 scales, bytes 576..582 | pad; KvQuantSparseAttnSharedKv
-// constraints). The tile in shared memory is the same as for fp8 rows: d 0..63
-// (d-block 0) is the rope, d 64..511 the nope. Thread (row_lo, j): rows
-// row_lo and row_lo + 32; of each row the 16-byte pieces j (rope elements
-// 8j .. 8j + 7, copied as they are) and 8 + m for m = 8i + j, i = 0..3
-// (nope elements 16m .. 16m + 15 of d-block 1 + m / 4 with scale m / 4;
-// i = 3 only for j < 4). Lane j = 4 of each row also loads the piece with
-// the seven scale bytes. Nope piece m lands in chunk (1 + 2i + j / 4) / 2:
-// chunk i for j < 4, chunk i + 1 for j >= 4. The loads of a tile are issued
-// after the previous tile is stored (the registers hold one tile).
 __device__ __forceinline__ float e8m0_value(uint32_t e) {
   // 2^(e - 127): the fp32 with biased exponent e (e = 0: the subnormal 2^-127)
   return e == 0xFFu ? __uint_as_float(0x7FC00000u) : e == 0u ? __uint_as_float(0x00400000u)
                                                              : __uint_as_float(e << 23);
 }
 
-__device__ void producer_role_packed(const qsfm_params& p, const Smem& sm, int* fault) {
-  const int ptid = threadIdx.x - kSoftThreads;  // 0..255 (8 producer warps)
-  const int lane = threadIdx.x & 31;
-  const int row_lo = ptid >> 3;  // 0..31
-  const int j = ptid & 7;
-  const int odd_first = j >> 2;  // j >= 4 stores its odd 16-B unit first (no bank conflicts)
-  const int* rows = reinterpret_cast<const int*>(sm.ptr + kSRows);
-  const int* kind = reinterpret_cast<const int*>(sm.ptr + kSRowKind);
-  constexpr int kRow = QSFM_PACKED_ROW_BYTES;
-
-  int pr[2];
-  uint4 Rr[2];     // rope piece j of each row (bf16)
-  uint4 Rn[4][2];  // nope pieces m = 8i + j (e4m3fn)
-  uint4 Rs[2];     // scale piece (lane j = 4 only)
-
-  auto fetch = [&](uint32_t n) -> bool {
-    const uint32_t slot = n % kRing;
-    if (!warp_wait_or_abort(sm, kBarRowsFull + slot, (n / kRing) & 1, fault)) return false;
-    const int kd = kind[slot];
-    pr[0] = rows[slot * kTileRows + row_lo];
-    pr[1] = rows[slot * kTileRows + row_lo + 32];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.bar(kBarRowsEmpty + slot));
-    if (kd < 0) return false;
-    const uint8_t* pool = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv);
-    const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const bool v = pr[u] >= 0;
-      const uint8_t* base = pool + size_t(v ? pr[u] : 0) * kRow;
-      Rr[u] = v ? ldg_stream_v4(base + 16 * j) : z;
-#pragma unroll
-      for (int i = 0; i < 3; ++i) Rn[i][u] = v ? ldg_stream_v4(base + 128 + 16 * (8 * i + j)) : z;
-      Rn[3][u] = (v && j < 4) ? ldg_stream_v4(base + 128 + 16 * (24 + j)) : z;
-      Rs[u] = (v && j == 4) ? ldg_stream_v4(base + 576) : z;
-    }
-    return true;
-  };
-
-  for (uint32_t n = 0; fetch(n); ++n) {
-    const uint32_t st = n & 1;
-    uint4 D[4][2][2];  // [i][row][16-byte half] of nope piece 8i + j, bf16
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const uint32_t w0 = __shfl_sync(0xffffffffu, Rs[u].x, (lane & ~7) | 4);  // scale bytes 0..3
-      const uint32_t w1 = __shfl_sync(0xffffffffu, Rs[u].y, (lane & ~7) | 4);  // scale bytes 4..6
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int sidx = 2 * i + (j >> 2);  // scale of nope piece 8i + j
-        const uint32_t e = (sidx < 4 ? w0 >> (8 * sidx) : w1 >> (8 * (sidx - 4))) & 0xFFu;
-        dequant16(Rn[i][u], e8m0_value(e), D[i][u][0], D[i][u][1]);
-      }
-    }
-    if (!warp_wait_or_abort(sm, kBarKvEmpty + st, ((n >> 1) & 1) ^ 1, fault)) return;
-    const uint32_t stage = sm.base + kSK + st * kStageBytes;
-    if (j == 0) {
-      int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + st * kTileRows;
-      valid[row_lo] = pr[0] >= 0;
-      valid[row_lo + 32] = pr[1] >= 0;
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int r = row_lo + 32 * u;
-        const uint32_t sw = uint32_t(r & 7);
-        if (c == 0) sts_v4(stage + r * 128 + ((uint32_t(j) ^ sw) << 4), Rr[u]);  // rope: d-block 0
-        // nope piece of this chunk: i = c (j < 4) or i = c - 1 (j >= 4)
-        const bool has = j < 4 || (c >= 1);
-        if (has) {
-          const uint4 lo = (j < 4) ? D[c][u][0] : D[c > 0 ? c - 1 : 0][u][0];
-          const uint4 hi = (j < 4) ? D[c][u][1] : D[c > 0 ? c - 1 : 0][u][1];
-          const int db = 1 + 2 * ((j < 4) ? c : c - 1) + (j >> 2);
-          const uint32_t rowb = stage + db * kDBlockBytes + r * 128;
-          const uint32_t c0 = 2 * (j & 3);
-          sts_v4(rowb + (((c0 + odd_first) ^ sw) << 4), odd_first ? hi : lo);
-          sts_v4(rowb + (((c0 + 1 - odd_first) ^ sw) << 4), odd_first ? lo : hi);
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(kBarKvFull + 4 * st + c));
-    }
-  }
-}
-
-// Producers for bf16 rows (1024 bytes, no quantisation): the row's 16-byte
-// piece q holds elements 8q .. 8q + 7, i.e. unit q % 8 of d-block q / 8.
-// Thread (row_lo, j): rows row_lo and row_lo + 32, pieces 16c + j and
-// 16c + 8 + j of chunk c (unit j of d-blocks 2c and 2c + 1), copied as they
-// are. The loads of a tile are issued after the previous tile is stored.
-__device__ void producer_role_bf16(const qsfm_params& p, const Smem& sm, int* fault) {
-  const int ptid = threadIdx.x - kSoftThreads;  // 0..255 (8 producer warps)
-  const int lane = threadIdx.x & 31;
-  const int row_lo = ptid >> 3;  // 0..31
-  const int j = ptid & 7;
-  const int* rows = reinterpret_cast<const int*>(sm.ptr + kSRows);
-  const int* kind = reinterpret_cast<const int*>(sm.ptr + kSRowKind);
-  constexpr int kRow = QSFM_BF16_ROW_BYTES;
-
-  int pr[2];
-  uint4 R[4][2][2];  // [chunk][row][d-block of the chunk]
-
-  auto fetch = [&](uint32_t n) -> bool {
-    const uint32_t slot = n % kRing;
-    if (!warp_wait_or_abort(sm, kBarRowsFull + slot, (n / kRing) & 1, fault)) return false;
-    const int kd = kind[slot];
-    pr[0] = rows[slot * kTileRows + row_lo];
-    pr[1] = rows[slot * kTileRows + row_lo + 32];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.bar(kBarRowsEmpty + slot));
-    if (kd < 0) return false;
-    const uint8_t* pool = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv);
-    const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const bool v = pr[u] >= 0;
-      const uint8_t* base = pool + size_t(v ? pr[u] : 0) * kRow + 16 * j;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        R[c][u][0] = v ? ldg_stream_v4(base + 256 * c) : z;
-        R[c][u][1] = v ? ldg_stream_v4(base + 256 * c + 128) : z;
-      }
-    }
-    return true;
-  };
-
-  for (uint32_t n = 0; fetch(n); ++n) {
-    const uint32_t st = n & 1;
-    if (!warp_wait_or_abort(sm, kBarKvEmpty + st, ((n >> 1) & 1) ^ 1, fault)) return;
-    const uint32_t stage = sm.base + kSK + st * kStageBytes;
-    if (j == 0) {
-      int* valid = reinterpret_cast<int*>(sm.ptr + kSValid) + st * kTileRows;
-      valid[row_lo] = pr[0] >= 0;
-      valid[row_lo + 32] = pr[1] >= 0;
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int r = row_lo + 32 * u;
-        const uint32_t unit = (uint32_t(j) ^ uint32_t(r & 7)) << 4;
-        sts_v4(stage + (2 * c) * kDBlockBytes + r * 128 + unit, R[c][u][0]);
-        sts_v4(stage + (2 * c + 1) * kDBlockBytes + r * 128 + unit, R[c][u][1]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(kBarKvFull + 4 * st + c));
-    }
-  }
-}
-
 // ------------------------------------------------------------- MMA issue
-// k-step s of d-block db: A (K~) at +db*8 KB + s*32 B, B (Q) at +db*8 KB + s*32 B.
+// QK^T k-step s of d-block db: A (K~, K-major) at + db * 16 KB + s * 32 B,
+// B (Q, K-major) at + db * 8 KB + s * 32 B.
 template <int kDb, int kS>
 __device__ __forceinline__ void qk_mma(uint32_t d, uint64_t a0, uint64_t b0) {
-  constexpr uint32_t off = uint32_t((kDb * 8192 + kS * 32) >> 4);
+  constexpr uint32_t offa = uint32_t((kDb * kSlabBytes + kS * 32) >> 4);
+  constexpr uint32_t offb = uint32_t((kDb * 8192 + kS * 32) >> 4);
   if constexpr ((kDb | kS) == 0)
-    mma_bf16_at<off, off>(d, a0, b0, kIdescQK, 0u);
+    mma_bf16_at<offa, offb>(d, a0, b0, kIdescQK, 0u);
   else
-    mma_bf16_acc_at<off, off>(d, a0, b0, kIdescQK);
-}
-
-// PV for head-dim chunk kC: A (V~^T, MN-major) at +kC*16 KB + ks*2 KB,
-// B (P, MN-major) at +ks*2 KB.
-template <int kC>
-__device__ __forceinline__ void pv_chunk(uint32_t tmem, uint64_t a0, uint64_t b0, uint32_t acc0) {
-  const uint32_t d = tmem + kTmemO + kC * 64;
-  mma_bf16_at<uint32_t((kC * 16384 + 0 * 2048) >> 4), uint32_t((0 * 2048) >> 4)>(d, a0, b0, kIdescPV, acc0);
-  mma_bf16_acc_at<uint32_t((kC * 16384 + 1 * 2048) >> 4), uint32_t((1 * 2048) >> 4)>(d, a0, b0, kIdescPV);
-  mma_bf16_acc_at<uint32_t((kC * 16384 + 2 * 2048) >> 4), uint32_t((2 * 2048) >> 4)>(d, a0, b0, kIdescPV);
-  mma_bf16_acc_at<uint32_t((kC * 16384 + 3 * 2048) >> 4), uint32_t((3 * 2048) >> 4)>(d, a0, b0, kIdescPV);
+    mma_bf16_acc_at<offa, offb>(d, a0, b0, kIdescQK);
 }
 
 template <int kC>
-__device__ __forceinline__ void qk_issue(uint32_t d, uint64_t a0, uint64_t b0) {
+__device__ __forceinline__ void qk_chunk(uint32_t d, uint64_t a0, uint64_t b0) {
   qk_mma<2 * kC, 0>(d, a0, b0); qk_mma<2 * kC, 1>(d, a0, b0);
   qk_mma<2 * kC, 2>(d, a0, b0); qk_mma<2 * kC, 3>(d, a0, b0);
   qk_mma<2 * kC + 1, 0>(d, a0, b0); qk_mma<2 * kC + 1, 1>(d, a0, b0);
   qk_mma<2 * kC + 1, 2>(d, a0, b0); qk_mma<2 * kC + 1, 3>(d, a0, b0);
 }
 
-// Tile n of the CTA's sequence uses stage n & 1 (K~, S^T, P buffers); each
-// barrier of a stage completes once per tile of that stage, so tile n waits
-// for phase parity (n >> 1) & 1. Two threads issue tensor-core work, each
-// blocking on its own inputs in program order: this one QK^T (and Q), the PV
-// thread the PV products. QK^T(n) cannot run more than two tiles ahead of
-// PV: its stage is refilled only after PV(n - 2) has completed.
-__device__ void qk_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
-                        const CUtensorMap* qmap, int* fault) {
+// PV k-step ks of head-dim chunk c: A (V~^T, MN-major: 64-d atoms 16 KB
+// apart, 8-row groups 1 KB apart) at + c * 32 KB + ks * 2 KB, B (P^T,
+// MN-major) at + ks * 2 KB.
+template <int kC, int kS>
+__device__ __forceinline__ void pv_mma(uint32_t d, uint64_t a0, uint64_t b0, uint32_t acc0) {
+  constexpr uint32_t offa = uint32_t((kC * 2 * kSlabBytes + kS * 2048) >> 4);
+  constexpr uint32_t offb = uint32_t((kS * 2048) >> 4);
+  if constexpr (kS == 0)
+    mma_bf16_at<offa, offb>(d, a0, b0, kIdescPV, acc0);
+  else
+    mma_bf16_acc_at<offa, offb>(d, a0, b0, kIdescPV);
+}
+
+template <int kC>
+__device__ __forceinline__ void pv_chunk(uint32_t tmem, uint64_t a0, uint64_t b0, uint32_t acc0) {
+  const uint32_t d = tmem + kTmemO + kC * 64;
+  pv_mma<kC, 0>(d, a0, b0, acc0); pv_mma<kC, 1>(d, a0, b0, acc0);
+  pv_mma<kC, 2>(d, a0, b0, acc0); pv_mma<kC, 3>(d, a0, b0, acc0);
+  pv_mma<kC, 4>(d, a0, b0, acc0); pv_mma<kC, 5>(d, a0, b0, acc0);
+  pv_mma<kC, 6>(d, a0, b0, acc0); pv_mma<kC, 7>(d, a0, b0, acc0);
+}
+
+// Tile n of the CTA's sequence: every per-tile barrier completes once per
+// tile, so a wait for tile n uses phase parity n & 1. A phase can never run
+// two ahead of its waiter: each completion needs the waiter's own next step.
+__device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
+                         const CUtensorMap* qmap, int* fault) {
   if ((threadIdx.x & 31) != 0) return;
   PieceIter pieces(&p, rg, T);
   TokenGeom g;
@@ -581,45 +376,70 @@ __device__ void qk_role(const qsfm_params& p, const Smem& sm, Range rg, int T, u
       if (lo_ < hi_) return true;
     return false;
   };
-  auto load_q = [&](int t_) {
-    mbar_arrive_expect_tx(sm.bar(kBarQFull), 64 * 1024);
+  auto load_q = [&](int unit) {
+    mbar_arrive_expect_tx(sm.bar(kBarQFull), kHeads * kDim * 2);
 #pragma unroll
     for (int db = 0; db < 8; ++db)
-      tma_load_2d(sm.base + kSQ + db * 8192, qmap, db * 64, t_ * 64, sm.bar(kBarQFull));
+      tma_load_2d(sm.base + kSQ + db * 8192, qmap, db * 64, unit * 64, sm.bar(kBarQFull));
   };
+  const uint64_t qa = make_sdesc_sw128(sm.base + kSK, 16, 1024);
+  const uint64_t qb = make_sdesc_sw128(sm.base + kSQ, 16, 1024);
+  const uint64_t pa = make_sdesc_sw128(sm.base + kSK, kSlabBytes, 1024);
+  const uint64_t pb = make_sdesc_sw128(sm.base + kSP, 16, 1024);
+  const uint32_t ds = tmem + kTmemS;
+  // QK^T of tile n, chunk by chunk as the producers publish the chunks
+  auto qk_tile = [&](uint32_t n) -> bool {
+    const uint32_t par = n & 1;
+    if (!wait_or_abort(sm, kBarFull + 0, par, fault)) return false;
+    tc_fence_after();
+    qk_chunk<0>(ds, qa, qb);
+    if (!wait_or_abort(sm, kBarFull + 1, par, fault)) return false;
+    tc_fence_after();
+    qk_chunk<1>(ds, qa, qb);
+    if (!wait_or_abort(sm, kBarFull + 2, par, fault)) return false;
+    tc_fence_after();
+    qk_chunk<2>(ds, qa, qb);
+    if (!wait_or_abort(sm, kBarFull + 3, par, fault)) return false;
+    tc_fence_after();
+    qk_chunk<3>(ds, qa, qb);
+    mma_commit(sm.bar(kBarSFull));
+    return true;
+  };
+
   int tok, lo, hi;
-  bool have = next_live(tok, lo, hi);
-  if (!have) return;
+  if (!next_live(tok, lo, hi)) return;
   load_q(tok);
+  if (!wait_or_abort(sm, kBarQFull, 0, fault)) return;
+  if (!qk_tile(0)) return;
   uint32_t n = 0, piece = 0;
+  bool have = true;
   while (have) {
     int ntok = 0, nlo = 0, nhi = 0;
     const bool have_next = next_live(ntok, nlo, nhi);
-    if (!wait_or_abort(sm, kBarQFull, piece & 1, fault)) return;
     for (int k = lo; k < hi; ++k, ++n) {
-      const uint32_t st = n & 1, par = (n >> 1) & 1;
-      // S^T buffer st is free once the softmax has read tile n - 2's scores
-      if (!wait_or_abort(sm, kBarSFree + st, par ^ 1, fault)) return;
-      const uint32_t d = tmem + kTmemS + 64 * st;
-      const uint64_t a0 = make_sdesc_sw128(sm.base + kSK + st * kStageBytes, 16, 1024);
-      const uint64_t b0 = make_sdesc_sw128(sm.base + kSQ, 16, 1024);
-      if (!wait_or_abort(sm, kBarKvFull + 4 * st + 0, par, fault)) return;
+      const bool last = k == hi - 1;
+      // P(n) written (so S^T(n) has been read and QK^T(n) is complete)
+      if (!wait_or_abort(sm, kBarPFull, n & 1, fault)) return;
       tc_fence_after();
-      qk_issue<0>(d, a0, b0);
-      if (!wait_or_abort(sm, kBarKvFull + 4 * st + 1, par, fault)) return;
-      tc_fence_after();
-      qk_issue<1>(d, a0, b0);
-      if (!wait_or_abort(sm, kBarKvFull + 4 * st + 2, par, fault)) return;
-      tc_fence_after();
-      qk_issue<2>(d, a0, b0);
-      if (!wait_or_abort(sm, kBarKvFull + 4 * st + 3, par, fault)) return;
-      tc_fence_after();
-      qk_issue<3>(d, a0, b0);
-      mma_commit(sm.bar(kBarSFull + st));
-      if (k == hi - 1 && have_next) {
-        // Q of the next token once this token's last QK^T has read Q
-        if (!wait_or_abort(sm, kBarSFull + st, par, fault)) return;
-        load_q(ntok);
+      if (k == lo && piece > 0) {
+        // the previous piece's epilogue must have read O^T before it is overwritten
+        if (!wait_or_abort(sm, kBarOFree, (piece - 1) & 1, fault)) return;
+        tc_fence_after();
+      }
+      if (last && have_next) load_q(ntok);  // Q is free: QK^T(n) has completed
+      // Two commits per tile (each drains the tensor pipe for about 140
+      // cycles): chunks 0 and 1 are freed first, so the producers store the
+      // next tile's chunks 0 and 1 while chunks 2 and 3 are multiplied.
+      const uint32_t acc0 = k == lo ? 0u : 1u;
+      pv_chunk<0>(tmem, pa, pb, acc0);
+      pv_chunk<1>(tmem, pa, pb, acc0);
+      mma_commit(sm.bar(kBarFree + 0));
+      pv_chunk<2>(tmem, pa, pb, acc0);
+      pv_chunk<3>(tmem, pa, pb, acc0);
+      mma_commit(sm.bar(kBarFree + 1));
+      if (!last || have_next) {
+        if (last && !wait_or_abort(sm, kBarQFull, (piece + 1) & 1, fault)) return;
+        if (!qk_tile(n + 1)) return;
       }
     }
     ++piece;
@@ -630,57 +450,181 @@ __device__ void qk_role(const qsfm_params& p, const Smem& sm, Range rg, int T, u
   }
 }
 
-__device__ void pv_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
-                        int* fault) {
-  if ((threadIdx.x & 31) != 0) return;
-  PieceIter pieces(&p, rg, T);
-  TokenGeom g;
-  int tok, lo, hi;
-  uint32_t n = 0, piece = 0;
-  while (pieces.next(tok, g, lo, hi)) {
-    if (lo >= hi) continue;
-    for (int k = lo; k < hi; ++k, ++n) {
-      const uint32_t st = n & 1;
-      if (!wait_or_abort(sm, kBarPFull + st, (n >> 1) & 1, fault)) return;
-      if (k == lo && piece > 0) {
-        // the previous piece's epilogue must have read O^T before it is overwritten
-        if (!wait_or_abort(sm, kBarOFree, (piece - 1) & 1, fault)) return;
-      }
-      tc_fence_after();
-      const uint64_t a0 = make_sdesc_sw128(sm.base + kSK + st * kStageBytes, kDBlockBytes, 1024);
-      const uint64_t b0 = make_sdesc_sw128(sm.base + kSP + st * kPBytes, 16, 1024);
-      const uint32_t acc0 = k == lo ? 0u : 1u;
-      pv_chunk<0>(tmem, a0, b0, acc0);
-      pv_chunk<1>(tmem, a0, b0, acc0);
-      pv_chunk<2>(tmem, a0, b0, acc0);
-      pv_chunk<3>(tmem, a0, b0, acc0);
-      mma_commit(sm.bar(kBarKvEmpty + st));  // stage (K~ and P) released
-      if (k == hi - 1) mma_commit(sm.bar(kBarODone));
-    }
-    ++piece;
-  }
-}
-
-// ------------------------------------------------------ softmax + epilogue
-// Warp q reads the 16 tensor-memory lanes 32q..32q+15 of an S^T buffer, i.e.
-// tile rows 16q..16q+15. In the accumulator-fragment layout thread l holds
-// rows ra = 16q + l/4 and ra + 8, heads 8j + 2(l%4) + e (j = 0..7, e = 0, 1):
-//   x[4j + 2r + e] = S^T[ra + 8r, 8j + 2(l%4) + e].
-// Its 16 heads are indexed i = 2j + e in l[].
-__device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
-                             const Workspace& ws, int c_idx, int* fault) {
+// ------------------------------------------------------------- workers
+// Producer view, thread (row_lo, j): rows row_lo + kRowStride u (u < kRPT)
+// of a tile, 16-byte piece j of each 128-d chunk c (d 128 c .. 128 c + 127):
+//   fp8 rows     fp8 bytes 128 c + 16 j .. + 15 of the row (d 128 c + 16 j
+//                .. + 15, d-block 2 c + j / 4, scale index 2 c + j / 4; lane
+//                j holds scale j of each of its rows);
+//   packed rows  chunk 0: bf16 rope bytes 16 j .. + 15 (d 8 j .. + 7 of
+//                d-block 0) and, for j < 4, nope bytes 128 + 16 j .. + 15
+//                (d 64 + 16 j .., d-block 1, e8m0 scale 0); chunk c >= 1:
+//                nope bytes 64 + 128 c + 16 j .. + 15 (the same d as fp8
+//                rows, e8m0 scale 2 c - 1 + j / 4); lane j = 4 of each row
+//                loads the seven scale bytes (576 .. 583);
+//   bf16 rows    bytes 256 c + 16 j and 256 c + 128 + 16 j: unit j of
+//                d-blocks 2 c and 2 c + 1, copied as they are (chunks 2 and
+//                3 are loaded into the registers of chunks 0 and 1 once
+//                those are stored: a whole bf16 tile would not fit).
+template <int kFmt>
+__device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
+                            const Workspace& ws, int c_idx, int* fault) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = tid;  // epilogue: head-dim element inside a 128-d chunk
-  const int ra = 16 * warp + (lane >> 2);
-  const int hq = 2 * (lane & 3);
-  const uint32_t lane_base = uint32_t(32 * warp) << 16;
+  // softmax / epilogue view
+  const int qd = warp & 3;             // tensor-memory lane quadrant
+  const int h0 = kHPT * (warp >> 2);   // first of this warp's kHPT heads
+  const int r = 32 * qd + lane;      // tile row of this thread (softmax)
+  const uint32_t lane_base = uint32_t(32 * qd) << 16;
+  const uint32_t s_addr = tmem + kTmemS + h0 + lane_base;
+  const uint32_t prow_addr = sm.base + kSP + uint32_t(r) * 128;
   const float qk_scale = p.softmax_scale * kLog2e;
   float* m_used = sm.f(kSMUsed);
   float* alpha = sm.f(kSAlpha);
   float* inv = sm.f(kSInv);
   float* red = sm.f(kSRed);
+  int* valid = reinterpret_cast<int*>(sm.ptr + kSValid);
+  // producer view
+  const int row_lo = tid >> 3;  // 0 .. kRowStride - 1
+  const int j = tid & 7;        // == lane & 7
+  const int odd = j >> 2;       // j >= 4 stores its odd 16-B unit first (no bank conflicts)
+  const int grp = lane & ~7;    // first lane of this row's group of 8
+  const int* rows = reinterpret_cast<const int*>(sm.ptr + kSRows);
+  const int* kind = reinterpret_cast<const int*>(sm.ptr + kSRowKind);
+  constexpr int kRowB = kv_row_bytes(kFmt);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+
+  int pr[kRPT];       // physical rows of the tile to store next
+  int kd = 0;         // their pool (0 ori, 1 cmp)
+  uint2 sc[kRPT];     // its scales: fp8 scale j (x), packed e8m0 bytes (lane 4)
+  uint4 R[4][kRPT];   // its raw pieces: [chunk][row] (bf16: [2 (chunk & 1) + half][row])
+  uint4 RR[kRPT];     // packed rows: the rope piece of chunk 0
+
+  // Rows of tile n from the ring; false at the end mark or on abort.
+  auto take_rows = [&](uint32_t n) -> bool {
+    const uint32_t slot = n % kRing;
+    if (!warp_wait_or_abort(sm, kBarRowsFull + slot, (n / kRing) & 1, fault)) return false;
+    kd = kind[slot];
+#pragma unroll
+    for (int u = 0; u < kRPT; ++u) pr[u] = rows[slot * kTileRows + row_lo + kRowStride * u];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(kBarRowsEmpty + slot));
+    return kd >= 0;
+  };
+
+  // Loads of raw chunk c of row u (bf16: into the registers of chunk c & 1).
+  auto load_chunk = [&](int c, int u) {
+    const bool v = pr[u] >= 0;
+    const uint8_t* row = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv) + size_t(v ? pr[u] : 0) * kRowB;
+    if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
+      R[c][u] = v ? ldg_stream_v4(row + 128 * c + 16 * j) : z;
+    } else if constexpr (kFmt == QSFM_KV_BF16) {
+      R[2 * (c & 1)][u] = v ? ldg_stream_v4(row + 256 * c + 16 * j) : z;
+      R[2 * (c & 1) + 1][u] = v ? ldg_stream_v4(row + 256 * c + 128 + 16 * j) : z;
+    } else {
+      if (c == 0) {
+        RR[u] = v ? ldg_stream_v4(row + 16 * j) : z;
+        R[0][u] = (v && j < 4) ? ldg_stream_v4(row + 128 + 16 * j) : z;
+      } else {
+        R[c][u] = v ? ldg_stream_v4(row + 64 + 128 * c + 16 * j) : z;
+      }
+    }
+  };
+
+  // The raw rows of a whole tile (two chunks for bf16) and its scales.
+  auto load_tile = [&]() {
+#pragma unroll
+    for (int u = 0; u < kRPT; ++u) {
+      const bool v = pr[u] >= 0;
+      if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
+        const float* spool = kd ? p.cmp_scale : p.ori_scale;
+        sc[u].x = v ? __float_as_uint(__ldg(spool + size_t(pr[u]) * kScales + j)) : 0u;
+      } else if constexpr (kFmt == QSFM_KV_PACKED640) {
+        const uint8_t* row = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv) + size_t(v ? pr[u] : 0) * kRowB;
+        sc[u] = (v && j == 4) ? ldg_stream_v2(row + 576) : make_uint2(0, 0);
+      }
+#pragma unroll
+      for (int c = 0; c < (kFmt == QSFM_KV_BF16 ? 2 : 4); ++c) load_chunk(c, u);
+    }
+  };
+
+  // Chunk c of the raw tile, converted to bf16 row by row and stored into
+  // its two slabs, then published.
+  auto store_chunk = [&](int c) {
+    const uint32_t tile = sm.base + kSK;
+#pragma unroll
+    for (int u = 0; u < kRPT; ++u) {
+      const int rr = row_lo + kRowStride * u;
+      const uint32_t sw = uint32_t(rr & 7);
+      if constexpr (kFmt == QSFM_KV_BF16) {
+        const uint32_t unit = (uint32_t(j) ^ sw) << 4;
+        sts_v4(tile + (2 * c) * kSlabBytes + rr * 128 + unit, R[2 * (c & 1)][u]);
+        sts_v4(tile + (2 * c + 1) * kSlabBytes + rr * 128 + unit, R[2 * (c & 1) + 1][u]);
+        continue;
+      }
+      uint4 lo, hi;
+      if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
+        const float s = __shfl_sync(0xffffffffu, __uint_as_float(sc[u].x), grp | (2 * c + odd));
+        dequant16_x2(R[c][u], s, lo, hi);
+      } else {
+        const uint32_t w0 = __shfl_sync(0xffffffffu, sc[u].x, grp | 4);  // scale bytes 0..3
+        const uint32_t w1 = __shfl_sync(0xffffffffu, sc[u].y, grp | 4);  // scale bytes 4..6
+        if (c == 0) {
+          sts_v4(tile + rr * 128 + ((uint32_t(j) ^ sw) << 4), RR[u]);  // rope: d-block 0
+          if (j < 4) {
+            dequant16(R[0][u], e8m0_value(w0 & 0xFFu), lo, hi);
+            const uint32_t rowb = tile + kSlabBytes + rr * 128;  // nope d 64..127: d-block 1
+            sts_v4(rowb + ((uint32_t(2 * j) ^ sw) << 4), lo);
+            sts_v4(rowb + ((uint32_t(2 * j + 1) ^ sw) << 4), hi);
+          }
+          continue;
+        }
+        const int sidx = 2 * c - 1 + odd;
+        const uint32_t e = (sidx < 4 ? w0 >> (8 * sidx) : w1 >> (8 * (sidx - 4))) & 0xFFu;
+        dequant16(R[c][u], e8m0_value(e), lo, hi);
+      }
+      const uint32_t rowb = tile + (2 * c + odd) * kSlabBytes + rr * 128;
+      const uint32_t c0 = 2 * (j & 3);
+      sts_v4(rowb + (((c0 + odd) ^ sw) << 4), odd ? hi : lo);
+      sts_v4(rowb + (((c0 + 1 - odd) ^ sw) << 4), odd ? lo : hi);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(kBarFull + c));
+    if constexpr (kFmt == QSFM_KV_BF16) {
+      if (c < 2) {
+#pragma unroll
+        for (int u = 0; u < kRPT; ++u) load_chunk(c + 2, u);
+      }
+    }
+  };
+
+  // Tile n from the registers into the tile buffer, chunk c once PV(n - 1)
+  // has read it; then the rows of tile n + 1 and their loads.
+  uint32_t n_store = 0;
+  bool have_tile = take_rows(0);
+  if (have_tile) load_tile();
+  auto store_next = [&]() {
+    if (!have_tile) return;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {  // unrolled: the raw registers are indexed by c
+      if (n_store > 0 && (c & 1) == 0 && !warp_wait_or_abort(sm, kBarFree + (c >> 1), (n_store - 1) & 1, fault)) {
+        have_tile = false;
+        return;
+      }
+      if (c == 0 && j == 0) {
+#pragma unroll
+        for (int u = 0; u < kRPT; ++u) valid[row_lo + kRowStride * u] = pr[u] >= 0;
+      }
+      store_chunk(c);
+    }
+    ++n_store;
+    have_tile = take_rows(n_store);
+    if (have_tile) load_tile();
+  };
+  store_next();  // tile 0
+
   PieceIter pieces(&p, rg, T);
-  uint32_t n = 0, pieces_live = 0;
+  uint32_t n = 0;
   int t, lo, hi;
   TokenGeom g;
   bool have = pieces.next(t, g, lo, hi);
@@ -693,27 +637,23 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
     const int slot = (t == rg.t0) ? 2 * c_idx : 2 * c_idx + 1;
     const bool writable = whole || slot < ws.slots;  // split pieces need the workspace
     if (!writable && tid == 0) atomicOr(fault, QSFM_FAULT_METADATA);
-    float l[16], m[16];  // row sums and running max (log2 units) of this thread's 16 heads
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      l[i] = 0.f;
-      m[i] = -INFINITY;
-    }
+    // Lane i of the warp keeps the running sum of P for head h0 + i % kHPT
+    // over this warp's 32 rows: each tile's P is folded in with a lane
+    // reduction once P is published (one register instead of kHPT).
+    float l_sum = 0.f;
     if (tid < 64) m_used[tid] = -INFINITY;
-    named_sync(kBarSoft, kSoftThreads);
+    named_sync(kBarWork, kWorkThreads);
     for (int k = lo; k < hi; ++k, ++n) {
-      const uint32_t st = n & 1, par = (n >> 1) & 1;
+      const uint32_t par = n & 1;
       // Lane 0 of each warp polls. After an abort the waits fall through at
-      // once; the softmax warps keep running the same named-barrier sequence
-      // so that none of them blocks.
-      warp_wait_or_abort(sm, kBarKvFull + 4 * st, par, fault);
-      const int* valid = reinterpret_cast<const int*>(sm.ptr + kSValid) + st * kTileRows;
-      const bool va = valid[ra] != 0, vb = valid[ra + 8] != 0;
-      warp_wait_or_abort(sm, kBarSFull + st, par, fault);
+      // once; the workers keep running the same named-barrier sequence so
+      // that none of them blocks.
+      warp_wait_or_abort(sm, kBarFull + 0, par, fault);  // the tile's valid flags
+      const bool v = valid[r] != 0;
+      warp_wait_or_abort(sm, kBarSFull, par, fault);
       tc_fence_after();
-      const uint32_t s_addr = tmem + kTmemS + 64 * st + lane_base;
-      float x[32];
-      tmem_ld16x256b_x8(s_addr, x);
+      float x[kHPT];
+      tmem_load(s_addr, x);
       tmem_ld_wait();
       bool move = true;  // the first tile of a piece always sets the max
       if (k != lo) {
@@ -721,46 +661,33 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
         // before the vote; valid only if no t exceeds 8 anywhere in the tile.
         float tmax = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int ia = 4 * (i >> 1) + (i & 1);
-          const float ta = va ? fmaf(x[ia], qk_scale, -m[i]) : -INFINITY;
-          const float tb = vb ? fmaf(x[ia + 2], qk_scale, -m[i]) : -INFINITY;
-          tmax = fmaxf(tmax, fmaxf(ta, tb));
-          x[ia] = ex2_approx(ta);
-          x[ia + 2] = ex2_approx(tb);
+        for (int i = 0; i < kHPT; i += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(m_used + h0 + i);
+          const float t0 = v ? fmaf(x[i], qk_scale, -m4.x) : -INFINITY;
+          const float t1 = v ? fmaf(x[i + 1], qk_scale, -m4.y) : -INFINITY;
+          const float t2 = v ? fmaf(x[i + 2], qk_scale, -m4.z) : -INFINITY;
+          const float t3 = v ? fmaf(x[i + 3], qk_scale, -m4.w) : -INFINITY;
+          tmax = fmaxf(tmax, fmaxf(fmaxf(t0, t1), fmaxf(t2, t3)));
+          x[i] = ex2_approx(t0);
+          x[i + 1] = ex2_approx(t1);
+          x[i + 2] = ex2_approx(t2);
+          x[i + 3] = ex2_approx(t3);
         }
-        move = named_sync_or(kBarSoft, kSoftThreads, tmax > kRescaleLog2);  // also true against -inf
-        if (!move) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int ia = 4 * (i >> 1) + (i & 1);
-            l[i] += x[ia] + x[ia + 2];
-          }
-        }
+        move = named_sync_or(kBarWork, kWorkThreads, tmax > kRescaleLog2);  // also true against -inf
       }
+      float lscale = 1.f;  // 0 after a moved max: the running sums take alpha first
       if (move) {
-        // Slow path: the scores again (S^T buffer st is not reused before
-        // this tile's PV has completed), then move the running max.
+        // Slow path: the scores again, the tile max per head over its 128
+        // rows, the new running max, then O^T and the row sums rescaled.
         if (k != lo) {
-          tmem_ld16x256b_x8(s_addr, x);
+          tmem_load(s_addr, x);
           tmem_ld_wait();
         }
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          x[4 * jj + 0] = va ? x[4 * jj + 0] * qk_scale : -INFINITY;
-          x[4 * jj + 1] = va ? x[4 * jj + 1] * qk_scale : -INFINITY;
-          x[4 * jj + 2] = vb ? x[4 * jj + 2] * qk_scale : -INFINITY;
-          x[4 * jj + 3] = vb ? x[4 * jj + 3] * qk_scale : -INFINITY;
-        }
-        // tile max per head over the 64 rows
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          v[i] = fmaxf(x[4 * (i >> 1) + (i & 1)], x[4 * (i >> 1) + 2 + (i & 1)]);
-        reduce_rows16<true>(v);  // lane l: heads 2l, 2l + 1
-        red[warp * 64 + 2 * lane] = v[0];
-        red[warp * 64 + 2 * lane + 1] = v[1];
-        named_sync(kBarSoft, kSoftThreads);
+        for (int i = 0; i < kHPT; ++i) x[i] = v ? x[i] * qk_scale : -INFINITY;
+        const float mx = reduce_lanes<true>(x);  // head h0 + lane % kHPT, this quadrant's rows
+        if (lane < kHPT) red[qd * 64 + h0 + lane] = mx;
+        named_sync(kBarWork, kWorkThreads);
         if (tid < 64) {
           const float mt = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
           const float mu = m_used[tid];
@@ -771,60 +698,59 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
           }
           alpha[tid] = a;
         }
-        named_sync(kBarSoft, kSoftThreads);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int h = 8 * (i >> 1) + hq + (i & 1);
-          l[i] *= alpha[h];
-          m[i] = m_used[h];
-        }
+        named_sync(kBarWork, kWorkThreads);
         if (k != lo) {
-          // O^T at this thread's head-dim lane, all heads, once the PV product
-          // of tile n - 1 has completed
-          warp_wait_or_abort(sm, kBarKvEmpty + ((n - 1) & 1), ((n - 1) >> 1) & 1, fault);
-          tc_fence_after();
+          // O^T at this thread's lane, its kHPT heads, every chunk. The PV
+          // products of the earlier tiles have completed: S^T(n) was
+          // committed after them.
 #pragma unroll 1
-          for (int q16 = 0; q16 < 16; ++q16) {
-            float o[16];
-            const uint32_t addr = tmem + kTmemO + 16 * q16 + lane_base;
-            tmem_ld16(addr, o);
+          for (int c = 0; c < 4; ++c) {
+            float o[kHPT];
+            const uint32_t addr = tmem + kTmemO + 64 * c + h0 + lane_base;
+            tmem_load(addr, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha[16 * (q16 & 3) + i];
-            tmem_st16(addr, o);
+            for (int i = 0; i < kHPT; ++i) o[i] *= alpha[h0 + i];
+            tmem_store(addr, o);
           }
           tmem_st_wait();
         }
-        // P = 2^(x - m_used) and the row sums
+        tmem_load(s_addr, x);
+        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float mz = m[i] == -INFINITY ? 0.f : m[i];
-          const int ia = 4 * (i >> 1) + (i & 1);
-          x[ia] = ex2_approx(x[ia] - mz);
-          x[ia + 2] = ex2_approx(x[ia + 2] - mz);
-          l[i] += x[ia] + x[ia + 2];
+        for (int i = 0; i < kHPT; ++i) {
+          const float m = m_used[h0 + i];
+          const float mz = m == -INFINITY ? 0.f : m;
+          x[i] = ex2_approx(v ? fmaf(x[i], qk_scale, -mz) : -INFINITY);
         }
+        lscale = 0.f;
       }
-      // the scores are no longer needed: the buffer can take tile n + 2
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(kBarSFree + st));
-      // P into its stage as [64 rows][64 heads] bf16 with the 128-B swizzle
-      // (the MN-major B operand of PV)
-      const uint32_t pbase = sm.base + kSP + st * kPBytes;
-      const int mi = lane >> 3, jr = lane & 7;
-      const uint32_t prow = pbase + uint32_t(16 * warp + 8 * (mi & 1) + jr) * 128;
+      // P into the P buffer as [128 rows][64 heads] bf16 with the 128-B
+      // swizzle (the MN-major B operand of PV): this thread's row, its
+      // 16-byte units of 8 heads
 #pragma unroll
-      for (int gq = 0; gq < 4; ++gq) {
-        const uint32_t hg = uint32_t(2 * gq + (mi >> 1));
-        stmatrix_x4(prow + ((hg ^ uint32_t(jr)) << 4),
-                    pack_bf16(x[8 * gq + 0], x[8 * gq + 1]), pack_bf16(x[8 * gq + 2], x[8 * gq + 3]),
-                    pack_bf16(x[8 * gq + 4], x[8 * gq + 5]), pack_bf16(x[8 * gq + 6], x[8 * gq + 7]));
+      for (int vv = 0; vv < kHPT / 8; ++vv) {
+        const uint32_t u = uint32_t((h0 >> 3) + vv);
+        uint4 pk;
+        pk.x = pack_bf16(x[8 * vv + 0], x[8 * vv + 1]);
+        pk.y = pack_bf16(x[8 * vv + 2], x[8 * vv + 3]);
+        pk.z = pack_bf16(x[8 * vv + 4], x[8 * vv + 5]);
+        pk.w = pack_bf16(x[8 * vv + 6], x[8 * vv + 7]);
+        sts_v4(prow_addr + ((u ^ uint32_t(r & 7)) << 4), pk);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(kBarPFull + st));
+      if (lane == 0) mbar_arrive(sm.bar(kBarPFull));
+      {
+        // running sums += this tile's P, folded over the warp's rows (after
+        // P is published: off the PV path); a moved max rescales them first
+        const float tile_sum = reduce_lanes<false>(x);
+        if (lscale == 0.f) l_sum *= alpha[h0 + (lane % kHPT)];
+        l_sum += tile_sum;
+      }
+      // the next tile into the buffer as PV(n) frees it
+      store_next();
     }
     // The next piece's geometry, read now: its loads overlap the wait for
     // this piece's last PV product.
@@ -833,12 +759,8 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
     const int n_tiles_next = g.n_tiles;
     // ---------------- epilogue of the piece
     const bool any = lo < hi;
-    if (any) {
-      reduce_rows16<false>(l);  // lane l: heads 2l, 2l + 1 of this warp's rows
-      red[warp * 64 + 2 * lane] = l[0];
-      red[warp * 64 + 2 * lane + 1] = l[1];
-    }
-    named_sync(kBarSoft, kSoftThreads);
+    if (any && lane < kHPT) red[qd * 64 + h0 + lane] = l_sum;
+    named_sync(kBarWork, kWorkThreads);
     if (tid < 64 && writable) {
       const float lt = any ? (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]) : 0.f;
       const float mu = m_used[tid];
@@ -853,74 +775,58 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
         ws.lse[size_t(slot) * 64 + tid] = lse2 * kLn2;
       }
     }
-    named_sync(kBarSoft, kSoftThreads);
-    if (any) {
-      warp_wait_or_abort(sm, kBarODone, pieces_live & 1, fault);
-      tc_fence_after();
-    }
-    // O^T in blocks of 128 d x 32 heads: lane = head-dim element, columns =
-    // heads. Whole tokens go out through the P buffers, idle now: each block
-    // is written there as 32 rows of 256 bytes ([head][d], bf16), then read
-    // back 16 bytes per thread and stored with 16-byte stores (a warp writes
-    // two 256-byte output rows per store); the two buffers alternate, so one
-    // barrier per block suffices. Split pieces store fp32 rows directly (the
-    // 32 lanes of a warp write 128 consecutive bytes per head).
+    named_sync(kBarWork, kWorkThreads);
+    // O^T chunk by chunk once the last PV product has completed it: this
+    // thread holds head-dim element d = 128 c + 32 qd + lane of its kHPT
+    // heads. Whole units: the two lanes of a pair swap values so that each
+    // stores two adjacent d (4 bytes) of kHPT / 2 heads; a warp writes 64
+    // contiguous bytes per head. Split pieces store fp32 rows (128 bytes per
+    // head per warp).
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const int h0 = 32 * half;
-        const int blk = 2 * c + half;
-        float o[32];
-        if (any) {
-          tmem_ld32(tmem + kTmemO + 64 * c + 32 * half + lane_base, o);
-          tmem_ld_wait();
-          // 1 / denominator per head, read into registers before any store
-          // (the stores below could alias inv[] as far as the compiler knows)
-          float iv[32];
+      float o[kHPT];
+      if (any) {
+        if ((c & 1) == 0) warp_wait_or_abort(sm, kBarFree + (c >> 1), (n - 1) & 1, fault);
+        tc_fence_after();
+        tmem_load(tmem + kTmemO + 64 * c + h0 + lane_base, o);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 v4 = *reinterpret_cast<const float4*>(inv + h0 + i);
-            iv[i] = v4.x;
-            iv[i + 1] = v4.y;
-            iv[i + 2] = v4.z;
-            iv[i + 3] = v4.w;
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= iv[i];
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        for (int i = 0; i < kHPT; i += 4) {
+          const float4 iv = *reinterpret_cast<const float4*>(inv + h0 + i);
+          o[i] *= iv.x;
+          o[i + 1] *= iv.y;
+          o[i + 2] *= iv.z;
+          o[i + 3] *= iv.w;
         }
-        if (whole) {
-          // every thread has read block blk - 2 back from this buffer before
-          // the barrier of block blk - 1
-          const uint32_t box = sm.base + kSP + uint32_t(blk & 1) * kPBytes;
+      } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sts_b16(box + uint32_t(i * 256 + 2 * row), __float2bfloat16_rn(o[i]));
-          named_sync(kBarSoft, kSoftThreads);
-          uint8_t* out = static_cast<uint8_t*>(p.attn_out) +
-                         ((size_t(t) * 64 + h0) * kDim + 128 * c) * 2;
+        for (int i = 0; i < kHPT; ++i) o[i] = 0.f;
+      }
+      const int d = 128 * c + 32 * qd + lane;
+      if (whole) {
+        const int od = lane & 1;
+        uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.attn_out) +
+                                                    (size_t(t) * 64 + h0 + od) * kDim + (d & ~1));
 #pragma unroll
-          for (int q = tid; q < 512; q += kSoftThreads) {  // q = 16-byte piece: head q / 16
-            const uint32_t off = uint32_t(q >> 4) * 256 + uint32_t(q & 15) * 16;
-            const uint4 v = lds_v4(box + off);
-            *reinterpret_cast<uint4*>(out + size_t(q >> 4) * kDim * 2 + (q & 15) * 16) = v;
-          }
-        } else if (writable) {
-          float* out = ws.out + (size_t(slot) * 64 + h0) * kDim + 128 * c + row;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) out[size_t(i) * kDim] = o[i];
+        for (int i = 0; i < kHPT / 2; ++i) {
+          const float send = od ? o[2 * i] : o[2 * i + 1];
+          const float got = __shfl_xor_sync(0xffffffffu, send, 1);
+          const float lo_v = od ? got : o[2 * i];
+          const float hi_v = od ? o[2 * i + 1] : got;
+          out[size_t(2 * i) * (kDim / 2)] = pack_bf16(lo_v, hi_v);
         }
+      } else if (writable) {
+        float* out = ws.out + (size_t(slot) * 64 + h0) * kDim + d;
+#pragma unroll
+        for (int i = 0; i < kHPT; ++i) out[size_t(i) * kDim] = o[i];
       }
     }
     if (any) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(kBarOFree));
-      ++pieces_live;
     }
-    named_sync(kBarSoft, kSoftThreads);  // m_used / inv / red are reused by the next piece
+    named_sync(kBarWork, kWorkThreads);  // m_used / inv / red are reused by the next piece
     if (*sm.abort_flag()) break;         // uniform: read after the barrier
     have = have_next;
     t = t_next;
@@ -931,51 +837,34 @@ __device__ void softmax_role(const qsfm_params& p, const Smem& sm, Range rg, int
 }
 
 // Runs before the plan is readable, while the plan kernel still runs: warms
-// L2 with the inputs of the token this CTA most likely starts with (the plan
-// cuts equal-cost tokens evenly, so CTA c of G starts near token c T / G):
-// its Q, its index list, its first two ori tiles and its first four cmp
-// tiles. Only prefetches, so a wrong guess costs bandwidth, never results;
-// each address is checked against its buffer first. Thread i of the
-// producer warps takes ori slot i (i < 128) or cmp slot i - 128.
+// L2 with the inputs of the unit this CTA most likely starts with (the plan
+// cuts equal-cost units evenly, so CTA c of G starts near unit c T / G): its
+// Q and its first tile's rows, resolved by the library's one row resolution
+// (warp 0 of the workers). Only the first tile: every CTA does this at the
+// same moment, and more would queue the first tiles behind later ones. Only
+// prefetches, and no fault bits (the inputs may still be in flight from
+// earlier work on the stream), so a wrong guess costs bandwidth, never
+// results.
 template <int kFmt>
 __device__ __noinline__ void warm_first_token(const qsfm_params& p, int T, int c, int G, int i) {
   const int t = int((long long)c * T / G);
-  if (t >= T) return;
-  if (i == 0)
-    bulk_prefetch_l2(static_cast<const uint8_t*>(p.q) + size_t(t) * kHeads * kDim * 2,
-                     kHeads * kDim * 2);
-  if (p.cmp_sparse_indices != nullptr && i < 32 && 32 * i < p.k2)
-    prefetch_l2(p.cmp_sparse_indices + size_t(t >> unit_shift(p)) * p.k2 + 32 * i);
+  if (t >= T || i >= 64) return;
+  if (i == 32) {
+    bulk_prefetch_l2(static_cast<const uint8_t*>(p.q) + size_t(t) * kHeads * kDim * 2, kHeads * kDim * 2);
+    return;
+  }
+  if (i >= 32) return;
   const TokenGeom g = token_geom(p, t);
-  int pos = -1;
-  bool cmp = false;
-  if (i < 2 * kTileRows) {
-    if (i < g.n_ori) pos = g.ori_lo + i;
-  } else {
-    const int k = i - 2 * kTileRows;
-    if (k < g.n_cmp) {
-      cmp = true;
-      pos = p.cmp_sparse_indices != nullptr ? __ldg(p.cmp_sparse_indices + size_t(g.tok) * p.k2 + k) : k;
-      if (pos >= g.cmp_vis) pos = -1;
-    }
-  }
-  if (pos < 0) return;
-  const int col = pos / kBlock;
-  const int width = cmp ? p.cmp_max_blocks : p.ori_max_blocks;
-  if (col >= width) return;
-  const int blk = __ldg((cmp ? p.cmp_block_table : p.ori_block_table) + size_t(g.b) * width + col);
-  if (blk < 0 || blk >= (cmp ? p.cmp_num_blocks : p.ori_num_blocks)) return;
-  const size_t row = size_t(blk) * kBlock + pos % kBlock;
-  if constexpr (kFmt == QSFM_KV_PACKED640) {
-    bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * QSFM_PACKED_ROW_BYTES,
-                     QSFM_PACKED_ROW_BYTES);
-  } else if constexpr (kFmt == QSFM_KV_BF16) {
-    bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * QSFM_BF16_ROW_BYTES,
-                     QSFM_BF16_ROW_BYTES);
-  } else {
-    bulk_prefetch_l2(static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv) + row * kDim, kDim);
-    prefetch_l2((cmp ? p.cmp_scale : p.ori_scale) + row * kScales);
-  }
+  const int k[1] = {0};
+  const bool live[1] = {g.n_tiles > 0};
+  int lg[1][4], pr[1][4];
+  bool cmp[1];
+  resolve_tile_rows<1>(p, g, k, live, i, nullptr, lg, pr, cmp);
+  const uint8_t* pool = static_cast<const uint8_t*>(cmp[0] ? p.cmp_kv : p.ori_kv);
+  const float* spool = cmp[0] ? p.cmp_scale : p.ori_scale;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (pr[0][u] >= 0) prefetch_row<kFmt>(pool, spool, pr[0][u]);
 }
 
 template <int kFmt>
@@ -989,9 +878,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.ptr = smem_raw + (sm.base - raw_addr);
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  if (warp >= kSoftWarps && warp < kSoftWarps + kProdWarps)
-    warm_first_token<kFmt>(p, T, blockIdx.x, gridDim.x, tid - kSoftThreads);
-  grid_dependency_wait();   // the plan (and every input) is written by now
+  if (warp < 2) warm_first_token<kFmt>(p, T, blockIdx.x, gridDim.x, tid);
+  grid_dependency_wait();    // the plan (and every input) is written by now
   grid_launch_dependents();  // the combine kernel may take SMs as CTAs finish
   const int* meta = p.metadata;
   if (meta[0] != kMetaMagic || meta[2] != T) {
@@ -1016,19 +904,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(sm.bar(kBarQFull), 1);
-    for (int i = 0; i < 4 * kStages; ++i) mbar_init(sm.bar(kBarKvFull + i), kProdWarps);
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(sm.bar(kBarKvEmpty + i), 1);
-      mbar_init(sm.bar(kBarSFull + i), 1);
-      mbar_init(sm.bar(kBarSFree + i), kSoftWarps);
-      mbar_init(sm.bar(kBarPFull + i), kSoftWarps);
-    }
-    mbar_init(sm.bar(kBarODone), 1);
-    mbar_init(sm.bar(kBarOFree), kSoftWarps);
+    for (int i = 0; i < 4; ++i) mbar_init(sm.bar(kBarFull + i), kWorkWarps);
+    for (int i = 0; i < 2; ++i) mbar_init(sm.bar(kBarFree + i), 1);
+    mbar_init(sm.bar(kBarSFull), 1);
+    mbar_init(sm.bar(kBarPFull), kWorkWarps);
+    mbar_init(sm.bar(kBarOFree), kWorkWarps);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(sm.bar(kBarRowsFull + i), 1);
-      mbar_init(sm.bar(kBarRowsEmpty + i), kProdWarps);
+      mbar_init(sm.bar(kBarRowsEmpty + i), kWorkWarps);
     }
+    mbar_init(sm.bar(kBarDrain), 1);
     *sm.abort_flag() = 0;
     fence_mbar_init();
   }
@@ -1038,19 +923,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot();
 
-  if (warp < kSoftWarps) {
-    softmax_role(p, sm, rg, T, tmem, ws, c, fault);
-  } else if (warp < kMmaWarp) {
-    if constexpr (kFmt == QSFM_KV_PACKED640)
-      producer_role_packed(p, sm, fault);
-    else if constexpr (kFmt == QSFM_KV_BF16)
-      producer_role_bf16(p, sm, fault);
-    else
-      producer_role(p, sm, fault);
+  if (warp < kWorkWarps) {
+    worker_role<kFmt>(p, sm, rg, T, tmem, ws, c, fault);
   } else if (warp == kMmaWarp) {
-    qk_role(p, sm, rg, T, tmem, &qmap, fault);
-  } else if (warp == kPvWarp) {
-    pv_role(p, sm, rg, T, tmem, fault);
+    mma_role(p, sm, rg, T, tmem, &qmap, fault);
+    if ((tid & 31) == 0) {
+      // every MMA issued above has completed before tensor memory is freed
+      // (after an abort some may still be in flight)
+      mma_commit(sm.bar(kBarDrain));
+      wait_or_abort(sm, kBarDrain, 0, fault);
+    }
   } else {
     resolver_role<kFmt>(p, sm, rg, T, fault);
   }

@@ -117,8 +117,13 @@ __global__ void __launch_bounds__(kCombineThreads)
   const int32_t* meta = p.metadata;
   if (meta[0] != kMetaMagic || meta[2] != T) return;
   const int G = meta[1];
-  if (G < 0 || G > QSFM_MAX_CTAS) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // A plan made for more CTAs (or without split mode) than this call's
+  // workspace holds would send the reads below past the workspace: refuse it.
+  if (G < 0 || G > QSFM_MAX_CTAS || 2 * G > ws.slots || meta[4] != 1) {
+    if (tid == 0 && blockIdx.x == 0) atomicOr(fault, QSFM_FAULT_METADATA);
+    return;
+  }
   for (int i = tid; i < 2 * (G + 1); i += kCombineThreads) s_cut[i] = meta[kMetaHeader + i];
   __syncthreads();
   // cut c (1 <= c < G) owns its token when it falls inside it and the
@@ -226,9 +231,12 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
-// One CTA per requested token: writes the token's row slots in the order the
-// attention kernel visits them (ori window rows, then cmp slots), without the
-// padding of partial tiles.
+// One CTA per requested token, one warp per tile: every tile is resolved by
+// resolve_tile_rows with the lane mapping of the attention kernel's resolver
+// warp (lane l: slots l, l + 32, l + 64, l + 96 of the tile), and each
+// slot's logical row, and optionally its pool bytes, are written in the
+// order the kernel visits them (ori window rows, then cmp slots), without
+// the padding of partial tiles.
 __global__ void __launch_bounds__(128)
     debug_gather_kernel(const qsfm_params p, const int T, const int32_t* tokens, int max_rows,
                         uint8_t* rows_out, float* scales_out, int32_t* row_ids_out,
@@ -240,31 +248,34 @@ __global__ void __launch_bounds__(128)
     return;
   }
   const TokenGeom g = token_geom(p, t << unit_shift(p));  // the token's first unit
-  const int n_slots = g.n_ori + g.n_cmp;
-  if (threadIdx.x == 0) counts_out[i] = n_slots;
-  const int lim = min(n_slots, max_rows);
-  for (int s = threadIdx.x; s < lim; s += blockDim.x) {
-    int k, r;
-    if (s < g.n_ori) {
-      k = s / kTileRows;
-      r = s % kTileRows;
-    } else {
-      const int cs = s - g.n_ori;
-      k = g.ori_tiles + cs / kTileRows;
-      r = cs % kTileRows;
-    }
-    const RowRef ref = resolve_slot(p, g, k, r, fault);
-    row_ids_out[size_t(i) * max_rows + s] = ref.row >= 0 ? (ref.source << 30) | ref.row : -1;
-    if (rows_out == nullptr) continue;  // row ids only (any row format)
-    uint4* dst = reinterpret_cast<uint4*>(rows_out + (size_t(i) * max_rows + s) * kDim);
-    float* dsc = scales_out + (size_t(i) * max_rows + s) * kScales;
-    if (ref.row >= 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(ref.kv);
-      for (int j = 0; j < kDim / 16; ++j) dst[j] = src[j];
-      for (int j = 0; j < kScales; ++j) dsc[j] = ref.sc[j];
-    } else {
-      for (int j = 0; j < kDim / 16; ++j) dst[j] = make_uint4(0, 0, 0, 0);
-      for (int j = 0; j < kScales; ++j) dsc[j] = 0.f;
+  if (threadIdx.x == 0) counts_out[i] = g.n_ori + g.n_cmp;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int row_bytes = kv_row_bytes(p.kv_layout);
+  for (int k = warp; k < g.n_tiles; k += blockDim.x >> 5) {
+    const int ks[1] = {k};
+    const bool live[1] = {true};
+    int lgs[1][4], prs[1][4];
+    bool cmps[1];
+    resolve_tile_rows<1>(p, g, ks, live, lane, fault, lgs, prs, cmps);
+    const bool cmp = cmps[0];
+    const int* lg = lgs[0];
+    const int* pr = prs[0];
+    const uint8_t* pool = static_cast<const uint8_t*>(cmp ? p.cmp_kv : p.ori_kv);
+    const float* spool = cmp ? p.cmp_scale : p.ori_scale;
+    for (int u = 0; u < 4; ++u) {
+      const int in_tile = (cmp ? (k - g.ori_tiles) : k) * kTileRows + lane + 32 * u;
+      if (in_tile >= (cmp ? g.n_cmp : g.n_ori)) continue;  // padding of a partial tile
+      const int s = cmp ? g.n_ori + in_tile : in_tile;
+      if (s >= max_rows) continue;
+      row_ids_out[size_t(i) * max_rows + s] = lg[u] >= 0 ? (int(cmp) << 30) | lg[u] : -1;
+      if (rows_out == nullptr) continue;  // row ids only
+      uint4* dst = reinterpret_cast<uint4*>(rows_out + (size_t(i) * max_rows + s) * row_bytes);
+      const uint4* src = reinterpret_cast<const uint4*>(pool + size_t(pr[u] >= 0 ? pr[u] : 0) * row_bytes);
+      for (int q = 0; q < row_bytes / 16; ++q) dst[q] = pr[u] >= 0 ? src[q] : make_uint4(0, 0, 0, 0);
+      if (scales_out != nullptr) {
+        float* dsc = scales_out + (size_t(i) * max_rows + s) * kScales;
+        for (int q = 0; q < kScales; ++q) dsc[q] = pr[u] >= 0 ? spool[size_t(pr[u]) * kScales + q] : 0.f;
+      }
     }
   }
 }

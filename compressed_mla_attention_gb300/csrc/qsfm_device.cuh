@@ -24,7 +24,7 @@ constexpr int kHeads = QSFM_NUM_HEADS;        // N1
 constexpr int kDim = QSFM_HEAD_DIM;           // D
 constexpr int kBlock = QSFM_BLOCK_SIZE;       // tokens per KV block
 constexpr int kScales = QSFM_SCALES_PER_ROW;  // fp32 scales per row
-constexpr int kTileRows = 64;                 // KV rows per attention tile
+constexpr int kTileRows = 128;                // KV rows per attention tile
 constexpr int kMetaMagic = 0x51534D31;        // "QSM1"
 constexpr int kMetaHeader = 8;
 // metadata layout (int32[1024]):
@@ -131,106 +131,80 @@ static __device__ __noinline__ TokenGeom token_geom(const qsfm_params& p, int u)
   return g;
 }
 
-// One resolved KV row: byte pointer to its 512 fp8 values and to its 8 scales.
-struct RowRef {
-  const uint8_t* kv;
-  const float* sc;
-  int row;     // logical row; -1 when the slot is masked out
-  int source;  // 0 ori, 1 cmp
-};
-
-// Row for slot `i` of tile `k` of token t. Slots past the token's rows, -1
-// or invisible CSA entries resolve to row = -1. Bad block ids set a fault
-// bit and also resolve to -1 (the row is skipped, never read).
-static __device__ __noinline__ RowRef resolve_slot(const qsfm_params& p, const TokenGeom& g, int k,
-                                                   int i, int* fault) {
-  RowRef r{nullptr, nullptr, -1, 0};
-  int row;
-  const uint8_t* pool;
-  const float* scales;
-  const int32_t* table;
-  int width, nblocks, src;
-  if (k < g.ori_tiles) {
-    const int slot = k * kTileRows + i;
-    if (slot >= g.n_ori) return r;
-    row = g.ori_lo + slot;
-    pool = static_cast<const uint8_t*>(p.ori_kv); scales = p.ori_scale;
-    table = p.ori_block_table; width = p.ori_max_blocks; nblocks = p.ori_num_blocks; src = 0;
-  } else {
-    const int slot = (k - g.ori_tiles) * kTileRows + i;
-    if (slot >= g.n_cmp) return r;
-    if (p.cmp_sparse_indices != nullptr) {
-      row = __ldg(p.cmp_sparse_indices + (size_t)g.tok * p.k2 + slot);
-      if (row < 0 || row >= g.cmp_vis) return r;
-    } else {
-      row = slot;
+// Rows of the four slots i0, i0 + 32, i0 + 64, i0 + 96 of tiles k[t] of unit
+// g, for kN tiles t at once (0 <= i0 < 32): the one row resolution of the
+// library. The attention kernel's resolver warp (up to four tiles of a unit
+// per call), its L2 warm-up and the debug gather (one tile per call) all
+// call it with lane = i0, so the debug export shows exactly the rows the
+// kernel reads.
+//   logical[t][u]: the logical row of the slot in its KV sequence, -1 when
+//               the slot is past the token's rows, a -1 / invisible CSA
+//               entry, or its block could not be resolved;
+//   prow[t][u]: block * 128 + offset in the KV pool, -1 when logical is -1;
+//   cmp[t]:     false for ori tiles, true for cmp tiles.
+// Tiles with live[t] false are skipped (all -1). A table column past the
+// table width or a block id outside the pool sets a fault bit (when fault
+// is not null) and masks the slot: it is never read. The index loads of all
+// slots are in flight together, then all their block-table loads.
+template <int kN>
+__device__ __forceinline__ void resolve_tile_rows(const qsfm_params& p, const TokenGeom& g,
+                                                  const int (&k)[kN], const bool (&live)[kN], int i0,
+                                                  int* fault, int (&logical)[kN][4],
+                                                  int (&prow)[kN][4], bool (&cmp)[kN]) {
+  int row[kN][4];
+  bool ok[kN][4];
+  const int32_t* idx = p.cmp_sparse_indices + (size_t)g.tok * p.k2;
+#pragma unroll
+  for (int t = 0; t < kN; ++t) {
+    const bool ori = k[t] < g.ori_tiles;
+    cmp[t] = !ori;
+    const int base = (ori ? k[t] : k[t] - g.ori_tiles) * kTileRows + i0;
+    const int n = ori ? g.n_ori : g.n_cmp;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int slot = base + 32 * u;
+      ok[t][u] = live[t] && slot < n;
+      row[t][u] = ori ? g.ori_lo + slot : slot;
+      if (!ori && p.cmp_sparse_indices != nullptr && ok[t][u]) row[t][u] = __ldg(idx + slot);
     }
-    pool = static_cast<const uint8_t*>(p.cmp_kv); scales = p.cmp_scale;
-    table = p.cmp_block_table; width = p.cmp_max_blocks; nblocks = p.cmp_num_blocks; src = 1;
   }
-  const int col = row / kBlock;
-  if (col >= width) {
-    atomicOr(fault, src ? QSFM_FAULT_CMP_TABLE_COL : QSFM_FAULT_ORI_TABLE_COL);
-    return r;
+  int blk[kN][4];
+#pragma unroll
+  for (int t = 0; t < kN; ++t) {
+    const bool ori = !cmp[t];
+    const int32_t* table = ori ? p.ori_block_table : p.cmp_block_table;
+    const int width = ori ? p.ori_max_blocks : p.cmp_max_blocks;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (!ori && p.cmp_sparse_indices != nullptr)
+        ok[t][u] = ok[t][u] && row[t][u] >= 0 && row[t][u] < g.cmp_vis;
+      const int col = ok[t][u] ? row[t][u] / kBlock : 0;
+      if (ok[t][u] && col >= width) {
+        if (fault != nullptr) atomicOr(fault, ori ? QSFM_FAULT_ORI_TABLE_COL : QSFM_FAULT_CMP_TABLE_COL);
+        ok[t][u] = false;
+      }
+      blk[t][u] = ok[t][u] ? __ldg(table + (size_t)g.b * width + col) : 0;
+    }
   }
-  const int blk = __ldg(table + (size_t)g.b * width + col);
-  if (blk < 0 || blk >= nblocks) {
-    atomicOr(fault, src ? QSFM_FAULT_CMP_BLOCK_ID : QSFM_FAULT_ORI_BLOCK_ID);
-    return r;
+#pragma unroll
+  for (int t = 0; t < kN; ++t) {
+    const bool ori = !cmp[t];
+    const int nblocks = ori ? p.ori_num_blocks : p.cmp_num_blocks;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (ok[t][u] && (blk[t][u] < 0 || blk[t][u] >= nblocks)) {
+        if (fault != nullptr) atomicOr(fault, ori ? QSFM_FAULT_ORI_BLOCK_ID : QSFM_FAULT_CMP_BLOCK_ID);
+        ok[t][u] = false;
+      }
+      logical[t][u] = ok[t][u] ? row[t][u] : -1;
+      prow[t][u] = ok[t][u] ? blk[t][u] * kBlock + row[t][u] % kBlock : -1;
+    }
   }
-  const size_t prow = (size_t)blk * kBlock + (row % kBlock);
-  r.kv = pool + prow * kDim;
-  r.sc = scales + prow * kScales;
-  r.row = row;
-  r.source = src;
-  return r;
 }
 
-// Physical rows (block * kBlock + offset; -1 when masked) of slots i0 and
-// i0 + 32 of tile k of the unit g, by the rules of resolve_slot, with the
-// index loads of both slots in flight together and then their block-table
-// loads.
-__device__ __forceinline__ void resolve_two(const qsfm_params& p, const TokenGeom& g, int k, int i0,
-                                            int* fault, int (&prow)[2]) {
-  const bool ori = k < g.ori_tiles;
-  const int base = (ori ? k : k - g.ori_tiles) * kTileRows + i0;
-  const int n = ori ? g.n_ori : g.n_cmp;
-  int row[2];
-  bool ok[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int slot = base + 32 * u;
-    ok[u] = slot < n;
-    row[u] = ori ? g.ori_lo + slot : slot;
-  }
-  if (!ori && p.cmp_sparse_indices != nullptr) {
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-      if (ok[u]) row[u] = __ldg(p.cmp_sparse_indices + (size_t)g.tok * p.k2 + base + 32 * u);
-#pragma unroll
-    for (int u = 0; u < 2; ++u) ok[u] = ok[u] && row[u] >= 0 && row[u] < g.cmp_vis;
-  }
-  const int32_t* table = ori ? p.ori_block_table : p.cmp_block_table;
-  const int width = ori ? p.ori_max_blocks : p.cmp_max_blocks;
-  const int nblocks = ori ? p.ori_num_blocks : p.cmp_num_blocks;
-  int blk[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int col = row[u] / kBlock;
-    if (ok[u] && col >= width) {
-      atomicOr(fault, ori ? QSFM_FAULT_ORI_TABLE_COL : QSFM_FAULT_CMP_TABLE_COL);
-      ok[u] = false;
-    }
-    blk[u] = ok[u] ? __ldg(table + (size_t)g.b * width + col) : 0;
-  }
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    if (ok[u] && (blk[u] < 0 || blk[u] >= nblocks)) {
-      atomicOr(fault, ori ? QSFM_FAULT_ORI_BLOCK_ID : QSFM_FAULT_CMP_BLOCK_ID);
-      ok[u] = false;
-    }
-    prow[u] = ok[u] ? blk[u] * kBlock + row[u] % kBlock : -1;
-  }
+// Bytes of one KV row in the pool of each row format.
+__host__ __device__ constexpr int kv_row_bytes(int fmt) {
+  return fmt == QSFM_KV_PACKED640 ? QSFM_PACKED_ROW_BYTES : fmt == QSFM_KV_BF16 ? QSFM_BF16_ROW_BYTES : kDim;
 }
 
 // ------------------------------------------------------------ PTX wrappers
@@ -532,6 +506,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])));
+}
+
 // 16 lanes x 256 bit, 8 repetitions along the columns (64 columns). Thread t
 // of the warp receives, for repetition j, the accumulator-fragment quad
 //   v[4j+0] = (lane t/4,     column 8j + 2(t%4)),  v[4j+1] = its column + 1,
@@ -641,6 +633,13 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* ptr) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(ptr));
+  return v;
+}
+
+// Streaming read of 8 bytes (8-byte aligned).
+__device__ __forceinline__ uint2 ldg_stream_v2(const void* ptr) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ptr));
   return v;
 }
 

@@ -176,13 +176,34 @@ def test_kv_layout_checks(lib):
     assert _status(lib, p) == 1
 
 
-def test_debug_gather_exports_bytes_for_fp8_rows_only(lib):
+def test_debug_gather_argument_rules(lib):
+    """Row bytes are exported in every row format; separate scales exist for
+    fp8 rows only. Every case below is refused on the host (no launch)."""
     p = _valid(lib)
+    # fp8 rows: rows and scales go together
+    assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, 0x1000, None, 0x1000, 0x1000, None) == 1
+    assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, None, 0x1000, 0x1000, 0x1000, None) == 1
+    # row bytes must be 16-byte aligned
+    assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, 0x1008, 0x1000, 0x1000, 0x1000, None) == 1
     for layout in (1, 2):
         p.kv_layout, p.ori_scale = layout, None
-        assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, 0x1000, 0x1000, 0x1000, 0x1000, None) == 2
-        # row ids only (rows and scales NULL) are allowed for every format, but need the id buffer
+        # packed and bf16 rows have no separate scales to export
+        assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, 0x1000, 0x1000, 0x1000, 0x1000, None) == 1
+        # row ids (with or without row bytes) need the id buffer
         assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, None, None, None, 0x1000, None) == 1
+        assert lib.qsfm_debug_gather(ctypes.byref(p), 0x1000, 1, 1, 0x1000, None, None, 0x1000, None) == 1
+
+
+def test_noalloc_scratch_size_matches_header():
+    """The binding reads the scratch size from the C header, not a copy."""
+    import re
+
+    import compressed_mla_attention_gb300 as Q
+
+    text = open(os.path.join(ROOT, "include", "qsfm.h")).read()
+    m = re.search(r"#define QSFM_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m is not None
+    assert Q.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
 
 
 @pytest.mark.parametrize("why,change", [

@@ -29,25 +29,46 @@ def built():
 
 
 # ------------------------------------------------------- the five workloads
-def _config_tokens(i, w):
-    if i == 0:
+def _plan_starts(w, device, num_ctas=0):
+    """First unit of every planned CTA (the plan the bench's launch uses)."""
+    a = {k: v for k, v in W.device_inputs(w, device).items() if k != "return_softmax_lse"}
+    plan = torch.empty(1024, dtype=torch.int32, device=device)
+    p = Q.make_params(attn_out=torch.empty_like(a["q"]), metadata=plan, num_ctas=num_ctas, **a)
+    Q.metadata(p, plan)
+    m = plan.cpu().numpy()
+    g = int(m[1])
+    return [int(m[8 + 2 * c]) for c in range(g)]
+
+
+def _config_tokens(i, w, device):
+    """Tokens compared element by element with the oracle: every token of the
+    decode workloads; for the prefill workloads, every batch's first and last
+    token, every planned CTA's first and last token, and a seeded sample."""
+    if i in (0, 2, 3):
         return list(range(w.total_t))
-    if i == 1:  # early positions (short windows), a random sample, batch ends
+    ends = np.cumsum(w.q_lens)
+    edges = [int(x) - 1 for x in ends] + [int(x) for x in ends[:-1]] + [0]
+    starts = _plan_starts(w, device)
+    cta_edges = starts + [s - 1 for s in starts if s > 0]
+    if i == 1:  # early positions (short windows), a random sample, batch and CTA ends
         early = list(range(0, 160))
-        ends = [int(x) - 1 for x in np.cumsum(w.q_lens)]
-        return sorted(set(early + ends + W.subset_tokens(w, 96, seed=1).tolist()))
-    if i == 2:
-        return W.subset_tokens(w, 48, seed=2).tolist()
-    if i == 3:
-        return list(range(w.total_t))
-    return W.subset_tokens(w, 64, seed=4).tolist()
+        return sorted(set(early + edges + cta_edges + W.subset_tokens(w, 96, seed=1).tolist()))
+    # chunked prefill: 128 random tokens of each batch (1024 in all), plus the edges
+    tb = w.token_batch()
+    g = torch.Generator().manual_seed(4)
+    strat = []
+    for b in range(w.batch):
+        idx = np.flatnonzero(tb == b)
+        pick = torch.randperm(idx.size, generator=g)[:128].numpy()
+        strat += idx[pick].tolist()
+    return sorted(set(strat + edges + cta_edges))
 
 
 @pytest.mark.parametrize("i", range(5))
 def test_config_parity(cuda_device, i):
     w = W.config(i)
     out, lse = run_gpu(w, cuda_device, lse=True)
-    toks = _config_tokens(i, w)
+    toks = _config_tokens(i, w, cuda_device)
     assert np.isfinite(out).all()
     # Workload 1 returns no lse; its first tokens attend 1..127 rows, where the
     # lse carries the bf16 rounding of single logits, so its lse is held to
@@ -237,20 +258,31 @@ def test_index_permutation_invariance(cuda_device):
 
 
 # ------------------------------------------------------ row resolution
+def _pool_bytes(kv):
+    """A paged KV pool as the raw bytes of each row: uint8 [blocks, 128, row bytes]."""
+    if kv.dtype == torch.bfloat16:
+        kv = kv.contiguous().view(torch.uint8)
+    return kv.reshape(kv.shape[0], kv.shape[1], -1).numpy()
+
+
 def _expected_slots(w, t, with_bytes=True):
-    """(row ids, bytes, scales) of token t's slots, gathered in Python
-    (with_bytes=False: row ids only, bytes and scales left empty)."""
+    """(row ids, row bytes, scales) of token t's slots, resolved in Python
+    from the oracle's row sets and the block tables (with_bytes=False: ids
+    only). Scales are separate only for fp8 rows (else None)."""
     b, s = int(w.token_batch()[t]), int(w.token_pos()[t])
     ori, _ = O.token_rows(w, t, b, s)
     ids, rows_b, rows_s = [], [], []
     tab = w.ori_block_table[b].numpy()
+    fp8 = w.ori_scale is not None
     if with_bytes:
-        kv, sc = w.ori_kv.numpy(), w.ori_scale.numpy()
+        kv = _pool_bytes(w.ori_kv)
+        sc = w.ori_scale.numpy() if fp8 else None
     for r in ori or []:
         ids.append(r)
         if with_bytes:
-            rows_b.append(kv[tab[r // 128], r % 128, 0])
-            rows_s.append(sc[tab[r // 128], r % 128, 0])
+            rows_b.append(kv[tab[r // 128], r % 128])
+            if fp8:
+                rows_s.append(sc[tab[r // 128], r % 128, 0])
     if w.cmp_kv is not None and ori is not None:
         s1, s2 = int(w.q_lens[b]), int(w.seqused_ori_kv[b])
         cmp_len = s2 // w.cmp_ratio
@@ -263,57 +295,78 @@ def _expected_slots(w, t, with_bytes=True):
             entries = entries[:int(w.cmp_topk_length[t])]
         ctab = w.cmp_block_table[b].numpy()
         if with_bytes:
-            ckv, csc = w.cmp_kv.numpy(), w.cmp_scale.numpy()
+            ckv = _pool_bytes(w.cmp_kv)
+            csc = w.cmp_scale.numpy() if fp8 else None
         for e in entries:
             ok = 0 <= e < v
             ids.append((1 << 30) | e if ok else -1)
             if with_bytes:
-                rows_b.append(ckv[ctab[e // 128], e % 128, 0] if ok else np.zeros(512, np.uint8))
-                rows_s.append(csc[ctab[e // 128], e % 128, 0] if ok else np.zeros(8, np.float32))
-    return ids, rows_b, rows_s
+                rows_b.append(ckv[ctab[e // 128], e % 128] if ok else np.zeros(ckv.shape[-1], np.uint8))
+                if fp8:
+                    rows_s.append(csc[ctab[e // 128], e % 128, 0] if ok else np.zeros(8, np.float32))
+    return ids, rows_b, (rows_s if fp8 else None)
 
 
-@pytest.mark.parametrize("i", [0, 2, 3, 4])
-def test_debug_gather_bit_exact(cuda_device, i):
-    w = W.config(i)
-    toks = W.subset_tokens(w, 12, seed=i).tolist()
+GATHER_CASES = {
+    "tiny_csa_decode": lambda: W.config(0),
+    "csa_decode_batch": lambda: W.config(2),
+    "csa_decode_batch_n1_128": lambda: W.config(2, n1=128),
+    "hca_long_decode": lambda: W.config(3),
+    "csa_chunked_prefill": lambda: W.config(4),
+    "k2_1024": lambda: W.build("k2 1024", layout="BSND", q_lens=[2] * 4, s2=[8000, 30000, 5000, 12000],
+                               cmp_ratio=4, mode="CSA", k2=1024, seed=7),
+    "tiny_csa_decode_packed": lambda: W.config(0, kv_format="packed640"),
+    "csa_decode_batch_packed": lambda: W.config(2, kv_format="packed640"),
+    "hca_long_decode_bf16": lambda: W.config(3, kv_format="bf16"),
+    "csa_chunked_prefill_bf16": lambda: W.config(4, kv_format="bf16"),
+    "hca_tnd_packed": lambda: W.build("hca tnd", layout="TND", q_lens=[3, 5], s2=[3000, 40000], cmp_ratio=128,
+                                      mode="HCA", kv_format="packed640", seed=5),
+    "k2_1024_bf16": lambda: W.build("k2 1024 bf16", layout="BSND", q_lens=[2] * 2, s2=[30000, 9000],
+                                    cmp_ratio=4, mode="CSA", k2=1024, kv_format="bf16", seed=8),
+}
+
+
+@pytest.mark.parametrize("case", sorted(GATHER_CASES))
+def test_debug_gather_bit_exact(cuda_device, case):
+    """The row resolution of the attention kernel (the same device function
+    its resolver warp runs, with the same lane mapping) exported for sampled
+    tokens: logical row ids, the bytes of each resolved row in the pool's own
+    format and, for fp8 rows, the scale row, all bit for bit against a Python
+    gather through the block tables."""
+    w = GATHER_CASES[case]()
+    toks = W.subset_tokens(w, 12, seed=len(case)).tolist()
     args = W.device_inputs(w, cuda_device)
     out = torch.empty_like(args["q"])
     p = Q.make_params(attn_out=out, **{k: v for k, v in args.items() if k != "return_softmax_lse"})
+    fp8 = w.ori_scale is not None
+    row_bytes = _pool_bytes(w.ori_kv).shape[-1]
     max_rows = 1280
     n = len(toks)
     tok = torch.tensor(toks, dtype=torch.int32, device=cuda_device)
-    rows = torch.empty(n, max_rows, 512, dtype=torch.uint8, device=cuda_device)
-    scales = torch.empty(n, max_rows, 8, dtype=torch.float32, device=cuda_device)
+    rows = torch.empty(n, max_rows, row_bytes, dtype=torch.uint8, device=cuda_device)
+    scales = torch.empty(n, max_rows, 8, dtype=torch.float32, device=cuda_device) if fp8 else None
     ids = torch.empty(n, max_rows, dtype=torch.int32, device=cuda_device)
     counts = torch.empty(n, dtype=torch.int32, device=cuda_device)
     Q.debug_gather(p, tok, max_rows, rows, scales, ids, counts)
     torch.cuda.synchronize()
     assert Q.device_status() == 0
-    rows, scales, ids, counts = rows.cpu().numpy(), scales.cpu().numpy(), ids.cpu().numpy(), counts.cpu().numpy()
+    rows, ids, counts = rows.cpu().numpy(), ids.cpu().numpy(), counts.cpu().numpy()
+    if fp8:
+        scales = scales.cpu().numpy()
     for j, t in enumerate(toks):
         e_ids, e_b, e_s = _expected_slots(w, t)
         assert counts[j] == len(e_ids)
         m = min(len(e_ids), max_rows)
         assert np.array_equal(ids[j, :m], np.array(e_ids[:m], dtype=np.int32))
         assert np.array_equal(rows[j, :m], np.stack(e_b[:m]))
-        assert np.array_equal(scales[j, :m].view(np.uint32), np.stack(e_s[:m]).view(np.uint32))
+        if fp8:
+            assert np.array_equal(scales[j, :m].view(np.uint32), np.stack(e_s[:m]).view(np.uint32))
 
 
-GATHER_ID_CASES = {
-    "tiny_csa_decode": lambda f: W.config(0, kv_format=f),
-    "csa_chunked_prefill": lambda f: W.config(4, kv_format=f),
-    "hca_tnd": lambda f: W.build("hca", layout="TND", q_lens=[3, 5], s2=[3000, 40000], cmp_ratio=128,
-                                 mode="HCA", kv_format=f, seed=5),
-}
-
-
-@pytest.mark.parametrize("kv_format", ["packed640", "bf16"])
-@pytest.mark.parametrize("case", sorted(GATHER_ID_CASES))
-def test_debug_gather_row_ids_of_other_formats(cuda_device, kv_format, case):
-    """Row ids only (no row bytes), which every row format supports."""
-    w = GATHER_ID_CASES[case](kv_format)
-    toks = W.subset_tokens(w, 12, seed=len(case)).tolist()
+def test_debug_gather_row_ids_only(cuda_device):
+    """Row ids and counts alone (no row bytes), as the bench counts rows."""
+    w = W.config(4, kv_format="packed640")
+    toks = W.subset_tokens(w, 12, seed=3).tolist()
     args = W.device_inputs(w, cuda_device)
     out = torch.empty_like(args["q"])
     p = Q.make_params(attn_out=out, **{k: v for k, v in args.items() if k != "return_softmax_lse"})
@@ -331,11 +384,6 @@ def test_debug_gather_row_ids_of_other_formats(cuda_device, kv_format, case):
         assert counts[j] == len(e_ids)
         m = min(len(e_ids), max_rows)
         assert np.array_equal(ids[j, :m], np.array(e_ids[:m], dtype=np.int32))
-    rows = torch.empty(n, max_rows, 512, dtype=torch.uint8, device=cuda_device)
-    ids_d = torch.empty(n, max_rows, dtype=torch.int32, device=cuda_device)
-    counts_d = torch.empty(n, dtype=torch.int32, device=cuda_device)
-    with pytest.raises(Q.QsfmError):  # row bytes are exported for fp8 rows only (refused before launch)
-        Q.debug_gather(p, tok, max_rows, rows, None, ids_d, counts_d)
 
 
 # --------------------------------------------------------- fault reporting
@@ -385,6 +433,26 @@ def test_stale_metadata_is_rejected(cuda_device):
                        **{k: v for k, v in a2.items() if k != "return_softmax_lse"})
     ws = torch.empty(max(Q.workspace_size(p2), 1), dtype=torch.uint8, device=cuda_device)
     Q.forward(p2, ws)
+    torch.cuda.synchronize()
+    assert Q.device_status() & Q.FAULT_METADATA
+    assert (out.float() == 0).all()
+
+
+def test_plan_for_more_ctas_than_the_call_is_refused(cuda_device):
+    """A split plan made for 24 CTAs, reused by a forward call planned over 8
+    (whose workspace holds 8 CTAs' partial results): both kernels see the
+    mismatch, set the metadata fault bit and write nothing."""
+    w = W.config(0)
+    a = {k: v for k, v in W.device_inputs(w, cuda_device).items() if k != "return_softmax_lse"}
+    plan = torch.empty(1024, dtype=torch.int32, device=cuda_device)
+    big = Q.make_params(attn_out=torch.empty_like(a["q"]), metadata=plan, num_ctas=24, **a)
+    Q.metadata(big, plan)
+    assert int(plan[1].item()) > 8  # split over more CTAs than the call below plans
+    out = torch.zeros_like(a["q"])
+    small = Q.make_params(attn_out=out, metadata=plan, num_ctas=8, **a)
+    ws = torch.empty(Q.workspace_size(small), dtype=torch.uint8, device=cuda_device)
+    assert 0 < ws.numel() < Q.workspace_size(big)
+    Q.forward(small, ws)
     torch.cuda.synchronize()
     assert Q.device_status() & Q.FAULT_METADATA
     assert (out.float() == 0).all()
