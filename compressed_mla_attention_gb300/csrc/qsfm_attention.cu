@@ -70,7 +70,7 @@ namespace {
 
 static_assert(kTileRows == 128, "the kernel's layouts assume 128-row tiles");
 
-constexpr int kWorkWarps = 16;
+constexpr int kWorkWarps = 8;
 constexpr int kWorkThreads = kWorkWarps * 32;
 constexpr int kHPT = 256 / kWorkWarps;       // heads per worker thread (softmax, epilogue)
 constexpr int kRPT = 32 / kWorkWarps;        // tile rows per worker thread (producer)
@@ -108,9 +108,10 @@ constexpr int kBarSFull = 7;      // S^T of the tile complete (commit)
 constexpr int kBarPFull = 8;      // P of the tile written (one arrive per worker warp)
 constexpr int kBarOFree = 9;      // O^T read by the epilogue (one arrive per worker warp)
 constexpr int kBarDrain = 10;     // every MMA of the CTA completed (commit)
+constexpr int kBarQReady = 27;    // Q converted to f16 (one arrive per worker warp; fp8 rows)
 constexpr int kBarRowsFull = 11;  // [ring slot]
 constexpr int kBarRowsEmpty = 19; // [ring slot], one arrive per worker warp
-constexpr int kNumBars = 27;
+constexpr int kNumBars = 28;
 static_assert(kNumBars * 8 <= 224, "barriers overlap the tmem slot");
 
 constexpr uint32_t kTmemCols = 512;
@@ -119,8 +120,19 @@ constexpr uint32_t kTmemO = 256;  // + 64 * chunk
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kIdescQK = make_idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);
-constexpr uint32_t kIdescPV = make_idesc_bf16(128, 64, /*a_mn=*/1, /*b_mn=*/1);
+// Operand type of the products: fp8 rows are dequantised to f16 (one exact
+// e4m3 -> f16 conversion and one f16 multiply per pair of values; q is
+// converted to f16 when it lands, with an exact power-of-two prescale);
+// packed and bf16 rows keep bf16 (their bf16 rope / rows need its range).
+template <int kFmt>
+constexpr bool kF16Ops = kFmt == QSFM_KV_FP8_FP32_SCALES;
+template <int kFmt>
+constexpr uint32_t kIdescQK = make_idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0, kF16Ops<kFmt>);
+template <int kFmt>
+constexpr uint32_t kIdescPV = make_idesc_bf16(128, 64, /*a_mn=*/1, /*b_mn=*/1, kF16Ops<kFmt>);
+// Largest per-row power-of-two prescale of fp8 rows: P (<= 2^8 by the lazy
+// max) times 2^7 stays inside f16.
+constexpr int kMaxRowShift = 7;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 struct Range {
@@ -141,25 +153,6 @@ struct PieceIter {
     lo = (t == r.t0) ? min(r.k0, g.n_tiles) : 0;
     hi = (t == r.t1) ? min(r.k1, g.n_tiles) : g.n_tiles;
     ++t;
-    return true;
-  }
-};
-
-// Walks the (unit, tile) jobs of the range, skipping units without tiles.
-struct JobIter {
-  PieceIter pieces;
-  int tok = -1, k = 0, hi = 0;
-  TokenGeom g;
-  __device__ JobIter(const qsfm_params* p, Range r, int T) : pieces(p, r, T) {}
-  __device__ bool next(int& tok_out, int& k_out, TokenGeom& g_out) {
-    while (tok < 0 || k >= hi) {
-      int lo;
-      if (!pieces.next(tok, g, lo, hi)) return false;
-      k = lo;
-    }
-    tok_out = tok;
-    k_out = k++;
-    g_out = g;
     return true;
   }
 };
@@ -323,51 +316,55 @@ __device__ __forceinline__ float e8m0_value(uint32_t e) {
 // ------------------------------------------------------------- MMA issue
 // QK^T k-step s of d-block db: A (K~, K-major) at + db * 16 KB + s * 32 B,
 // B (Q, K-major) at + db * 8 KB + s * 32 B.
-template <int kDb, int kS>
+template <int kFmt, int kDb, int kS>
 __device__ __forceinline__ void qk_mma(uint32_t d, uint64_t a0, uint64_t b0) {
   constexpr uint32_t offa = uint32_t((kDb * kSlabBytes + kS * 32) >> 4);
   constexpr uint32_t offb = uint32_t((kDb * 8192 + kS * 32) >> 4);
   if constexpr ((kDb | kS) == 0)
-    mma_bf16_at<offa, offb>(d, a0, b0, kIdescQK, 0u);
+    mma_bf16_at<offa, offb>(d, a0, b0, kIdescQK<kFmt>, 0u);
   else
-    mma_bf16_acc_at<offa, offb>(d, a0, b0, kIdescQK);
+    mma_bf16_acc_at<offa, offb>(d, a0, b0, kIdescQK<kFmt>);
 }
 
-template <int kC>
+template <int kFmt, int kC>
 __device__ __forceinline__ void qk_chunk(uint32_t d, uint64_t a0, uint64_t b0) {
-  qk_mma<2 * kC, 0>(d, a0, b0); qk_mma<2 * kC, 1>(d, a0, b0);
-  qk_mma<2 * kC, 2>(d, a0, b0); qk_mma<2 * kC, 3>(d, a0, b0);
-  qk_mma<2 * kC + 1, 0>(d, a0, b0); qk_mma<2 * kC + 1, 1>(d, a0, b0);
-  qk_mma<2 * kC + 1, 2>(d, a0, b0); qk_mma<2 * kC + 1, 3>(d, a0, b0);
+  qk_mma<kFmt, 2 * kC, 0>(d, a0, b0); qk_mma<kFmt, 2 * kC, 1>(d, a0, b0);
+  qk_mma<kFmt, 2 * kC, 2>(d, a0, b0); qk_mma<kFmt, 2 * kC, 3>(d, a0, b0);
+  qk_mma<kFmt, 2 * kC + 1, 0>(d, a0, b0); qk_mma<kFmt, 2 * kC + 1, 1>(d, a0, b0);
+  qk_mma<kFmt, 2 * kC + 1, 2>(d, a0, b0); qk_mma<kFmt, 2 * kC + 1, 3>(d, a0, b0);
 }
 
 // PV k-step ks of head-dim chunk c: A (V~^T, MN-major: 64-d atoms 16 KB
 // apart, 8-row groups 1 KB apart) at + c * 32 KB + ks * 2 KB, B (P^T,
 // MN-major) at + ks * 2 KB.
-template <int kC, int kS>
+template <int kFmt, int kC, int kS>
 __device__ __forceinline__ void pv_mma(uint32_t d, uint64_t a0, uint64_t b0, uint32_t acc0) {
   constexpr uint32_t offa = uint32_t((kC * 2 * kSlabBytes + kS * 2048) >> 4);
   constexpr uint32_t offb = uint32_t((kS * 2048) >> 4);
   if constexpr (kS == 0)
-    mma_bf16_at<offa, offb>(d, a0, b0, kIdescPV, acc0);
+    mma_bf16_at<offa, offb>(d, a0, b0, kIdescPV<kFmt>, acc0);
   else
-    mma_bf16_acc_at<offa, offb>(d, a0, b0, kIdescPV);
+    mma_bf16_acc_at<offa, offb>(d, a0, b0, kIdescPV<kFmt>);
 }
 
-template <int kC>
+template <int kFmt, int kC>
 __device__ __forceinline__ void pv_chunk(uint32_t tmem, uint64_t a0, uint64_t b0, uint32_t acc0) {
   const uint32_t d = tmem + kTmemO + kC * 64;
-  pv_mma<kC, 0>(d, a0, b0, acc0); pv_mma<kC, 1>(d, a0, b0, acc0);
-  pv_mma<kC, 2>(d, a0, b0, acc0); pv_mma<kC, 3>(d, a0, b0, acc0);
-  pv_mma<kC, 4>(d, a0, b0, acc0); pv_mma<kC, 5>(d, a0, b0, acc0);
-  pv_mma<kC, 6>(d, a0, b0, acc0); pv_mma<kC, 7>(d, a0, b0, acc0);
+  pv_mma<kFmt, kC, 0>(d, a0, b0, acc0); pv_mma<kFmt, kC, 1>(d, a0, b0, acc0);
+  pv_mma<kFmt, kC, 2>(d, a0, b0, acc0); pv_mma<kFmt, kC, 3>(d, a0, b0, acc0);
+  pv_mma<kFmt, kC, 4>(d, a0, b0, acc0); pv_mma<kFmt, kC, 5>(d, a0, b0, acc0);
+  pv_mma<kFmt, kC, 6>(d, a0, b0, acc0); pv_mma<kFmt, kC, 7>(d, a0, b0, acc0);
 }
 
 // Tile n of the CTA's sequence: every per-tile barrier completes once per
 // tile, so a wait for tile n uses phase parity n & 1. A phase can never run
 // two ahead of its waiter: each completion needs the waiter's own next step.
+template <int kFmt>
 __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, uint32_t tmem,
                          const CUtensorMap* qmap, int* fault) {
+  // Q of a piece is ready for its products once it has landed (bf16 rows)
+  // or once the workers have converted it to f16 (fp8 rows)
+  constexpr int kBarQ = kF16Ops<kFmt> ? kBarQReady : kBarQFull;
   if ((threadIdx.x & 31) != 0) return;
   PieceIter pieces(&p, rg, T);
   TokenGeom g;
@@ -392,16 +389,16 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
     const uint32_t par = n & 1;
     if (!wait_or_abort(sm, kBarFull + 0, par, fault)) return false;
     tc_fence_after();
-    qk_chunk<0>(ds, qa, qb);
+    qk_chunk<kFmt, 0>(ds, qa, qb);
     if (!wait_or_abort(sm, kBarFull + 1, par, fault)) return false;
     tc_fence_after();
-    qk_chunk<1>(ds, qa, qb);
+    qk_chunk<kFmt, 1>(ds, qa, qb);
     if (!wait_or_abort(sm, kBarFull + 2, par, fault)) return false;
     tc_fence_after();
-    qk_chunk<2>(ds, qa, qb);
+    qk_chunk<kFmt, 2>(ds, qa, qb);
     if (!wait_or_abort(sm, kBarFull + 3, par, fault)) return false;
     tc_fence_after();
-    qk_chunk<3>(ds, qa, qb);
+    qk_chunk<kFmt, 3>(ds, qa, qb);
     mma_commit(sm.bar(kBarSFull));
     return true;
   };
@@ -409,7 +406,7 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
   int tok, lo, hi;
   if (!next_live(tok, lo, hi)) return;
   load_q(tok);
-  if (!wait_or_abort(sm, kBarQFull, 0, fault)) return;
+  if (!wait_or_abort(sm, kBarQ, 0, fault)) return;
   if (!qk_tile(0)) return;
   uint32_t n = 0, piece = 0;
   bool have = true;
@@ -431,14 +428,14 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
       // cycles): chunks 0 and 1 are freed first, so the producers store the
       // next tile's chunks 0 and 1 while chunks 2 and 3 are multiplied.
       const uint32_t acc0 = k == lo ? 0u : 1u;
-      pv_chunk<0>(tmem, pa, pb, acc0);
-      pv_chunk<1>(tmem, pa, pb, acc0);
+      pv_chunk<kFmt, 0>(tmem, pa, pb, acc0);
+      pv_chunk<kFmt, 1>(tmem, pa, pb, acc0);
       mma_commit(sm.bar(kBarFree + 0));
-      pv_chunk<2>(tmem, pa, pb, acc0);
-      pv_chunk<3>(tmem, pa, pb, acc0);
+      pv_chunk<kFmt, 2>(tmem, pa, pb, acc0);
+      pv_chunk<kFmt, 3>(tmem, pa, pb, acc0);
       mma_commit(sm.bar(kBarFree + 1));
       if (!last || have_next) {
-        if (last && !wait_or_abort(sm, kBarQFull, (piece + 1) & 1, fault)) return;
+        if (last && !wait_or_abort(sm, kBarQ, (piece + 1) & 1, fault)) return;
         if (!qk_tile(n + 1)) return;
       }
     }
@@ -477,7 +474,6 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
   const uint32_t lane_base = uint32_t(32 * qd) << 16;
   const uint32_t s_addr = tmem + kTmemS + h0 + lane_base;
   const uint32_t prow_addr = sm.base + kSP + uint32_t(r) * 128;
-  const float qk_scale = p.softmax_scale * kLog2e;
   float* m_used = sm.f(kSMUsed);
   float* alpha = sm.f(kSAlpha);
   float* inv = sm.f(kSInv);
@@ -493,28 +489,40 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
   constexpr int kRowB = kv_row_bytes(kFmt);
   const uint4 z = make_uint4(0, 0, 0, 0);
 
-  int pr[kRPT];       // physical rows of the tile to store next
-  int kd = 0;         // their pool (0 ori, 1 cmp)
-  uint2 sc[kRPT];     // its scales: fp8 scale j (x), packed e8m0 bytes (lane 4)
-  uint4 R[4][kRPT];   // its raw pieces: [chunk][row] (bf16: [2 (chunk & 1) + half][row])
-  uint4 RR[kRPT];     // packed rows: the rope piece of chunk 0
+  int pr[kRPT], pr_n[kRPT];    // physical rows of the tile to store next / of the one after
+  int kd = 0, kd_n = 0;        // their pools (0 ori, 1 cmp)
+  uint2 sc[kRPT], sc_n[kRPT];  // their scales: fp8 scale j (x), packed e8m0 bytes (lane 4)
+  uint4 R[4][kRPT];            // raw pieces: [chunk][row] (bf16: [2 (chunk & 1) + half][row])
+  uint4 RR[kRPT];              // packed rows: the rope piece of chunk 0
+  float rsc[kRPT];             // fp8 rows: the row's prescale 2^-k (f16 range)
+  int rsh[kRPT];               // fp8 rows: k
 
-  // Rows of tile n from the ring; false at the end mark or on abort.
-  auto take_rows = [&](uint32_t n) -> bool {
+  // Rows of tile n from the ring into (prr, kdd); false at the end mark or
+  // on abort.
+  auto take_rows = [&](uint32_t n, int (&prr)[kRPT], int& kdd) -> bool {
     const uint32_t slot = n % kRing;
     if (!warp_wait_or_abort(sm, kBarRowsFull + slot, (n / kRing) & 1, fault)) return false;
-    kd = kind[slot];
+    kdd = kind[slot];
 #pragma unroll
-    for (int u = 0; u < kRPT; ++u) pr[u] = rows[slot * kTileRows + row_lo + kRowStride * u];
+    for (int u = 0; u < kRPT; ++u) prr[u] = rows[slot * kTileRows + row_lo + kRowStride * u];
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.bar(kBarRowsEmpty + slot));
-    return kd >= 0;
+    return kdd >= 0;
   };
 
-  // Loads of raw chunk c of row u (bf16: into the registers of chunk c & 1).
-  auto load_chunk = [&](int c, int u) {
-    const bool v = pr[u] >= 0;
-    const uint8_t* row = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv) + size_t(v ? pr[u] : 0) * kRowB;
+  // Loads of raw chunk c of row u of the tile with rows (prr, kdd) (bf16:
+  // into the registers of chunk c & 1), and with chunk 0 the row's scales.
+  auto load_chunk = [&](int c, int u, const int (&prr)[kRPT], int kdd, uint2 (&scl)[kRPT]) {
+    const bool v = prr[u] >= 0;
+    const uint8_t* row = static_cast<const uint8_t*>(kdd ? p.cmp_kv : p.ori_kv) + size_t(v ? prr[u] : 0) * kRowB;
+    if (c == 0) {
+      if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
+        const float* spool = kdd ? p.cmp_scale : p.ori_scale;
+        scl[u].x = ldg_pred_u32(spool + size_t(v ? prr[u] : 0) * kScales + j, v);
+      } else if constexpr (kFmt == QSFM_KV_PACKED640) {
+        scl[u] = (v && j == 4) ? ldg_stream_v2(row + 576) : make_uint2(0, 0);
+      }
+    }
     if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
       R[c][u] = v ? ldg_stream_v4(row + 128 * c + 16 * j) : z;
     } else if constexpr (kFmt == QSFM_KV_BF16) {
@@ -527,23 +535,6 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
       } else {
         R[c][u] = v ? ldg_stream_v4(row + 64 + 128 * c + 16 * j) : z;
       }
-    }
-  };
-
-  // The raw rows of a whole tile (two chunks for bf16) and its scales.
-  auto load_tile = [&]() {
-#pragma unroll
-    for (int u = 0; u < kRPT; ++u) {
-      const bool v = pr[u] >= 0;
-      if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
-        const float* spool = kd ? p.cmp_scale : p.ori_scale;
-        sc[u].x = v ? __float_as_uint(__ldg(spool + size_t(pr[u]) * kScales + j)) : 0u;
-      } else if constexpr (kFmt == QSFM_KV_PACKED640) {
-        const uint8_t* row = static_cast<const uint8_t*>(kd ? p.cmp_kv : p.ori_kv) + size_t(v ? pr[u] : 0) * kRowB;
-        sc[u] = (v && j == 4) ? ldg_stream_v2(row + 576) : make_uint2(0, 0);
-      }
-#pragma unroll
-      for (int c = 0; c < (kFmt == QSFM_KV_BF16 ? 2 : 4); ++c) load_chunk(c, u);
     }
   };
 
@@ -563,8 +554,12 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
       }
       uint4 lo, hi;
       if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
-        const float s = __shfl_sync(0xffffffffu, __uint_as_float(sc[u].x), grp | (2 * c + odd));
-        dequant16_x2(R[c][u], s, lo, hi);
+        // f16 operands: e4m3 -> f16 is exact, then one f16 multiply by the
+        // block's scale times the row's prescale 2^-k
+        // (the clamp only acts on rows past 2^22, which are flagged)
+        const float s = fminf(__shfl_sync(0xffffffffu, __uint_as_float(sc[u].x), grp | (2 * c + odd)) * rsc[u],
+                              65504.f / 448.f);
+        dequant16_f16(R[c][u], pack_f16(s, s), lo, hi);
       } else {
         const uint32_t w0 = __shfl_sync(0xffffffffu, sc[u].x, grp | 4);  // scale bytes 0..3
         const uint32_t w1 = __shfl_sync(0xffffffffu, sc[u].y, grp | 4);  // scale bytes 4..6
@@ -590,47 +585,146 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.bar(kBarFull + c));
-    if constexpr (kFmt == QSFM_KV_BF16) {
-      if (c < 2) {
-#pragma unroll
-        for (int u = 0; u < kRPT; ++u) load_chunk(c + 2, u);
-      }
-    }
   };
 
   // Tile n from the registers into the tile buffer, chunk c once PV(n - 1)
-  // has read it; then the rows of tile n + 1 and their loads.
+  // has read it. The rows of tile n + 1 are taken first; as each chunk's
+  // registers are stored they are reloaded with the same chunk of tile n + 1
+  // (bf16 rows: chunks c + 2 of tile n, then chunks 0 and 1 of tile n + 1),
+  // so the loads are issued a chunk at a time and have about a tile's time
+  // in flight.
   uint32_t n_store = 0;
-  bool have_tile = take_rows(0);
-  if (have_tile) load_tile();
+  bool have_tile = take_rows(0, pr, kd);
+  if (have_tile) {
+#pragma unroll
+    for (int u = 0; u < kRPT; ++u) {
+#pragma unroll
+      for (int c = 0; c < (kFmt == QSFM_KV_BF16 ? 2 : 4); ++c) load_chunk(c, u, pr, kd, sc);
+    }
+  }
   auto store_next = [&]() {
     if (!have_tile) return;
+    const bool more = take_rows(n_store + 1, pr_n, kd_n);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {  // unrolled: the raw registers are indexed by c
-      if (n_store > 0 && (c & 1) == 0 && !warp_wait_or_abort(sm, kBarFree + (c >> 1), (n_store - 1) & 1, fault)) {
+      if (n_store > 0 && (c & 1) == 0 &&
+          !warp_wait_or_abort(sm, kBarFree + (c >> 1), (n_store - 1) & 1, fault)) {
         have_tile = false;
         return;
       }
-      if (c == 0 && j == 0) {
+      if (c == 0) {
+        if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
+          // Per-row prescale: the smallest k with 448 * max scale * 2^-k <=
+          // 2^15, so every dequantised value fits in f16 (k = 0 for any
+          // row whose values stay within 2^15). The softmax multiplies the
+          // row's logits and its P by 2^k; k <= 7 keeps P inside f16.
 #pragma unroll
-        for (int u = 0; u < kRPT; ++u) valid[row_lo + kRowStride * u] = pr[u] >= 0;
+          for (int u = 0; u < kRPT; ++u) {
+            float m = fabsf(__uint_as_float(sc[u].x));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            float t = m * (448.f / 32768.f);
+            int k = 0;
+            while (t > 1.f && k < kMaxRowShift) {
+              t *= 0.5f;
+              ++k;
+            }
+            if (t > 1.f && j == 0) atomicOr(fault, QSFM_FAULT_RANGE);
+            rsh[u] = k;
+            rsc[u] = __int_as_float((127 - k) << 23);
+          }
+        }
+        if (j == 0) {
+#pragma unroll
+          for (int u = 0; u < kRPT; ++u) {
+            int flag = pr[u] >= 0 ? 1 : 0;
+            if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) flag = pr[u] >= 0 ? rsh[u] + 1 : 0;
+            valid[row_lo + kRowStride * u] = flag;
+          }
+        }
       }
       store_chunk(c);
+#pragma unroll
+      for (int u = 0; u < kRPT; ++u) {
+        if constexpr (kFmt == QSFM_KV_BF16) {
+          if (c < 2) load_chunk(c + 2, u, pr, kd, sc);
+          else if (more) load_chunk(c - 2, u, pr_n, kd_n, sc_n);
+        } else {
+          if (more) load_chunk(c, u, pr_n, kd_n, sc_n);
+        }
+      }
     }
     ++n_store;
-    have_tile = take_rows(n_store);
-    if (have_tile) load_tile();
+    have_tile = more;
+#pragma unroll
+    for (int u = 0; u < kRPT; ++u) {
+      pr[u] = pr_n[u];
+      sc[u] = sc_n[u];
+    }
+    kd = kd_n;
   };
   store_next();  // tile 0
 
+  // fp8 rows: q of the next live piece, landed in bf16 by TMA, converted to
+  // f16 in place with the exact prescale 2^-kq (kq >= 0, the smallest with
+  // max |q| 2^-kq < 2^15); returns the piece's logit factor
+  // softmax_scale * log2(e) * 2^kq. Every worker thread converts 16 of the
+  // 4096 16-byte units (the swizzle is irrelevant to an elementwise pass).
+  uint32_t q_conv = 0;  // conversions done (one per live piece)
+  auto convert_q = [&]() -> float {
+    warp_wait_or_abort(sm, kBarQFull, q_conv & 1, fault);
+    ++q_conv;
+    const uint32_t qb = sm.base + kSQ;
+    uint32_t mx = 0;  // largest bf16 magnitude bit pattern
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const uint4 v = lds_v4(qb + 16 * uint32_t(tid + kWorkThreads * i));
+      mx = max(mx, max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu)));
+      mx = max(mx, max(max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu)));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    uint32_t* qred = reinterpret_cast<uint32_t*>(red);
+    if (lane == 0) qred[warp] = mx;
+    named_sync(kBarWork, kWorkThreads);
+#pragma unroll
+    for (int w = 0; w < kWorkWarps; ++w) mx = max(mx, qred[w]);
+    named_sync(kBarWork, kWorkThreads);  // qred (red) is free again
+    // bf16 exponent field e: |q| < 2^(e - 126); kq = max(0, e - 141)
+    const int kq = max(0, int((mx >> 7) & 0xFFu) - 141);
+    const float f = __int_as_float((127 - kq) << 23);
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t a = qb + 16 * uint32_t(tid + kWorkThreads * i);
+      const uint4 v = lds_v4(a);
+      uint4 o;
+      o.x = pack_f16(__uint_as_float(v.x << 16) * f, __uint_as_float(v.x & 0xFFFF0000u) * f);
+      o.y = pack_f16(__uint_as_float(v.y << 16) * f, __uint_as_float(v.y & 0xFFFF0000u) * f);
+      o.z = pack_f16(__uint_as_float(v.z << 16) * f, __uint_as_float(v.z & 0xFFFF0000u) * f);
+      o.w = pack_f16(__uint_as_float(v.w << 16) * f, __uint_as_float(v.w & 0xFFFF0000u) * f);
+      sts_v4(a, o);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(kBarQReady));
+    return p.softmax_scale * kLog2e * __int_as_float((127 + kq) << 23);
+  };
+  float qk_next = p.softmax_scale * kLog2e;  // logit factor of the next piece (fp8: set by convert_q)
+
   PieceIter pieces(&p, rg, T);
-  uint32_t n = 0;
+  uint32_t n = 0, pieces_live = 0;
   int t, lo, hi;
   TokenGeom g;
   bool have = pieces.next(t, g, lo, hi);
   int n_tiles = g.n_tiles;
   while (have) {
     const bool whole = (lo == 0 && hi == n_tiles);
+    if constexpr (kF16Ops<kFmt>) {
+      // q of this piece, unless it was converted at the end of the last one
+      if (lo < hi && q_conv == pieces_live) qk_next = convert_q();
+    }
+    const float qk_scale = qk_next;
     // this thread's head sink (log2 units); the unit's heads start at unit_head0
     const float sink2 =
         (tid < 64 && p.sinks != nullptr) ? __ldg(p.sinks + unit_head0(p, t) + tid) * kLog2e : -INFINITY;
@@ -649,7 +743,11 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
       // once; the workers keep running the same named-barrier sequence so
       // that none of them blocks.
       warp_wait_or_abort(sm, kBarFull + 0, par, fault);  // the tile's valid flags
-      const bool v = valid[r] != 0;
+      const int vflag = valid[r];
+      const bool v = vflag != 0;
+      // fp8 rows: the row's values were prescaled by 2^-k (flag = k + 1)
+      const float fr = kF16Ops<kFmt> && v ? __int_as_float((126 + vflag) << 23) : 1.f;
+      const float qk_row = qk_scale * fr;
       warp_wait_or_abort(sm, kBarSFull, par, fault);
       tc_fence_after();
       float x[kHPT];
@@ -663,10 +761,10 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
 #pragma unroll
         for (int i = 0; i < kHPT; i += 4) {
           const float4 m4 = *reinterpret_cast<const float4*>(m_used + h0 + i);
-          const float t0 = v ? fmaf(x[i], qk_scale, -m4.x) : -INFINITY;
-          const float t1 = v ? fmaf(x[i + 1], qk_scale, -m4.y) : -INFINITY;
-          const float t2 = v ? fmaf(x[i + 2], qk_scale, -m4.z) : -INFINITY;
-          const float t3 = v ? fmaf(x[i + 3], qk_scale, -m4.w) : -INFINITY;
+          const float t0 = v ? fmaf(x[i], qk_row, -m4.x) : -INFINITY;
+          const float t1 = v ? fmaf(x[i + 1], qk_row, -m4.y) : -INFINITY;
+          const float t2 = v ? fmaf(x[i + 2], qk_row, -m4.z) : -INFINITY;
+          const float t3 = v ? fmaf(x[i + 3], qk_row, -m4.w) : -INFINITY;
           tmax = fmaxf(tmax, fmaxf(fmaxf(t0, t1), fmaxf(t2, t3)));
           x[i] = ex2_approx(t0);
           x[i + 1] = ex2_approx(t1);
@@ -684,7 +782,7 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
           tmem_ld_wait();
         }
 #pragma unroll
-        for (int i = 0; i < kHPT; ++i) x[i] = v ? x[i] * qk_scale : -INFINITY;
+        for (int i = 0; i < kHPT; ++i) x[i] = v ? x[i] * qk_row : -INFINITY;
         const float mx = reduce_lanes<true>(x);  // head h0 + lane % kHPT, this quadrant's rows
         if (lane < kHPT) red[qd * 64 + h0 + lane] = mx;
         named_sync(kBarWork, kWorkThreads);
@@ -721,7 +819,7 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
         for (int i = 0; i < kHPT; ++i) {
           const float m = m_used[h0 + i];
           const float mz = m == -INFINITY ? 0.f : m;
-          x[i] = ex2_approx(v ? fmaf(x[i], qk_scale, -mz) : -INFINITY);
+          x[i] = ex2_approx(v ? fmaf(x[i], qk_row, -mz) : -INFINITY);
         }
         lscale = 0.f;
       }
@@ -732,10 +830,18 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
       for (int vv = 0; vv < kHPT / 8; ++vv) {
         const uint32_t u = uint32_t((h0 >> 3) + vv);
         uint4 pk;
-        pk.x = pack_bf16(x[8 * vv + 0], x[8 * vv + 1]);
-        pk.y = pack_bf16(x[8 * vv + 2], x[8 * vv + 3]);
-        pk.z = pack_bf16(x[8 * vv + 4], x[8 * vv + 5]);
-        pk.w = pack_bf16(x[8 * vv + 6], x[8 * vv + 7]);
+        if constexpr (kF16Ops<kFmt>) {
+          // P times the row factor (the row's V~ values carry 2^-k)
+          pk.x = pack_f16(x[8 * vv + 0] * fr, x[8 * vv + 1] * fr);
+          pk.y = pack_f16(x[8 * vv + 2] * fr, x[8 * vv + 3] * fr);
+          pk.z = pack_f16(x[8 * vv + 4] * fr, x[8 * vv + 5] * fr);
+          pk.w = pack_f16(x[8 * vv + 6] * fr, x[8 * vv + 7] * fr);
+        } else {
+          pk.x = pack_bf16(x[8 * vv + 0], x[8 * vv + 1]);
+          pk.y = pack_bf16(x[8 * vv + 2], x[8 * vv + 3]);
+          pk.z = pack_bf16(x[8 * vv + 4], x[8 * vv + 5]);
+          pk.w = pack_bf16(x[8 * vv + 6], x[8 * vv + 7]);
+        }
         sts_v4(prow_addr + ((u ^ uint32_t(r & 7)) << 4), pk);
       }
       fence_proxy_async_smem();
@@ -757,6 +863,11 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
     int t_next = 0, lo_next = 0, hi_next = 0;
     const bool have_next = pieces.next(t_next, g, lo_next, hi_next);
     const int n_tiles_next = g.n_tiles;
+    if constexpr (kF16Ops<kFmt>) {
+      // the next piece's q before this epilogue, so that its first QK^T
+      // does not wait for the epilogue
+      if (have_next && lo_next < hi_next && lo < hi) qk_next = convert_q();
+    }
     // ---------------- epilogue of the piece
     const bool any = lo < hi;
     if (any && lane < kHPT) red[qd * 64 + h0 + lane] = l_sum;
@@ -825,6 +936,7 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(kBarOFree));
+      ++pieces_live;
     }
     named_sync(kBarWork, kWorkThreads);  // m_used / inv / red are reused by the next piece
     if (*sm.abort_flag()) break;         // uniform: read after the barrier
@@ -914,6 +1026,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sm.bar(kBarRowsEmpty + i), kWorkWarps);
     }
     mbar_init(sm.bar(kBarDrain), 1);
+    mbar_init(sm.bar(kBarQReady), kWorkWarps);
     *sm.abort_flag() = 0;
     fence_mbar_init();
   }
@@ -926,7 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kWorkWarps) {
     worker_role<kFmt>(p, sm, rg, T, tmem, ws, c, fault);
   } else if (warp == kMmaWarp) {
-    mma_role(p, sm, rg, T, tmem, &qmap, fault);
+    mma_role<kFmt>(p, sm, rg, T, tmem, &qmap, fault);
     if ((tid & 31) == 0) {
       // every MMA issued above has completed before tensor memory is freed
       // (after an abort some may still be in flight)

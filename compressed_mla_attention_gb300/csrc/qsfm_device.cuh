@@ -83,7 +83,7 @@ __device__ __forceinline__ void token_batch(const qsfm_params& p, int t, int& b,
 // Not inlined: called once per token / tile, and every inlined copy would
 // grow the instruction footprint of the hot loops around it.
 // Geometry of work unit u (its token's rows; see unit_shift).
-static __device__ __noinline__ TokenGeom token_geom(const qsfm_params& p, int u) {
+static __device__ __forceinline__ TokenGeom token_geom(const qsfm_params& p, int u) {
   TokenGeom g;
   const int t = u >> unit_shift(p);
   g.tok = t;
@@ -288,7 +288,7 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
 // so the loop polls rarely; only long waits back off further with sleeps.
 // The polling loop is out of line, so each call site adds one test and a
 // call: the many waits of a kernel then share one copy of the loop.
-static __device__ __noinline__ bool mbar_wait_poll(uint32_t addr, uint32_t parity, volatile int* abort,
+static __device__ __forceinline__ bool mbar_wait_poll(uint32_t addr, uint32_t parity, volatile int* abort,
                                             uint64_t timeout_ns) {
   const uint64_t start = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -438,12 +438,12 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A/B bf16,
-// M x N, each operand K-major (0) or MN-major (1).
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int m, int n, int a_mn, int b_mn) {
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A/B bf16 (or
+// both f16 with f16 = true), M x N, each operand K-major (0) or MN-major (1).
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int m, int n, int a_mn, int b_mn, bool f16 = false) {
   return (1u << 4)                          // D format: f32
-         | (1u << 7)                        // A format: bf16
-         | (1u << 10)                       // B format: bf16
+         | (f16 ? 0u : (1u << 7))           // A format: f16 (0) or bf16 (1)
+         | (f16 ? 0u : (1u << 10))          // B format: f16 (0) or bf16 (1)
          | (uint32_t(a_mn) << 15)           // A major
          | (uint32_t(b_mn) << 16)           // B major
          | (uint32_t(n >> 3) << 17)         // N / 8
@@ -606,6 +606,34 @@ __device__ __forceinline__ void dequant16_x2(const uint4& in, float scale, uint4
   hi.w = dequant2_x2(uint16_t(in.w >> 16), s2);
 }
 
+// 2 e4m3fn values (low byte first) -> f16x2 (exact), times the f16x2 scale
+// pair s2 (one f16 multiply per lane, rounded once).
+__device__ __forceinline__ uint32_t dequant2_f16(uint16_t two, uint32_t s2) {
+  uint32_t h, r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(s2));
+  return r;
+}
+
+// 16 fp8 bytes -> 16 f16 (two 16-byte chunks) with the scale pair s2.
+__device__ __forceinline__ void dequant16_f16(const uint4& in, uint32_t s2, uint4& lo, uint4& hi) {
+  lo.x = dequant2_f16(uint16_t(in.x & 0xFFFF), s2);
+  lo.y = dequant2_f16(uint16_t(in.x >> 16), s2);
+  lo.z = dequant2_f16(uint16_t(in.y & 0xFFFF), s2);
+  lo.w = dequant2_f16(uint16_t(in.y >> 16), s2);
+  hi.x = dequant2_f16(uint16_t(in.z & 0xFFFF), s2);
+  hi.y = dequant2_f16(uint16_t(in.z >> 16), s2);
+  hi.z = dequant2_f16(uint16_t(in.w & 0xFFFF), s2);
+  hi.w = dequant2_f16(uint16_t(in.w >> 16), s2);
+}
+
+// Two fp32 values rounded to an f16x2 pair (a in the low half).
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
 // 16 fp8 bytes -> 16 bf16 (two 16-byte chunks).
 __device__ __forceinline__ void dequant16(const uint4& in, float scale, uint4& lo, uint4& hi) {
   lo.x = dequant2(uint16_t(in.x & 0xFFFF), scale);
@@ -633,6 +661,16 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* ptr) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(ptr));
+  return v;
+}
+
+// 4-byte read when pred is true, else 0. Predicated (not a load and a
+// select), so nothing waits for the load until its value is used.
+__device__ __forceinline__ uint32_t ldg_pred_u32(const void* ptr, bool pred) {
+  uint32_t v = 0;
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p ld.global.nc.b32 %0, [%1];\n}"
+               : "+r"(v)
+               : "l"(ptr), "r"(uint32_t(pred)));
   return v;
 }
 

@@ -6,8 +6,8 @@
  * formula O = softmax(Q K~^T * softmax_scale) V~ with K~ = V~; the per-head
  * sink is the "sinks" row of its "参数说明" (parameter) table):
  *
- *   for every query token t (batch b, position s) and head h (N1 = 64 heads,
- *   D = 512, one latent KV head, N2 = 1):
+ *   for every query token t (batch b, position s) and head h (N1 = 64 or
+ *   128 heads, D = 512, one latent KV head, N2 = 1):
  *     rows(t) = ori rows inside the band / causal window of t
  *             ++ cmp rows (CSA: the valid entries of cmp_sparse_indices[t];
  *                          HCA: every causally visible compressed row)
@@ -24,11 +24,11 @@
  *
  * Data layout (all device memory is owned by the caller; the library never
  * allocates, frees or keeps pointers after a call returns):
- *   q            bf16  BSND [B, S1, 64, 512] or TND [T1, 64, 512]
+ *   q            bf16  BSND [B, S1, N1, 512] or TND [T1, N1, 512]
  *   attn_out     bf16  same shape as q
- *   softmax_lse  fp32  BSND [B, 1, S1, 64] / TND [1, T1, 64]
+ *   softmax_lse  fp32  BSND [B, 1, S1, N1] / TND [1, T1, N1]
  *                      (KvQuantSparseAttnSharedKv, parameter table, row
- *                      softmax_lse); element (token t, head h) at t*64 + h
+ *                      softmax_lse); element (token t, head h) at t*N1 + h
  *   ori_kv       fp8 e4m3fn, paged [ori_num_blocks, 128, 1, 512]
  *   cmp_kv       fp8 e4m3fn, paged [cmp_num_blocks, 128, 1, 512]
  *   ori_scale / cmp_scale
@@ -50,7 +50,7 @@
  *   cmp_residual_kv int32 [B] or NULL (default 0), 0 <= r_b < cmp_ratio
  *   cmp_topk_length int32 [T] or NULL: only the first n entries of the
  *                token's index row are read
- *   sinks        fp32 [64] or NULL (NULL: no sink)
+ *   sinks        fp32 [N1] or NULL (NULL: no sink)
  *   metadata     int32 [1024] written by qsfm_metadata()
  *
  * Query position alignment is bottom-right: p = S2 - S1_b + s on the ori
@@ -123,6 +123,8 @@ typedef enum { QSFM_LAYOUT_BSND = 0, QSFM_LAYOUT_TND = 1 } qsfm_q_layout;
 #define QSFM_FAULT_CMP_TABLE_COL  0x8  /* cmp row beyond the table width     */
 #define QSFM_FAULT_METADATA       0x10 /* metadata header does not match     */
 #define QSFM_FAULT_TIMEOUT        0x20 /* a bounded device wait ran out      */
+#define QSFM_FAULT_RANGE          0x40 /* an fp8 KV row dequantises past
+                                          2^22: its values were clamped    */
 
 /*
  * All inputs, attributes and outputs of one forward call. Pointers are
@@ -258,17 +260,20 @@ qsfm_status qsfm_forward_noalloc(const qsfm_params* p, void* stream);
  * of the n query tokens in tokens[] (device int32), writes the token's row
  * slots in the kernel's order (ori window rows, then cmp slots), up to
  * max_rows of them:
- *   rows_out    uint8 [n, max_rows, 512]  the fp8 bytes of the resolved row
- *   scales_out  fp32  [n, max_rows, 8]    its dequant scales
+ *   rows_out    uint8 [n, max_rows, R]    the bytes of the resolved row in
+ *                                         the pool's own format, R = 512
+ *                                         (fp8), 640 (packed) or 1024 (bf16)
+ *   scales_out  fp32  [n, max_rows, 8]    its dequant scales (fp8 only)
  *   row_ids_out int32 [n, max_rows]       (source << 30) | logical row, with
  *                                         source 0 = ori, 1 = cmp; -1 for a
  *                                         slot that is masked out
  *   counts_out  int32 [n]                 number of slots of the token
- * Masked slots get zero bytes and zero scales. All buffers are device memory.
- * rows_out and scales_out may both be NULL: then only the row ids and counts
- * are written, for any kv_layout. Row bytes and scales are exported only for
- * kv_layout QSFM_KV_FP8_FP32_SCALES (QSFM_ERR_UNSUPPORTED for the others
- * when rows_out or scales_out is given).
+ * Masked slots get zero bytes and zero scales. All buffers are device memory
+ * and rows_out must be 16-byte aligned. rows_out and scales_out may both be
+ * NULL: then only the row ids and counts are written. For the fp8 format
+ * rows_out and scales_out are given together or not at all; for the others
+ * scales_out must be NULL (QSFM_ERR_INVALID_ARG otherwise). row_ids_out is
+ * required when max_rows > 0.
  */
 qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens,
                               int32_t n, int32_t max_rows, uint8_t* rows_out,
