@@ -80,7 +80,8 @@ constexpr int kMmaWarp = kWorkWarps;
 constexpr int kResolverWarp = kMmaWarp + 1;
 constexpr int kThreads = (kResolverWarp + 1) * 32;
 constexpr int kRing = 8;     // tiles of resolved rows in flight
-constexpr int kResolveTiles = 4;  // tiles the resolver resolves per pass (loads in flight together)
+constexpr int kResolveTiles = 1;  // tiles per resolver pass (more keeps more loads in flight, at a
+                                  // larger instruction footprint; the ring already runs 8 tiles ahead)
 constexpr int kBarWork = 1;  // named barrier id of the worker warps
 
 // shared memory map (byte offsets from a 1024-aligned base)
@@ -314,46 +315,42 @@ __device__ __forceinline__ float e8m0_value(uint32_t e) {
 }
 
 // ------------------------------------------------------------- MMA issue
-// QK^T k-step s of d-block db: A (K~, K-major) at + db * 16 KB + s * 32 B,
-// B (Q, K-major) at + db * 8 KB + s * 32 B.
-template <int kFmt, int kDb, int kS>
-__device__ __forceinline__ void qk_mma(uint32_t d, uint64_t a0, uint64_t b0) {
-  constexpr uint32_t offa = uint32_t((kDb * kSlabBytes + kS * 32) >> 4);
-  constexpr uint32_t offb = uint32_t((kDb * 8192 + kS * 32) >> 4);
-  if constexpr ((kDb | kS) == 0)
-    mma_bf16_at<offa, offb>(d, a0, b0, kIdescQK<kFmt>, 0u);
-  else
-    mma_bf16_acc_at<offa, offb>(d, a0, b0, kIdescQK<kFmt>);
+// QK^T of chunk c (d-blocks 2c, 2c + 1), k-step s of d-block db: A (K~,
+// K-major) at + db * 16 KB + s * 32 B, B (Q, K-major) at + db * 8 KB + s * 32
+// B. The chunk is a runtime argument (one copy of the code for all four);
+// its eight MMAs are unrolled with constant offsets from the chunk's base
+// descriptors, so the issuing thread keeps ahead of the tensor pipe.
+template <int kFmt, uint32_t kDb, uint32_t kS>
+__device__ __forceinline__ void qk_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+  mma_f16_at<((kDb * kSlabBytes + kS * 32) >> 4), ((kDb * 8192 + kS * 32) >> 4)>(d, a, b, kIdescQK<kFmt>, acc);
 }
 
-template <int kFmt, int kC>
-__device__ __forceinline__ void qk_chunk(uint32_t d, uint64_t a0, uint64_t b0) {
-  qk_mma<kFmt, 2 * kC, 0>(d, a0, b0); qk_mma<kFmt, 2 * kC, 1>(d, a0, b0);
-  qk_mma<kFmt, 2 * kC, 2>(d, a0, b0); qk_mma<kFmt, 2 * kC, 3>(d, a0, b0);
-  qk_mma<kFmt, 2 * kC + 1, 0>(d, a0, b0); qk_mma<kFmt, 2 * kC + 1, 1>(d, a0, b0);
-  qk_mma<kFmt, 2 * kC + 1, 2>(d, a0, b0); qk_mma<kFmt, 2 * kC + 1, 3>(d, a0, b0);
+template <int kFmt>
+__device__ __forceinline__ void qk_chunk(uint32_t d, uint64_t a0, uint64_t b0, int c) {
+  const uint64_t a = a0 + ((uint32_t(c) * 2 * kSlabBytes) >> 4);
+  const uint64_t b = b0 + ((uint32_t(c) * 2 * 8192) >> 4);
+  qk_mma<kFmt, 0, 0>(d, a, b, c != 0 ? 1u : 0u);
+  qk_mma<kFmt, 0, 1>(d, a, b, 1u); qk_mma<kFmt, 0, 2>(d, a, b, 1u); qk_mma<kFmt, 0, 3>(d, a, b, 1u);
+  qk_mma<kFmt, 1, 0>(d, a, b, 1u); qk_mma<kFmt, 1, 1>(d, a, b, 1u);
+  qk_mma<kFmt, 1, 2>(d, a, b, 1u); qk_mma<kFmt, 1, 3>(d, a, b, 1u);
 }
 
-// PV k-step ks of head-dim chunk c: A (V~^T, MN-major: 64-d atoms 16 KB
-// apart, 8-row groups 1 KB apart) at + c * 32 KB + ks * 2 KB, B (P^T,
-// MN-major) at + ks * 2 KB.
-template <int kFmt, int kC, int kS>
-__device__ __forceinline__ void pv_mma(uint32_t d, uint64_t a0, uint64_t b0, uint32_t acc0) {
-  constexpr uint32_t offa = uint32_t((kC * 2 * kSlabBytes + kS * 2048) >> 4);
-  constexpr uint32_t offb = uint32_t((kS * 2048) >> 4);
-  if constexpr (kS == 0)
-    mma_bf16_at<offa, offb>(d, a0, b0, kIdescPV<kFmt>, acc0);
-  else
-    mma_bf16_acc_at<offa, offb>(d, a0, b0, kIdescPV<kFmt>);
+// PV of head-dim chunk c, k-step s: A (V~^T, MN-major: 64-d atoms 16 KB
+// apart, 8-row groups 1 KB apart) at + c * 32 KB + s * 2 KB, B (P^T,
+// MN-major) at + s * 2 KB; accumulates into O^T columns 64 c .. + 63.
+template <int kFmt, uint32_t kS>
+__device__ __forceinline__ void pv_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+  mma_f16_at<((kS * 2048) >> 4), ((kS * 2048) >> 4)>(d, a, b, kIdescPV<kFmt>, acc);
 }
 
-template <int kFmt, int kC>
-__device__ __forceinline__ void pv_chunk(uint32_t tmem, uint64_t a0, uint64_t b0, uint32_t acc0) {
-  const uint32_t d = tmem + kTmemO + kC * 64;
-  pv_mma<kFmt, kC, 0>(d, a0, b0, acc0); pv_mma<kFmt, kC, 1>(d, a0, b0, acc0);
-  pv_mma<kFmt, kC, 2>(d, a0, b0, acc0); pv_mma<kFmt, kC, 3>(d, a0, b0, acc0);
-  pv_mma<kFmt, kC, 4>(d, a0, b0, acc0); pv_mma<kFmt, kC, 5>(d, a0, b0, acc0);
-  pv_mma<kFmt, kC, 6>(d, a0, b0, acc0); pv_mma<kFmt, kC, 7>(d, a0, b0, acc0);
+template <int kFmt>
+__device__ __forceinline__ void pv_chunk(uint32_t tmem, uint64_t a0, uint64_t b0, uint32_t acc0, int c) {
+  const uint32_t d = tmem + kTmemO + uint32_t(c) * 64;
+  const uint64_t a = a0 + ((uint32_t(c) * 2 * kSlabBytes) >> 4);
+  pv_mma<kFmt, 0>(d, a, b0, acc0);
+  pv_mma<kFmt, 1>(d, a, b0, 1u); pv_mma<kFmt, 2>(d, a, b0, 1u); pv_mma<kFmt, 3>(d, a, b0, 1u);
+  pv_mma<kFmt, 4>(d, a, b0, 1u); pv_mma<kFmt, 5>(d, a, b0, 1u);
+  pv_mma<kFmt, 6>(d, a, b0, 1u); pv_mma<kFmt, 7>(d, a, b0, 1u);
 }
 
 // Tile n of the CTA's sequence: every per-tile barrier completes once per
@@ -387,18 +384,12 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
   // QK^T of tile n, chunk by chunk as the producers publish the chunks
   auto qk_tile = [&](uint32_t n) -> bool {
     const uint32_t par = n & 1;
-    if (!wait_or_abort(sm, kBarFull + 0, par, fault)) return false;
-    tc_fence_after();
-    qk_chunk<kFmt, 0>(ds, qa, qb);
-    if (!wait_or_abort(sm, kBarFull + 1, par, fault)) return false;
-    tc_fence_after();
-    qk_chunk<kFmt, 1>(ds, qa, qb);
-    if (!wait_or_abort(sm, kBarFull + 2, par, fault)) return false;
-    tc_fence_after();
-    qk_chunk<kFmt, 2>(ds, qa, qb);
-    if (!wait_or_abort(sm, kBarFull + 3, par, fault)) return false;
-    tc_fence_after();
-    qk_chunk<kFmt, 3>(ds, qa, qb);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      if (!wait_or_abort(sm, kBarFull + c, par, fault)) return false;
+      tc_fence_after();
+      qk_chunk<kFmt>(ds, qa, qb, c);
+    }
     mma_commit(sm.bar(kBarSFull));
     return true;
   };
@@ -406,15 +397,17 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
   int tok, lo, hi;
   if (!next_live(tok, lo, hi)) return;
   load_q(tok);
-  if (!wait_or_abort(sm, kBarQ, 0, fault)) return;
-  if (!qk_tile(0)) return;
   uint32_t n = 0, piece = 0;
   bool have = true;
   while (have) {
     int ntok = 0, nlo = 0, nhi = 0;
     const bool have_next = next_live(ntok, nlo, nhi);
+#pragma unroll 1
     for (int k = lo; k < hi; ++k, ++n) {
       const bool last = k == hi - 1;
+      // QK^T(n) right after PV(n - 1): the piece's q first
+      if (k == lo && !wait_or_abort(sm, kBarQ, piece & 1, fault)) return;
+      if (!qk_tile(n)) return;
       // P(n) written (so S^T(n) has been read and QK^T(n) is complete)
       if (!wait_or_abort(sm, kBarPFull, n & 1, fault)) return;
       tc_fence_after();
@@ -428,15 +421,10 @@ __device__ void mma_role(const qsfm_params& p, const Smem& sm, Range rg, int T, 
       // cycles): chunks 0 and 1 are freed first, so the producers store the
       // next tile's chunks 0 and 1 while chunks 2 and 3 are multiplied.
       const uint32_t acc0 = k == lo ? 0u : 1u;
-      pv_chunk<kFmt, 0>(tmem, pa, pb, acc0);
-      pv_chunk<kFmt, 1>(tmem, pa, pb, acc0);
-      mma_commit(sm.bar(kBarFree + 0));
-      pv_chunk<kFmt, 2>(tmem, pa, pb, acc0);
-      pv_chunk<kFmt, 3>(tmem, pa, pb, acc0);
-      mma_commit(sm.bar(kBarFree + 1));
-      if (!last || have_next) {
-        if (last && !wait_or_abort(sm, kBarQ, (piece + 1) & 1, fault)) return;
-        if (!qk_tile(n + 1)) return;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        pv_chunk<kFmt>(tmem, pa, pb, acc0, c);
+        if (c & 1) mma_commit(sm.bar(kBarFree + (c >> 1)));
       }
     }
     ++piece;
@@ -604,45 +592,55 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
   }
   auto store_next = [&]() {
     if (!have_tile) return;
+    // this tile's scales were loaded with its chunk 0 a tile ago; taking
+    // them over only now keeps the copy from waiting on those loads
+    if (n_store > 0) {
+#pragma unroll
+      for (int u = 0; u < kRPT; ++u) sc[u] = sc_n[u];
+    }
     const bool more = take_rows(n_store + 1, pr_n, kd_n);
+    if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
+      // Per-row prescale: the smallest k with 448 * max scale * 2^-k <=
+      // 2^15, so every dequantised value fits in f16 (k = 0 for any row
+      // whose values stay within 2^15). The softmax multiplies the row's
+      // logits and its P by 2^k; k <= 7 keeps P inside f16. Computed before
+      // the wait for the buffer: it needs only the scales.
+#pragma unroll
+      for (int u = 0; u < kRPT; ++u) {
+        float m = fabsf(__uint_as_float(sc[u].x));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        // k = clamp(ceil(log2(m * 448 / 2^15)), 0, kMaxRowShift) from the
+        // exponent field (exact for the power-of-two thresholds)
+        const float t = m * (448.f / 32768.f);
+        const int e = int((__float_as_uint(t) >> 23) & 0xFFu) - 127;  // t in [2^e, 2^(e+1))
+        const bool pow2 = (__float_as_uint(t) & 0x7FFFFFu) == 0u;
+        int k = t > 1.f ? (pow2 ? e : e + 1) : 0;
+        if (k > kMaxRowShift) {
+          if (j == 0) atomicOr(fault, QSFM_FAULT_RANGE);
+          k = kMaxRowShift;
+        }
+        rsh[u] = k;
+        rsc[u] = __int_as_float((127 - k) << 23);
+      }
+    }
+    // the tile's valid flags (read by the softmax once chunk 0 is published;
+    // every worker has read the previous tile's flags before P was written)
+    if (j == 0) {
+#pragma unroll
+      for (int u = 0; u < kRPT; ++u) {
+        int flag = pr[u] >= 0 ? 1 : 0;
+        if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) flag = pr[u] >= 0 ? rsh[u] + 1 : 0;
+        valid[row_lo + kRowStride * u] = flag;
+      }
+    }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {  // unrolled: the raw registers are indexed by c
       if (n_store > 0 && (c & 1) == 0 &&
           !warp_wait_or_abort(sm, kBarFree + (c >> 1), (n_store - 1) & 1, fault)) {
         have_tile = false;
         return;
-      }
-      if (c == 0) {
-        if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) {
-          // Per-row prescale: the smallest k with 448 * max scale * 2^-k <=
-          // 2^15, so every dequantised value fits in f16 (k = 0 for any
-          // row whose values stay within 2^15). The softmax multiplies the
-          // row's logits and its P by 2^k; k <= 7 keeps P inside f16.
-#pragma unroll
-          for (int u = 0; u < kRPT; ++u) {
-            float m = fabsf(__uint_as_float(sc[u].x));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            float t = m * (448.f / 32768.f);
-            int k = 0;
-            while (t > 1.f && k < kMaxRowShift) {
-              t *= 0.5f;
-              ++k;
-            }
-            if (t > 1.f && j == 0) atomicOr(fault, QSFM_FAULT_RANGE);
-            rsh[u] = k;
-            rsc[u] = __int_as_float((127 - k) << 23);
-          }
-        }
-        if (j == 0) {
-#pragma unroll
-          for (int u = 0; u < kRPT; ++u) {
-            int flag = pr[u] >= 0 ? 1 : 0;
-            if constexpr (kFmt == QSFM_KV_FP8_FP32_SCALES) flag = pr[u] >= 0 ? rsh[u] + 1 : 0;
-            valid[row_lo + kRowStride * u] = flag;
-          }
-        }
       }
       store_chunk(c);
 #pragma unroll
@@ -658,13 +656,9 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
     ++n_store;
     have_tile = more;
 #pragma unroll
-    for (int u = 0; u < kRPT; ++u) {
-      pr[u] = pr_n[u];
-      sc[u] = sc_n[u];
-    }
+    for (int u = 0; u < kRPT; ++u) pr[u] = pr_n[u];
     kd = kd_n;
   };
-  store_next();  // tile 0
 
   // fp8 rows: q of the next live piece, landed in bf16 by TMA, converted to
   // f16 in place with the exact prescale 2^-kq (kq >= 0, the smallest with
@@ -737,7 +731,15 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
     float l_sum = 0.f;
     if (tid < 64) m_used[tid] = -INFINITY;
     named_sync(kBarWork, kWorkThreads);
-    for (int k = lo; k < hi; ++k, ++n) {
+    // One call site for the tile stores (the code stays small): the next
+    // tile goes into the buffer at the top of each iteration, as PV(n - 1)
+    // frees it; tile 0 right after the first q conversion (q lands first).
+    bool pending = n_store == 0;
+#pragma unroll 1
+    for (int k = lo;; ++k) {
+      if (pending) store_next();
+      if (k >= hi) break;
+      pending = true;
       const uint32_t par = n & 1;
       // Lane 0 of each warp polls. After an abort the waits fall through at
       // once; the workers keep running the same named-barrier sequence so
@@ -855,8 +857,7 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
         if (lscale == 0.f) l_sum *= alpha[h0 + (lane % kHPT)];
         l_sum += tile_sum;
       }
-      // the next tile into the buffer as PV(n) frees it
-      store_next();
+      ++n;
     }
     // The next piece's geometry, read now: its loads overlap the wait for
     // this piece's last PV product.
@@ -949,34 +950,19 @@ __device__ void worker_role(const qsfm_params& p, const Smem& sm, Range rg, int 
 }
 
 // Runs before the plan is readable, while the plan kernel still runs: warms
-// L2 with the inputs of the unit this CTA most likely starts with (the plan
-// cuts equal-cost units evenly, so CTA c of G starts near unit c T / G): its
-// Q and its first tile's rows, resolved by the library's one row resolution
-// (warp 0 of the workers). Only the first tile: every CTA does this at the
-// same moment, and more would queue the first tiles behind later ones. Only
-// prefetches, and no fault bits (the inputs may still be in flight from
-// earlier work on the stream), so a wrong guess costs bandwidth, never
-// results.
-template <int kFmt>
-__device__ __noinline__ void warm_first_token(const qsfm_params& p, int T, int c, int G, int i) {
+// L2 with the Q and the sparse-index row of the unit this CTA most likely
+// starts with (the plan cuts equal-cost units evenly, so CTA c of G starts
+// near unit c T / G). Prefetches only, no loads to wait for, no fault bits:
+// a wrong guess costs bandwidth, never results or time.
+__device__ __forceinline__ void warm_first_token(const qsfm_params& p, int T, int c, int G, int lane) {
   const int t = int((long long)c * T / G);
-  if (t >= T || i >= 64) return;
-  if (i == 32) {
+  if (t >= T) return;
+  if (lane == 0)
     bulk_prefetch_l2(static_cast<const uint8_t*>(p.q) + size_t(t) * kHeads * kDim * 2, kHeads * kDim * 2);
-    return;
+  if (p.cmp_sparse_indices != nullptr) {
+    const uint8_t* ix = reinterpret_cast<const uint8_t*>(p.cmp_sparse_indices + size_t(t >> unit_shift(p)) * p.k2);
+    for (int off = 128 * lane; off < 4 * p.k2; off += 32 * 128) prefetch_l2(ix + off);
   }
-  if (i >= 32) return;
-  const TokenGeom g = token_geom(p, t);
-  const int k[1] = {0};
-  const bool live[1] = {g.n_tiles > 0};
-  int lg[1][4], pr[1][4];
-  bool cmp[1];
-  resolve_tile_rows<1>(p, g, k, live, i, nullptr, lg, pr, cmp);
-  const uint8_t* pool = static_cast<const uint8_t*>(cmp[0] ? p.cmp_kv : p.ori_kv);
-  const float* spool = cmp[0] ? p.cmp_scale : p.ori_scale;
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-    if (pr[0][u] >= 0) prefetch_row<kFmt>(pool, spool, pr[0][u]);
 }
 
 template <int kFmt>
@@ -990,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.ptr = smem_raw + (sm.base - raw_addr);
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  if (warp < 2) warm_first_token<kFmt>(p, T, blockIdx.x, gridDim.x, tid);
+  if (warp == 0) warm_first_token(p, T, blockIdx.x, gridDim.x, tid);
   grid_dependency_wait();    // the plan (and every input) is written by now
   grid_launch_dependents();  // the combine kernel may take SMs as CTAs finish
   const int* meta = p.metadata;

@@ -394,16 +394,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
-// As mma_bf16, with the descriptors given as a base plus compile-time
-// offsets (in 16-byte units) added inside the asm, so that an unrolled
-// sequence of MMAs keeps only the two base descriptors in registers.
-// The offsets only move the 14-bit start-address field in the low word (the
-// whole shared-memory window is below 256 KB), so a 32-bit add on the low
-// word gives the same descriptor as a 64-bit add, in fewer instructions on
-// the single issuing thread.
+// One MMA with descriptors a_base + kAOff, b_base + kBOff, accumulating when
+// `accumulate` != 0. The offsets (16-byte units, compile-time immediates)
+// only move the 14-bit start-address field in the low word (the whole
+// shared-memory window is below 256 KB), so a 32-bit add on the low word
+// gives the same descriptor as a 64-bit add, in fewer instructions on the
+// single issuing thread.
 template <uint32_t kAOff, uint32_t kBOff>
-__device__ __forceinline__ void mma_bf16_at(uint32_t d_tmem, uint64_t a_base, uint64_t b_base,
-                                            uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16_at(uint32_t d_tmem, uint64_t a_base, uint64_t b_base, uint32_t idesc,
+                                           uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n .reg .b32 alo, ahi, blo, bhi;\n .reg .b64 a, b;\n"
       " mov.b64 {alo, ahi}, %1;\n mov.b64 {blo, bhi}, %2;\n"
@@ -412,21 +411,6 @@ __device__ __forceinline__ void mma_bf16_at(uint32_t d_tmem, uint64_t a_base, ui
       " setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n}" ::"r"(d_tmem),
       "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(kAOff), "n"(kBOff)
-      : "memory");
-}
-
-// Same, accumulating into D (every MMA of a tile's product but the first).
-template <uint32_t kAOff, uint32_t kBOff>
-__device__ __forceinline__ void mma_bf16_acc_at(uint32_t d_tmem, uint64_t a_base, uint64_t b_base,
-                                                uint32_t idesc) {
-  asm volatile(
-      "{\n .reg .pred p;\n .reg .b32 alo, ahi, blo, bhi;\n .reg .b64 a, b;\n"
-      " mov.b64 {alo, ahi}, %1;\n mov.b64 {blo, bhi}, %2;\n"
-      " add.u32 alo, alo, %4;\n add.u32 blo, blo, %5;\n"
-      " mov.b64 a, {alo, ahi};\n mov.b64 b, {blo, bhi};\n"
-      " setp.ne.b32 p, 1, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a_base), "l"(b_base), "r"(idesc), "n"(kAOff), "n"(kBOff)
       : "memory");
 }
 
