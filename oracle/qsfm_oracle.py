@@ -45,7 +45,21 @@ design notes of the repository):
      by softmax_scale and with no value vector;
   R6 lse = log sum_j exp(x_j) over attended rows, the sink excluded;
   R7 a token with no attended row (or a padded query row) gets O = 0 and
-     lse = -inf, even when a sink is given.
+     lse = -inf, even when a sink is given;
+  R13 ori_sparse_indices (QuantSparseFlashMla parameter table: discrete
+     picks from ori_kv, -1 = invalid; ori_topk_length: how many entries
+     take part) replace the contiguous ori range: the token's ori rows are
+     the entries of its index row (the first ori_topk_length of them when
+     given) that are not -1 and lie inside its ori mask range (R1, R2),
+     each occurrence counted, in index order;
+  R14 non-paged KV (QuantSparseFlashMla constraints on layout_kv): BSND
+     ori_kv [B, S2, 1, D] holds batch b's row j at [b, j]; TND ori_kv
+     [T2, 1, D] holds it at cu_seqlens_ori_kv[b] + j (cmp_kv alike with
+     cu_seqlens_cmp_kv). The ori length S2_b is seqused_ori_kv[b] (BSND;
+     the tensor's S dimension when absent) or cu[b + 1] - cu[b] (TND); the
+     cmp length is seqused_cmp_kv[b] when given, else the tensor's S
+     dimension (BSND) or the cu_seqlens_cmp_kv difference (TND), and
+     floor(S2 / cmp_ratio) for paged KV as before.
 """
 
 from __future__ import annotations
@@ -168,6 +182,48 @@ def cmp_visible_count(p_c: int, cmp_len: int, ratio: int, mode: int) -> int:
     raise ValueError(f"cmp_mask_mode {mode}")
 
 
+def kv_layout_of(w) -> str:
+    return getattr(w, "layout_kv", "PA_BBND")
+
+
+def ori_length(w, b: int) -> int:
+    """S2 of batch b (R14)."""
+    lay = kv_layout_of(w)
+    if lay == "TND":
+        cu = w.cu_seqlens_ori_kv
+        return int(cu[b + 1]) - int(cu[b])
+    if w.seqused_ori_kv is not None:
+        return int(w.seqused_ori_kv[b])
+    if lay == "BSND":
+        return int(w.ori_kv.shape[1])
+    raise ValueError("paged KV needs seqused_ori_kv")
+
+
+def cmp_length(w, b: int, s2: int) -> int:
+    """Compressed length of batch b (QuantSparseFlashMla constraints on
+    seqused_cmp_kv; R14)."""
+    if w.seqused_cmp_kv is not None:
+        return int(w.seqused_cmp_kv[b])
+    lay = kv_layout_of(w)
+    if lay == "BSND":
+        return int(w.cmp_kv.shape[1])
+    if lay == "TND":
+        cu = w.cu_seqlens_cmp_kv
+        return int(cu[b + 1]) - int(cu[b])
+    return s2 // int(w.cmp_ratio)
+
+
+def ori_picks(w, t: int, lo: int, hi: int) -> list:
+    """ori rows of token t picked by ori_sparse_indices (R13): the entries
+    of its index row (the first ori_topk_length[t] when given) that are not
+    -1 and lie in the mask range [lo, hi], in index order, repeats kept."""
+    idx = w.ori_sparse_indices
+    n = int(idx.shape[-1])
+    if w.ori_topk_length is not None:
+        n = min(n, int(w.ori_topk_length[t]))
+    return [int(e) for e in np.asarray(idx[t, 0, :max(n, 0)]).tolist() if e != -1 and lo <= e <= hi]
+
+
 def token_rows(w, t: int, b: int, s: int):
     """Attended rows of query token t (batch b, position s in the chunk).
 
@@ -177,14 +233,17 @@ def token_rows(w, t: int, b: int, s: int):
     s1_b = int(w.q_lens[b])
     if w.seqused_q is not None and s >= int(w.seqused_q[b]):
         return None, None
-    s2 = int(w.seqused_ori_kv[b])
+    s2 = ori_length(w, b)
     p = s2 - s1_b + s
     lo, hi = ori_row_range(p, s2, w.ori_mask_mode, w.ori_win_left, w.ori_win_right)
-    ori = list(range(lo, hi + 1))
+    if getattr(w, "ori_sparse_indices", None) is None:
+        ori = list(range(lo, hi + 1))
+    else:
+        ori = ori_picks(w, t, lo, hi)
     cmp_rows: list = []
     if w.cmp_kv is not None:
         r = int(w.cmp_ratio)
-        cmp_len = int(w.seqused_cmp_kv[b]) if w.seqused_cmp_kv is not None else s2 // r
+        cmp_len = cmp_length(w, b, s2)
         res = int(w.cmp_residual_kv[b]) if w.cmp_residual_kv is not None else 0
         p_c = cmp_len * r + res - s1_b + s
         v = cmp_visible_count(p_c, cmp_len, r, w.cmp_mask_mode)
@@ -266,18 +325,42 @@ def pool_bytes(pool) -> np.ndarray:
     return np.asarray(pool)
 
 
+def gather_dense(kv, scales, w, b: int, rows, cu):
+    """Bytes and scales of logical rows of batch b in non-paged KV (R14):
+    BSND kv [B, S, 1, row] at [b, j]; TND kv [T, 1, row] at cu[b] + j."""
+    kv = pool_bytes(kv)
+    sc = None if scales is None else np.asarray(scales)
+    idx = np.asarray(rows, dtype=np.int64)
+    if kv_layout_of(w) == "BSND":
+        out_b = kv[b, idx, 0]
+        out_s = None if sc is None else sc[b, idx, 0]
+    else:
+        flat = int(cu[b]) + idx
+        out_b = kv[flat, 0]
+        out_s = None if sc is None else sc[flat, 0]
+    out_b = np.asarray(out_b).reshape(len(idx), kv.shape[-1])
+    return out_b, None if out_s is None else np.asarray(out_s).reshape(len(idx), sc.shape[-1])
+
+
 def token_kv(w, t: int, b: int, s: int):
     """Dequantised K~ = V~ rows [n, 512] of token t: ori rows, then cmp rows."""
     ori, cmp_rows = token_rows(w, t, b, s)
     if ori is None:
         return None
     parts = []
-    ob, os_ = gather_paged(pool_bytes(w.ori_kv), None if w.ori_scale is None else np.asarray(w.ori_scale),
-                           np.asarray(w.ori_block_table[b]), ori)
+    paged = kv_layout_of(w) == "PA_BBND"
+    if paged:
+        ob, os_ = gather_paged(pool_bytes(w.ori_kv), None if w.ori_scale is None else np.asarray(w.ori_scale),
+                               np.asarray(w.ori_block_table[b]), ori)
+    else:
+        ob, os_ = gather_dense(w.ori_kv, w.ori_scale, w, b, ori, w.cu_seqlens_ori_kv)
     parts.append(decode_rows(ob, os_))
     if cmp_rows:
-        cb, cs = gather_paged(pool_bytes(w.cmp_kv), None if w.cmp_scale is None else np.asarray(w.cmp_scale),
-                              np.asarray(w.cmp_block_table[b]), cmp_rows)
+        if paged:
+            cb, cs = gather_paged(pool_bytes(w.cmp_kv), None if w.cmp_scale is None else np.asarray(w.cmp_scale),
+                                  np.asarray(w.cmp_block_table[b]), cmp_rows)
+        else:
+            cb, cs = gather_dense(w.cmp_kv, w.cmp_scale, w, b, cmp_rows, w.cu_seqlens_cmp_kv)
         parts.append(decode_rows(cb, cs))
     return np.concatenate(parts, axis=0)
 

@@ -18,6 +18,13 @@ prefill):
 * KV lives in 128-token blocks. Each batch takes its blocks from a randomly
   permuted physical pool sized to the exact total, so block tables are
   shuffled.
+* KV storage is paged (PA_BBND, the default: 128-token blocks through block
+  tables) or, for the non-paged layouts of QuantSparseFlashMla's layout_kv,
+  BSND ([B, S2max, 1, row] with each batch's rows from row 0 of its slab)
+  or TND ([T2, 1, row] with the batches' rows back to back, located by
+  cu_seqlens_ori_kv / cu_seqlens_cmp_kv).
+* ori_sparse_indices (when asked for) are drawn distinct and uniform from
+  the ori rows inside the token's mask range, valid entries first, -1 after.
 * CSA indices are drawn distinct and uniform from the compressed rows a token
   can see. The bound used for drawing is computed here from the
   bottom-right-aligned position; the oracle and the kernel each apply their
@@ -60,10 +67,10 @@ class Workload:
     q_lens: np.ndarray  # int64 [B]: query tokens per batch
     cu_seqlens_q: Optional[torch.Tensor]  # int32 [B+1] (TND)
     q: torch.Tensor  # bf16 [T, N1, 512], N1 = 64 or 128 (BSND memory is identical)
-    ori_kv: torch.Tensor  # uint8 [nb, 128, 1, 512], uint8 [nb, 128, 1, 640] packed rows, or bf16 [nb, 128, 1, 512]
+    ori_kv: torch.Tensor  # paged pool [nb, 128, 1, row] (uint8 512 fp8 / 640 packed, or bf16 512); see layout_kv
     ori_scale: Optional[torch.Tensor]  # fp32 [nb, 128, 1, 8]; None for packed and bf16 rows
-    ori_block_table: torch.Tensor  # int32 [B, wo]
-    seqused_ori_kv: torch.Tensor  # int32 [B]
+    ori_block_table: Optional[torch.Tensor]  # int32 [B, wo]; None for non-paged KV
+    seqused_ori_kv: Optional[torch.Tensor]  # int32 [B]; None for TND KV (and optionally BSND KV)
     cmp_kv: Optional[torch.Tensor]
     cmp_scale: Optional[torch.Tensor]
     cmp_block_table: Optional[torch.Tensor]
@@ -81,6 +88,15 @@ class Workload:
     ori_win_right: int
     return_lse: bool
     seed: int
+    # KV storage: "PA_BBND" (paged, the tensors above are pools and the
+    # tables map blocks), "BSND" (ori_kv [B, S2max, 1, row], cmp_kv
+    # [B, S3max, 1, row], no tables) or "TND" (ori_kv [T2, 1, row], cmp_kv
+    # [T3, 1, row], rows of batch b from cu_seqlens_*_kv[b])
+    layout_kv: str = "PA_BBND"
+    cu_seqlens_ori_kv: Optional[torch.Tensor] = None  # int32 [B+1] (TND KV)
+    cu_seqlens_cmp_kv: Optional[torch.Tensor] = None  # int32 [B+1] (TND KV with cmp_kv)
+    ori_sparse_indices: Optional[torch.Tensor] = None  # int32 [T, 1, K1]
+    ori_topk_length: Optional[torch.Tensor] = None  # int32 [T]
 
     @property
     def total_t(self) -> int:
@@ -93,6 +109,10 @@ class Workload:
     @property
     def k2(self) -> int:
         return 0 if self.cmp_sparse_indices is None else int(self.cmp_sparse_indices.shape[-1])
+
+    @property
+    def k1(self) -> int:
+        return 0 if self.ori_sparse_indices is None else int(self.ori_sparse_indices.shape[-1])
 
     @property
     def mode(self) -> str:
@@ -206,6 +226,50 @@ def _paged_pool(lengths: np.ndarray, gen: torch.Generator, min_width: int = 0,
     return kv, sc, table
 
 
+def _dense_rows(n: int, gen: torch.Generator, fmt: str):
+    """n random rows of a row format: (rows, scales or None); rows are uint8
+    [n, 512] (fp8), uint8 [n, 640] (packed) or bf16 [n, 512]."""
+    if fmt == "packed640":
+        return _random_packed_rows(n, gen), None
+    if fmt == "bf16":
+        return _random_bf16_rows(n, gen), None
+    return _random_rows(n, gen)
+
+
+def _dense_kv(lengths: np.ndarray, gen: torch.Generator, layout_kv: str, fmt: str, pad: int = 0):
+    """Non-paged KV of the given per-batch lengths: BSND [B, max + pad, 1, row]
+    (rows past a batch's length are random filler) or TND [sum + pad, 1, row]
+    with the prefix sums of the lengths. Returns (kv, scales, cu or None)."""
+    B = len(lengths)
+    if layout_kv == "BSND":
+        s = max([int(l) for l in lengths] + [0]) + pad
+        rows, sc = _dense_rows(max(B * s, 1), gen, fmt)
+        rows = rows[:B * s].reshape(B, s, 1, rows.shape[-1])
+        sc = None if sc is None else sc[:B * s].reshape(B, s, 1, SCALES_PER_ROW)
+        return rows, sc, None
+    assert layout_kv == "TND"
+    cu = torch.zeros(B + 1, dtype=torch.int32)
+    cu[1:] = torch.from_numpy(np.cumsum(np.asarray(lengths, dtype=np.int64))).to(torch.int32)
+    n = int(cu[-1]) + pad
+    rows, sc = _dense_rows(max(n, 1), gen, fmt)
+    rows = rows[:max(n, 1)].reshape(max(n, 1), 1, rows.shape[-1])
+    sc = None if sc is None else sc[:max(n, 1)].reshape(max(n, 1), 1, SCALES_PER_ROW)
+    return rows, sc, cu
+
+
+def _ori_draw_range(s2: int, s1: int, s: int, mode: int, wl: int, wr: int):
+    """Inclusive [lo, hi] of ori rows token s may draw ori indices from (the
+    bottom-right-aligned mask range; empty when hi < lo)."""
+    p = s2 - s1 + s
+    if mode == 0:
+        return 0, s2 - 1
+    if mode == 3:
+        return 0, min(s2 - 1, p)
+    lo = 0 if wl == -1 else max(0, p - wl)
+    hi = s2 - 1 if wr == -1 else min(s2 - 1, p + wr)
+    return lo, hi
+
+
 def _index_draw_bound(s2: int, s1: int, s: int, cmp_len: int, res: int, r: int) -> int:
     """Number of compressed rows token s may draw indices from (see module doc)."""
     p_c = cmp_len * r + res - s1 + s
@@ -237,8 +301,23 @@ def build(
     block_size: int = BLOCK,
     n1: int = NUM_HEADS,
     kv_format: str = "fp8_fp32_scales",
+    layout_kv: str = "PA_BBND",
+    kv_pad: int = 0,
+    bsnd_seqused: bool = True,
+    ori_k1: Optional[int] = None,
+    ori_n_valid: Optional[int] = None,
+    ori_topk_length: Optional[list] = None,
 ) -> Workload:
-    """Build one workload. q_lens / s2 are per-batch query and ori lengths."""
+    """Build one workload. q_lens / s2 are per-batch query and ori lengths.
+
+    layout_kv: "PA_BBND" (paged), "BSND" or "TND" (non-paged); kv_pad adds
+    filler rows past the last batch's rows (BSND: to every batch's slab);
+    bsnd_seqused False leaves seqused_ori_kv / seqused_cmp_kv out for BSND KV
+    (the lengths are then the tensors' S dimensions: every batch must fill
+    its slab). ori_k1 > 0 adds ori_sparse_indices [T, 1, K1] with up to
+    ori_n_valid (default K1) distinct rows of the token's ori mask range,
+    -1 after; ori_topk_length [T] optionally cuts each row.
+    """
     gen = torch.Generator().manual_seed(seed)
     q_lens = np.asarray(q_lens, dtype=np.int64)
     s2 = np.asarray(s2, dtype=np.int64)
@@ -247,7 +326,15 @@ def build(
     T = int(q_lens.sum())
     q = (torch.randn(T, n1, HEAD_DIM, generator=gen) * q_scale).to(torch.bfloat16)
     assert kv_format in ("fp8_fp32_scales", "packed640", "bf16")
-    ori_kv, ori_scale, ori_table = _paged_pool(s2, gen, block=block_size, fmt=kv_format)
+    assert layout_kv in ("PA_BBND", "BSND", "TND")
+    paged = layout_kv == "PA_BBND"
+    cu_ori = cu_cmp = None
+    if paged:
+        ori_kv, ori_scale, ori_table = _paged_pool(s2, gen, block=block_size, fmt=kv_format)
+    else:
+        assert layout_kv == layout, "non-paged KV needs layout_kv == layout_q"
+        ori_kv, ori_scale, cu_ori = _dense_kv(s2, gen, layout_kv, kv_format, pad=kv_pad)
+        ori_table = None
     sink = torch.randn(n1, generator=gen, dtype=torch.float32) if sinks else None
     cu = None
     if layout == "TND":
@@ -260,8 +347,13 @@ def build(
         cmp_len = s2 // cmp_ratio
         res = (s2 % cmp_ratio) if with_residual else np.zeros_like(s2)
         cmp_w = (int(s2.max()) // cmp_ratio + block_size - 1) // block_size if B else 1
-        cmp_kv, cmp_scale, cmp_table = _paged_pool(cmp_len, gen, min_width=cmp_w,
-                                                   block=block_size, fmt=kv_format)
+        if paged:
+            cmp_kv, cmp_scale, cmp_table = _paged_pool(cmp_len, gen, min_width=cmp_w,
+                                                       block=block_size, fmt=kv_format)
+        else:
+            cmp_kv, cmp_scale, cu_cmp = _dense_kv(cmp_len, gen, layout_kv, kv_format, pad=kv_pad)
+            if layout_kv == "BSND" and bsnd_seqused:
+                used_cmp = torch.from_numpy(cmp_len.astype(np.int32))
         resid = torch.from_numpy(res.astype(np.int32))
         if mode == "CSA":
             idx = torch.full((T, 1, k2), -1, dtype=torch.int32)
@@ -276,11 +368,32 @@ def build(
         if cmp_topk_length is not None:
             topk = torch.tensor(cmp_topk_length, dtype=torch.int32)
     used_q = torch.tensor(seqused_q, dtype=torch.int32) if seqused_q is not None else None
+    ori_idx = ori_topk = None
+    if ori_k1:
+        ori_idx = torch.full((T, 1, ori_k1), -1, dtype=torch.int32)
+        t = 0
+        for b in range(B):
+            for s in range(int(q_lens[b])):
+                lo, hi = _ori_draw_range(int(s2[b]), int(q_lens[b]), s, ori_mask_mode, ori_win_left, ori_win_right)
+                v = max(0, hi - lo + 1)
+                n = min(ori_k1 if ori_n_valid is None else ori_n_valid, v)
+                if n > 0:
+                    ori_idx[t, 0, :n] = (torch.randperm(v, generator=gen)[:n] + lo).to(torch.int32)
+                t += 1
+        if ori_topk_length is not None:
+            ori_topk = torch.tensor(ori_topk_length, dtype=torch.int32)
+    if layout_kv == "TND":
+        used_ori = None  # the lengths come from cu_seqlens_ori_kv
+    elif layout_kv == "BSND" and not bsnd_seqused:
+        assert len(set(s2.tolist())) <= 1 and kv_pad == 0, "without seqused every batch fills its slab"
+        used_ori = None
+    else:
+        used_ori = torch.from_numpy(s2.astype(np.int32))
     return Workload(
         name=name, layout=layout, batch=B, max_s1=int(q_lens.max()) if B else 0,
         q_lens=q_lens, cu_seqlens_q=cu, q=q,
         ori_kv=ori_kv, ori_scale=ori_scale, ori_block_table=ori_table,
-        seqused_ori_kv=torch.from_numpy(s2.astype(np.int32)),
+        seqused_ori_kv=used_ori,
         cmp_kv=cmp_kv, cmp_scale=cmp_scale, cmp_block_table=cmp_table,
         cmp_sparse_indices=idx, seqused_cmp_kv=used_cmp, cmp_residual_kv=resid,
         cmp_topk_length=topk, seqused_q=used_q, sinks=sink,
@@ -289,6 +402,8 @@ def build(
         ori_mask_mode=ori_mask_mode, cmp_mask_mode=cmp_mask_mode,
         ori_win_left=ori_win_left, ori_win_right=ori_win_right,
         return_lse=return_lse, seed=seed,
+        layout_kv=layout_kv, cu_seqlens_ori_kv=cu_ori, cu_seqlens_cmp_kv=cu_cmp,
+        ori_sparse_indices=ori_idx, ori_topk_length=ori_topk,
     )
 
 
@@ -378,4 +493,7 @@ def device_inputs(w: Workload, device) -> dict:
         softmax_scale=w.softmax_scale, cmp_ratio=w.cmp_ratio, ori_mask_mode=w.ori_mask_mode,
         cmp_mask_mode=w.cmp_mask_mode, ori_win_left=w.ori_win_left,
         ori_win_right=w.ori_win_right, return_softmax_lse=w.return_lse,
+        layout_kv=w.layout_kv, cu_seqlens_ori_kv=mv(w.cu_seqlens_ori_kv),
+        cu_seqlens_cmp_kv=mv(w.cu_seqlens_cmp_kv), ori_sparse_indices=mv(w.ori_sparse_indices),
+        ori_topk_length=mv(w.ori_topk_length),
     )
