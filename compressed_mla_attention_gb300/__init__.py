@@ -46,6 +46,9 @@ FAULT_ORI_TABLE_COL = 0x4
 FAULT_CMP_TABLE_COL = 0x8
 FAULT_METADATA = 0x10
 FAULT_TIMEOUT = 0x20
+FAULT_RANGE = 0x40
+FAULT_KV_ROW = 0x80
+LAYOUT_KV = {"PA_BBND": 0, "BSND": 1, "TND": 2}
 
 _i32 = ctypes.c_int32
 _ptr = ctypes.c_void_p
@@ -69,6 +72,9 @@ class QsfmParams(ctypes.Structure):
         ("layout_q", _i32), ("return_lse", _i32),
         ("attn_out", _ptr), ("softmax_lse", _ptr),
         ("kv_layout", _i32),
+        ("layout_kv", _i32), ("ori_kv_len", _i32), ("cmp_kv_len", _i32), ("k1", _i32),
+        ("cu_seqlens_ori_kv", _ptr), ("cu_seqlens_cmp_kv", _ptr), ("ori_sparse_indices", _ptr),
+        ("ori_topk_length", _ptr),
     ]
 
 
@@ -164,14 +170,23 @@ def make_params(
     ori_win_right: int = 0,
     return_lse: bool = False,
     num_ctas: int = 0,
+    layout_kv: str = "PA_BBND",
+    cu_seqlens_ori_kv=None,
+    cu_seqlens_cmp_kv=None,
+    ori_sparse_indices=None,
+    ori_topk_length=None,
 ) -> QsfmParams:
     """Fill a QsfmParams from device tensors (shapes as in include/qsfm.h).
 
     q / attn_out: BSND [B, S1, N1, 512] or TND [T1, N1, 512] bf16, N1 = 64 or 128.
-    Paged KV: [blocks, 128, 1, 512] uint8 (fp8 e4m3fn bytes) with fp32 scales
-    [blocks, 128, 1, 8], or packed [blocks, 128, 1, 640] uint8 rows (bf16 rope,
-    e4m3fn nope, e8m0 scales; scales None), or bf16 rows [blocks, 128, 1, 512]
-    (scales None); block tables int32 [B, width].
+    Paged KV (layout_kv "PA_BBND"): [blocks, 128, 1, 512] uint8 (fp8 e4m3fn
+    bytes) with fp32 scales [blocks, 128, 1, 8], or packed [blocks, 128, 1,
+    640] uint8 rows (bf16 rope, e4m3fn nope, e8m0 scales; scales None), or
+    bf16 rows [blocks, 128, 1, 512] (scales None); block tables int32 [B,
+    width]. Non-paged KV: layout_kv "BSND" ([B, S, 1, row], q BSND) or "TND"
+    ([T, 1, row], q TND, cu_seqlens_ori_kv / cu_seqlens_cmp_kv int32 [B+1]),
+    no block tables. ori_sparse_indices int32 [T, 1, K1] (or BSND
+    [B, S1, 1, K1]) with optional ori_topk_length int32 [T].
     """
     p = QsfmParams()
     lib().qsfm_params_init(ctypes.byref(p))
@@ -203,13 +218,25 @@ def make_params(
         p.kv_layout = KV_PACKED640
     else:
         p.kv_layout = KV_FP8_FP32_SCALES
-    p.ori_block_size = int(ori_kv.shape[1])
-    p.ori_max_blocks = int(ori_block_table.shape[-1])
-    p.ori_num_blocks = int(ori_kv.shape[0])
-    if cmp_kv is not None:
-        p.cmp_block_size = int(cmp_kv.shape[1])
-        p.cmp_max_blocks = int(cmp_block_table.shape[-1])
-        p.cmp_num_blocks = int(cmp_kv.shape[0])
+    if layout_kv not in LAYOUT_KV:
+        raise ValueError(layout_kv)
+    p.layout_kv = LAYOUT_KV[layout_kv]
+    if layout_kv == "PA_BBND":
+        p.ori_block_size = int(ori_kv.shape[1])
+        p.ori_max_blocks = int(ori_block_table.shape[-1])
+        p.ori_num_blocks = int(ori_kv.shape[0])
+        if cmp_kv is not None:
+            p.cmp_block_size = int(cmp_kv.shape[1])
+            p.cmp_max_blocks = int(cmp_block_table.shape[-1])
+            p.cmp_num_blocks = int(cmp_kv.shape[0])
+    else:  # the length of the sequence axis: S of [B, S, 1, row], T of [T, 1, row]
+        axis = 1 if layout_kv == "BSND" else 0
+        p.ori_kv_len = int(ori_kv.shape[axis])
+        if cmp_kv is not None:
+            p.cmp_kv_len = int(cmp_kv.shape[axis])
+    p.k1 = int(ori_sparse_indices.shape[-1]) if ori_sparse_indices is not None else 0
+    p.cu_seqlens_ori_kv, p.cu_seqlens_cmp_kv = _dptr(cu_seqlens_ori_kv), _dptr(cu_seqlens_cmp_kv)
+    p.ori_sparse_indices, p.ori_topk_length = _dptr(ori_sparse_indices), _dptr(ori_topk_length)
     p.num_ctas = int(num_ctas)
     p.q, p.attn_out = _dptr(q), _dptr(attn_out)
     p.ori_kv, p.ori_scale = _dptr(ori_kv), _dptr(ori_scale)
@@ -341,6 +368,11 @@ def quant_sparse_flash_mla(
     num_ctas: int = 0,
     out=None,
     stream=None,
+    layout_kv: str = "PA_BBND",
+    cu_seqlens_ori_kv=None,
+    cu_seqlens_cmp_kv=None,
+    ori_sparse_indices=None,
+    ori_topk_length=None,
 ):
     """One forward call: plan (unless metadata is given), attention, combine.
 
@@ -366,7 +398,9 @@ def quant_sparse_flash_mla(
         cmp_topk_length=cmp_topk_length, sinks=sinks, metadata=plan, softmax_lse=lse,
         softmax_scale=softmax_scale, cmp_ratio=cmp_ratio, ori_mask_mode=ori_mask_mode,
         cmp_mask_mode=cmp_mask_mode, ori_win_left=ori_win_left, ori_win_right=ori_win_right,
-        return_lse=return_softmax_lse, num_ctas=num_ctas)
+        return_lse=return_softmax_lse, num_ctas=num_ctas, layout_kv=layout_kv,
+        cu_seqlens_ori_kv=cu_seqlens_ori_kv, cu_seqlens_cmp_kv=cu_seqlens_cmp_kv,
+        ori_sparse_indices=ori_sparse_indices, ori_topk_length=ori_topk_length)
     if metadata is None:
         globals()["metadata"](p, plan, stream)
     if workspace is None:

@@ -104,9 +104,6 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   if (tokens * (p.n1 / QSFM_NUM_HEADS) > kMaxUnits) return QSFM_ERR_UNSUPPORTED;
   if (p.k2 < 0) return QSFM_ERR_INVALID_ARG;
   if (p.k2 > kMaxK2) return QSFM_ERR_UNSUPPORTED;
-  // paged ori KV is always present
-  if (p.ori_block_size < 1 || p.ori_block_size > 1024) return QSFM_ERR_INVALID_ARG;
-  if (p.ori_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
   if (p.kv_layout != QSFM_KV_FP8_FP32_SCALES && p.kv_layout != QSFM_KV_PACKED640 &&
       p.kv_layout != QSFM_KV_BF16)
     return QSFM_ERR_INVALID_ARG;
@@ -114,22 +111,58 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   // packed rows carry their scales and bf16 rows need none: a separate scale
   // tensor with them is a mistake
   if (no_scales && (p.ori_scale != nullptr || p.cmp_scale != nullptr)) return QSFM_ERR_INVALID_ARG;
-  if (p.ori_kv == nullptr || (!no_scales && p.ori_scale == nullptr) || p.ori_block_table == nullptr ||
-      p.seqused_ori_kv == nullptr)
-    return QSFM_ERR_INVALID_ARG;
-  if (p.ori_max_blocks < 1 || p.ori_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
-  if ((long long)p.ori_num_blocks * p.ori_block_size > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
+  if (p.ori_kv == nullptr || (!no_scales && p.ori_scale == nullptr)) return QSFM_ERR_INVALID_ARG;
   if (p.cmp_ratio < 1 || p.cmp_ratio > 128) return QSFM_ERR_INVALID_ARG;
   if (p.cmp_kv == nullptr) {
     if (p.cmp_ratio != 1) return QSFM_ERR_INVALID_ARG;  // SWA keeps the default 1
     if (p.cmp_sparse_indices != nullptr) return QSFM_ERR_INVALID_ARG;  // CSA needs cmp_kv
+  } else if (!no_scales && p.cmp_scale == nullptr) {
+    return QSFM_ERR_INVALID_ARG;
+  }
+  // KV storage (QuantSparseFlashMla constraints on layout_kv): BSND / TND KV
+  // only with the same q layout; block tables and seqused_ori_kv only where
+  // the layout uses them
+  if (p.layout_kv == QSFM_LAYOUT_KV_PA_BBND) {
+    if (p.cu_seqlens_ori_kv != nullptr || p.cu_seqlens_cmp_kv != nullptr) return QSFM_ERR_INVALID_ARG;
+    if (p.ori_block_size < 1 || p.ori_block_size > 1024) return QSFM_ERR_INVALID_ARG;
+    if (p.ori_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
+    if (p.ori_block_table == nullptr || p.seqused_ori_kv == nullptr) return QSFM_ERR_INVALID_ARG;
+    if (p.ori_max_blocks < 1 || p.ori_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
+    if ((long long)p.ori_num_blocks * p.ori_block_size > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
+    if (p.cmp_kv != nullptr) {
+      if (p.cmp_block_size < 1 || p.cmp_block_size > 1024) return QSFM_ERR_INVALID_ARG;
+      if (p.cmp_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
+      if (p.cmp_block_table == nullptr) return QSFM_ERR_INVALID_ARG;
+      if (p.cmp_max_blocks < 1 || p.cmp_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
+      if ((long long)p.cmp_num_blocks * p.cmp_block_size > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
+    }
+  } else if (p.layout_kv == QSFM_LAYOUT_KV_BSND || p.layout_kv == QSFM_LAYOUT_KV_TND) {
+    const bool tnd = p.layout_kv == QSFM_LAYOUT_KV_TND;
+    if (p.layout_q != (tnd ? QSFM_LAYOUT_TND : QSFM_LAYOUT_BSND)) return QSFM_ERR_INVALID_ARG;
+    if (p.ori_block_table != nullptr || p.cmp_block_table != nullptr) return QSFM_ERR_INVALID_ARG;
+    if (p.ori_kv_len < 1 || (p.cmp_kv != nullptr && p.cmp_kv_len < 1)) return QSFM_ERR_INVALID_ARG;
+    if (tnd) {
+      if (p.seqused_ori_kv != nullptr || (p.cu_seqlens_ori_kv == nullptr && p.batch > 0))
+        return QSFM_ERR_INVALID_ARG;
+      if (p.cmp_kv != nullptr && p.cu_seqlens_cmp_kv == nullptr && p.batch > 0) return QSFM_ERR_INVALID_ARG;
+      if (p.cmp_kv == nullptr && p.cu_seqlens_cmp_kv != nullptr) return QSFM_ERR_INVALID_ARG;
+    } else {
+      if (p.cu_seqlens_ori_kv != nullptr || p.cu_seqlens_cmp_kv != nullptr) return QSFM_ERR_INVALID_ARG;
+      // rows b * S + j of the whole tensor stay below 2^31
+      if ((long long)p.batch * p.ori_kv_len > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
+      if (p.cmp_kv != nullptr && (long long)p.batch * p.cmp_kv_len > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
+    }
   } else {
-    if (p.cmp_block_size < 1 || p.cmp_block_size > 1024) return QSFM_ERR_INVALID_ARG;
-    if (p.cmp_block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
-    if ((!no_scales && p.cmp_scale == nullptr) || p.cmp_block_table == nullptr) return QSFM_ERR_INVALID_ARG;
-    if (p.cmp_max_blocks < 1 || p.cmp_num_blocks < 1) return QSFM_ERR_INVALID_ARG;
-    if ((long long)p.cmp_num_blocks * p.cmp_block_size > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
-    if (p.cmp_sparse_indices != nullptr && p.k2 < 1) return QSFM_ERR_INVALID_ARG;
+    return QSFM_ERR_INVALID_ARG;
+  }
+  if (p.cmp_sparse_indices != nullptr && p.k2 < 1) return QSFM_ERR_INVALID_ARG;
+  // discrete ori picks (QuantSparseFlashMla parameter table rows
+  // ori_sparse_indices and ori_topk_length)
+  if (p.ori_sparse_indices != nullptr) {
+    if (p.k1 < 1) return QSFM_ERR_INVALID_ARG;
+    if (p.k1 > kMaxK2) return QSFM_ERR_UNSUPPORTED;
+  } else if (p.k1 != 0 || p.ori_topk_length != nullptr) {
+    return QSFM_ERR_INVALID_ARG;
   }
   if (p.ori_mask_mode != 0 && p.ori_mask_mode != 3 && p.ori_mask_mode != 4)
     return QSFM_ERR_INVALID_ARG;
@@ -151,7 +184,8 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
   const void* words[] = {p.ori_scale, p.cmp_scale, p.cmp_sparse_indices, p.ori_block_table,
                          p.cmp_block_table, p.cu_seqlens_q, p.seqused_q, p.seqused_ori_kv,
                          p.seqused_cmp_kv, p.cmp_residual_kv, p.cmp_topk_length, p.sinks,
-                         p.metadata, p.softmax_lse};
+                         p.metadata, p.softmax_lse, p.cu_seqlens_ori_kv, p.cu_seqlens_cmp_kv,
+                         p.ori_sparse_indices, p.ori_topk_length};
   for (const void* w : words)
     if (!aligned(w, 4)) return QSFM_ERR_INVALID_ARG;
   return QSFM_OK;

@@ -38,10 +38,13 @@ struct TokenGeom {
   int b;          // batch of the token
   int s2;         // ori length S2 of the batch
   int tok;        // query token of the unit
-  int ori_lo;     // first ori row attended
-  int n_ori;      // ori rows attended (contiguous from ori_lo)
+  int ori_lo;     // first ori row of the mask range
+  int ori_hi;     // last ori row of the mask range (ori picks must lie in it)
+  int n_ori;      // ori slots: rows ori_lo .. ori_hi, or ori index entries scanned
   int n_cmp;      // cmp slots: CSA index entries scanned, HCA visible rows
   int cmp_vis;    // visible compressed rows V (CSA entries must be < V)
+  int ori_base;   // non-paged KV: tensor row of the batch's ori row 0
+  int cmp_base;   // non-paged KV: tensor row of the batch's cmp row 0
   int ori_tiles;  // ceil(n_ori / kTileRows)
   int n_tiles;    // ori tiles + ceil(n_cmp / kTileRows)
 };
@@ -90,14 +93,27 @@ static __device__ __forceinline__ TokenGeom token_geom(const qsfm_params& p, int
   int s, s1;
   token_batch(p, t, g.b, s, s1);
   // every per-batch / per-token length this token may need, loaded together
-  // (one memory round trip instead of a chain of them)
-  const int s2 = __ldg(p.seqused_ori_kv + g.b);
+  // (one memory round trip instead of a chain of them). KV storage
+  // (QuantSparseFlashMla constraints on layout_kv): S2 is seqused_ori_kv
+  // (paged; BSND when given, else the S dimension) or the cu_seqlens_ori_kv
+  // difference (TND); the cmp length defaults to floor(S2 / r) (paged), the
+  // S dimension (BSND) or the cu_seqlens_cmp_kv difference (TND).
+  const bool tnd_kv = p.layout_kv == QSFM_LAYOUT_KV_TND;
+  const int used_ori = p.seqused_ori_kv != nullptr ? __ldg(p.seqused_ori_kv + g.b) : p.ori_kv_len;
+  const int cu_o0 = tnd_kv ? __ldg(p.cu_seqlens_ori_kv + g.b) : 0;
+  const int cu_o1 = tnd_kv ? __ldg(p.cu_seqlens_ori_kv + g.b + 1) : 0;
+  const bool tnd_cmp = tnd_kv && p.cmp_kv != nullptr;
+  const int cu_c0 = tnd_cmp ? __ldg(p.cu_seqlens_cmp_kv + g.b) : 0;
+  const int cu_c1 = tnd_cmp ? __ldg(p.cu_seqlens_cmp_kv + g.b + 1) : 0;
   const int used_q = p.seqused_q != nullptr ? __ldg(p.seqused_q + g.b) : 0;
   const int used_cmp = p.seqused_cmp_kv != nullptr ? __ldg(p.seqused_cmp_kv + g.b) : 0;
   const int resid = p.cmp_residual_kv != nullptr ? __ldg(p.cmp_residual_kv + g.b) : 0;
   const int topk = p.cmp_topk_length != nullptr ? __ldg(p.cmp_topk_length + t) : 0;
-  g.s2 = s2;
-  g.ori_lo = 0; g.n_ori = 0; g.n_cmp = 0; g.cmp_vis = 0;
+  const int otopk = p.ori_topk_length != nullptr ? __ldg(p.ori_topk_length + t) : 0;
+  g.s2 = tnd_kv ? cu_o1 - cu_o0 : used_ori;
+  g.ori_base = tnd_kv ? cu_o0 : p.layout_kv == QSFM_LAYOUT_KV_BSND ? g.b * p.ori_kv_len : 0;
+  g.cmp_base = tnd_kv ? cu_c0 : p.layout_kv == QSFM_LAYOUT_KV_BSND ? g.b * p.cmp_kv_len : 0;
+  g.ori_lo = 0; g.ori_hi = -1; g.n_ori = 0; g.n_cmp = 0; g.cmp_vis = 0;
   bool live = !(p.seqused_q != nullptr && s >= used_q);
   if (live) {
     const int pos = g.s2 - s1 + s;  // bottom-right aligned position
@@ -111,10 +127,17 @@ static __device__ __forceinline__ TokenGeom token_geom(const qsfm_params& p, int
       hi = p.ori_win_right < 0 ? g.s2 - 1 : min(g.s2 - 1, pos + p.ori_win_right);
     }
     g.ori_lo = lo;
-    g.n_ori = max(0, hi - lo + 1);
+    g.ori_hi = hi;
+    if (p.ori_sparse_indices != nullptr)  // discrete picks: slots = index entries scanned
+      g.n_ori = p.ori_topk_length != nullptr ? max(0, min(p.k1, otopk)) : p.k1;
+    else
+      g.n_ori = max(0, hi - lo + 1);
     if (p.cmp_kv != nullptr) {
       const int r = p.cmp_ratio;
-      const int cmp_len = p.seqused_cmp_kv ? used_cmp : g.s2 / r;
+      const int cmp_len = p.seqused_cmp_kv ? used_cmp
+                          : tnd_kv          ? cu_c1 - cu_c0
+                          : p.layout_kv == QSFM_LAYOUT_KV_BSND ? p.cmp_kv_len
+                                                               : g.s2 / r;
       const int res = resid;
       const int pc = cmp_len * r + res - s1 + s;
       g.cmp_vis = p.cmp_mask_mode == 3 ? max(0, min(cmp_len, div_floor(pc + 1, r))) : cmp_len;
@@ -133,19 +156,21 @@ static __device__ __forceinline__ TokenGeom token_geom(const qsfm_params& p, int
 
 // Rows of the four slots i0, i0 + 32, i0 + 64, i0 + 96 of tiles k[t] of unit
 // g, for kN tiles t at once (0 <= i0 < 32): the one row resolution of the
-// library. The attention kernel's resolver warp (up to four tiles of a unit
-// per call), its L2 warm-up and the debug gather (one tile per call) all
-// call it with lane = i0, so the debug export shows exactly the rows the
-// kernel reads.
+// library. The attention kernel's resolver warp and the debug gather (one
+// tile per call) call it with lane = i0, so the debug export shows exactly
+// the rows the kernel reads.
 //   logical[t][u]: the logical row of the slot in its KV sequence, -1 when
-//               the slot is past the token's rows, a -1 / invisible CSA
-//               entry, or its block could not be resolved;
-//   prow[t][u]: block * 128 + offset in the KV pool, -1 when logical is -1;
+//               the slot is past the token's rows, a -1 / out-of-range
+//               ori or cmp pick, or a row that could not be resolved;
+//   prow[t][u]: the row's index in the KV tensor (paged: block * 128 +
+//               offset; BSND: b * S + row; TND: cu_seqlens_*_kv[b] + row),
+//               -1 when logical is -1;
 //   cmp[t]:     false for ori tiles, true for cmp tiles.
 // Tiles with live[t] false are skipped (all -1). A table column past the
-// table width or a block id outside the pool sets a fault bit (when fault
-// is not null) and masks the slot: it is never read. The index loads of all
-// slots are in flight together, then all their block-table loads.
+// table width, a block id outside the pool or a non-paged row past the end
+// of its tensor sets a fault bit (when fault is not null) and masks the
+// slot: it is never read. The index loads of all slots are in flight
+// together, then all their block-table loads.
 template <int kN>
 __device__ __forceinline__ void resolve_tile_rows(const qsfm_params& p, const TokenGeom& g,
                                                   const int (&k)[kN], const bool (&live)[kN], int i0,
@@ -153,21 +178,24 @@ __device__ __forceinline__ void resolve_tile_rows(const qsfm_params& p, const To
                                                   int (&prow)[kN][4], bool (&cmp)[kN]) {
   int row[kN][4];
   bool ok[kN][4];
-  const int32_t* idx = p.cmp_sparse_indices + (size_t)g.tok * p.k2;
+  const int32_t* cidx = p.cmp_sparse_indices + (size_t)g.tok * p.k2;
+  const int32_t* oidx = p.ori_sparse_indices + (size_t)g.tok * p.k1;
 #pragma unroll
   for (int t = 0; t < kN; ++t) {
     const bool ori = k[t] < g.ori_tiles;
     cmp[t] = !ori;
     const int base = (ori ? k[t] : k[t] - g.ori_tiles) * kTileRows + i0;
     const int n = ori ? g.n_ori : g.n_cmp;
+    const bool picks = ori ? p.ori_sparse_indices != nullptr : p.cmp_sparse_indices != nullptr;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int slot = base + 32 * u;
       ok[t][u] = live[t] && slot < n;
       row[t][u] = ori ? g.ori_lo + slot : slot;
-      if (!ori && p.cmp_sparse_indices != nullptr && ok[t][u]) row[t][u] = __ldg(idx + slot);
+      if (picks && ok[t][u]) row[t][u] = __ldg((ori ? oidx : cidx) + slot);
     }
   }
+  const bool paged = p.layout_kv == QSFM_LAYOUT_KV_PA_BBND;
   int blk[kN][4];
 #pragma unroll
   for (int t = 0; t < kN; ++t) {
@@ -176,28 +204,49 @@ __device__ __forceinline__ void resolve_tile_rows(const qsfm_params& p, const To
     const int width = ori ? p.ori_max_blocks : p.cmp_max_blocks;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
+      // picks count only inside the token's range: ori picks in its ori mask
+      // range, cmp picks below the visible count (-1 never passes)
+      if (ori && p.ori_sparse_indices != nullptr)
+        ok[t][u] = ok[t][u] && row[t][u] >= g.ori_lo && row[t][u] <= g.ori_hi;
       if (!ori && p.cmp_sparse_indices != nullptr)
         ok[t][u] = ok[t][u] && row[t][u] >= 0 && row[t][u] < g.cmp_vis;
       const int col = ok[t][u] ? row[t][u] / kBlock : 0;
-      if (ok[t][u] && col >= width) {
+      if (paged && ok[t][u] && col >= width) {
         if (fault != nullptr) atomicOr(fault, ori ? QSFM_FAULT_ORI_TABLE_COL : QSFM_FAULT_CMP_TABLE_COL);
         ok[t][u] = false;
       }
-      blk[t][u] = ok[t][u] ? __ldg(table + (size_t)g.b * width + col) : 0;
+      blk[t][u] = (paged && ok[t][u]) ? __ldg(table + (size_t)g.b * width + col) : 0;
     }
   }
 #pragma unroll
   for (int t = 0; t < kN; ++t) {
     const bool ori = !cmp[t];
-    const int nblocks = ori ? p.ori_num_blocks : p.cmp_num_blocks;
+    if (paged) {
+      const int nblocks = ori ? p.ori_num_blocks : p.cmp_num_blocks;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (ok[t][u] && (blk[t][u] < 0 || blk[t][u] >= nblocks)) {
-        if (fault != nullptr) atomicOr(fault, ori ? QSFM_FAULT_ORI_BLOCK_ID : QSFM_FAULT_CMP_BLOCK_ID);
-        ok[t][u] = false;
+      for (int u = 0; u < 4; ++u) {
+        if (ok[t][u] && (blk[t][u] < 0 || blk[t][u] >= nblocks)) {
+          if (fault != nullptr) atomicOr(fault, ori ? QSFM_FAULT_ORI_BLOCK_ID : QSFM_FAULT_CMP_BLOCK_ID);
+          ok[t][u] = false;
+        }
+        logical[t][u] = ok[t][u] ? row[t][u] : -1;
+        prow[t][u] = ok[t][u] ? blk[t][u] * kBlock + row[t][u] % kBlock : -1;
       }
-      logical[t][u] = ok[t][u] ? row[t][u] : -1;
-      prow[t][u] = ok[t][u] ? blk[t][u] * kBlock + row[t][u] % kBlock : -1;
+    } else {
+      // BSND / TND KV: the batch's rows start at its base row; a row past
+      // the end of the tensor (lengths larger than the tensor) is skipped
+      const int rbase = ori ? g.ori_base : g.cmp_base;
+      const int len = ori ? p.ori_kv_len : p.cmp_kv_len;
+      const int lim = p.layout_kv == QSFM_LAYOUT_KV_TND ? len - rbase : len;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (ok[t][u] && row[t][u] >= lim) {
+          if (fault != nullptr) atomicOr(fault, QSFM_FAULT_KV_ROW);
+          ok[t][u] = false;
+        }
+        logical[t][u] = ok[t][u] ? row[t][u] : -1;
+        prow[t][u] = ok[t][u] ? rbase + row[t][u] : -1;
+      }
     }
   }
 }

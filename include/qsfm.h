@@ -38,6 +38,18 @@
  *                kv_quant_mode and tile_size: per-tile quantisation, tile 64)
  *   *_block_table int32 [B, *_max_blocks]: logical block -> physical block
  *                (QuantSparseFlashMla, "约束说明", PageAttention bullets)
+ *   non-paged KV (layout_kv BSND / TND, QuantSparseFlashMla "约束说明" on
+ *   layout_kv): ori_kv [B, S2, 1, row] / [T2, 1, row] and cmp_kv
+ *                [B, S3, 1, row] / [T3, 1, row], scales [.., 8] alike;
+ *                batch b's row j is at [b, j] (BSND) or at
+ *                cu_seqlens_ori_kv[b] + j / cu_seqlens_cmp_kv[b] + j (TND);
+ *                no block tables
+ *   ori_sparse_indices int32 BSND [B, S1, 1, K1] / TND [T1, 1, K1] or NULL:
+ *                discrete picks of ori rows (a logical ori row of the
+ *                token's batch; -1 = invalid). When given they replace the
+ *                contiguous ori range: the token attends the entries (the
+ *                first ori_topk_length[t] when that is given) that lie in
+ *                its ori mask range, each occurrence once, in index order
  *   cmp_sparse_indices int32 BSND [B, S1, 1, K2] / TND [T1, 1, K2];
  *                an entry is a logical compressed-row index of the token's
  *                own batch; -1 (or any value outside the visible range) is
@@ -45,8 +57,13 @@
  *   cu_seqlens_q int32 [B + 1], prefix sums from 0 (required for TND)
  *   seqused_q    int32 [B] or NULL (BSND: rows s >= seqused_q[b] are
  *                padding; they get O = 0, lse = -inf)
- *   seqused_ori_kv int32 [B], required (ori length S2 of each batch)
- *   seqused_cmp_kv int32 [B] or NULL (default floor(S2 / cmp_ratio))
+ *   seqused_ori_kv int32 [B]: ori length S2 of each batch. Required for
+ *                paged KV; optional for BSND KV (default: the S2
+ *                dimension); must be NULL for TND KV (S2 = cu_seqlens_ori_kv
+ *                difference)
+ *   seqused_cmp_kv int32 [B] or NULL (default: floor(S2 / cmp_ratio) for
+ *                paged KV, the S3 dimension for BSND KV, the
+ *                cu_seqlens_cmp_kv difference for TND KV)
  *   cmp_residual_kv int32 [B] or NULL (default 0), 0 <= r_b < cmp_ratio
  *   cmp_topk_length int32 [T] or NULL: only the first n entries of the
  *                token's index row are read
@@ -78,7 +95,7 @@
 extern "C" {
 #endif
 
-#define QSFM_ABI_VERSION 2
+#define QSFM_ABI_VERSION 3
 #define QSFM_NUM_HEADS 64
 #define QSFM_HEAD_DIM 512
 #define QSFM_BLOCK_SIZE 128
@@ -116,6 +133,15 @@ typedef enum {
 
 typedef enum { QSFM_LAYOUT_BSND = 0, QSFM_LAYOUT_TND = 1 } qsfm_q_layout;
 
+/* KV storage (qsfm_params.layout_kv; QuantSparseFlashMla parameter table
+ * row layout_kv and its constraints: BSND / TND KV only with the same q
+ * layout, paged KV with either). */
+typedef enum {
+  QSFM_LAYOUT_KV_PA_BBND = 0, /* paged 128-row blocks through block tables  */
+  QSFM_LAYOUT_KV_BSND = 1,    /* [B, S, 1, row] per batch slab              */
+  QSFM_LAYOUT_KV_TND = 2      /* [T, 1, row], batches at cu_seqlens_*_kv    */
+} qsfm_layout_kv;
+
 /* Device fault word bits (qsfm_get_device_status). */
 #define QSFM_FAULT_ORI_BLOCK_ID   0x1  /* ori block table entry outside pool */
 #define QSFM_FAULT_CMP_BLOCK_ID   0x2  /* cmp block table entry outside pool */
@@ -125,6 +151,8 @@ typedef enum { QSFM_LAYOUT_BSND = 0, QSFM_LAYOUT_TND = 1 } qsfm_q_layout;
 #define QSFM_FAULT_TIMEOUT        0x20 /* a bounded device wait ran out      */
 #define QSFM_FAULT_RANGE          0x40 /* an fp8 KV row dequantises past
                                           2^22: its values were clamped    */
+#define QSFM_FAULT_KV_ROW         0x80 /* a non-paged KV row past the end of
+                                          its tensor (skipped)             */
 
 /*
  * All inputs, attributes and outputs of one forward call. Pointers are
@@ -188,6 +216,17 @@ typedef struct qsfm_params {
   float* softmax_lse;
   /* appended in ABI version 2 */
   int32_t kv_layout;      /* qsfm_kv_layout of ori_kv and cmp_kv (both)      */
+  /* appended in ABI version 3 */
+  int32_t layout_kv;      /* qsfm_layout_kv of ori_kv and cmp_kv (both)      */
+  int32_t ori_kv_len;     /* BSND / TND KV: length of ori_kv's sequence axis
+                             (S2 of [B, S2, 1, row], T2 of [T2, 1, row])     */
+  int32_t cmp_kv_len;     /* the same for cmp_kv (S3 / T3)                   */
+  int32_t k1;             /* ori_sparse_indices row length K1; 0 without     */
+  const int32_t* cu_seqlens_ori_kv;  /* int32 [B + 1]: TND KV (required)      */
+  const int32_t* cu_seqlens_cmp_kv;  /* int32 [B + 1]: TND KV with cmp_kv    */
+  const int32_t* ori_sparse_indices; /* see the data layout above            */
+  const int32_t* ori_topk_length;    /* int32 [T] or NULL: entries of the
+                                        token's ori index row that count    */
 } qsfm_params;
 
 /* Fill *p with the defaults of the op: n1 64, d 512, block size 128,

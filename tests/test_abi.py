@@ -37,7 +37,8 @@ def test_every_declared_function_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) <= set(Q.EXPORTS)
-    assert lib.qsfm_abi_version() == 2  # version 2 appended qsfm_params.kv_layout
+    # version 2 appended qsfm_params.kv_layout, version 3 the KV storage layouts and ori picks
+    assert lib.qsfm_abi_version() == 3
 
 
 def test_exports_are_c_symbols(lib):
@@ -174,6 +175,71 @@ def test_kv_layout_checks(lib):
     p.ori_scale = None
     p.kv_layout = 7
     assert _status(lib, p) == 1
+
+
+def _non_paged(lib, layout_kv):
+    """Valid params with non-paged ori KV (BSND with BSND q, TND with TND q)."""
+    p = _valid(lib)
+    p.ori_block_table = None
+    p.layout_kv = Q.LAYOUT_KV[layout_kv]
+    p.ori_kv_len = 100
+    if layout_kv == "TND":
+        p.layout_q, p.total_t, p.cu_seqlens_q = 1, 2, 0x1000
+        p.seqused_ori_kv, p.cu_seqlens_ori_kv = None, 0x1000
+    return p
+
+
+NON_PAGED_INVALID = [
+    ("BSND KV with TND q", "BSND", dict(layout_q=1, total_t=2, cu_seqlens_q=0x1000)),
+    ("TND KV with BSND q", "TND", dict(layout_q=0, max_s1=1)),
+    ("BSND KV with a block table", "BSND", dict(ori_block_table=0x1000)),
+    ("BSND KV with no length", "BSND", dict(ori_kv_len=0)),
+    ("BSND KV with cu_seqlens_ori_kv", "BSND", dict(cu_seqlens_ori_kv=0x1000)),
+    ("TND KV without cu_seqlens_ori_kv", "TND", dict(cu_seqlens_ori_kv=None)),
+    ("TND KV with seqused_ori_kv", "TND", dict(seqused_ori_kv=0x1000)),
+    ("TND KV cmp without cu_seqlens_cmp_kv", "TND", dict(cmp_kv=0x1000, cmp_ratio=4, cmp_scale=0x1000,
+                                                        cmp_kv_len=10)),
+    ("TND KV cmp without length", "TND", dict(cmp_kv=0x1000, cmp_ratio=4, cmp_scale=0x1000,
+                                              cu_seqlens_cmp_kv=0x1000)),
+    ("cu_seqlens_cmp_kv without cmp_kv", "TND", dict(cu_seqlens_cmp_kv=0x1000)),
+    ("layout_kv 3", "BSND", dict(layout_kv=3)),
+    ("ori picks without K1", "BSND", dict(ori_sparse_indices=0x1000)),
+    ("K1 without ori picks", "BSND", dict(k1=8)),
+    ("ori_topk_length without ori picks", "BSND", dict(ori_topk_length=0x1000)),
+    ("ori picks not 4-byte aligned", "BSND", dict(ori_sparse_indices=0x1002, k1=8)),
+    ("cu_seqlens_ori_kv not 4-byte aligned", "TND", dict(cu_seqlens_ori_kv=0x1001)),
+]
+
+
+@pytest.mark.parametrize("why,layout_kv,change", NON_PAGED_INVALID, ids=[c[0] for c in NON_PAGED_INVALID])
+def test_non_paged_kv_and_ori_picks_rules(lib, why, layout_kv, change):
+    p = _non_paged(lib, layout_kv)
+    assert _status(lib, p, "size") == 0, "the base case must be valid"
+    for k, v in change.items():
+        setattr(p, k, v)
+    assert _status(lib, p, "size") == 1
+
+
+def test_non_paged_kv_and_ori_picks_valid_cases(lib):
+    p = _non_paged(lib, "BSND")
+    p.seqused_ori_kv = None  # optional for BSND KV
+    p.ori_sparse_indices, p.k1, p.ori_topk_length = 0x1000, 512, 0x2000
+    p.cmp_kv, p.cmp_ratio, p.cmp_scale, p.cmp_kv_len = 0x1000, 4, 0x1000, 25
+    assert _status(lib, p, "size") == 0
+    p = _non_paged(lib, "TND")
+    p.cmp_kv, p.cmp_ratio, p.cmp_scale, p.cmp_kv_len, p.cu_seqlens_cmp_kv = 0x1000, 4, 0x1000, 25, 0x1000
+    assert _status(lib, p, "size") == 0
+    p = _valid(lib)  # paged KV with ori picks
+    p.ori_sparse_indices, p.k1 = 0x1000, 64
+    assert _status(lib, p, "size") == 0
+    p.k1 = 1 << 17
+    assert _status(lib, p, "size") == 2  # K1 past the index limit
+
+
+def test_bsnd_kv_row_limit_is_refused(lib):
+    p = _non_paged(lib, "BSND")
+    p.batch, p.ori_kv_len = 1 << 10, 1 << 21  # 2^31 rows
+    assert _status(lib, p, "size") == 2
 
 
 def test_debug_gather_argument_rules(lib):

@@ -190,6 +190,52 @@ def test_wide_shape_parity(cuda_device, name, ctas):
     assert_parity(out, lse, w, range(w.total_t))
 
 
+# KV storage layouts and ori picks (QuantSparseFlashMla parameter table rows
+# layout_kv, cu_seqlens_ori_kv / cu_seqlens_cmp_kv, ori_sparse_indices,
+# ori_topk_length; its constraints on the BSND / TND KV layouts)
+LAYOUTS = {
+    "bsnd_kv_csa_decode_picks": dict(layout="BSND", q_lens=[2] * 8,
+                                     s2=[5000, 9000, 700, 20000, 4096, 3000, 130, 12000], cmp_ratio=4,
+                                     mode="CSA", k2=512, layout_kv="BSND", ori_k1=128),
+    "tnd_kv_csa_prefill_picks_topk": dict(layout="TND", q_lens=[40, 7, 100], s2=[3000, 900, 8000], cmp_ratio=4,
+                                          mode="CSA", k2=512, layout_kv="TND", kv_pad=33, ori_k1=256,
+                                          ori_mask_mode=3, ori_win_left=-1, ori_win_right=-1,
+                                          ori_topk_length=[(37 * i) % 300 for i in range(147)]),
+    "tnd_kv_hca_packed": dict(layout="TND", q_lens=[3, 5], s2=[3000, 40000], cmp_ratio=64, mode="HCA",
+                              layout_kv="TND", kv_format="packed640"),
+    "bsnd_kv_swa_no_seqused": dict(layout="BSND", q_lens=[3, 3], s2=[500, 500], mode="SWA", layout_kv="BSND",
+                                   bsnd_seqused=False, ori_win_left=200, ori_win_right=3),
+    "paged_picks_no_mask": dict(layout="BSND", q_lens=[2, 2, 2], s2=[9000, 300, 20000], cmp_ratio=4, mode="CSA",
+                                k2=512, ori_k1=512, ori_n_valid=480, ori_mask_mode=0, ori_win_left=-1,
+                                ori_win_right=-1),
+    "bsnd_kv_bf16_picks_n1_128": dict(layout="BSND", q_lens=[2, 2], s2=[6000, 2500], cmp_ratio=4, mode="CSA",
+                                      k2=512, layout_kv="BSND", kv_format="bf16", ori_k1=64, n1=128),
+    "tnd_kv_swa_picks_none_valid": dict(layout="TND", q_lens=[5, 9], s2=[64, 900], mode="SWA",
+                                        layout_kv="TND", ori_k1=32, ori_n_valid=0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LAYOUTS))
+@pytest.mark.parametrize("ctas", [0, 5])
+def test_kv_layout_and_ori_picks_parity(cuda_device, name, ctas):
+    w = W.build(name, seed=zlib.crc32(name.encode()) % 1000, return_lse=True, **LAYOUTS[name])
+    out, lse = run_gpu(w, cuda_device, num_ctas=ctas)
+    assert_parity(out, lse, w, range(w.total_t), derived=True)
+
+
+def test_non_paged_kv_equals_paged_bitwise(cuda_device):
+    """The same logical rows stored BSND and paged give the same bits: the
+    storage only changes where a row is read from."""
+    from tests.test_oracle_ori_sparse_layouts import _paged_copy
+
+    w = W.build("same rows", layout="BSND", q_lens=[2] * 4, s2=[5000, 900, 12000, 3000], cmp_ratio=4,
+                mode="CSA", k2=512, layout_kv="BSND", ori_k1=100, seed=51, return_lse=True)
+    pa = _paged_copy(w, block=128, seed=2)
+    out1, lse1 = run_gpu(w, cuda_device)
+    out2, lse2 = run_gpu(pa, cuda_device)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+
+
 def test_sparse_compressed_flash_attention_entry(cuda_device):
     """The bf16-KV entry point with SparseCompressedFlashAttention's argument
     layout (flat query and KV, q_act_seqs without the leading zero, win_size)
@@ -258,34 +304,46 @@ def test_index_permutation_invariance(cuda_device):
 
 
 # ------------------------------------------------------ row resolution
-def _pool_bytes(kv):
-    """A paged KV pool as the raw bytes of each row: uint8 [blocks, 128, row bytes]."""
+def _storage_row(w, kv, b, e, table, cu):
+    """Row e of batch b in a KV tensor of any storage layout, found here from
+    the layout's definition: paged [blocks, 128, ...] through the block
+    table, BSND [B, S, 1, ...] at [b, e], TND [T, 1, ...] at cu[b] + e."""
+    lay = getattr(w, "layout_kv", "PA_BBND")
+    if lay == "BSND":
+        return kv[b, e].reshape(-1)
+    if lay == "TND":
+        return kv[int(cu[b]) + e].reshape(-1)
+    return kv[table[e // 128], e % 128].reshape(-1)
+
+
+def _raw(kv):
+    """KV tensor as raw row bytes keeping its leading axes (bf16 -> 2 bytes per element)."""
     if kv.dtype == torch.bfloat16:
         kv = kv.contiguous().view(torch.uint8)
-    return kv.reshape(kv.shape[0], kv.shape[1], -1).numpy()
+    return kv.numpy()
 
 
 def _expected_slots(w, t, with_bytes=True):
-    """(row ids, row bytes, scales) of token t's slots, resolved in Python
-    from the oracle's row sets and the block tables (with_bytes=False: ids
-    only). Scales are separate only for fp8 rows (else None)."""
+    """(row ids, row bytes, scales) of token t's slots in the kernel's order
+    (ori slots, then cmp slots), resolved in Python from the token's mask
+    ranges, its index rows and the KV storage (with_bytes=False: ids only).
+    A slot that attends nothing has id -1 and zero bytes. Scales are
+    separate only for fp8 rows (else None)."""
     b, s = int(w.token_batch()[t]), int(w.token_pos()[t])
-    ori, _ = O.token_rows(w, t, b, s)
-    ids, rows_b, rows_s = [], [], []
-    tab = w.ori_block_table[b].numpy()
     fp8 = w.ori_scale is not None
-    if with_bytes:
-        kv = _pool_bytes(w.ori_kv)
-        sc = w.ori_scale.numpy() if fp8 else None
-    for r in ori or []:
-        ids.append(r)
-        if with_bytes:
-            rows_b.append(kv[tab[r // 128], r % 128])
-            if fp8:
-                rows_s.append(sc[tab[r // 128], r % 128, 0])
-    if w.cmp_kv is not None and ori is not None:
-        s1, s2 = int(w.q_lens[b]), int(w.seqused_ori_kv[b])
-        cmp_len = s2 // w.cmp_ratio
+    ids, rows_b, rows_s = [], [], []
+    if w.seqused_q is not None and s >= int(w.seqused_q[b]):
+        return ids, rows_b, (rows_s if fp8 else None)
+    s1, s2 = int(w.q_lens[b]), O.ori_length(w, b)
+    lo, hi = O.ori_row_range(s2 - s1 + s, s2, w.ori_mask_mode, w.ori_win_left, w.ori_win_right)
+    if w.ori_sparse_indices is None:
+        ori_ids = list(range(lo, hi + 1))
+    else:
+        n = w.k1 if w.ori_topk_length is None else max(0, min(w.k1, int(w.ori_topk_length[t])))
+        ori_ids = [e if (e != -1 and lo <= e <= hi) else -1 for e in w.ori_sparse_indices[t, 0, :n].tolist()]
+    slots = [(0, e) for e in ori_ids]
+    if w.cmp_kv is not None:
+        cmp_len = O.cmp_length(w, b, s2)
         res = int(w.cmp_residual_kv[b]) if w.cmp_residual_kv is not None else 0
         v = O.cmp_visible_count(cmp_len * w.cmp_ratio + res - s1 + s, cmp_len, w.cmp_ratio,
                                 w.cmp_mask_mode)
@@ -293,17 +351,22 @@ def _expected_slots(w, t, with_bytes=True):
                    else list(range(v)))
         if w.cmp_topk_length is not None:
             entries = entries[:int(w.cmp_topk_length[t])]
-        ctab = w.cmp_block_table[b].numpy()
+        slots += [(1, e if 0 <= e < v else -1) for e in entries]
+    if with_bytes:
+        kvs = {0: _raw(w.ori_kv), 1: None if w.cmp_kv is None else _raw(w.cmp_kv)}
+        scs = {0: w.ori_scale.numpy() if fp8 else None, 1: w.cmp_scale.numpy() if fp8 and w.cmp_kv is not None else None}
+        tabs = {0: None if w.ori_block_table is None else w.ori_block_table[b].numpy(),
+                1: None if w.cmp_block_table is None else w.cmp_block_table[b].numpy()}
+        cus = {0: w.cu_seqlens_ori_kv, 1: w.cu_seqlens_cmp_kv}
+    for src, e in slots:
+        ids.append(-1 if e < 0 else (src << 30) | e)
         if with_bytes:
-            ckv = _pool_bytes(w.cmp_kv)
-            csc = w.cmp_scale.numpy() if fp8 else None
-        for e in entries:
-            ok = 0 <= e < v
-            ids.append((1 << 30) | e if ok else -1)
-            if with_bytes:
-                rows_b.append(ckv[ctab[e // 128], e % 128] if ok else np.zeros(ckv.shape[-1], np.uint8))
-                if fp8:
-                    rows_s.append(csc[ctab[e // 128], e % 128, 0] if ok else np.zeros(8, np.float32))
+            width = kvs[src].shape[-1]
+            rows_b.append(np.zeros(width, np.uint8) if e < 0 else
+                          _storage_row(w, kvs[src], b, e, tabs[src], cus[src]))
+            if fp8:
+                rows_s.append(np.zeros(8, np.float32) if e < 0 else
+                              _storage_row(w, scs[src], b, e, tabs[src], cus[src]))
     return ids, rows_b, (rows_s if fp8 else None)
 
 
@@ -323,6 +386,12 @@ GATHER_CASES = {
                                       mode="HCA", kv_format="packed640", seed=5),
     "k2_1024_bf16": lambda: W.build("k2 1024 bf16", layout="BSND", q_lens=[2] * 2, s2=[30000, 9000],
                                     cmp_ratio=4, mode="CSA", k2=1024, kv_format="bf16", seed=8),
+    # non-paged KV and ori picks
+    "bsnd_kv_csa_ori_picks": lambda: W.build("bsnd kv picks", **LAYOUTS["bsnd_kv_csa_decode_picks"], seed=9),
+    "tnd_kv_prefill_picks_topk": lambda: W.build("tnd kv picks", **LAYOUTS["tnd_kv_csa_prefill_picks_topk"],
+                                                 seed=10),
+    "tnd_kv_hca_packed": lambda: W.build("tnd kv hca packed", **LAYOUTS["tnd_kv_hca_packed"], seed=11),
+    "paged_picks_mode0": lambda: W.build("paged picks", **LAYOUTS["paged_picks_no_mask"], seed=12),
 }
 
 
@@ -339,7 +408,7 @@ def test_debug_gather_bit_exact(cuda_device, case):
     out = torch.empty_like(args["q"])
     p = Q.make_params(attn_out=out, **{k: v for k, v in args.items() if k != "return_softmax_lse"})
     fp8 = w.ori_scale is not None
-    row_bytes = _pool_bytes(w.ori_kv).shape[-1]
+    row_bytes = _raw(w.ori_kv).shape[-1]
     max_rows = 1280
     n = len(toks)
     tok = torch.tensor(toks, dtype=torch.int32, device=cuda_device)
