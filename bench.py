@@ -197,6 +197,140 @@ def algorithmic_work(Q, p, w, dev):
     return uniq, pairs
 
 
+PER_STEP_KEYS = ("q", "ori_block_table", "cmp_block_table", "cmp_sparse_indices", "seqused_ori_kv",
+                 "seqused_cmp_kv", "cmp_residual_kv", "cmp_topk_length", "cu_seqlens_q", "seqused_q",
+                 "sinks", "cu_seqlens_ori_kv", "cu_seqlens_cmp_kv", "ori_sparse_indices", "ori_topk_length")
+
+
+def _step_input_sets(a, n_sets: int, seed: int):
+    """n_sets host copies of one step's per-step inputs (everything but the
+    resident KV tensors). Sets after the first get a fresh q and block
+    tables permuted over the same pools (a bijection of the pool's blocks),
+    so consecutive steps read mostly different KV rows (each set touches
+    about as many bytes as one step reads; three sets exceed L2)."""
+    g = torch.Generator().manual_seed(seed)
+    base = {k: a[k].cpu() for k in PER_STEP_KEYS if isinstance(a.get(k), torch.Tensor)}
+    sets = [base]
+    for _ in range(n_sets - 1):
+        s = dict(base)
+        s["q"] = torch.randn(base["q"].shape, generator=g).to(base["q"].dtype)
+        for tk, pool in (("ori_block_table", "ori_kv"), ("cmp_block_table", "cmp_kv")):
+            if tk in base:
+                perm = torch.randperm(int(a[pool].shape[0]), generator=g).to(torch.int32)
+                t = base[tk]
+                s[tk] = torch.where(t >= 0, perm[t.clamp(min=0).long()], t)
+        sets.append(s)
+    return sets
+
+
+def _pack(tensors, align=256, pin=True):
+    """One (pinned) byte buffer holding `tensors` back to back (256-byte
+    aligned) and the (offset, nbytes, dtype, shape) of each."""
+    layout, off = {}, 0
+    for k, t in tensors.items():
+        n = t.numel() * t.element_size()
+        layout[k] = (off, n, t.dtype, tuple(t.shape))
+        off += (n + align - 1) // align * align
+    buf = torch.empty(max(off, align), dtype=torch.uint8)
+    if pin:
+        buf = buf.pin_memory()
+    for k, t in tensors.items():
+        o, n, _, _ = layout[k]
+        buf[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+    return buf, layout
+
+
+def _views(buf, layout):
+    return {k: buf[o:o + n].view(dt).view(shape) for k, (o, n, dt, shape) in layout.items()}
+
+
+def e2e_pipeline(Q, args, w, a, out, lse, lse_wanted, dev, world):
+    """Query tokens/s through the public API (qsfm_metadata + qsfm_forward
+    on parameter blocks made once per buffer slot) with every step's inputs
+    uploaded from pinned host memory and its output read back to pinned
+    host memory, pipelined over three streams: step k + 1's
+    upload and step k - 1's read-back overlap step k's kernels (two device
+    slots for inputs and outputs, events between the streams). Per step:
+    one host-to-device copy of the packed inputs, one device-to-host copy
+    of attn_out (and lse). The last two steps' outputs are checked bit for
+    bit against quant_sparse_flash_mla run on the same inputs without the
+    pipeline."""
+    n_sets = 3
+    sets = _step_input_sets(a, n_sets, seed=1234)
+    packed = [_pack(s) for s in sets]
+    layout = packed[0][1]
+    h2d = packed[0][0].numel()
+    slots_in = [torch.empty_like(packed[0][0], device=dev) for _ in range(2)]
+    slots_out = [torch.empty_like(out) for _ in range(2)]
+    slots_lse = [torch.empty_like(lse) for _ in range(2)] if lse_wanted else [None, None]
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    host_lse = [torch.empty(lse.shape, dtype=torch.float32).pin_memory() for _ in range(2)] if lse_wanted \
+        else [None, None]
+    d2h = out.numel() * out.element_size() + (lse.numel() * 4 if lse_wanted else 0)
+    s_c = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    fixed = {k: v for k, v in a.items() if k not in layout}
+    # One parameter block, plan and workspace per slot, made once (a serving
+    # loop's setup); every step is then the library's two calls,
+    # qsfm_metadata() and qsfm_forward(), on the slot's buffers.
+    plans = [torch.empty(Q.METADATA_INTS, dtype=torch.int32, device=dev) for _ in range(2)]
+    params, wss = [], []
+    for slot in range(2):
+        kw = dict(fixed)
+        kw.update(_views(slots_in[slot], layout))
+        pp = Q.make_params(attn_out=slots_out[slot], softmax_lse=slots_lse[slot], metadata=plans[slot],
+                           return_lse=lse_wanted, num_ctas=args.ctas, **kw)
+        nb = Q.workspace_size(pp)
+        params.append(pp)
+        wss.append(torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None)
+    n = max(200, min(args.steps, 400))  # long enough that the pipeline's fill and drain are small
+
+    def run(n_steps):
+        ev_in = [torch.cuda.Event() for _ in range(n_steps)]
+        ev_done = [torch.cuda.Event() for _ in range(n_steps)]
+        ev_out = [torch.cuda.Event() for _ in range(n_steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s_c)
+        s_in.wait_stream(s_c)
+        s_out.wait_stream(s_c)
+        for k in range(n_steps):
+            slot = k % 2
+            if k >= 2:
+                s_in.wait_event(ev_done[k - 2])  # step k - 2 has read this input slot
+            with torch.cuda.stream(s_in):
+                slots_in[slot].copy_(packed[k % n_sets][0], non_blocking=True)
+                ev_in[k].record(s_in)
+            s_c.wait_event(ev_in[k])
+            if k >= 2:
+                s_c.wait_event(ev_out[k - 2])  # step k - 2's output is read back
+            Q.metadata(params[slot], plans[slot], s_c)
+            Q.forward(params[slot], wss[slot], s_c)
+            ev_done[k].record(s_c)
+            s_out.wait_event(ev_done[k])
+            with torch.cuda.stream(s_out):
+                host_out[slot].copy_(slots_out[slot], non_blocking=True)
+                if lse_wanted:
+                    host_lse[slot].copy_(slots_lse[slot], non_blocking=True)
+                ev_out[k].record(s_out)
+        s_c.wait_event(ev_out[n_steps - 1])
+        t1.record(s_c)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    run(max(args.warmup, 3))
+    ms = run(n) / n
+    # result check: the last two steps again, kernels only, same inputs
+    for k in (n - 2, n - 1):
+        kw = dict(fixed)
+        kw.update({kk: v.to(dev) for kk, v in sets[k % n_sets].items()})
+        o, l = Q.quant_sparse_flash_mla(return_softmax_lse=lse_wanted, num_ctas=args.ctas, **kw)
+        torch.cuda.synchronize()
+        if not torch.equal(o.cpu(), host_out[k % 2]) or (lse_wanted and not torch.equal(l.cpu(), host_lse[k % 2])):
+            raise RuntimeError(f"e2e step {k}: the read-back result differs from the kernels' result")
+    (ms,) = max_over_ranks([ms], dev)
+    return dict(ms=ms, h2d=h2d, d2h=d2h, n=n, sets=n_sets)
+
+
 def run_gpu_arm(args, w, rank, world, local):
     import compressed_mla_attention_gb300 as Q
 
@@ -281,63 +415,7 @@ def run_gpu_arm(args, w, rank, world, local):
 
     # ---- end to end through the public API with pinned host buffers
     if not args.quick:
-        host = {}
-        for k_, v in a.items():
-            if isinstance(v, torch.Tensor) and k_ not in ("ori_kv", "ori_scale", "cmp_kv", "cmp_scale"):
-                host[k_] = v.cpu().pin_memory()
-        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * out_host.element_size() + (lse.numel() * 4 if lse_wanted else 0)
-        lse_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory() if lse_wanted else None
-        dev_in = {k_: torch.empty_like(v, device=dev) for k_, v in host.items()}
-        n_e2e = min(args.steps, 200)
-
-        def e2e_step():
-            # this step's inputs from pinned host memory, the public API call,
-            # and the result read back to pinned host memory
-            for k_, v in host.items():
-                dev_in[k_].copy_(v, non_blocking=True)
-            kw = dict(a)
-            kw.update(dev_in)
-            o, l = Q.quant_sparse_flash_mla(out=out, return_softmax_lse=lse_wanted, num_ctas=args.ctas, **kw)
-            out_host.copy_(o, non_blocking=True)
-            if lse_wanted:
-                lse_host.copy_(l, non_blocking=True)
-
-        def timed(run):
-            times = []
-            for k in range(args.warmup + n_e2e):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(torch.cuda.current_stream())
-                run()
-                e1.record(torch.cuda.current_stream())
-                e1.synchronize()
-                if k >= args.warmup:
-                    times.append(e0.elapsed_time(e1))
-            return statistics.mean(times)
-
-        eager_ms = timed(e2e_step)
-        # The same step captured once in a CUDA graph and replayed: the
-        # copies and kernels of a step without the host's per-call launch
-        # work (the library's calls are stream-ordered and capturable).
-        graph_ms = None
-        try:
-            side = torch.cuda.Stream()
-            side.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.stream(side):
-                for _ in range(3):
-                    e2e_step()
-            torch.cuda.current_stream().wait_stream(side)
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                e2e_step()
-            graph_ms = timed(graph.replay)
-        except Exception as exc:  # capture unsupported here: the eager number stands
-            print(f"e2e graph capture failed: {exc}", file=sys.stderr)
-        e2e_ms = graph_ms if graph_ms is not None else eager_ms
-        e2e_ms, eager_ms = max_over_ranks([e2e_ms, eager_ms], dev)
-        res["e2e"] = dict(ms=e2e_ms, eager_ms=eager_ms, graph=graph_ms is not None, h2d=h2d, d2h=d2h)
+        res["e2e"] = e2e_pipeline(Q, args, w, a, out, lse, lse_wanted, dev, world)
     res["work"] = algorithmic_work(Q, p, w, dev)
     return res
 
@@ -424,7 +502,8 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16" if args.kv_format == "fp8_fp32_scales" else "bf16",
+        "data": "synthetic",
         "config": {"workload": w.name, "query_tokens": T, "global_batch": w.batch * world,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (512 MiB write, outside the timed events)",
@@ -441,21 +520,41 @@ def main():
         lse_bytes = T * n1 * 4 if w.return_lse else 0
         alg_bytes = uniq * KV_ROW_BYTES[args.kv_format] + q_bytes + o_bytes + idx_bytes + lse_bytes
         flops = pairs * FLOPS_PER_ROW_HEAD * n1
-        achieved = alg_bytes / (res["ms_attn"] / 1e3) / 1e9
+        sec = res["ms_attn"] / 1e3
+        gbs, tflops = alg_bytes / sec / 1e9, flops / sec / 1e12
+        hbm_frac, tc_frac = gbs / hbm, tflops / tf
+        # The roofline time is the slower of the two floors, max(bytes / HBM
+        # peak, FLOPs / tensor peak); frac = that time / the measured time,
+        # i.e. the larger of the two fractions, and `bound` names the floor
+        # that sets it.
+        tensor_bound = tc_frac > hbm_frac
         # the recorded ncu traffic is for the default format and head count
         default_shape = args.kv_format == "fp8_fp32_scales" and n1 == 64 and not args.profile_size
-        line["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                            "frac": achieved / hbm,
-                            "traffic": recorded_traffic(args.workload) if default_shape else None,
-                            "peak_kind": kind, "algorithmic_bytes": alg_bytes,
-                            "tensor_tflops": flops / (res["ms_attn"] / 1e3) / 1e12,
-                            "tensor_frac": flops / (res["ms_attn"] / 1e3) / 1e12 / tf}
+        line["roofline"] = {
+            "bound": "tensor" if tensor_bound else "hbm",
+            "achieved": tflops if tensor_bound else gbs,
+            "peak": tf if tensor_bound else hbm,
+            "unit": "TFLOP/s" if tensor_bound else "GB/s",
+            "frac": max(hbm_frac, tc_frac),
+            "traffic": recorded_traffic(args.workload) if default_shape else None,
+            "peak_kind": kind,
+            "hbm": {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": hbm_frac,
+                    "algorithmic_bytes": alg_bytes},
+            "tensor": {"achieved": tflops, "peak": tf, "unit": "TFLOP/s", "frac": tc_frac,
+                       "algorithmic_flops": flops,
+                       "dtype": "f16 operands (fp8 rows dequantised), fp32 accumulate"
+                       if args.kv_format == "fp8_fp32_scales" else "bf16 operands, fp32 accumulate"},
+            "roofline_ms": max(alg_bytes / (hbm * 1e9), flops / (tf * 1e12)) * 1e3,
+            "kernel_ms": res["ms_attn"],
+        }
     if "e2e" in res:  # not in --quick runs
         e = res["e2e"]
         line["e2e"] = {"value": job_throughput(world, T, e["ms"]), "unit": UNIT,
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "cuda_graph": e["graph"],
-                       "eager_value": job_throughput(world, T, e["eager_ms"])}
+                       "ms_per_step": e["ms"], "steps": e["n"],
+                       "pipeline": "3 streams: upload k+1 | kernels k | read-back k-1; "
+                                   f"{e['sets']} rotating input sets (fresh q, block tables permuted "
+                                   "over the resident pools); last two results checked bitwise"}
     if res["clocks"] is not None:
         line["clocks"] = res["clocks"]
     if cpu is not None:
