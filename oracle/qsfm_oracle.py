@@ -46,13 +46,13 @@ design notes of the repository):
   R6 lse = log sum_j exp(x_j) over attended rows, the sink excluded;
   R7 a token with no attended row (or a padded query row) gets O = 0 and
      lse = -inf, even when a sink is given;
-  R13 ori_sparse_indices (QuantSparseFlashMla parameter table: discrete
+  R16 ori_sparse_indices (QuantSparseFlashMla parameter table: discrete
      picks from ori_kv, -1 = invalid; ori_topk_length: how many entries
      take part) replace the contiguous ori range: the token's ori rows are
      the entries of its index row (the first ori_topk_length of them when
      given) that are not -1 and lie inside its ori mask range (R1, R2),
      each occurrence counted, in index order;
-  R14 non-paged KV (QuantSparseFlashMla constraints on layout_kv): BSND
+  R17 non-paged KV (QuantSparseFlashMla constraints on layout_kv): BSND
      ori_kv [B, S2, 1, D] holds batch b's row j at [b, j]; TND ori_kv
      [T2, 1, D] holds it at cu_seqlens_ori_kv[b] + j (cmp_kv alike with
      cu_seqlens_cmp_kv). The ori length S2_b is seqused_ori_kv[b] (BSND;
@@ -187,7 +187,7 @@ def kv_layout_of(w) -> str:
 
 
 def ori_length(w, b: int) -> int:
-    """S2 of batch b (R14)."""
+    """S2 of batch b (R17)."""
     lay = kv_layout_of(w)
     if lay == "TND":
         cu = w.cu_seqlens_ori_kv
@@ -201,7 +201,7 @@ def ori_length(w, b: int) -> int:
 
 def cmp_length(w, b: int, s2: int) -> int:
     """Compressed length of batch b (QuantSparseFlashMla constraints on
-    seqused_cmp_kv; R14)."""
+    seqused_cmp_kv; R17)."""
     if w.seqused_cmp_kv is not None:
         return int(w.seqused_cmp_kv[b])
     lay = kv_layout_of(w)
@@ -214,7 +214,7 @@ def cmp_length(w, b: int, s2: int) -> int:
 
 
 def ori_picks(w, t: int, lo: int, hi: int) -> list:
-    """ori rows of token t picked by ori_sparse_indices (R13): the entries
+    """ori rows of token t picked by ori_sparse_indices (R16): the entries
     of its index row (the first ori_topk_length[t] when given) that are not
     -1 and lie in the mask range [lo, hi], in index order, repeats kept."""
     idx = w.ori_sparse_indices
@@ -326,7 +326,7 @@ def pool_bytes(pool) -> np.ndarray:
 
 
 def gather_dense(kv, scales, w, b: int, rows, cu):
-    """Bytes and scales of logical rows of batch b in non-paged KV (R14):
+    """Bytes and scales of logical rows of batch b in non-paged KV (R17):
     BSND kv [B, S, 1, row] at [b, j]; TND kv [T, 1, row] at cu[b] + j."""
     kv = pool_bytes(kv)
     sc = None if scales is None else np.asarray(scales)
