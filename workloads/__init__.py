@@ -497,3 +497,115 @@ def device_inputs(w: Workload, device) -> dict:
         cu_seqlens_cmp_kv=mv(w.cu_seqlens_cmp_kv), ori_sparse_indices=mv(w.ori_sparse_indices),
         ori_topk_length=mv(w.ori_topk_length),
     )
+
+
+# --------------------------------------------------------------------------
+# Inputs of the lightning-indexer top-k (QuantLightningIndexerV2, quant
+# mode 1): e4m3fn index queries and keys with fp32 dequant scales, fp32
+# head weights. Rows ~ N(0, 1) quantised with scale = amax / 448 (one scale
+# per query head of a token, one per key row); weights ~ N(0, 1). Keys are
+# paged in 128-row blocks through a shuffled block table.
+# --------------------------------------------------------------------------
+@dataclasses.dataclass
+class IndexerWorkload:
+    name: str
+    layout: str  # "BSND" or "TND"
+    batch: int
+    q_lens: np.ndarray  # int64 [B]
+    cu_seqlens_q: Optional[torch.Tensor]  # int32 [B+1] (TND)
+    query: torch.Tensor  # uint8 e4m3fn bytes [T, g, d]
+    query_scale: torch.Tensor  # fp32 [T, g]
+    weights: torch.Tensor  # fp32 [T, g]
+    key: torch.Tensor  # uint8 e4m3fn bytes [blocks, 128, 1, d]
+    key_scale: torch.Tensor  # fp32 [blocks, 128, 1]
+    block_table: torch.Tensor  # int32 [B, width]
+    seqused_k: torch.Tensor  # int32 [B]
+    cmp_residual_k: Optional[torch.Tensor]  # int32 [B]
+    seqused_q: Optional[torch.Tensor]  # int32 [B]
+    topk: int
+    mask_mode: int
+    cmp_ratio: int
+    seed: int
+
+    @property
+    def total_t(self) -> int:
+        return int(self.query.shape[0])
+
+    @property
+    def heads(self) -> int:
+        return int(self.query.shape[1])
+
+    def token_batch(self) -> np.ndarray:
+        return np.repeat(np.arange(self.batch), self.q_lens)
+
+    def token_pos(self) -> np.ndarray:
+        return np.concatenate([np.arange(n) for n in self.q_lens]) if self.total_t else np.zeros(0, np.int64)
+
+
+def _quantize_rows_e4m3(x: torch.Tensor):
+    """Rows of x as e4m3fn bytes with one fp32 scale per row (amax / 448)."""
+    amax = x.abs().amax(dim=-1, keepdim=True).clamp(min=1e-12)
+    scale = amax / FP8_MAX
+    q = (x / scale).clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), scale.squeeze(-1).to(torch.float32)
+
+
+def build_indexer(name: str, *, layout: str, q_lens, sk, heads: int = 64, dim: int = 128, topk: int = 512,
+                  mask_mode: int = 3, cmp_ratio: int = 4, with_residual: bool = True,
+                  seqused_q: Optional[list] = None, seed: int = 0) -> IndexerWorkload:
+    """One indexer call: q_lens query tokens and sk keys per batch."""
+    gen = torch.Generator().manual_seed(seed)
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    sk = np.asarray(sk, dtype=np.int64)
+    B, T = len(q_lens), int(q_lens.sum())
+    qx = torch.randn(T, heads, dim, generator=gen)
+    query, qscale = _quantize_rows_e4m3(qx)
+    weights = torch.randn(T, heads, generator=gen, dtype=torch.float32)
+    nblk = [(int(l) + BLOCK - 1) // BLOCK for l in sk]
+    total = max(sum(nblk), 1)
+    perm = torch.randperm(total, generator=gen)[:sum(nblk)].to(torch.int32)
+    width = max(nblk + [1])
+    table = torch.full((B, width), -1, dtype=torch.int32)
+    off = 0
+    for b, k in enumerate(nblk):
+        table[b, :k] = perm[off:off + k]
+        off += k
+    kx = torch.randn(total * BLOCK, dim, generator=gen)
+    key, kscale = _quantize_rows_e4m3(kx)
+    cu = None
+    if layout == "TND":
+        cu = torch.zeros(B + 1, dtype=torch.int32)
+        cu[1:] = torch.from_numpy(np.cumsum(q_lens)).to(torch.int32)
+    else:
+        assert len(set(q_lens.tolist())) <= 1, "BSND needs equal S1"
+    res = None
+    if with_residual and mask_mode == 3:
+        res = torch.from_numpy((torch.randint(0, cmp_ratio, (B,), generator=gen)).numpy().astype(np.int32))
+    return IndexerWorkload(
+        name=name, layout=layout, batch=B, q_lens=q_lens, cu_seqlens_q=cu, query=query, query_scale=qscale,
+        weights=weights, key=key.view(total, BLOCK, 1, dim), key_scale=kscale.view(total, BLOCK, 1),
+        block_table=table, seqused_k=torch.from_numpy(sk.astype(np.int32)), cmp_residual_k=res,
+        seqused_q=torch.tensor(seqused_q, dtype=torch.int32) if seqused_q is not None else None,
+        topk=topk, mask_mode=mask_mode, cmp_ratio=cmp_ratio, seed=seed)
+
+
+def indexer_decode_batch(seed: int = 2) -> IndexerWorkload:
+    """The indexer call that feeds the CSA decode batch: B = 128, S1 = 2,
+    64 index heads of 128, compressed keys S2 / 4 with S2 ~ U[4K, 64K],
+    top-512 under the causal mask."""
+    gen = torch.Generator().manual_seed(10_000 + seed)
+    s2 = _uniform_int(gen, 4096, 65536, 128)
+    return build_indexer("indexer for the CSA decode batch B=128 S1=2 Sk=S2/4 g=64 d=128 top-512",
+                         layout="BSND", q_lens=[2] * 128, sk=s2 // 4, topk=512, mask_mode=3,
+                         cmp_ratio=4, seed=seed)
+
+
+def indexer_device_inputs(w: IndexerWorkload, device) -> dict:
+    """The indexer workload's tensors on `device` (data movement only)."""
+    def mv(t):
+        return None if t is None else t.contiguous().to(device)
+
+    return dict(query=mv(w.query), query_scale=mv(w.query_scale), weights=mv(w.weights), key=mv(w.key),
+                key_scale=mv(w.key_scale), block_table=mv(w.block_table), seqused_k=mv(w.seqused_k),
+                cmp_residual_k=mv(w.cmp_residual_k), seqused_q=mv(w.seqused_q), cu_seqlens_q=mv(w.cu_seqlens_q),
+                layout=w.layout, batch=w.batch, topk=w.topk, mask_mode=w.mask_mode, cmp_ratio=w.cmp_ratio)
