@@ -78,6 +78,19 @@ class QsfmParams(ctypes.Structure):
     ]
 
 
+class IndexerParams(ctypes.Structure):
+    """Mirror of ``qsfm_indexer_params`` (include/qsfm.h); field order must match."""
+
+    _fields_ = [
+        ("batch", _i32), ("max_s1", _i32), ("total_t", _i32), ("heads", _i32), ("dim", _i32), ("topk", _i32),
+        ("block_size", _i32), ("max_blocks", _i32), ("num_blocks", _i32), ("layout_q", _i32),
+        ("mask_mode", _i32), ("cmp_ratio", _i32), ("return_value", _i32),
+        ("query", _ptr), ("query_scale", _ptr), ("weights", _ptr), ("key", _ptr), ("key_scale", _ptr),
+        ("block_table", _ptr), ("seqused_k", _ptr), ("cmp_residual_k", _ptr), ("cu_seqlens_q", _ptr),
+        ("seqused_q", _ptr), ("sparse_indices", _ptr), ("sparse_values", _ptr),
+    ]
+
+
 class QsfmError(RuntimeError):
     def __init__(self, fn: str, code: int):
         super().__init__(f"{fn} returned {STATUS.get(code, code)}")
@@ -99,6 +112,8 @@ EXPORTS = {
     "qsfm_get_device_status": (_i32, [ctypes.POINTER(_i32)]),
     "qsfm_status_string": (ctypes.c_char_p, [_i32]),
     "qsfm_abi_version": (_i32, []),
+    "qsfm_indexer_params_init": (None, [ctypes.POINTER(IndexerParams)]),
+    "qsfm_lightning_indexer": (_i32, [ctypes.POINTER(IndexerParams), _ptr]),
 }
 
 
@@ -462,3 +477,72 @@ def sparse_compressed_flash_attention(
         ori_mask_mode=4, cmp_mask_mode=3, ori_win_left=int(win_size) - 1, ori_win_right=0,
         stream=stream)
     return out.view(t1 * n1, d)
+
+
+def lightning_indexer(
+    query,
+    query_scale,
+    weights,
+    key,
+    key_scale,
+    block_table,
+    seqused_k,
+    *,
+    layout: str = "BSND",
+    batch: Optional[int] = None,
+    cu_seqlens_q=None,
+    seqused_q=None,
+    cmp_residual_k=None,
+    topk: int = 2048,
+    mask_mode: int = 0,
+    cmp_ratio: int = 1,
+    return_value: bool = False,
+    out=None,
+    values=None,
+    stream=None,
+):
+    """QuantLightningIndexerV2's top-k (quant mode 1) through qsfm_lightning_indexer.
+
+    query uint8 e4m3fn bytes BSND [B, S1, g, 128] or TND [T, g, 128];
+    query_scale, weights fp32 [T, g]; key uint8 e4m3fn bytes [blocks, 128, 1,
+    128]; key_scale fp32 [blocks, 128, 1]; block_table int32 [B, width];
+    seqused_k int32 [B]. Returns (sparse_indices int32 [T, 1, topk],
+    sparse_values bf16 [T, 1, topk] or None). Argument marshalling only.
+    """
+    import torch
+
+    p = IndexerParams()
+    lib().qsfm_indexer_params_init(ctypes.byref(p))
+    if layout == "BSND":
+        p.layout_q = LAYOUT_BSND
+        if query.dim() == 4:
+            p.batch, p.max_s1 = int(query.shape[0]), int(query.shape[1])
+        else:
+            if batch is None:
+                raise ValueError("flat BSND query needs batch=")
+            p.batch = int(batch)
+            p.max_s1 = int(query.shape[0]) // max(1, p.batch)
+        T = p.batch * p.max_s1
+    elif layout == "TND":
+        p.layout_q = LAYOUT_TND
+        p.total_t = T = int(query.shape[0])
+        p.batch = int(cu_seqlens_q.shape[0]) - 1 if cu_seqlens_q is not None else int(batch or 0)
+    else:
+        raise ValueError(layout)
+    p.heads, p.dim = int(query.shape[-2]), int(query.shape[-1])
+    p.topk, p.mask_mode, p.cmp_ratio, p.return_value = int(topk), int(mask_mode), int(cmp_ratio), int(bool(return_value))
+    p.block_size, p.num_blocks = int(key.shape[1]), int(key.shape[0])
+    p.max_blocks = int(block_table.shape[-1])
+    dev = query.device
+    if out is None:
+        out = torch.empty(T, 1, int(topk), dtype=torch.int32, device=dev)
+    if return_value and values is None:
+        values = torch.empty(T, 1, int(topk), dtype=torch.bfloat16, device=dev)
+    p.query, p.query_scale, p.weights = _dptr(query), _dptr(query_scale), _dptr(weights)
+    p.key, p.key_scale, p.block_table = _dptr(key), _dptr(key_scale), _dptr(block_table)
+    p.seqused_k, p.cmp_residual_k = _dptr(seqused_k), _dptr(cmp_residual_k)
+    p.cu_seqlens_q, p.seqused_q = _dptr(cu_seqlens_q), _dptr(seqused_q)
+    p.sparse_indices = _dptr(out)
+    p.sparse_values = _dptr(values) if return_value else None
+    _check("qsfm_lightning_indexer", lib().qsfm_lightning_indexer(ctypes.byref(p), _stream_ptr(stream)))
+    return out, (values if return_value else None)

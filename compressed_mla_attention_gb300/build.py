@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libqsfm.so")
-SOURCES = ["qsfm_api.cu", "qsfm_attention.cu", "qsfm_aux.cu", "qsfm_noalloc.cu"]
+SOURCES = ["qsfm_api.cu", "qsfm_attention.cu", "qsfm_aux.cu", "qsfm_noalloc.cu", "qsfm_indexer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]

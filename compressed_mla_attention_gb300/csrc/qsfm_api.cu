@@ -340,6 +340,58 @@ qsfm_status qsfm_debug_bounded_wait(uint64_t timeout_ns, uint64_t* elapsed_ns_ou
       static_cast<cudaStream_t>(stream)));
 }
 
+void qsfm_indexer_params_init(qsfm_indexer_params* p) {
+  if (p == nullptr) return;
+  std::memset(p, 0, sizeof(*p));
+  p->heads = 64;
+  p->dim = 128;
+  p->topk = 2048;  // QuantLightningIndexerV2 parameter table: topk default
+  p->block_size = QSFM_BLOCK_SIZE;
+  p->cmp_ratio = 1;
+  p->layout_q = QSFM_LAYOUT_BSND;
+}
+
+// QuantLightningIndexerV2 constraints: query N in [1, 64], key N = 1, topk
+// in [1, 8192]; quant mode 1 (e4m3 query / key, fp32 scales and weights);
+// cu_seqlens_q required for TND and not allowed for BSND.
+qsfm_status qsfm_lightning_indexer(const qsfm_indexer_params* pp, void* stream) {
+  if (pp == nullptr) return QSFM_ERR_INVALID_ARG;
+  const qsfm_indexer_params& p = *pp;
+  if (p.batch < 0 || p.heads < 1 || p.dim < 1 || p.topk < 1) return QSFM_ERR_INVALID_ARG;
+  if (p.heads > 64 || p.topk > 8192) return QSFM_ERR_INVALID_ARG;
+  if (p.dim != 128) return QSFM_ERR_UNSUPPORTED;
+  if (p.block_size < 1 || p.block_size > 1024) return QSFM_ERR_INVALID_ARG;
+  if (p.block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
+  if (p.mask_mode != 0 && p.mask_mode != 3) return QSFM_ERR_INVALID_ARG;
+  if (p.cmp_ratio < 1 || p.cmp_ratio > 128) return QSFM_ERR_INVALID_ARG;
+  if (p.layout_q == QSFM_LAYOUT_BSND) {
+    if (p.max_s1 < 0 || p.cu_seqlens_q != nullptr) return QSFM_ERR_INVALID_ARG;
+  } else if (p.layout_q == QSFM_LAYOUT_TND) {
+    if (p.total_t < 0 || (p.cu_seqlens_q == nullptr && p.batch > 0) || p.seqused_q != nullptr)
+      return QSFM_ERR_INVALID_ARG;
+  } else {
+    return QSFM_ERR_INVALID_ARG;
+  }
+  const long long T = p.layout_q == QSFM_LAYOUT_BSND ? (long long)p.batch * p.max_s1 : p.total_t;
+  if (T == 0) return QSFM_OK;
+  if (T > kMaxUnits) return QSFM_ERR_UNSUPPORTED;
+  if (p.query == nullptr || p.query_scale == nullptr || p.weights == nullptr || p.key == nullptr ||
+      p.key_scale == nullptr || p.block_table == nullptr || p.seqused_k == nullptr || p.sparse_indices == nullptr)
+    return QSFM_ERR_INVALID_ARG;
+  if (p.return_value && p.sparse_values == nullptr) return QSFM_ERR_INVALID_ARG;
+  if (p.max_blocks < 1 || p.num_blocks < 1) return QSFM_ERR_INVALID_ARG;
+  if ((long long)p.num_blocks * p.block_size > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
+  if (!aligned(p.query, 16) || !aligned(p.key, 16) || !aligned(p.key_scale, 16)) return QSFM_ERR_INVALID_ARG;
+  const void* words[] = {p.query_scale, p.weights, p.block_table, p.seqused_k, p.cmp_residual_k,
+                         p.cu_seqlens_q, p.seqused_q, p.sparse_indices, p.sparse_values};
+  for (const void* w : words)
+    if (!aligned(w, 4)) return QSFM_ERR_INVALID_ARG;
+  int* fault = fault_ptr();
+  if (fault == nullptr) return QSFM_ERR_CUDA;
+  const NvtxRange range("qsfm_lightning_indexer");
+  return cuda_status(qsfm::launch_indexer(p, int(T), fault, static_cast<cudaStream_t>(stream)));
+}
+
 qsfm_status qsfm_get_device_status(int32_t* fault_word) {
   if (fault_word == nullptr) return QSFM_ERR_INVALID_ARG;
   int v = 0;

@@ -49,6 +49,7 @@ cudaError_t launch_attention(const qsfm_params& p, int num_tokens, int num_ctas,
                              const Workspace& ws, int* fault, cudaStream_t s);
 cudaError_t launch_combine(const qsfm_params& p, int num_tokens, int num_ctas,
                            const Workspace& ws, int* fault, cudaStream_t s);
+cudaError_t launch_indexer(const qsfm_indexer_params& p, int num_tokens, int* fault, cudaStream_t s);
 cudaError_t launch_bounded_wait(uint64_t timeout_ns, unsigned long long* elapsed, int* fault,
                                 cudaStream_t s);
 cudaError_t launch_debug_gather(const qsfm_params& p, const int32_t* tokens, int n,

@@ -95,7 +95,7 @@
 extern "C" {
 #endif
 
-#define QSFM_ABI_VERSION 3
+#define QSFM_ABI_VERSION 4
 #define QSFM_NUM_HEADS 64
 #define QSFM_HEAD_DIM 512
 #define QSFM_BLOCK_SIZE 128
@@ -331,6 +331,75 @@ qsfm_status qsfm_debug_gather(const qsfm_params* p, const int32_t* tokens,
  * above one second.
  */
 qsfm_status qsfm_debug_bounded_wait(uint64_t timeout_ns, uint64_t* elapsed_ns_out, void* stream);
+
+/*
+ * Lightning-indexer top-k (QuantLightningIndexerV2, "功能说明" formula and
+ * "参数说明" (parameter table); quant mode 1: FLOAT8_e4m3fn query and key,
+ * fp32 dequant scales and weights). For every query token t (batch b,
+ * position s) and every key j it may see:
+ *   score_j = sum_h weights[t, h] * ReLU(query_scale[t, h] * key_scale[j]
+ *                                        * sum_d query[t, h, d] key[j, d])
+ * and sparse_indices[t] lists the topk keys of largest score (the smaller
+ * key index first among equal scores) in ascending key order, then -1 up
+ * to topk (valid entries first, -1 after, as KvQuantSparseAttnSharedKv's
+ * constraints want of an index row). Keys visible to the token: all
+ * j < seqused_k[b] (mask_mode 0), or only j < floor((p_c + 1) / cmp_ratio)
+ * with p_c = seqused_k[b] * cmp_ratio + cmp_residual_k[b] - S1_b + s
+ * (mask_mode 3, the compressed rows' right-down-causal rule). A padded
+ * query row (seqused_q) gets -1 everywhere.
+ *
+ * Layout (all device memory, caller-owned):
+ *   query        e4m3fn bytes BSND [B, S1, heads, dim] / TND [T, heads, dim]
+ *   query_scale  fp32 [T, heads];  weights fp32 [T, heads]
+ *   key          e4m3fn bytes, paged [num_blocks, 128, 1, dim]
+ *   key_scale    fp32 [num_blocks, 128, 1], paged like key
+ *   block_table  int32 [B, max_blocks];  seqused_k int32 [B] (required)
+ *   cmp_residual_k int32 [B] or NULL (0);  cu_seqlens_q int32 [B + 1]
+ *                (required for TND);  seqused_q int32 [B] or NULL (BSND)
+ *   sparse_indices int32 [T, 1, topk] (out)
+ *   sparse_values  bf16 [T, 1, topk] (out, written when return_value != 0;
+ *                the scores of the listed keys, -inf after them)
+ * Built shapes (QSFM_ERR_UNSUPPORTED otherwise): dim = 128, 1 <= heads
+ * <= 64, 1 <= topk <= 8192, block size 128, at most 32768 keys per batch
+ * (a larger seqused_k is cut to 32768 and flagged with QSFM_FAULT_KV_ROW).
+ * Pointers: query, key, key_scale 16-byte aligned, the rest 4-byte aligned.
+ * Asynchronous on `stream`, no allocation, nothing read back.
+ */
+typedef struct qsfm_indexer_params {
+  int32_t batch;        /* B                                                */
+  int32_t max_s1;       /* BSND: S1                                         */
+  int32_t total_t;      /* TND: T (query rows)                              */
+  int32_t heads;        /* g, query heads of the indexer                    */
+  int32_t dim;          /* d, must be 128                                   */
+  int32_t topk;         /* 1 .. 8192                                        */
+  int32_t block_size;   /* keys per block; only 128 is built                */
+  int32_t max_blocks;   /* block_table row width                            */
+  int32_t num_blocks;   /* blocks in the key pool                           */
+  int32_t layout_q;     /* qsfm_q_layout                                    */
+  int32_t mask_mode;    /* 0 or 3                                           */
+  int32_t cmp_ratio;    /* 1 .. 128                                         */
+  int32_t return_value; /* non-zero: write sparse_values                    */
+  const void* query;
+  const float* query_scale;
+  const float* weights;
+  const void* key;
+  const float* key_scale;
+  const int32_t* block_table;
+  const int32_t* seqused_k;
+  const int32_t* cmp_residual_k;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqused_q;
+  int32_t* sparse_indices;
+  void* sparse_values;
+} qsfm_indexer_params;
+
+/* Defaults: dim 128, heads 64, topk 2048 (the page's default), block size
+ * 128, mask_mode 0, cmp_ratio 1, layout BSND, all pointers NULL. */
+void qsfm_indexer_params_init(qsfm_indexer_params* p);
+
+/* The indexer's top-k. Errors: QSFM_ERR_INVALID_ARG (missing or misaligned
+ * pointers, bad attributes), QSFM_ERR_UNSUPPORTED (shapes not built). */
+qsfm_status qsfm_lightning_indexer(const qsfm_indexer_params* p, void* stream);
 
 /* Synchronously read and clear the device fault word of the current
  * device (QSFM_FAULT_* bits). Returns QSFM_ERR_DEVICE_FAULT when non-zero. */

@@ -37,8 +37,9 @@ def test_every_declared_function_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) <= set(Q.EXPORTS)
-    # version 2 appended qsfm_params.kv_layout, version 3 the KV storage layouts and ori picks
-    assert lib.qsfm_abi_version() == 3
+    # version 2 appended qsfm_params.kv_layout, version 3 the KV storage layouts and ori
+    # picks, version 4 the lightning indexer's entry points
+    assert lib.qsfm_abi_version() == 4
 
 
 def test_exports_are_c_symbols(lib):
@@ -47,19 +48,20 @@ def test_exports_are_c_symbols(lib):
         assert re.search(rf"\bT {n}$", out, flags=re.M), n
 
 
-def test_struct_layout_matches_c(tmp_path):
+@pytest.mark.parametrize("cls,cname", [(Q.QsfmParams, "qsfm_params"), (Q.IndexerParams, "qsfm_indexer_params")])
+def test_struct_layout_matches_c(tmp_path, cls, cname):
     src = tmp_path / "layout.c"
-    fields = [f[0] for f in Q.QsfmParams._fields_]
-    body = "\n".join(f'  printf("{f} %zu\\n", offsetof(qsfm_params, {f}));' for f in fields)
+    fields = [f[0] for f in cls._fields_]
+    body = "\n".join(f'  printf("{f} %zu\\n", offsetof({cname}, {f}));' for f in fields)
     src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "qsfm.h"\nint main(void){\n'
-                   + body + '\n  printf("sizeof %zu\\n", sizeof(qsfm_params));\n  return 0;\n}\n')
+                   + body + f'\n  printf("sizeof %zu\\n", sizeof({cname}));\n  return 0;\n}}\n')
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
     got = dict(line.split() for line in out if line)
     for f in fields:
-        assert int(got[f]) == getattr(Q.QsfmParams, f).offset, f
-    assert int(got["sizeof"]) == ctypes.sizeof(Q.QsfmParams)
+        assert int(got[f]) == getattr(cls, f).offset, f
+    assert int(got["sizeof"]) == ctypes.sizeof(cls)
 
 
 def test_params_init_defaults(lib):
@@ -324,3 +326,49 @@ def test_status_strings(lib):
     for code in range(7):
         assert Q.status_string(code)
     assert "invalid" in Q.status_string(1)
+
+
+def _indexer_valid(lib):
+    p = Q.IndexerParams()
+    lib.qsfm_indexer_params_init(ctypes.byref(p))
+    p.batch, p.max_s1, p.topk, p.max_blocks, p.num_blocks = 2, 1, 512, 4, 8
+    for f in ("query", "query_scale", "weights", "key", "key_scale", "block_table", "seqused_k", "sparse_indices"):
+        setattr(p, f, 0x1000)
+    return p
+
+
+def test_indexer_params_init_defaults(lib):
+    p = Q.IndexerParams()
+    lib.qsfm_indexer_params_init(ctypes.byref(p))
+    assert (p.heads, p.dim, p.topk, p.block_size, p.mask_mode, p.cmp_ratio, p.layout_q) == (64, 128, 2048, 128, 0, 1, 0)
+
+
+INDEXER_INVALID = [
+    ("heads 0", dict(heads=0), 1), ("heads 65", dict(heads=65), 1), ("topk 0", dict(topk=0), 1),
+    ("topk 8193", dict(topk=8193), 1), ("dim 64 not built", dict(dim=64), 2),
+    ("block 64 not built", dict(block_size=64), 2), ("mask mode 4", dict(mask_mode=4), 1),
+    ("cmp_ratio 0", dict(cmp_ratio=0), 1), ("cmp_ratio 129", dict(cmp_ratio=129), 1),
+    ("BSND with cu_seqlens_q", dict(cu_seqlens_q=0x1000), 1),
+    ("TND without cu_seqlens_q", dict(layout_q=1, total_t=4), 1),
+    ("TND with seqused_q", dict(layout_q=1, total_t=4, cu_seqlens_q=0x1000, seqused_q=0x1000), 1),
+    ("no query", dict(query=None), 1), ("no key scale", dict(key_scale=None), 1),
+    ("no block table", dict(block_table=None), 1), ("no seqused_k", dict(seqused_k=None), 1),
+    ("no output", dict(sparse_indices=None), 1), ("values without buffer", dict(return_value=1), 1),
+    ("key not 16-byte aligned", dict(key=0x1008), 1), ("key scale not 16-byte aligned", dict(key_scale=0x1004), 1),
+    ("weights not 4-byte aligned", dict(weights=0x1002), 1), ("no blocks", dict(num_blocks=0), 1),
+]
+
+
+@pytest.mark.parametrize("why,change,code", INDEXER_INVALID, ids=[c[0] for c in INDEXER_INVALID])
+def test_indexer_rejects_invalid_arguments(lib, why, change, code):
+    p = _indexer_valid(lib)
+    for k, v in change.items():
+        setattr(p, k, v)
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), None) == code
+
+
+def test_indexer_empty_call_is_ok(lib):
+    p = _indexer_valid(lib)
+    p.batch = 0
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), None) == 0
+    assert lib.qsfm_lightning_indexer(None, None) == 1
