@@ -420,6 +420,80 @@ def run_gpu_arm(args, w, rank, world, local):
     return res
 
 
+def run_indexer(args, rank, world, local):
+    """The lightning-indexer top-k (qsfm_lightning_indexer) on the call that
+    feeds the CSA decode batch: K timed calls after W warm-up calls, L2
+    flushed between calls, CUDA events on the launching stream. Algorithmic
+    work: every batch's visible keys read once (128 e4m3 bytes + a 4-byte
+    scale each) plus the queries, scales, weights and the index rows; FLOPs
+    of the key-query products (2 per e4m3 pair) against the fp8 tensor peak
+    (the measured bf16 peak times the nominal fp8 / bf16 ratio of 2)."""
+    import compressed_mla_attention_gb300 as Q
+    from compressed_mla_attention_gb300 import build
+
+    build.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = W.indexer_decode_batch()
+    a = W.indexer_device_inputs(w, dev)
+    out = torch.empty(w.total_t, 1, w.topk, dtype=torch.int32, device=dev)
+    ws = torch.empty(w.total_t * 32768 * 4, dtype=torch.uint8, device=dev)  # the largest score rows
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        Q.lightning_indexer(a["query"], a["query_scale"], a["weights"], a["key"], a["key_scale"],
+                            a["block_table"], a["seqused_k"], layout=w.layout, batch=w.batch,
+                            cmp_residual_k=a["cmp_residual_k"], topk=w.topk, mask_mode=w.mask_mode,
+                            cmp_ratio=w.cmp_ratio, out=out, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    if Q.device_status() != 0:
+        raise RuntimeError("device fault in the indexer warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        evs[k][0].record(stream)
+        call()
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    # visible keys per token (the causal rule of the compressed keys)
+    sk = w.seqused_k.numpy().astype(np.int64)
+    res = w.cmp_residual_k.numpy().astype(np.int64) if w.cmp_residual_k is not None else np.zeros_like(sk)
+    tb, tp = w.token_batch(), w.token_pos()
+    s1 = w.q_lens[tb]
+    pc = sk[tb] * w.cmp_ratio + res[tb] - s1 + tp
+    vis = np.clip(np.floor_divide(pc + 1, w.cmp_ratio), 0, sk[tb]) if w.mask_mode == 3 else sk[tb]
+    per_batch = np.zeros(w.batch, dtype=np.int64)
+    np.maximum.at(per_batch, tb, vis)
+    g = w.heads
+    alg_bytes = int(per_batch.sum()) * (128 + 4) + w.total_t * (g * 128 + 2 * g * 4 + w.topk * 4)
+    flops = int(vis.sum()) * g * 128 * 2
+    hbm, tf, kind = measured_peaks()
+    sec = ms / 1e3
+    gbs, tfl = alg_bytes / sec / 1e9, flops / sec / 1e12
+    hf, tcf = gbs / hbm, tfl / (2 * tf)
+    line = {
+        "metric": "indexer query-tokens/s (64 heads, d=128, top-512)", "value": w.total_t / sec,
+        "unit": "query-tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": w.name, "query_tokens": w.total_t,
+                   "l2": "flushed between calls (512 MiB write, outside the timed events)"},
+        "gpu_launches": 2 * args.steps,  # score kernel + select kernel per call
+        "roofline": {"bound": "tensor" if tcf > hf else "hbm", "frac": max(hf, tcf), "peak_kind": kind,
+                     "hbm": {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": hf, "algorithmic_bytes": alg_bytes},
+                     "tensor": {"achieved": tfl, "peak": 2 * tf, "unit": "TFLOP/s", "frac": tcf,
+                                "algorithmic_flops": flops, "peak_note": "measured bf16 x 2 (nominal fp8 ratio)"},
+                     "roofline_ms": max(alg_bytes / (hbm * 1e9), flops / (2 * tf * 1e12)) * 1e3},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,6 +507,8 @@ def main():
     ap.add_argument("--ctas", type=int, default=0, help="planned CTAs (0 = SM count)")
     ap.add_argument("--quick", action="store_true", help="kernels only: no e2e, clocks, baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--indexer", action="store_true",
+                    help="time the lightning-indexer top-k on the call that feeds the CSA decode batch")
     ap.add_argument("--profile-size", action="store_true",
                     help="the CSA decode batch with S2 ~ U[4K, 8K] (for ncu captures)")
     args = ap.parse_args()
@@ -445,6 +521,10 @@ def main():
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
 
+    if args.indexer:
+        if args.impl == "qsfm":
+            run_indexer(args, rank, world, local)
+        return
     w = W.profile_case() if args.profile_size else W.config(args.workload, kv_format=args.kv_format,
                                                              n1=args.n1)
     T = w.total_t

@@ -92,9 +92,11 @@ class IndexerParams(ctypes.Structure):
 
 
 class QsfmError(RuntimeError):
-    def __init__(self, fn: str, code: int):
-        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+    def __init__(self, fn: str, code: int, cuda_error: str = ""):
+        detail = f" ({cuda_error})" if cuda_error else ""
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}{detail}")
         self.code = code
+        self.cuda_error = cuda_error
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -112,8 +114,11 @@ EXPORTS = {
     "qsfm_get_device_status": (_i32, [ctypes.POINTER(_i32)]),
     "qsfm_status_string": (ctypes.c_char_p, [_i32]),
     "qsfm_abi_version": (_i32, []),
+    "qsfm_last_cuda_error": (_i32, [ctypes.POINTER(ctypes.c_char_p)]),
     "qsfm_indexer_params_init": (None, [ctypes.POINTER(IndexerParams)]),
-    "qsfm_lightning_indexer": (_i32, [ctypes.POINTER(IndexerParams), _ptr]),
+    "qsfm_lightning_indexer_workspace_size": (_i32, [ctypes.POINTER(IndexerParams),
+                                                     ctypes.POINTER(ctypes.c_size_t)]),
+    "qsfm_lightning_indexer": (_i32, [ctypes.POINTER(IndexerParams), _ptr, ctypes.c_size_t, _ptr]),
 }
 
 
@@ -136,7 +141,12 @@ def lib() -> ctypes.CDLL:
 
 def _check(fn: str, code: int):
     if code != 0:
-        raise QsfmError(fn, code)
+        name = ""
+        if code == 3:  # QSFM_ERR_CUDA: name the runtime error behind it
+            s = ctypes.c_char_p()
+            lib().qsfm_last_cuda_error(ctypes.byref(s))
+            name = (s.value or b"").decode()
+        raise QsfmError(fn, code, name)
 
 
 def _dptr(t) -> Optional[int]:
@@ -499,6 +509,7 @@ def lightning_indexer(
     return_value: bool = False,
     out=None,
     values=None,
+    workspace=None,
     stream=None,
 ):
     """QuantLightningIndexerV2's top-k (quant mode 1) through qsfm_lightning_indexer.
@@ -507,7 +518,9 @@ def lightning_indexer(
     query_scale, weights fp32 [T, g]; key uint8 e4m3fn bytes [blocks, 128, 1,
     128]; key_scale fp32 [blocks, 128, 1]; block_table int32 [B, width];
     seqused_k int32 [B]. Returns (sparse_indices int32 [T, 1, topk],
-    sparse_values bf16 [T, 1, topk] or None). Argument marshalling only.
+    sparse_values bf16 [T, 1, topk] or None). workspace: a device uint8
+    tensor of at least indexer_workspace_size() bytes, allocated when None.
+    Argument marshalling only.
     """
     import torch
 
@@ -544,5 +557,11 @@ def lightning_indexer(
     p.cu_seqlens_q, p.seqused_q = _dptr(cu_seqlens_q), _dptr(seqused_q)
     p.sparse_indices = _dptr(out)
     p.sparse_values = _dptr(values) if return_value else None
-    _check("qsfm_lightning_indexer", lib().qsfm_lightning_indexer(ctypes.byref(p), _stream_ptr(stream)))
+    need = ctypes.c_size_t(0)
+    _check("qsfm_lightning_indexer_workspace_size",
+           lib().qsfm_lightning_indexer_workspace_size(ctypes.byref(p), ctypes.byref(need)))
+    if workspace is None:
+        workspace = torch.empty(max(16, need.value), dtype=torch.uint8, device=dev)
+    _check("qsfm_lightning_indexer", lib().qsfm_lightning_indexer(
+        ctypes.byref(p), _dptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
     return out, (values if return_value else None)

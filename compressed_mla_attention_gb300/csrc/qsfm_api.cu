@@ -195,7 +195,15 @@ qsfm_status validate(const qsfm_params* pp, bool need_outputs) {
 // tokens than CTAs (decode); longer batches are cut at token starts.
 int split_mode(int tokens, int ctas) { return tokens < ctas ? 1 : 0; }
 
-qsfm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QSFM_OK : QSFM_ERR_CUDA; }
+// The last CUDA runtime error an entry point returned QSFM_ERR_CUDA for, on
+// this host thread (read by qsfm_last_cuda_error).
+thread_local int g_last_cuda_error = 0;
+
+qsfm_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return QSFM_OK;
+  g_last_cuda_error = int(e);
+  return QSFM_ERR_CUDA;
+}
 
 // A named NVTX range around each launch, so that a profiler timeline shows
 // which entry point a kernel belongs to. With no tool attached a range costs
@@ -223,6 +231,38 @@ qsfm_status prepare_forward(const qsfm_params* p, void* workspace, size_t ws_byt
   }
   *fault = fault_ptr();
   if (*fault == nullptr) return QSFM_ERR_CUDA;
+  return QSFM_OK;
+}
+
+}  // namespace
+
+namespace {
+
+constexpr long long kMaxIndexerTokens = 1ll << 20;
+
+// Checks shared by the indexer's size query and launch; *T gets the query
+// rows.
+qsfm_status check_indexer(const qsfm_indexer_params* pp, long long* T) {
+  if (pp == nullptr || T == nullptr) return QSFM_ERR_INVALID_ARG;
+  const qsfm_indexer_params& p = *pp;
+  if (p.batch < 0 || p.heads < 1 || p.dim < 1 || p.topk < 1) return QSFM_ERR_INVALID_ARG;
+  if (p.heads > 64 || p.topk > 8192) return QSFM_ERR_INVALID_ARG;
+  if (p.dim != 128) return QSFM_ERR_UNSUPPORTED;
+  if (p.block_size < 1 || p.block_size > 1024) return QSFM_ERR_INVALID_ARG;
+  if (p.block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
+  if (p.mask_mode != 0 && p.mask_mode != 3) return QSFM_ERR_INVALID_ARG;
+  if (p.cmp_ratio < 1 || p.cmp_ratio > 128) return QSFM_ERR_INVALID_ARG;
+  if (p.layout_q == QSFM_LAYOUT_BSND) {
+    if (p.max_s1 < 0 || p.cu_seqlens_q != nullptr) return QSFM_ERR_INVALID_ARG;
+  } else if (p.layout_q == QSFM_LAYOUT_TND) {
+    if (p.total_t < 0 || (p.cu_seqlens_q == nullptr && p.batch > 0) || p.seqused_q != nullptr)
+      return QSFM_ERR_INVALID_ARG;
+  } else {
+    return QSFM_ERR_INVALID_ARG;
+  }
+  if (p.max_blocks < 1 || p.num_blocks < 1) return QSFM_ERR_INVALID_ARG;
+  *T = p.layout_q == QSFM_LAYOUT_BSND ? (long long)p.batch * p.max_s1 : p.total_t;
+  if (*T > kMaxIndexerTokens) return QSFM_ERR_UNSUPPORTED;
   return QSFM_OK;
 }
 
@@ -354,42 +394,39 @@ void qsfm_indexer_params_init(qsfm_indexer_params* p) {
 // QuantLightningIndexerV2 constraints: query N in [1, 64], key N = 1, topk
 // in [1, 8192]; quant mode 1 (e4m3 query / key, fp32 scales and weights);
 // cu_seqlens_q required for TND and not allowed for BSND.
-qsfm_status qsfm_lightning_indexer(const qsfm_indexer_params* pp, void* stream) {
-  if (pp == nullptr) return QSFM_ERR_INVALID_ARG;
+qsfm_status qsfm_lightning_indexer_workspace_size(const qsfm_indexer_params* p, size_t* bytes) {
+  if (bytes == nullptr) return QSFM_ERR_INVALID_ARG;
+  long long T = 0;
+  const qsfm_status st = check_indexer(p, &T);
+  if (st != QSFM_OK) return st;
+  *bytes = qsfm::indexer_workspace_bytes(*p, int(T));
+  return QSFM_OK;
+}
+
+qsfm_status qsfm_lightning_indexer(const qsfm_indexer_params* pp, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  long long T = 0;
+  const qsfm_status st = check_indexer(pp, &T);
+  if (st != QSFM_OK) return st;
   const qsfm_indexer_params& p = *pp;
-  if (p.batch < 0 || p.heads < 1 || p.dim < 1 || p.topk < 1) return QSFM_ERR_INVALID_ARG;
-  if (p.heads > 64 || p.topk > 8192) return QSFM_ERR_INVALID_ARG;
-  if (p.dim != 128) return QSFM_ERR_UNSUPPORTED;
-  if (p.block_size < 1 || p.block_size > 1024) return QSFM_ERR_INVALID_ARG;
-  if (p.block_size != QSFM_BLOCK_SIZE) return QSFM_ERR_UNSUPPORTED;
-  if (p.mask_mode != 0 && p.mask_mode != 3) return QSFM_ERR_INVALID_ARG;
-  if (p.cmp_ratio < 1 || p.cmp_ratio > 128) return QSFM_ERR_INVALID_ARG;
-  if (p.layout_q == QSFM_LAYOUT_BSND) {
-    if (p.max_s1 < 0 || p.cu_seqlens_q != nullptr) return QSFM_ERR_INVALID_ARG;
-  } else if (p.layout_q == QSFM_LAYOUT_TND) {
-    if (p.total_t < 0 || (p.cu_seqlens_q == nullptr && p.batch > 0) || p.seqused_q != nullptr)
-      return QSFM_ERR_INVALID_ARG;
-  } else {
-    return QSFM_ERR_INVALID_ARG;
-  }
-  const long long T = p.layout_q == QSFM_LAYOUT_BSND ? (long long)p.batch * p.max_s1 : p.total_t;
   if (T == 0) return QSFM_OK;
-  if (T > kMaxUnits) return QSFM_ERR_UNSUPPORTED;
   if (p.query == nullptr || p.query_scale == nullptr || p.weights == nullptr || p.key == nullptr ||
       p.key_scale == nullptr || p.block_table == nullptr || p.seqused_k == nullptr || p.sparse_indices == nullptr)
     return QSFM_ERR_INVALID_ARG;
   if (p.return_value && p.sparse_values == nullptr) return QSFM_ERR_INVALID_ARG;
-  if (p.max_blocks < 1 || p.num_blocks < 1) return QSFM_ERR_INVALID_ARG;
   if ((long long)p.num_blocks * p.block_size > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
   if (!aligned(p.query, 16) || !aligned(p.key, 16) || !aligned(p.key_scale, 16)) return QSFM_ERR_INVALID_ARG;
   const void* words[] = {p.query_scale, p.weights, p.block_table, p.seqused_k, p.cmp_residual_k,
                          p.cu_seqlens_q, p.seqused_q, p.sparse_indices, p.sparse_values};
   for (const void* w : words)
     if (!aligned(w, 4)) return QSFM_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 16) ||
+      workspace_bytes < qsfm::indexer_workspace_bytes(p, int(T)))
+    return QSFM_ERR_WORKSPACE;
   int* fault = fault_ptr();
   if (fault == nullptr) return QSFM_ERR_CUDA;
   const NvtxRange range("qsfm_lightning_indexer");
-  return cuda_status(qsfm::launch_indexer(p, int(T), fault, static_cast<cudaStream_t>(stream)));
+  return cuda_status(qsfm::launch_indexer(p, int(T), workspace, fault, static_cast<cudaStream_t>(stream)));
 }
 
 qsfm_status qsfm_get_device_status(int32_t* fault_word) {
@@ -416,5 +453,11 @@ const char* qsfm_status_string(qsfm_status s) {
 }
 
 int32_t qsfm_abi_version(void) { return QSFM_ABI_VERSION; }
+
+int32_t qsfm_last_cuda_error(const char** name) {
+  const int e = g_last_cuda_error;
+  if (name != nullptr) *name = e != 0 ? cudaGetErrorName(cudaError_t(e)) : "cudaSuccess";
+  return e;
+}
 
 }  // extern "C"

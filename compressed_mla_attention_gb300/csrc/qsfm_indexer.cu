@@ -4,26 +4,42 @@
 // over the keys it may see, then the topk keys of largest score
 // (QuantLightningIndexerV2, "功能说明": the formula and its three steps).
 //
-// One CTA per SM, persistent over query tokens. Per token:
-//   * Q (heads x 128 e4m3 bytes) is copied by the threads into shared
-//     memory with the 128-byte swizzle, zero rows up to N = heads rounded up
-//     to 16 (the MMA's N);
-//   * the keys stream in 128-row tiles, one paged block per tile: one TMA
-//     box (128 rows x 128 bytes, 128-byte swizzle) plus a 512-byte bulk copy
-//     of the block's key scales, four stages deep;
-//   * S^T[j, h] = sum_d K[j, d] Q[h, d] on the tensor cores: tcgen05.mma
-//     kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate), M = 128 keys, N, K = 32 per
-//     MMA, 4 MMAs per tile, into one of two TMEM accumulators;
-//   * 8 epilogue warps read S^T (warp w: TMEM lane quarter w mod 4, heads
-//     32 (w / 4 mod 2) .. + 31), each thread one key row, and reduce its heads
-//     to a partial score; two partials per key make its score, kept in
-//     shared memory (up to 32768 keys: 128 KB);
-//   * all 320 threads then select the topk: a 4-pass radix select on the
-//     scores' order-preserving 32-bit keys finds the k-th largest score,
-//     and a block-wide scan writes the selected keys in ascending order
-//     (equal scores: smaller key first), then -1.
-// Roles: warp 0 TMA producer, warp 1 MMA issue, warps 2-9 epilogue; every
-// mbarrier wait is bounded (timeout -> fault bit, abort flag, orderly exit).
+// Two kernels on one stream.
+//
+// ix_score_kernel, one CTA per SM. The query tokens of a batch are taken in
+// rows of up to G consecutive tokens (G x heads rounded up to 16 <= 256, the
+// largest MMA N), a row's keys in 128-key tiles (one paged block each). The
+// tiles of all rows, laid end to end, are cut into equal contiguous ranges,
+// one per CTA, so every SM streams the same number of key bytes whatever the
+// mix of sequence lengths, and each key block is read once for all the
+// tokens of its row. Per tile:
+//   * TMA brings the key block (128 rows x 128 bytes, 128-byte swizzle) into
+//     one of as many stages as shared memory holds (11 for two tokens of 64
+//     heads; freed by the MMAs) and a bulk copy its 128 key scales into one
+//     of 16 scale slots (freed by the epilogue);
+//   * S^T[j, (g, h)] = K[j] . Q[g, h] for all the row's tokens at once:
+//     tcgen05.mma kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate), M = 128 keys,
+//     N = G x padded heads, four MMAs of K = 32, into one of two TMEM
+//     accumulators. The row's Q arrives as one 3-D TMA box (heads past the
+//     real ones zero-filled), double-buffered so the next row's Q lands
+//     while this row computes;
+//   * 16 epilogue warps in four groups read S^T (one thread per key) and
+//     reduce each token's heads to the key's score, stored to that token's
+//     fp32 score row in the workspace; the groups take the (tile, token)
+//     items in turn, and up to 4 accumulators let the MMAs run ahead.
+// Roles: warp 0 TMA producer, warp 1 MMA issue, warps 2-17 epilogue.
+//
+// ix_select_kernel, one CTA per query token, launched with programmatic
+// serialization so its launch overlaps the score kernel's tail. It loads the
+// token's scores into registers as order-preserving 32-bit keys and finds
+// the k-th largest by a radix select whose first digit starts at the
+// highest bit where the largest key and a lower bound of the k-th largest
+// differ (keys below the bound are never counted, and the digits resolve the
+// upper tail where the threshold lies). It writes the selected keys in
+// ascending order (equal scores: the smaller key first), then -1.
+//
+// Every mbarrier wait is bounded (timeout -> fault bit, abort flag, orderly
+// exit).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -31,47 +47,53 @@
 #include <mutex>
 
 #include "qsfm_device.cuh"
+#include "qsfm_internal.h"
 
 namespace qsfm {
 namespace {
 
-constexpr int kIxThreads = 320;
-constexpr int kIxWarps = kIxThreads / 32;
+constexpr int kIxThreads = 576;  // warp 0 producer, warp 1 MMA, warps 2-17 epilogue
+constexpr int kIxEpiWarps = 16;
+constexpr int kIxGroups = kIxEpiWarps / 4;
 constexpr int kIxDim = 128;        // bytes (= e4m3 elements) per query / key row
 constexpr int kIxTile = 128;       // keys per tile (one paged block)
-constexpr int kIxStages = 4;
-constexpr int kIxMaxKeys = 32768;  // keys per token kept in shared memory
+constexpr int kIxMaxStages = 12;  // key stages (as many as shared memory holds)
+constexpr int kIxSSlots = 16;      // key-scale ring (freed by the epilogue, which trails the MMAs)
+constexpr int kIxMaxKeys = 32768;  // keys per token the select holds in shared memory
 constexpr int kIxMaxHeads = 64;
-constexpr int kIxBarEpi = 1;       // named barrier of the 8 epilogue warps
-constexpr int kIxEpiThreads = 256;
+constexpr int kIxMaxN = 256;       // MMA N = tokens of a row x padded heads
+constexpr int kIxMaxG = 16;        // tokens per row (16 padded heads each)
 constexpr uint64_t kIxTimeoutNs = 2000000000ull;
 
-// shared memory map (byte offsets from a 1024-aligned base)
-constexpr uint32_t kXKey = 0;                                      // [stage] 16 KB key tiles
-constexpr uint32_t kXQ = kXKey + kIxStages * kIxTile * kIxDim;       // 64 rows x 128 B
-constexpr uint32_t kXKs = kXQ + kIxMaxHeads * kIxDim;              // [stage][128] f32 key scales
-constexpr uint32_t kXScore = kXKs + kIxStages * kIxTile * 4;       // [32768] f32 scores
-constexpr uint32_t kXPart = kXScore + kIxMaxKeys * 4;              // [2 acc][2 half][128] f32
-constexpr uint32_t kXW = kXPart + 2 * 2 * kIxTile * 4;             // [64] f32 weights
-constexpr uint32_t kXSq = kXW + 256;                               // [64] f32 query scales
-constexpr uint32_t kXHist = kXSq + 256;                            // [256] i32
-constexpr uint32_t kXScan = kXHist + 1024;                         // [64] i32 scan scratch
-constexpr uint32_t kXValid = kXScan + 256;                         // [stage] i32 tile valid
-constexpr uint32_t kXBar = kXValid + 64;                           // barriers, tmem slot, flags
-constexpr uint32_t kXBytes = kXBar + 256;
-constexpr uint32_t kXAlloc = kXBytes + 1024;
-static_assert(kXAlloc <= 232448, "indexer shared memory");
+// score kernel shared memory (byte offsets from a 1024-aligned base): a
+// fixed region, then two Q slots of x.qslot bytes, then x.stages key stages
+constexpr uint32_t kXKs = 0;                                    // [scale slot][128] f32 key scales
+constexpr uint32_t kXCw = kXKs + kIxSSlots * kIxTile * 4;       // [2][256] f32 W * Sq
+constexpr uint32_t kXRow = kXCw + 2 * kIxMaxN * 4;              // [2][32] i32: nvis per token, flag
+constexpr uint32_t kXValid = kXRow + 2 * 32 * 4;                // [scale slot] i32 tile valid
+constexpr uint32_t kXScan = kXValid + kIxSSlots * 4;            // [64] i32 scan scratch
+constexpr uint32_t kXBar = kXScan + 256;                        // barriers, tmem slot, flags, plan
+constexpr uint32_t kXFixed = (kXBar + 640 + 1023) & ~1023u;     // the Q slots start here
+constexpr uint32_t kXSmemMax = 232448;                          // dynamic shared memory of a CTA
+constexpr uint32_t kXStage = kIxTile * kIxDim;                  // 16 KB key stage
 
-// barriers: full[4], empty[4], tfull[2], tempty[2]
-constexpr int kXbFull = 0, kXbEmpty = 4, kXbTFull = 8, kXbTEmpty = 10, kXbDrain = 12, kXbCount = 13;
-static_assert(kXbCount * 8 <= 128, "barriers overlap the tmem slot");
+// barriers: key stage full / empty, accumulator full / empty (up to 4
+// accumulators), Q slot full / empty, head factors of a slot published,
+// key-scale slot full / empty, drain
+constexpr int kIxMaxAcc = 4;
+constexpr int kXbFull = 0, kXbEmpty = kIxMaxStages, kXbTFull = 2 * kIxMaxStages, kXbTEmpty = kXbTFull + kIxMaxAcc,
+              kXbQFull = kXbTEmpty + kIxMaxAcc, kXbQEmpty = kXbQFull + 2, kXbCwFull = kXbQEmpty + 2,
+              kXbSFull = kXbCwFull + 2, kXbSEmpty = kXbSFull + kIxSSlots, kXbDrain = kXbSEmpty + kIxSSlots,
+              kXbCount = kXbDrain + 1;
+static_assert(kXbCount * 8 <= 576, "barriers overlap the tmem slot");
 
 struct IxSmem {
   uint32_t base;
   uint8_t* ptr;
   __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(ptr + kXBar) + i; }
-  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(ptr + kXBar + 128); }
-  __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(ptr + kXBar + 136); }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(ptr + kXBar + 576); }
+  __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(ptr + kXBar + 584); }
+  __device__ int* plan() const { return reinterpret_cast<int*>(ptr + kXBar + 592); }
   __device__ float* f(uint32_t off) const { return reinterpret_cast<float*>(ptr + off); }
   __device__ int* i(uint32_t off) const { return reinterpret_cast<int*>(ptr + off); }
 };
@@ -93,12 +115,40 @@ __device__ __forceinline__ bool ix_warp_wait(const IxSmem& sm, int bar, uint32_t
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// 1-D bulk copy global -> shared, completing on `bar` (both addresses and
-// the size multiples of 16 bytes).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+// L2 policy for data read once (the key blocks and their scales): evicted
+// first, so the streamed keys do not push the score rows out of L2 before
+// the select kernel reads them.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 2-D tiled TMA load with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, int x, int y, uint64_t* bar,
+                                                 uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared with an L2 cache policy, completing on
+// `bar` (both addresses and the size multiples of 16 bytes).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -110,10 +160,9 @@ __device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint3
       : "memory");
 }
 
-// Batch, position and chunk length of query token t, and the keys it may
-// see (0 for a padded row).
-__device__ __forceinline__ void ix_token(const qsfm_indexer_params& p, int t, int& b, int& s, int& nvis) {
-  int s1;
+// Batch b, position s, chunk length s1 and rows in use s1e (seqused_q) of
+// query token t.
+__device__ __forceinline__ void ix_token(const qsfm_indexer_params& p, int t, int& b, int& s, int& s1, int& s1e) {
   if (p.layout_q == QSFM_LAYOUT_BSND) {
     b = t / p.max_s1;
     s = t - b * p.max_s1;
@@ -129,19 +178,59 @@ __device__ __forceinline__ void ix_token(const qsfm_indexer_params& p, int t, in
     s = t - c0;
     s1 = __ldg(p.cu_seqlens_q + b + 1) - c0;
   }
+  s1e = p.seqused_q != nullptr ? min(s1, __ldg(p.seqused_q + b)) : s1;
+}
+
+// Keys the token at position s of batch b (chunk length s1) may see: all
+// seqused_k[b] (mask_mode 0), or the compressed keys whose last original
+// token is at or before p_c (mask_mode 3). Not capped.
+__device__ __forceinline__ int ix_visible(const qsfm_indexer_params& p, int b, int s, int s1) {
   const int sk = __ldg(p.seqused_k + b);
-  if (p.seqused_q != nullptr && s >= __ldg(p.seqused_q + b)) {
-    nvis = 0;
-    return;
+  if (p.mask_mode == 0) return sk;
+  const int r = p.cmp_ratio;
+  const int res = p.cmp_residual_k != nullptr ? __ldg(p.cmp_residual_k + b) : 0;
+  const int pc = sk * r + res - s1 + s;
+  return max(0, min(sk, div_floor(pc + 1, r)));
+}
+
+// The row that starts at token t: its batch b, tokens g (0 when no row
+// starts at t) and tiles. Rows start at positions 0, G, 2G ... of the rows
+// in use; the last token of a row sees the most keys (p_c grows with s).
+__device__ __forceinline__ int ix_row(const qsfm_indexer_params& p, int t, int gmax, int kcap, int& b, int& g) {
+  int s, s1, s1e;
+  ix_token(p, t, b, s, s1, s1e);
+  if (s >= s1e || s % gmax != 0) {
+    g = 0;
+    return 0;
   }
-  if (p.mask_mode == 0) {
-    nvis = sk;
-  } else {
-    const int r = p.cmp_ratio;
-    const int res = p.cmp_residual_k != nullptr ? __ldg(p.cmp_residual_k + b) : 0;
-    const int pc = sk * r + res - s1 + s;
-    nvis = max(0, min(sk, div_floor(pc + 1, r)));
+  g = min(gmax, s1e - s);
+  const int nv = min(kcap, ix_visible(p, b, s + g - 1, s1));
+  return (nv + kIxTile - 1) / kIxTile;
+}
+
+// A CTA's walk over the rows that hold tiles: row start token t, its batch,
+// tokens and tiles, and the global index of its first tile.
+struct IxWalk {
+  int t, b, g, tiles, start;
+};
+
+// Advance to the next row with tiles; false past the last token.
+__device__ __forceinline__ bool ix_next(const qsfm_indexer_params& p, int T, int gmax, int kcap, IxWalk& w) {
+  w.start += w.tiles;
+  int t = w.t + max(w.g, 1);
+  while (t < T) {
+    int b, g;
+    const int tiles = ix_row(p, t, gmax, kcap, b, g);
+    if (tiles > 0) {
+      w.t = t;
+      w.b = b;
+      w.g = g;
+      w.tiles = tiles;
+      return true;
+    }
+    t += max(g, 1);
   }
+  return false;
 }
 
 // Order-preserving 32-bit key of a score (-0 taken as +0).
@@ -150,8 +239,11 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix sum of v over the block's 320 threads (scratch: 16 ints).
+// Exclusive prefix sum of v over the block's NT threads (scratch: 64 ints),
+// the total in `total`.
+template <int NT>
 __device__ __forceinline__ int block_exclusive_scan(int v, int tid, int* scratch, int& total) {
+  constexpr int kW = NT / 32;
   const int lane = tid & 31, warp = tid >> 5;
   int incl = v;
 #pragma unroll
@@ -162,288 +254,604 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int tid, int* scratch
   if (lane == 31) scratch[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < kIxWarps ? scratch[lane] : 0;
+    int w = lane < kW ? scratch[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int u = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += u;
     }
-    if (lane < kIxWarps) scratch[16 + lane] = w;
+    if (lane < kW) scratch[32 + lane] = w;
   }
   __syncthreads();
-  total = scratch[16 + kIxWarps - 1];
-  const int r = (warp ? scratch[16 + warp - 1] : 0) + incl - v;
+  total = scratch[32 + kW - 1];
+  const int r = (warp ? scratch[32 + warp - 1] : 0) + incl - v;
   __syncthreads();  // scratch is reused by the next call
   return r;
 }
 
+// Shape of a launch of the score kernel.
+struct IxShape {
+  int T;        // query tokens
+  int gmax;     // tokens per row at most
+  int hp;       // heads rounded up to 16
+  int kcap;     // keys per token at most
+  int kstride;  // floats per token's score row in the workspace
+  int nacc;     // TMEM columns of one accumulator (gmax * hp rounded up to 32)
+  int na;       // accumulators (4 when they fit in 512 columns, else 2)
+  int tcols;    // TMEM columns allocated (a power of two >= na * nacc)
+  int qslot;    // bytes of a Q slot (gmax * hp * 128 rounded up to 1024)
+  int stages;   // key stages
+  __host__ __device__ uint32_t q_off(int slot) const { return kXFixed + uint32_t(slot) * uint32_t(qslot); }
+  __host__ __device__ uint32_t key_off(uint32_t st) const { return kXFixed + 2u * uint32_t(qslot) + st * kXStage; }
+  __host__ __device__ uint32_t smem_bytes() const { return key_off(uint32_t(stages)) + 1024; }
+};
 
-// Top-k of the scores 0 .. n - 1 in shared memory into out[0 .. k): the keys
-// of the k largest scores (the smaller key first among equal ones) in
-// ascending key order, then -1; vals (bf16, or null) get the scores, -inf
-// after them. Every thread of the block calls it.
-__device__ void ix_select(const IxSmem& sm, int n, int k, int tid, int32_t* out, __nv_bfloat16* vals) {
-  const float* sc = sm.f(kXScore);
-  int* hist = sm.i(kXHist);
-  int* scratch = sm.i(kXScan);
-  const bool all = n <= k;
-  uint32_t thr = 0;
-  int need = 0;
-  if (!all) {
-    // radix select of the k-th largest key, 8 bits a pass from the top
-    uint32_t prefix = 0, mask = 0;
-    int remaining = k;  // of the keys matching the prefix, the rank wanted
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      for (int i = tid; i < 256; i += kIxThreads) hist[i] = 0;
-      __syncthreads();
-      for (int j = tid; j < n; j += kIxThreads) {
-        const uint32_t u = score_key(sc[j]);
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+// ------------------------------------------------------------- producer
+// Per row: the row's Q (one 3-D box: hp heads x gmax tokens), then the row's
+// key tiles in this CTA's range (the block table read 32 entries at a time;
+// per tile the key block into a stage and its scales into a scale slot).
+// Once the first stages are in flight, the row's head factors W * Sq and the
+// keys each token sees are published for the epilogue.
+__device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const IxSmem& sm, IxWalk w, int lo,
+                           int hi, int* fault, const CUtensorMap* kmap, const CUtensorMap* qmap) {
+  const int lane = threadIdx.x & 31;
+  float* cwb = sm.f(kXCw);
+  int* rowi = sm.i(kXRow);
+  int* valid = sm.i(kXValid);
+  const uint32_t qbytes = uint32_t(x.gmax * x.hp * kIxDim);
+  const uint64_t pol = l2_evict_first();
+  uint32_t n = 0;  // tiles issued
+  for (uint32_t qn = 0;; ++qn) {
+    const int slot = int(qn & 1);
+    if (qn >= 2 && !ix_warp_wait(sm, kXbQEmpty + slot, ((qn >> 1) & 1) ^ 1, fault)) return;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(sm.bar(kXbQFull + slot), qbytes);
+      tma_load_3d(sm.base + x.q_off(slot), qmap, 0, 0, w.t, sm.bar(kXbQFull + slot));
+    }
+    auto publish = [&]() {
+      bool neg = false;  // a negative query scale (not produced by amax / 448 quantisation)
+      for (int i = lane; i < w.g * x.hp; i += 32) {
+        const int gg = i / x.hp, h = i - gg * x.hp;
+        float c = 0.f;
+        if (h < p.heads) {
+          const size_t o = size_t(w.t + gg) * p.heads + h;
+          const float sq = __ldg(p.query_scale + o);
+          c = __ldg(p.weights + o) * sq;
+          neg |= sq < 0.f;
+        }
+        cwb[slot * kIxMaxN + i] = c;
       }
-      __syncthreads();
-      if (tid < 32) {
-        // lane l holds bins 255 - 8l .. 248 - 8l, the largest first
-        int c[8], sum = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          c[q] = hist[255 - 8 * tid - q];
-          sum += c[q];
+      if (lane < w.g) {
+        int b, s, s1, s1e;
+        ix_token(p, w.t + lane, b, s, s1, s1e);
+        rowi[slot * 32 + lane] = min(x.kcap, ix_visible(p, b, s, s1));
+      }
+      const bool any_neg = __any_sync(0xffffffffu, neg);
+      if (lane == 0) rowi[slot * 32 + kIxMaxG] = any_neg ? 1 : 0;
+      mbar_arrive(sm.bar(kXbCwFull + slot));
+    };
+    const int i_lo = max(lo - w.start, 0), i_hi = min(hi - w.start, w.tiles);
+    const int i_pub = i_lo + min(x.stages, i_hi - i_lo);
+    bool published = false;
+    for (int i0 = i_lo; i0 < i_hi; i0 += 32) {
+      int mine = -1;
+      if (i0 + lane < i_hi) mine = __ldg(p.block_table + size_t(w.b) * p.max_blocks + i0 + lane);
+      const int i1 = min(i_hi, i0 + 32);
+      for (int i = i0; i < i1; ++i, ++n) {
+        if (i == i_pub) {
+          publish();
+          published = true;
         }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(0xffffffffu, incl, o);
-          if (tid >= o) incl += u;
-        }
-        const int excl = incl - sum;
-        if (excl < remaining && remaining <= incl) {  // exactly one lane
-          int acc = excl;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            if (acc + c[q] >= remaining) {
-              scratch[48] = 255 - 8 * tid - q;
-              scratch[49] = acc;  // keys of larger bins
-              break;
-            }
-            acc += c[q];
+        const int blk = __shfl_sync(0xffffffffu, mine, i - i0);
+        bool go = true;
+        if (lane == 0) {
+          const uint32_t ns = uint32_t(x.stages), st = n % ns, ss = n % kIxSSlots;
+          if ((n >= ns && !ix_wait(sm, kXbEmpty + st, ((n / ns) & 1) ^ 1, fault)) ||
+              (n >= kIxSSlots && !ix_wait(sm, kXbSEmpty + ss, ((n / kIxSSlots) & 1) ^ 1, fault))) {
+            go = false;
+          } else if (blk < 0 || blk >= p.num_blocks) {
+            atomicOr(fault, QSFM_FAULT_CMP_BLOCK_ID);
+            valid[ss] = 0;  // the tile's scores become -inf; nothing is read
+            mbar_arrive(sm.bar(kXbFull + st));
+            mbar_arrive(sm.bar(kXbSFull + ss));
+          } else {
+            valid[ss] = 1;
+            mbar_arrive_expect_tx(sm.bar(kXbFull + st), kIxTile * kIxDim);
+            tma_load_2d_hint(sm.base + x.key_off(st), kmap, 0, blk * kIxTile, sm.bar(kXbFull + st), pol);
+            mbar_arrive_expect_tx(sm.bar(kXbSFull + ss), kIxTile * 4);
+            bulk_g2s_hint(sm.base + kXKs + ss * (kIxTile * 4), p.key_scale + size_t(blk) * kIxTile, kIxTile * 4,
+                          sm.bar(kXbSFull + ss), pol);
           }
         }
+        if (__shfl_sync(0xffffffffu, go ? 1 : 0, 0) == 0) return;
       }
-      __syncthreads();
-      prefix |= uint32_t(scratch[48]) << shift;
-      mask |= 0xFFu << shift;
-      remaining -= scratch[49];
-      __syncthreads();
     }
-    thr = prefix;      // the k-th largest key
-    need = remaining;  // keys equal to it that are taken, smallest first
-  }
-  // ascending key order: thread tid owns keys j0 .. j1 - 1
-  const int per = (n + kIxThreads - 1) / kIxThreads;
-  const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
-  int eq = 0, gt = 0;
-  if (!all)
-    for (int j = j0; j < j1; ++j) {
-      const uint32_t u = score_key(sc[j]);
-      eq += u == thr;
-      gt += u > thr;
-    }
-  int tot = 0;
-  const int eq_rank0 = all ? 0 : block_exclusive_scan(eq, tid, scratch, tot);
-  const int mine = all ? j1 - j0 : gt + max(0, min(eq, need - eq_rank0));
-  int nsel = 0;
-  int pos = block_exclusive_scan(mine, tid, scratch, nsel);
-  int er = eq_rank0;
-  for (int j = j0; j < j1; ++j) {
-    bool take = all;
-    if (!all) {
-      const uint32_t u = score_key(sc[j]);
-      take = u > thr || (u == thr && er < need);
-      er += u == thr;
-    }
-    if (take) {
-      out[pos] = j;
-      if (vals != nullptr) vals[pos] = __float2bfloat16_rn(sc[j]);
-      ++pos;
-    }
-  }
-  for (int i = nsel + tid; i < k; i += kIxThreads) {
-    out[i] = -1;
-    if (vals != nullptr) vals[i] = __float2bfloat16_rn(-INFINITY);
+    if (!published) publish();
+    if (!ix_next(p, x.T, x.gmax, x.kcap, w) || w.start >= hi) return;
   }
 }
 
+// ------------------------------------------------------------- MMA issue
+// One thread. Per tile: S^T = K Q^T for the row's g tokens (N = g * hp) into
+// accumulator n mod na; the row's Q slot is released after its last tile.
+__device__ void ix_mma(const qsfm_indexer_params& p, const IxShape& x, const IxSmem& sm, IxWalk w, int lo, int hi,
+                       uint32_t tmem, int* fault) {
+  const uint32_t na = uint32_t(x.na);
+  uint32_t n = 0;
+  for (uint32_t qn = 0;; ++qn) {
+    const int slot = int(qn & 1);
+    if (!ix_wait(sm, kXbQFull + slot, (qn >> 1) & 1, fault)) return;
+    // e4m3 x e4m3 (format code 0 for A and B), fp32 accumulate, both K-major
+    const uint32_t idesc = make_idesc_bf16(128, w.g * x.hp, 0, 0, true);
+    const uint64_t bdesc = make_sdesc_sw128(sm.base + x.q_off(slot), 16, 1024);
+    const int i_lo = max(lo - w.start, 0), i_hi = min(hi - w.start, w.tiles);
+    for (int i = i_lo; i < i_hi; ++i, ++n) {
+      const uint32_t ns = uint32_t(x.stages), st = n % ns, a = n % na;
+      if (!ix_wait(sm, kXbFull + st, (n / ns) & 1, fault)) return;
+      if (n >= na && !ix_wait(sm, kXbTEmpty + a, ((n / na) & 1) ^ 1, fault)) return;
+      tc_fence_after();
+      const uint64_t adesc = make_sdesc_sw128(sm.base + x.key_off(st), 16, 1024);
+      const uint32_t d = tmem + a * uint32_t(x.nacc);
+#pragma unroll
+      for (int k = 0; k < kIxDim / 32; ++k)  // 32 e4m3 (32 bytes) of d per MMA
+        mma_f8(d, adesc + uint64_t((k * 32) >> 4), bdesc + uint64_t((k * 32) >> 4), idesc, k > 0 ? 1u : 0u);
+      mma_commit(sm.bar(kXbTFull + a));
+      mma_commit(sm.bar(kXbEmpty + st));
+    }
+    mma_commit(sm.bar(kXbQEmpty + slot));
+    if (!ix_next(p, x.T, x.gmax, x.kcap, w) || w.start >= hi) return;
+  }
+}
 
-__global__ void __launch_bounds__(kIxThreads, 1)
-    indexer_kernel(const qsfm_indexer_params p, const int T, int* fault, const __grid_constant__ CUtensorMap kmap) {
+// Score of one key for one token from its hp accumulator columns at taddr:
+// with non-negative scales W ReLU(Sq Sk x) = Sk (W Sq) ReLU(x), the head
+// factors cw = W * Sq (0 past the real heads, whose columns hold 0 from the
+// zero-filled Q rows); otherwise the formula as written.
+__device__ __forceinline__ float ix_key_score(const qsfm_indexer_params& p, uint32_t taddr, int hp, const float* cw,
+                                              bool fast, float sk, int t) {
+  const float* W = p.weights + size_t(t) * p.heads;
+  const float* Sq = p.query_scale + size_t(t) * p.heads;
+  if (hp == kIxMaxHeads) {  // two halves of 32 columns
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, acc = 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float v[32];
+      tmem_ld32(taddr + 32 * half, v);
+      tmem_ld_wait();
+      if (fast) {
+        const float4* c4 = reinterpret_cast<const float4*>(cw + 32 * half);
+#pragma unroll
+        for (int h = 0; h < 32; h += 4) {
+          const float4 c = c4[h >> 2];
+          s0 = fmaf(c.x, fmaxf(0.f, v[h]), s0);
+          s1 = fmaf(c.y, fmaxf(0.f, v[h + 1]), s1);
+          s2 = fmaf(c.z, fmaxf(0.f, v[h + 2]), s2);
+          s3 = fmaf(c.w, fmaxf(0.f, v[h + 3]), s3);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+          if (32 * half + h < p.heads)
+            acc += __ldg(W + 32 * half + h) * fmaxf(0.f, (__ldg(Sq + 32 * half + h) * sk) * v[h]);
+      }
+    }
+    return fast ? sk * ((s0 + s1) + (s2 + s3)) : acc;
+  }
+  float s0 = 0.f, acc = 0.f;
+  for (int c = 0; c < hp; c += 16) {
+    float v[16];
+    tmem_ld16(taddr + uint32_t(c), v);
+    tmem_ld_wait();
+    if (fast) {
+#pragma unroll
+      for (int h = 0; h < 16; ++h) s0 = fmaf(cw[c + h], fmaxf(0.f, v[h]), s0);
+    } else {
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        if (c + h < p.heads) acc += __ldg(W + c + h) * fmaxf(0.f, (__ldg(Sq + c + h) * sk) * v[h]);
+    }
+  }
+  return fast ? sk * s0 : acc;
+}
+
+// ------------------------------------------------------------- epilogue
+// Warps 2-17 in four groups of 4; warp w reads TMEM lanes 32 (w mod 4) ..
+// + 31, its key rows. Every warp visits every tile; the (tile n, token gg)
+// items go to the groups in turn (to group (n g + gg) mod 4), so the
+// groups share the tiles' tokens evenly whatever the tokens per row.
+__device__ void ix_epilogue(const qsfm_indexer_params& p, const IxShape& x, const IxSmem& sm, IxWalk w, int lo,
+                            int hi, uint32_t tmem, float* ws, int* fault) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3, grp = (warp - 2) >> 2;
+  const int row = 32 * quarter + lane;
+  const uint32_t na = uint32_t(x.na);
+  const float* cwb = sm.f(kXCw);
+  const int* rowi = sm.i(kXRow);
+  const float* ksm = sm.f(kXKs);
+  const int* valid = sm.i(kXValid);
+  uint32_t n = 0;
+  for (uint32_t qn = 0;; ++qn) {
+    const int slot = int(qn & 1);
+    if (!ix_warp_wait(sm, kXbCwFull + slot, (qn >> 1) & 1, fault)) return;
+    const bool neg = rowi[slot * 32 + kIxMaxG] != 0;
+    const int i_lo = max(lo - w.start, 0), i_hi = min(hi - w.start, w.tiles);
+    for (int i = i_lo; i < i_hi; ++i, ++n) {
+      const uint32_t ss = n % kIxSSlots, a = n % na;
+      // this group's first item of the tile: gg = grp - n g (mod 4)
+      const int first = int((uint32_t(grp) - n * uint32_t(w.g)) & uint32_t(kIxGroups - 1));
+      if (!ix_warp_wait(sm, kXbTFull + a, (n / na) & 1, fault)) return;
+      float sk = 0.f;
+      int ok = 0;
+      if (first < w.g) {
+        if (!ix_warp_wait(sm, kXbSFull + ss, (n / kIxSSlots) & 1, fault)) return;  // the scales landed
+        sk = ksm[ss * kIxTile + row];
+        ok = valid[ss];
+      }
+      tc_fence_after();
+      __syncwarp();
+      // the scale slot may be refilled (tile n's accumulator being full, the
+      // producer has already seen the slot's previous use released)
+      if (lane == 0) mbar_arrive(sm.bar(kXbSEmpty + ss));
+      const int j = i * kIxTile + row, jw = i * kIxTile + 32 * quarter;
+      const uint32_t taddr = tmem + a * uint32_t(x.nacc) + (uint32_t(32 * quarter) << 16);
+      const bool fast = __all_sync(0xffffffffu, !neg && sk >= 0.f);
+      for (int gg = first; gg < w.g; gg += kIxGroups) {
+        const int nv = rowi[slot * 32 + gg];
+        if (jw >= nv) continue;  // the warp's 32 keys are all past this token's
+        const float sc = ix_key_score(p, taddr + uint32_t(gg * x.hp), x.hp, cwb + slot * kIxMaxN + gg * x.hp, fast,
+                                      sk, w.t + gg);
+        if (j < nv) ws[size_t(w.t + gg) * x.kstride + j] = ok ? sc : -INFINITY;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(kXbTEmpty + a));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(kXbQEmpty + slot));
+    if (!ix_next(p, x.T, x.gmax, x.kcap, w) || w.start >= hi) return;
+  }
+}
+
+// ------------------------------------------------------------- score kernel
+__global__ void __maxnreg__(96)
+    ix_score_kernel(const qsfm_indexer_params p, const IxShape x, float* ws, int* fault,
+                    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   IxSmem sm;
   sm.base = (raw + 1023u) & ~1023u;
   sm.ptr = smem_raw + (sm.base - raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int heads = p.heads;
-  const int npad = max(16, (heads + 15) & ~15);  // the MMA's N
+  const uint32_t tcols = uint32_t(x.tcols);
+  grid_launch_dependents();  // the select kernel may be scheduled as CTAs finish
   if (tid == 0) {
-    for (int i = 0; i < kIxStages; ++i) {
+    for (int i = 0; i < x.stages; ++i) {
       mbar_init(sm.bar(kXbFull + i), 1);
-      mbar_init(sm.bar(kXbEmpty + i), 1 + 8);  // the MMAs' commit and the 8 epilogue warps
+      mbar_init(sm.bar(kXbEmpty + i), 1);  // the MMAs' commit
+    }
+    for (int i = 0; i < kIxSSlots; ++i) {
+      mbar_init(sm.bar(kXbSFull + i), 1);
+      mbar_init(sm.bar(kXbSEmpty + i), kIxEpiWarps);  // every epilogue warp
+    }
+    for (int i = 0; i < kIxMaxAcc; ++i) {
+      mbar_init(sm.bar(kXbTFull + i), 1);
+      mbar_init(sm.bar(kXbTEmpty + i), kIxEpiWarps);  // every epilogue warp
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(sm.bar(kXbTFull + i), 1);
-      mbar_init(sm.bar(kXbTEmpty + i), 8);
+      mbar_init(sm.bar(kXbQFull + i), 1);    // the Q box
+      mbar_init(sm.bar(kXbCwFull + i), 32);  // the producer's lanes
+      mbar_init(sm.bar(kXbQEmpty + i), 1 + kIxEpiWarps);  // the row's last MMAs and every epilogue warp
     }
     mbar_init(sm.bar(kXbDrain), 1);
     *sm.abort_flag() = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(sm.tmem_slot(), 128);
+  if (warp == 1) tmem_alloc(sm.tmem_slot(), tcols);
+  // This CTA's tiles [lo, hi) of all rows' tiles laid end to end: every
+  // thread counts the tiles of the rows starting in its run of tokens, a
+  // block scan places the runs, and the thread whose run holds tile lo
+  // finds the row (and that row's first global tile) it lies in.
+  int* scratch = sm.i(kXScan);
+  int* plan = sm.plan();
+  const int per = (x.T + kIxThreads - 1) / kIxThreads;
+  const int t0 = min(x.T, tid * per), t1 = min(x.T, t0 + per);
+  int mine = 0;
+  for (int t = t0; t < t1; ++t) {
+    int b, g;
+    mine += ix_row(p, t, x.gmax, x.kcap, b, g);
+  }
+  int total = 0;
+  const int excl = block_exclusive_scan<kIxThreads>(mine, tid, scratch, total);
+  const int lo = int((long long)blockIdx.x * total / gridDim.x);
+  const int hi = int((long long)(blockIdx.x + 1) * total / gridDim.x);
+  if (lo < hi && excl <= lo && lo < excl + mine) {
+    int acc = excl;
+    for (int t = t0; t < t1; ++t) {
+      int b, g;
+      const int nt = ix_row(p, t, x.gmax, x.kcap, b, g);
+      if (acc + nt > lo) {
+        plan[0] = t;
+        plan[1] = acc;
+        break;
+      }
+      acc += nt;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot();
-  // e4m3 x e4m3 (format code 0 for A and B), fp32 accumulate, both K-major
-  const uint32_t idesc = make_idesc_bf16(128, npad, 0, 0, true);
-  float* wsm = sm.f(kXW);
-  float* sqm = sm.f(kXSq);
-  float* part = sm.f(kXPart);
-  float* score = sm.f(kXScore);
-  const float* ksm = sm.f(kXKs);
-  int* valid = sm.i(kXValid);
-  const uint8_t* q8 = static_cast<const uint8_t*>(p.query);
-  uint32_t ctr = 0;  // tiles before this token (stage and phase of every barrier)
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    int b, s, nvis;
-    ix_token(p, t, b, s, nvis);
-    if (nvis > kIxMaxKeys) {
-      if (tid == 0) atomicOr(fault, QSFM_FAULT_KV_ROW);
-      nvis = kIxMaxKeys;
-    }
-    const int ntiles = (nvis + kIxTile - 1) / kIxTile;
-    // the token's Q (rows >= heads zero), weights and query scales
-    for (int i = tid; i < npad * 8; i += kIxThreads) {
-      const int row = i >> 3, c = i & 7;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (row < heads) v = ldg_nc_v4(q8 + (size_t(t) * heads + row) * kIxDim + 16 * c);
-      sts_v4(sm.base + kXQ + row * kIxDim + ((uint32_t(c) ^ uint32_t(row & 7)) << 4), v);
-    }
-    for (int i = tid; i < heads; i += kIxThreads) {
-      wsm[i] = __ldg(p.weights + size_t(t) * heads + i);
-      sqm[i] = __ldg(p.query_scale + size_t(t) * heads + i);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
+  if (lo < hi) {
+    IxWalk w;
+    w.t = plan[0];
+    w.start = plan[1];
+    w.tiles = ix_row(p, w.t, x.gmax, x.kcap, w.b, w.g);
     if (warp == 0) {
-      if (lane == 0) {
-        // producer: one paged block of keys and its scales per tile
-        for (int i = 0; i < ntiles; ++i) {
-          const uint32_t n = ctr + i, st = n % kIxStages;
-          if (n >= kIxStages && !ix_wait(sm, kXbEmpty + st, ((n / kIxStages) & 1) ^ 1, fault)) break;
-          int blk = -1;
-          if (i < p.max_blocks) blk = __ldg(p.block_table + size_t(b) * p.max_blocks + i);
-          else atomicOr(fault, QSFM_FAULT_CMP_TABLE_COL);
-          if (blk < 0 || blk >= p.num_blocks) {
-            if (i < p.max_blocks) atomicOr(fault, QSFM_FAULT_CMP_BLOCK_ID);
-            valid[st] = 0;  // the tile's scores become -inf; nothing is read
-            mbar_arrive(sm.bar(kXbFull + st));
-          } else {
-            valid[st] = 1;
-            mbar_arrive_expect_tx(sm.bar(kXbFull + st), kIxTile * kIxDim + kIxTile * 4);
-            tma_load_2d(sm.base + kXKey + st * (kIxTile * kIxDim), &kmap, 0, blk * kIxTile,
-                        sm.bar(kXbFull + st));
-            bulk_g2s(sm.base + kXKs + st * (kIxTile * 4), p.key_scale + size_t(blk) * kIxTile, kIxTile * 4,
-                     sm.bar(kXbFull + st));
-          }
-        }
-      }
+      ix_produce(p, x, sm, w, lo, hi, fault, &kmap, &qmap);
     } else if (warp == 1) {
-      if (lane == 0) {
-        const uint64_t bdesc = make_sdesc_sw128(sm.base + kXQ, 16, 1024);
-        for (int i = 0; i < ntiles; ++i) {
-          const uint32_t n = ctr + i, st = n % kIxStages, a = n & 1;
-          if (!ix_wait(sm, kXbFull + st, (n / kIxStages) & 1, fault)) break;
-          if (n >= 2 && !ix_wait(sm, kXbTEmpty + a, ((n >> 1) & 1) ^ 1, fault)) break;
-          tc_fence_after();
-          const uint64_t adesc = make_sdesc_sw128(sm.base + kXKey + st * (kIxTile * kIxDim), 16, 1024);
-          const uint32_t d = tmem + a * 64;
-#pragma unroll
-          for (int k = 0; k < kIxDim / 32; ++k)  // 32 e4m3 (32 bytes) of d per MMA
-            mma_f8(d, adesc + uint64_t((k * 32) >> 4), bdesc + uint64_t((k * 32) >> 4), idesc, k > 0 ? 1u : 0u);
-          mma_commit(sm.bar(kXbTFull + a));
-          mma_commit(sm.bar(kXbEmpty + st));
-        }
-      }
+      if (lane == 0) ix_mma(p, x, sm, w, lo, hi, tmem, fault);
     } else {
-      // epilogue: warp w reads TMEM lanes 32 (w mod 4) .. + 31 (its key rows)
-      // and heads 32 half .. + 31
-      const int quarter = warp & 3, half = (warp - 2) >> 2;
-      const int row = 32 * quarter + lane;
-      // After a timeout the waits fail at once; the warps keep running the
-      // same named-barrier sequence (no work) so that none of them blocks.
-      bool alive = !*sm.abort_flag();
-      for (int i = 0; i < ntiles; ++i) {
-        const uint32_t n = ctr + i, st = n % kIxStages, a = n & 1;
-        if (alive) alive = ix_warp_wait(sm, kXbTFull + a, (n >> 1) & 1, fault);
-        if (alive) alive = ix_warp_wait(sm, kXbFull + st, (n / kIxStages) & 1, fault);  // the scales landed
-        float acc = 0.f;
-        int ok = 0;
-        if (alive) {
-          tc_fence_after();
-          float x[32];
-          const bool mine = half * 32 < heads;
-          if (mine) {
-            tmem_ld32(tmem + a * 64 + half * 32 + (uint32_t(32 * quarter) << 16), x);
-            tmem_ld_wait();
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(sm.bar(kXbTEmpty + a));
-          const float sk = ksm[st * kIxTile + row];
-          ok = valid[st];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(sm.bar(kXbEmpty + st));  // the stage may be refilled
-          if (mine) {
-#pragma unroll
-            for (int h = 0; h < 32; ++h) {
-              const int hh = half * 32 + h;
-              if (hh < heads) acc += wsm[hh] * fmaxf(0.f, (sqm[hh] * sk) * x[h]);
-            }
-          }
-        }
-        part[(a * 2 + half) * kIxTile + row] = acc;
-        named_sync(kIxBarEpi, kIxEpiThreads);
-        if (half == 0 && alive) {
-          const int j = i * kIxTile + row;
-          if (j < nvis) score[j] = ok ? part[(a * 2) * kIxTile + row] + part[(a * 2 + 1) * kIxTile + row] : -INFINITY;
-        }
-      }
+      ix_epilogue(p, x, sm, w, lo, hi, tmem, ws, fault);
     }
-    __syncthreads();  // the token's scores are complete
-    ctr += ntiles;
-    if (*sm.abort_flag()) break;
-    __nv_bfloat16* vals = p.return_value ? static_cast<__nv_bfloat16*>(p.sparse_values) + size_t(t) * p.topk : nullptr;
-    ix_select(sm, nvis, p.topk, tid, p.sparse_indices + size_t(t) * p.topk, vals);
-    __syncthreads();  // scores and scratch are reused by the next token
   }
   if (warp == 1 && lane == 0) {
-    // every MMA issued above completes before tensor memory is freed
+    // every MMA issued above completes before tensor memory is freed (a
+    // bounded wait that an abort does not cut short)
     mma_commit(sm.bar(kXbDrain));
-    ix_wait(sm, kXbDrain, 0, fault);
+    volatile int never = 0;
+    if (!mbar_wait_poll(smem_u32(sm.bar(kXbDrain)), 0, &never, kIxTimeoutNs)) atomicOr(fault, QSFM_FAULT_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, tcols);
   }
 }
 
-// Tensor map of the key pool viewed as [num_blocks * 128 rows, 128 bytes],
-// boxes of one block (128 x 128 bytes) with the 128-byte swizzle of the
-// MMA's K-major operand.
-cudaError_t make_key_map(const void* key, int num_blocks, CUtensorMap* map) {
+// ------------------------------------------------------------- select kernel
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelBins = 4096;  // 12-bit digits
+constexpr int kSelBoundary = 256;  // boundary-bin keys ranked directly (more: further radix passes)
+
+// One CTA per query token. Thread tid keeps the keys of score groups
+// q = tid + 512 i (i < V; four keys 4q .. 4q+3 each) in registers, so a row
+// of up to 2048 V scores is read from the workspace once and every later
+// pass is over registers. Absent keys (past the row) are 0, below every
+// score's key.
+template <int V>
+__global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
+    ix_select_kernel(const qsfm_indexer_params p, const IxShape x, const float* ws, int* fault) {
+  __shared__ int hist[kSelBins];             // radix histogram, then the tie bitmap
+  __shared__ uint32_t bits[kIxMaxKeys / 32];  // selected keys
+  __shared__ int scratch[128];
+  uint32_t* uscr = reinterpret_cast<uint32_t*>(scratch);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = blockIdx.x;
+  int b, s, s1, s1e;
+  ix_token(p, t, b, s, s1, s1e);
+  int nv = s < s1e ? ix_visible(p, b, s, s1) : 0;
+  if (nv > x.kcap) {
+    if (tid == 0) atomicOr(fault, nv > kIxMaxKeys ? QSFM_FAULT_KV_ROW : QSFM_FAULT_CMP_TABLE_COL);
+    nv = x.kcap;
+  }
+  const int k = p.topk;
+  int32_t* out = p.sparse_indices + size_t(t) * k;
+  __nv_bfloat16* vals = p.return_value ? static_cast<__nv_bfloat16*>(p.sparse_values) + size_t(t) * k : nullptr;
+  const float* sc = ws + size_t(t) * x.kstride;
+  grid_dependency_wait();  // the score kernel's rows are complete and visible
+  if (nv <= k) {  // every visible key, then -1
+    for (int j = tid; j < k; j += kSelThreads) {
+      out[j] = j < nv ? j : -1;
+      if (vals != nullptr) vals[j] = __float2bfloat16_rn(j < nv ? __ldcg(sc + j) : -INFINITY);
+    }
+    return;
+  }
+  // 1. The keys, with the smallest, the largest, and this thread's largest.
+  // When k is at most the number of threads holding keys, lo = the smallest
+  // per-thread largest is a lower bound of the k-th largest key (that many
+  // distinct keys are >= lo); otherwise lo is the smallest key.
+  const int n4 = (nv + 3) >> 2, nw = (nv + 31) >> 5;
+  float4 f[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int q = tid + kSelThreads * i;
+    f[i] = q < n4 ? __ldcg(reinterpret_cast<const float4*>(sc) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  uint32_t u[V][4];
+  uint32_t kmin = 0xffffffffu, tmax = 0u;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int j = 4 * (tid + kSelThreads * i);
+    u[i][0] = j < nv ? score_key(f[i].x) : 0u;
+    u[i][1] = j + 1 < nv ? score_key(f[i].y) : 0u;
+    u[i][2] = j + 2 < nv ? score_key(f[i].z) : 0u;
+    u[i][3] = j + 3 < nv ? score_key(f[i].w) : 0u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      tmax = max(tmax, u[i][e]);
+      if (j + e < nv) kmin = min(kmin, u[i][e]);
+    }
+  }
+  for (int i = tid; i < nw; i += kSelThreads) bits[i] = 0u;
+  {
+    const uint32_t a = __reduce_min_sync(0xffffffffu, kmin);
+    const uint32_t c = __reduce_max_sync(0xffffffffu, tmax);
+    const uint32_t o = __reduce_min_sync(0xffffffffu, tid < n4 ? tmax : 0xffffffffu);
+    if (lane == 0) {
+      uscr[warp] = a;
+      uscr[kSelWarps + warp] = c;
+      uscr[2 * kSelWarps + warp] = o;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t a = lane < kSelWarps ? uscr[lane] : 0xffffffffu;
+    uint32_t c = lane < kSelWarps ? uscr[kSelWarps + lane] : 0u;
+    uint32_t o = lane < kSelWarps ? uscr[2 * kSelWarps + lane] : 0xffffffffu;
+    a = __reduce_min_sync(0xffffffffu, a);
+    c = __reduce_max_sync(0xffffffffu, c);
+    o = __reduce_min_sync(0xffffffffu, o);
+    if (lane == 0) {
+      uscr[100] = a;
+      uscr[101] = c;
+      uscr[102] = o;
+    }
+  }
+  __syncthreads();
+  const uint32_t kmax = uscr[101];
+  const uint32_t lo = k <= min(kSelThreads, n4) ? uscr[102] : uscr[100];
+
+  // 2. Radix select of the k-th largest key among the keys >= lo (it is one
+  // of them). They share the bits of lo and kmax above the highest bit where
+  // those two differ; the digits (12 bits at most) start below. A key >= lo
+  // is taken when its bits under `mask` beat `prefix`, or equal it and it is
+  // among the first `need` such keys (by score, then key index); `eq` counts
+  // those equal to the prefix. Passes stop once the boundary bin is taken
+  // whole or holds few enough keys to rank directly.
+  uint32_t mask, prefix;
+  int need, eq = -1;  // -1: not counted
+  const uint32_t diff = lo ^ kmax;
+  if (diff == 0u) {  // every key >= lo is equal: the first k of them
+    mask = 0xffffffffu;
+    prefix = kmax;
+    need = k;
+  } else {
+    int nbits = 32 - __clz(diff);
+    mask = nbits == 32 ? 0u : ~((1u << nbits) - 1u);
+    prefix = kmax & mask;
+    int remaining = k;  // of the keys matching the prefix, the rank wanted
+    while (nbits > 0) {
+      const int d = min(12, nbits), shift = nbits - d, nb = 1 << d;
+      for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t v = u[i][e];
+          if (v >= lo && (v & mask) == prefix) atomicAdd(&hist[(v >> shift) & uint32_t(nb - 1)], 1);
+        }
+      __syncthreads();
+      // thread i sums bins nb-1-i*per down to nb-i*per-per (largest first)
+      const int per = (nb + kSelThreads - 1) / kSelThreads;
+      const int top = nb - 1 - tid * per;
+      int sum = 0;
+      for (int q = 0; q < per; ++q)
+        if (top - q >= 0) sum += hist[top - q];
+      int tot = 0;
+      const int ex = block_exclusive_scan<kSelThreads>(sum, tid, scratch, tot);
+      if (ex < remaining && remaining <= ex + sum) {  // exactly one thread
+        int acc = ex;
+        for (int q = 0; q < per; ++q) {
+          const int c = hist[top - q];
+          if (acc + c >= remaining) {
+            scratch[96] = top - q;
+            scratch[97] = acc;  // keys in larger bins
+            scratch[98] = c;
+            break;
+          }
+          acc += c;
+        }
+      }
+      __syncthreads();
+      prefix |= uint32_t(scratch[96]) << shift;
+      mask |= uint32_t(nb - 1) << shift;
+      remaining -= scratch[97];
+      eq = scratch[98];
+      nbits = shift;
+      __syncthreads();
+      if (eq == remaining || eq <= kSelBoundary) break;  // taken whole, or ranked below
+    }
+    need = remaining;
+  }
+
+  // 3. Mark the selected keys: every key >= lo above the prefix; the equal
+  // ones too when all of them are taken. Otherwise a few equal ones are
+  // listed and ranked (score, then key index) directly; many (ties past the
+  // k-th) go through a tie bitmap in key order.
+  const bool all_eq = eq == need;
+  const bool listed = !all_eq && eq >= 0 && eq <= kSelBoundary;
+  uint32_t* tbits = reinterpret_cast<uint32_t*>(hist);   // kcap / 32 <= 1024 words
+  uint32_t* lkey = reinterpret_cast<uint32_t*>(hist);    // listed keys [256]
+  int* lidx = hist + kSelBoundary;                       // and their indices [256]
+  if (!all_eq && !listed)
+    for (int i = tid; i < nw; i += kSelThreads) tbits[i] = 0u;
+  if (tid == 0) scratch[99] = 0;  // listed count
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t v = u[i][e];
+      const int j = 4 * (tid + kSelThreads * i) + e;
+      if (v < lo) continue;
+      const uint32_t hv = v & mask;
+      if (hv > prefix || (hv == prefix && all_eq)) {
+        atomicOr(&bits[j >> 5], 1u << (j & 31));
+      } else if (hv == prefix) {
+        if (listed) {
+          const int slot = atomicAdd(&scratch[99], 1);  // < eq <= 256
+          lkey[slot] = v;
+          lidx[slot] = j;
+        } else {
+          atomicOr(&tbits[j >> 5], 1u << (j & 31));
+        }
+      }
+    }
+  __syncthreads();
+  if (listed) {  // warp w ranks listed keys w, w + 16, ...: larger first, then smaller index
+    for (int c = warp; c < eq; c += kSelWarps) {
+      const uint32_t v = lkey[c];
+      const int j = lidx[c];
+      int rank = 0;
+      for (int o = lane; o < eq; o += 32) {
+        const uint32_t w2 = lkey[o];
+        rank += w2 > v || (w2 == v && lidx[o] < j);
+      }
+      rank = __reduce_add_sync(0xffffffffu, rank);
+      if (lane == 0 && rank < need) atomicOr(&bits[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+  } else if (!all_eq) {  // thread i owns tie words 2i, 2i + 1 (nw <= 1024)
+    const int w0 = 2 * tid;
+    const uint32_t t0 = w0 < nw ? tbits[w0] : 0u, t1 = w0 + 1 < nw ? tbits[w0 + 1] : 0u;
+    int tot = 0;
+    int r = block_exclusive_scan<kSelThreads>(__popc(t0) + __popc(t1), tid, scratch, tot);
+    const uint32_t m[2] = {t0, t1};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t take = 0u;
+      for (uint32_t v = m[h]; v != 0u && r < need; v &= v - 1u, ++r) take |= v & (~v + 1u);
+      if (take != 0u) bits[w0 + h] |= take;  // the words are this thread's alone
+    }
+    __syncthreads();
+  }
+
+  // 4. The marked keys in ascending order: thread i owns words 2i, 2i + 1.
+  const int w0 = 2 * tid;
+  const uint32_t b0 = w0 < nw ? bits[w0] : 0u, b1 = w0 + 1 < nw ? bits[w0 + 1] : 0u;
+  int tot = 0;
+  int pos = block_exclusive_scan<kSelThreads>(__popc(b0) + __popc(b1), tid, scratch, tot);
+  const uint32_t m[2] = {b0, b1};
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    for (uint32_t v = m[h]; v != 0u; v &= v - 1u, ++pos) {
+      const int j = 32 * (w0 + h) + (__ffs(v) - 1);
+      out[pos] = j;
+      if (vals != nullptr) vals[pos] = __float2bfloat16_rn(__ldcg(sc + j));
+    }
+}
+
+template <int V>
+cudaError_t launch_select(const qsfm_indexer_params& p, const IxShape& x, const float* ws, int* fault,
+                          cudaStream_t s) {
+  return launch_after_predecessor(ix_select_kernel<V>, dim3(x.T), dim3(kSelThreads), 0, s, p, x, ws, fault);
+}
+
+// ------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -454,6 +862,14 @@ cudaError_t make_key_map(const void* key, int num_blocks, CUtensorMap* map) {
         qres == cudaDriverEntryPointSuccess)
       encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
+  return encode;
+}
+
+// The key pool viewed as [num_blocks * 128 rows, 128 bytes], boxes of one
+// block (128 x 128 bytes) with the 128-byte swizzle of the MMA's K-major
+// operand.
+cudaError_t make_key_map(const void* key, int num_blocks, CUtensorMap* map) {
+  const auto encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cuuint64_t(kIxDim), cuuint64_t(num_blocks) * kIxTile};
   const cuuint64_t strides[1] = {cuuint64_t(kIxDim)};
@@ -461,24 +877,75 @@ cudaError_t make_key_map(const void* key, int num_blocks, CUtensorMap* map) {
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(key), dims, strides, box,
                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The queries viewed as [T, heads, 128 bytes]; a box is one row of the score
+// kernel: gmax tokens x hp heads (heads past the real ones, and tokens past
+// T, read as zero), laid out as gmax * hp rows of 128 bytes with the 128-byte
+// swizzle, the MMA's K-major B operand.
+cudaError_t make_query_map(const void* query, int heads, int T, int hp, int gmax, CUtensorMap* map) {
+  const auto encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {cuuint64_t(kIxDim), cuuint64_t(heads), cuuint64_t(T)};
+  const cuuint64_t strides[2] = {cuuint64_t(kIxDim), cuuint64_t(heads) * kIxDim};
+  const cuuint32_t box[3] = {kIxDim, cuuint32_t(hp), cuuint32_t(gmax)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(query), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+IxShape indexer_shape(const qsfm_indexer_params& p, int T) {
+  IxShape x;
+  x.T = T;
+  x.hp = (p.heads + 15) & ~15;
+  x.gmax = kIxMaxN / x.hp < kIxMaxG ? kIxMaxN / x.hp : kIxMaxG;
+  if (p.layout_q == QSFM_LAYOUT_BSND && p.max_s1 < x.gmax) x.gmax = p.max_s1;
+  const long long keys = (long long)p.max_blocks * kIxTile;
+  x.kcap = int(keys < kIxMaxKeys ? keys : kIxMaxKeys);
+  x.kstride = x.kcap;
+  x.nacc = (x.gmax * x.hp + 31) & ~31;
+  x.na = kIxMaxAcc * x.nacc <= 512 ? kIxMaxAcc : 2;
+  x.tcols = 32;
+  while (x.tcols < x.na * x.nacc) x.tcols <<= 1;
+  x.qslot = (x.gmax * x.hp * kIxDim + 1023) & ~1023;
+  const int room = int(kXSmemMax) - 1024 - int(kXFixed) - 2 * x.qslot;
+  x.stages = room / int(kXStage) < kIxMaxStages ? room / int(kXStage) : kIxMaxStages;
+  return x;
+}
+
 }  // namespace
 
-cudaError_t launch_indexer(const qsfm_indexer_params& p, int T, int* fault, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXAlloc);
+size_t indexer_workspace_bytes(const qsfm_indexer_params& p, int num_tokens) {
+  return size_t(num_tokens) * size_t(indexer_shape(p, num_tokens).kstride) * sizeof(float);
+}
+
+cudaError_t launch_indexer(const qsfm_indexer_params& p, int T, void* workspace, int* fault, cudaStream_t s) {
+  const IxShape x = indexer_shape(p, T);
+  cudaError_t e =
+      cudaFuncSetAttribute(ix_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(x.smem_bytes()));
   if (e != cudaSuccess) return e;
-  CUtensorMap kmap;
-  e = make_key_map(p.key, p.num_blocks, &kmap);
-  if (e != cudaSuccess) return e;
+  CUtensorMap kmap, qmap;
+  if ((e = make_key_map(p.key, p.num_blocks, &kmap)) != cudaSuccess) return e;
+  if ((e = make_query_map(p.query, p.heads, T, x.hp, x.gmax, &qmap)) != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int grid = T < sms ? T : sms;
-  indexer_kernel<<<grid, kIxThreads, kXAlloc, s>>>(p, T, fault, kmap);
-  return cudaGetLastError();
+  float* ws = static_cast<float*>(workspace);
+  ix_score_kernel<<<sms, kIxThreads, x.smem_bytes(), s>>>(p, x, ws, fault, kmap, qmap);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // keys per thread: the row's 4-score groups over 512 threads, rounded up
+  // to a power of two
+  const int v = (x.kcap + 4 * kSelThreads - 1) / (4 * kSelThreads);
+  const float* cws = ws;
+  if (v <= 1) return launch_select<1>(p, x, cws, fault, s);
+  if (v <= 2) return launch_select<2>(p, x, cws, fault, s);
+  if (v <= 4) return launch_select<4>(p, x, cws, fault, s);
+  if (v <= 8) return launch_select<8>(p, x, cws, fault, s);
+  return launch_select<16>(p, x, cws, fault, s);
 }
 
 }  // namespace qsfm

@@ -49,7 +49,11 @@ cudaError_t launch_attention(const qsfm_params& p, int num_tokens, int num_ctas,
                              const Workspace& ws, int* fault, cudaStream_t s);
 cudaError_t launch_combine(const qsfm_params& p, int num_tokens, int num_ctas,
                            const Workspace& ws, int* fault, cudaStream_t s);
-cudaError_t launch_indexer(const qsfm_indexer_params& p, int num_tokens, int* fault, cudaStream_t s);
+// Lightning indexer: score kernel then select kernel; the workspace holds
+// num_tokens fp32 score rows.
+size_t indexer_workspace_bytes(const qsfm_indexer_params& p, int num_tokens);
+cudaError_t launch_indexer(const qsfm_indexer_params& p, int num_tokens, void* workspace, int* fault,
+                           cudaStream_t s);
 cudaError_t launch_bounded_wait(uint64_t timeout_ns, unsigned long long* elapsed, int* fault,
                                 cudaStream_t s);
 cudaError_t launch_debug_gather(const qsfm_params& p, const int32_t* tokens, int n,

@@ -95,7 +95,7 @@
 extern "C" {
 #endif
 
-#define QSFM_ABI_VERSION 4
+#define QSFM_ABI_VERSION 5
 #define QSFM_NUM_HEADS 64
 #define QSFM_HEAD_DIM 512
 #define QSFM_BLOCK_SIZE 128
@@ -360,10 +360,12 @@ qsfm_status qsfm_debug_bounded_wait(uint64_t timeout_ns, uint64_t* elapsed_ns_ou
  *   sparse_values  bf16 [T, 1, topk] (out, written when return_value != 0;
  *                the scores of the listed keys, -inf after them)
  * Built shapes (QSFM_ERR_UNSUPPORTED otherwise): dim = 128, 1 <= heads
- * <= 64, 1 <= topk <= 8192, block size 128, at most 32768 keys per batch
- * (a larger seqused_k is cut to 32768 and flagged with QSFM_FAULT_KV_ROW).
+ * <= 64, 1 <= topk <= 8192, block size 128, at most 2^20 query rows, at
+ * most min(32768, max_blocks * 128) keys per batch (a larger seqused_k is
+ * cut to that and flagged: QSFM_FAULT_KV_ROW past 32768, else
+ * QSFM_FAULT_CMP_TABLE_COL). A block id outside [0, num_blocks) is flagged
+ * with QSFM_FAULT_CMP_BLOCK_ID, its keys score -inf and are not read.
  * Pointers: query, key, key_scale 16-byte aligned, the rest 4-byte aligned.
- * Asynchronous on `stream`, no allocation, nothing read back.
  */
 typedef struct qsfm_indexer_params {
   int32_t batch;        /* B                                                */
@@ -397,9 +399,21 @@ typedef struct qsfm_indexer_params {
  * 128, mask_mode 0, cmp_ratio 1, layout BSND, all pointers NULL. */
 void qsfm_indexer_params_init(qsfm_indexer_params* p);
 
-/* The indexer's top-k. Errors: QSFM_ERR_INVALID_ARG (missing or misaligned
- * pointers, bad attributes), QSFM_ERR_UNSUPPORTED (shapes not built). */
-qsfm_status qsfm_lightning_indexer(const qsfm_indexer_params* p, void* stream);
+/* Bytes of device workspace qsfm_lightning_indexer() needs for p: one fp32
+ * score row of min(32768, max_blocks * 128) entries per query row. Reads
+ * no device memory. Errors as qsfm_lightning_indexer() for the attributes. */
+qsfm_status qsfm_lightning_indexer_workspace_size(const qsfm_indexer_params* p, size_t* bytes);
+
+/* The indexer's top-k: a score kernel writes every visible key's score into
+ * the workspace, a select kernel then lists each row's top-k. workspace:
+ * caller-owned device memory, 16-byte aligned, of at least
+ * qsfm_lightning_indexer_workspace_size() bytes, not read before it is
+ * written. Asynchronous on `stream`, no allocation, nothing read back.
+ * Errors: QSFM_ERR_INVALID_ARG (missing or misaligned pointers, bad
+ * attributes), QSFM_ERR_UNSUPPORTED (shapes not built), QSFM_ERR_WORKSPACE
+ * (workspace NULL, misaligned or too small). */
+qsfm_status qsfm_lightning_indexer(const qsfm_indexer_params* p, void* workspace, size_t workspace_bytes,
+                                   void* stream);
 
 /* Synchronously read and clear the device fault word of the current
  * device (QSFM_FAULT_* bits). Returns QSFM_ERR_DEVICE_FAULT when non-zero. */
@@ -407,6 +421,11 @@ qsfm_status qsfm_get_device_status(int32_t* fault_word);
 
 const char* qsfm_status_string(qsfm_status s);
 int32_t qsfm_abi_version(void);
+
+/* The CUDA runtime error code behind the last QSFM_ERR_CUDA an entry point
+ * returned on the calling host thread (0 if none), and its name in *name
+ * when name is not NULL (a static string). Not cleared by later calls. */
+int32_t qsfm_last_cuda_error(const char** name);
 
 #ifdef __cplusplus
 }

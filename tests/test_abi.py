@@ -39,7 +39,7 @@ def test_every_declared_function_is_exported(lib):
     assert set(names) <= set(Q.EXPORTS)
     # version 2 appended qsfm_params.kv_layout, version 3 the KV storage layouts and ori
     # picks, version 4 the lightning indexer's entry points
-    assert lib.qsfm_abi_version() == 4
+    assert lib.qsfm_abi_version() == 5
 
 
 def test_exports_are_c_symbols(lib):
@@ -364,11 +364,51 @@ def test_indexer_rejects_invalid_arguments(lib, why, change, code):
     p = _indexer_valid(lib)
     for k, v in change.items():
         setattr(p, k, v)
-    assert lib.qsfm_lightning_indexer(ctypes.byref(p), None) == code
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), 0x1000, 1 << 30, None) == code
+
+
+def _indexer_ws(lib, p):
+    n = ctypes.c_size_t(0)
+    assert lib.qsfm_lightning_indexer_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    return n.value
+
+
+def test_indexer_workspace_size(lib):
+    """One fp32 row of min(32768, max_blocks * 128) scores per query row."""
+    p = _indexer_valid(lib)
+    assert _indexer_ws(lib, p) == 2 * 4 * 128 * 4
+    p.max_blocks, p.batch, p.max_s1 = 1000, 3, 2
+    assert _indexer_ws(lib, p) == 6 * 32768 * 4
+    p.layout_q, p.total_t, p.cu_seqlens_q = 1, 5, 0x1000
+    assert _indexer_ws(lib, p) == 5 * 32768 * 4
+    p.heads = 0
+    assert lib.qsfm_lightning_indexer_workspace_size(ctypes.byref(p), ctypes.byref(ctypes.c_size_t())) == 1
+    assert lib.qsfm_lightning_indexer_workspace_size(ctypes.byref(p), None) == 1
+
+
+def test_indexer_rejects_missing_or_small_workspace(lib):
+    p = _indexer_valid(lib)
+    need = _indexer_ws(lib, p)
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), None, need, None) == 4
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), 0x1000, need - 1, None) == 4
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), 0x1008, need, None) == 4
+
+
+def test_indexer_rejects_too_many_query_rows(lib):
+    p = _indexer_valid(lib)
+    p.batch, p.max_s1 = 1 << 11, 1 << 10
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), 0x1000, 1 << 40, None) == 2
 
 
 def test_indexer_empty_call_is_ok(lib):
     p = _indexer_valid(lib)
     p.batch = 0
-    assert lib.qsfm_lightning_indexer(ctypes.byref(p), None) == 0
-    assert lib.qsfm_lightning_indexer(None, None) == 1
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), None, 0, None) == 0
+    assert lib.qsfm_lightning_indexer(None, None, 0, None) == 1
+
+
+def test_last_cuda_error_starts_clear(lib):
+    name = ctypes.c_char_p()
+    assert lib.qsfm_last_cuda_error(ctypes.byref(name)) == 0
+    assert name.value == b"cudaSuccess"
+    assert lib.qsfm_last_cuda_error(None) == 0
