@@ -233,10 +233,11 @@ __device__ __forceinline__ bool ix_next(const qsfm_indexer_params& p, int T, int
   return false;
 }
 
-// Order-preserving 32-bit key of a score (-0 taken as +0).
+// Order-preserving 32-bit key of a score (-0 taken as +0 by adding +0):
+// non-negative scores get the sign bit set, negative ones are inverted.
 __device__ __forceinline__ uint32_t score_key(float f) {
-  uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t u = __float_as_uint(f + 0.f);
+  return u ^ (uint32_t(int32_t(u) >> 31) | 0x80000000u);
 }
 
 // Exclusive prefix sum of v over the block's NT threads (scratch: 64 ints),
@@ -614,18 +615,28 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelBins = 4096;  // 12-bit digits
 constexpr int kSelBoundary = 256;  // boundary-bin keys ranked directly (more: further radix passes)
+constexpr int kSelCand = 8192;     // keys >= the lower bound listed in shared memory (more: register passes)
+
+// select kernel shared memory: histogram (later the tie bitmap or the
+// boundary list), selected-key bitmap, candidate keys and indices, scratch
+constexpr size_t kSelSmem = size_t(kSelBins) * 4 + size_t(kIxMaxKeys / 32) * 4 + size_t(kSelCand) * 8 + 128 * 4;
 
 // One CTA per query token. Thread tid keeps the keys of score groups
 // q = tid + 512 i (i < V; four keys 4q .. 4q+3 each) in registers, so a row
-// of up to 2048 V scores is read from the workspace once and every later
-// pass is over registers. Absent keys (past the row) are 0, below every
-// score's key.
+// of up to 2048 V scores is read from the workspace once. Absent keys (past
+// the row) are 0, below every score's key. The keys at or above a lower
+// bound of the k-th largest (about a fifth of a long row) are then listed
+// in shared memory, and every later pass runs over that list (over the
+// registers when the list would overflow).
 template <int V>
 __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
     ix_select_kernel(const qsfm_indexer_params p, const IxShape x, const float* ws, int* fault) {
-  __shared__ int hist[kSelBins];             // radix histogram, then the tie bitmap
-  __shared__ uint32_t bits[kIxMaxKeys / 32];  // selected keys
-  __shared__ int scratch[128];
+  extern __shared__ uint4 sel_smem[];
+  int* hist = reinterpret_cast<int*>(sel_smem);                  // radix histogram, then tie bitmap / list
+  uint32_t* bits = reinterpret_cast<uint32_t*>(hist + kSelBins);  // [kIxMaxKeys / 32] selected keys
+  uint32_t* ckey = bits + kIxMaxKeys / 32;                       // [kSelCand] candidate keys
+  int* cidx = reinterpret_cast<int*>(ckey + kSelCand);           // [kSelCand] their indices
+  int* scratch = cidx + kSelCand;                                // [128]
   uint32_t* uscr = reinterpret_cast<uint32_t*>(scratch);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t = blockIdx.x;
@@ -664,15 +675,22 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int j = 4 * (tid + kSelThreads * i);
-    u[i][0] = j < nv ? score_key(f[i].x) : 0u;
-    u[i][1] = j + 1 < nv ? score_key(f[i].y) : 0u;
-    u[i][2] = j + 2 < nv ? score_key(f[i].z) : 0u;
-    u[i][3] = j + 3 < nv ? score_key(f[i].w) : 0u;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      tmax = max(tmax, u[i][e]);
-      if (j + e < nv) kmin = min(kmin, u[i][e]);
+    if (j + 3 < nv) {  // a whole group
+      u[i][0] = score_key(f[i].x);
+      u[i][1] = score_key(f[i].y);
+      u[i][2] = score_key(f[i].z);
+      u[i][3] = score_key(f[i].w);
+      kmin = min(kmin, min(min(u[i][0], u[i][1]), min(u[i][2], u[i][3])));
+    } else {  // the row's last, partial group, or none
+      u[i][0] = j < nv ? score_key(f[i].x) : 0u;
+      u[i][1] = j + 1 < nv ? score_key(f[i].y) : 0u;
+      u[i][2] = j + 2 < nv ? score_key(f[i].z) : 0u;
+      u[i][3] = j + 3 < nv ? score_key(f[i].w) : 0u;
+      if (j < nv) kmin = min(kmin, u[i][0]);
+      if (j + 1 < nv) kmin = min(kmin, u[i][1]);
+      if (j + 2 < nv) kmin = min(kmin, u[i][2]);
     }
+    tmax = max(tmax, max(max(u[i][0], u[i][1]), max(u[i][2], u[i][3])));
   }
   for (int i = tid; i < nw; i += kSelThreads) bits[i] = 0u;
   {
@@ -703,17 +721,39 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
   const uint32_t kmax = uscr[101];
   const uint32_t lo = k <= min(kSelThreads, n4) ? uscr[102] : uscr[100];
 
-  // 2. Radix select of the k-th largest key among the keys >= lo (it is one
-  // of them). They share the bits of lo and kmax above the highest bit where
-  // those two differ; the digits (12 bits at most) start below. A key >= lo
-  // is taken when its bits under `mask` beat `prefix`, or equal it and it is
-  // among the first `need` such keys (by score, then key index); `eq` counts
-  // those equal to the prefix. Passes stop once the boundary bin is taken
-  // whole or holds few enough keys to rank directly.
+  // 2. The candidates (keys >= lo, among them the k-th largest), listed in
+  // thread order when they fit.
+  int mine = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mine += u[i][e] >= lo;
+  int ncand = 0;
+  int off = block_exclusive_scan<kSelThreads>(mine, tid, scratch, ncand);
+  const bool listed = ncand <= kSelCand;
+  if (listed) {
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (u[i][e] >= lo) {
+          ckey[off] = u[i][e];
+          cidx[off] = 4 * (tid + kSelThreads * i) + e;
+          ++off;
+        }
+  }
+
+  // 3. Radix select of the k-th largest candidate. The candidates share the
+  // bits of lo and kmax above the highest bit where those two differ; the
+  // digits (12 bits at most) start below. A candidate is taken when its bits
+  // under `mask` beat `prefix`, or equal it and it is among the first `need`
+  // such (by score, then key index); `eq` counts those equal to the prefix.
+  // Passes stop once the boundary bin is taken whole or holds few enough
+  // candidates to rank directly.
   uint32_t mask, prefix;
   int need, eq = -1;  // -1: not counted
   const uint32_t diff = lo ^ kmax;
-  if (diff == 0u) {  // every key >= lo is equal: the first k of them
+  if (diff == 0u) {  // every candidate is equal: the first k of them
     mask = 0xffffffffu;
     prefix = kmax;
     need = k;
@@ -721,18 +761,25 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
     int nbits = 32 - __clz(diff);
     mask = nbits == 32 ? 0u : ~((1u << nbits) - 1u);
     prefix = kmax & mask;
-    int remaining = k;  // of the keys matching the prefix, the rank wanted
+    int remaining = k;  // of the candidates matching the prefix, the rank wanted
     while (nbits > 0) {
       const int d = min(12, nbits), shift = nbits - d, nb = 1 << d;
       for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
       __syncthreads();
-#pragma unroll
-      for (int i = 0; i < V; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t v = u[i][e];
-          if (v >= lo && (v & mask) == prefix) atomicAdd(&hist[(v >> shift) & uint32_t(nb - 1)], 1);
+      if (listed) {
+        for (int c = tid; c < ncand; c += kSelThreads) {
+          const uint32_t v = ckey[c];
+          if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & uint32_t(nb - 1)], 1);
         }
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t v = u[i][e];
+            if (v >= lo && (v & mask) == prefix) atomicAdd(&hist[(v >> shift) & uint32_t(nb - 1)], 1);
+          }
+      }
       __syncthreads();
       // thread i sums bins nb-1-i*per down to nb-i*per-per (largest first)
       const int per = (nb + kSelThreads - 1) / kSelThreads;
@@ -748,7 +795,7 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
           const int c = hist[top - q];
           if (acc + c >= remaining) {
             scratch[96] = top - q;
-            scratch[97] = acc;  // keys in larger bins
+            scratch[97] = acc;  // candidates in larger bins
             scratch[98] = c;
             break;
           }
@@ -767,41 +814,44 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
     need = remaining;
   }
 
-  // 3. Mark the selected keys: every key >= lo above the prefix; the equal
+  // 4. Mark the selected keys: every candidate above the prefix; the equal
   // ones too when all of them are taken. Otherwise a few equal ones are
   // listed and ranked (score, then key index) directly; many (ties past the
   // k-th) go through a tie bitmap in key order.
   const bool all_eq = eq == need;
-  const bool listed = !all_eq && eq >= 0 && eq <= kSelBoundary;
-  uint32_t* tbits = reinterpret_cast<uint32_t*>(hist);   // kcap / 32 <= 1024 words
-  uint32_t* lkey = reinterpret_cast<uint32_t*>(hist);    // listed keys [256]
-  int* lidx = hist + kSelBoundary;                       // and their indices [256]
-  if (!all_eq && !listed)
+  const bool few = !all_eq && eq >= 0 && eq <= kSelBoundary;
+  uint32_t* tbits = reinterpret_cast<uint32_t*>(hist);  // kcap / 32 <= 1024 words
+  uint32_t* lkey = reinterpret_cast<uint32_t*>(hist);   // boundary keys [256]
+  int* lidx = hist + kSelBoundary;                      // and their indices [256]
+  if (!all_eq && !few)
     for (int i = tid; i < nw; i += kSelThreads) tbits[i] = 0u;
-  if (tid == 0) scratch[99] = 0;  // listed count
+  if (tid == 0) scratch[99] = 0;  // boundary count
   __syncthreads();
-#pragma unroll
-  for (int i = 0; i < V; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t v = u[i][e];
-      const int j = 4 * (tid + kSelThreads * i) + e;
-      if (v < lo) continue;
-      const uint32_t hv = v & mask;
-      if (hv > prefix || (hv == prefix && all_eq)) {
-        atomicOr(&bits[j >> 5], 1u << (j & 31));
-      } else if (hv == prefix) {
-        if (listed) {
-          const int slot = atomicAdd(&scratch[99], 1);  // < eq <= 256
-          lkey[slot] = v;
-          lidx[slot] = j;
-        } else {
-          atomicOr(&tbits[j >> 5], 1u << (j & 31));
-        }
+  auto mark = [&](uint32_t v, int j) {
+    const uint32_t hv = v & mask;
+    if (hv > prefix || (hv == prefix && all_eq)) {
+      atomicOr(&bits[j >> 5], 1u << (j & 31));
+    } else if (hv == prefix) {
+      if (few) {
+        const int slot = atomicAdd(&scratch[99], 1);  // < eq <= 256
+        lkey[slot] = v;
+        lidx[slot] = j;
+      } else {
+        atomicOr(&tbits[j >> 5], 1u << (j & 31));
       }
     }
+  };
+  if (listed) {
+    for (int c = tid; c < ncand; c += kSelThreads) mark(ckey[c], cidx[c]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (u[i][e] >= lo) mark(u[i][e], 4 * (tid + kSelThreads * i) + e);
+  }
   __syncthreads();
-  if (listed) {  // warp w ranks listed keys w, w + 16, ...: larger first, then smaller index
+  if (few) {  // warp w ranks boundary keys w, w + 16, ...: larger first, then smaller index
     for (int c = warp; c < eq; c += kSelWarps) {
       const uint32_t v = lkey[c];
       const int j = lidx[c];
@@ -829,7 +879,7 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
     __syncthreads();
   }
 
-  // 4. The marked keys in ascending order: thread i owns words 2i, 2i + 1.
+  // 5. The marked keys in ascending order: thread i owns words 2i, 2i + 1.
   const int w0 = 2 * tid;
   const uint32_t b0 = w0 < nw ? bits[w0] : 0u, b1 = w0 + 1 < nw ? bits[w0 + 1] : 0u;
   int tot = 0;
@@ -847,7 +897,11 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
 template <int V>
 cudaError_t launch_select(const qsfm_indexer_params& p, const IxShape& x, const float* ws, int* fault,
                           cudaStream_t s) {
-  return launch_after_predecessor(ix_select_kernel<V>, dim3(x.T), dim3(kSelThreads), 0, s, p, x, ws, fault);
+  const cudaError_t e =
+      cudaFuncSetAttribute(ix_select_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSelSmem));
+  if (e != cudaSuccess) return e;
+  return launch_after_predecessor(ix_select_kernel<V>, dim3(x.T), dim3(kSelThreads), kSelSmem, s, p, x, ws,
+                                  fault);
 }
 
 // ------------------------------------------------------------- host side
