@@ -404,6 +404,15 @@ __device__ void ix_mma(const qsfm_indexer_params& p, const IxShape& x, const IxS
   }
 }
 
+// (s0, s1) += (c0, c1) * (r0, r1): two fp32 FMAs in one packed instruction
+// (each lane rounds as fmaf does).
+__device__ __forceinline__ void fma2(float& s0, float& s1, float c0, float c1, float r0, float r1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 d, {%0, %1};\n"
+      " fma.rn.f32x2 d, a, b, d;\n mov.b64 {%0, %1}, d;\n}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(c0), "f"(c1), "f"(r0), "f"(r1));
+}
+
 // Score of one key for one token from its hp accumulator columns at taddr:
 // with non-negative scales W ReLU(Sq Sk x) = Sk (W Sq) ReLU(x), the head
 // factors cw = W * Sq (0 past the real heads, whose columns hold 0 from the
@@ -424,10 +433,8 @@ __device__ __forceinline__ float ix_key_score(const qsfm_indexer_params& p, uint
 #pragma unroll
         for (int h = 0; h < 32; h += 4) {
           const float4 c = c4[h >> 2];
-          s0 = fmaf(c.x, fmaxf(0.f, v[h]), s0);
-          s1 = fmaf(c.y, fmaxf(0.f, v[h + 1]), s1);
-          s2 = fmaf(c.z, fmaxf(0.f, v[h + 2]), s2);
-          s3 = fmaf(c.w, fmaxf(0.f, v[h + 3]), s3);
+          fma2(s0, s1, c.x, c.y, fmaxf(0.f, v[h]), fmaxf(0.f, v[h + 1]));
+          fma2(s2, s3, c.z, c.w, fmaxf(0.f, v[h + 2]), fmaxf(0.f, v[h + 3]));
         }
       } else {
 #pragma unroll
