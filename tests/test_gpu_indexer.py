@@ -140,3 +140,34 @@ def test_indexer_bad_block_is_reported_not_read(cuda_device):
     assert Q.device_status() & Q.FAULT_CMP_BLOCK_ID
     row = idx[0]
     assert np.all((row < 128) | (row >= 256))  # the bad block's keys are never picked
+
+
+@pytest.mark.parametrize("sk,topk", [([6000, 2000], 300), ([700, 90], 64)])
+def test_indexer_groups_of_equal_scores(cuda_device, sk, topk):
+    """Every key is one of 16 distinct rows (same bytes, same scale), so each
+    token's scores take at most 16 values and the k-th largest falls inside a
+    group of equal scores: the smaller key indices of that group are taken.
+    Large groups go through the full-depth radix and the tie bitmap, small
+    ones through the ranked boundary list."""
+    w = W.build_indexer("dups", layout="BSND", q_lens=[2, 2], sk=sk, topk=topk, mask_mode=3, cmp_ratio=4, seed=12)
+    flat = w.key.reshape(-1, w.key.shape[-1])
+    fs = w.key_scale.reshape(-1)
+    src = torch.arange(flat.shape[0]) % 16
+    flat.copy_(flat[src].clone())
+    fs.copy_(fs[src].clone())
+    idx, val = run(w, cuda_device)
+    assert Q.device_status() == 0
+    ref_i, _ = I.reference(w)
+    assert np.array_equal(idx, ref_i)
+    check(w, idx, val)
+
+
+def test_indexer_keys_past_the_table_are_cut_and_flagged(cuda_device):
+    """seqused_k larger than the block table holds: the row is cut to the
+    table's keys (max_blocks * 128) and QSFM_FAULT_CMP_TABLE_COL is raised."""
+    w = W.build_indexer("cut", layout="BSND", q_lens=[1], sk=[500], topk=16, mask_mode=0, seed=13)
+    w.seqused_k[0] = 900  # the table holds 4 blocks = 512 keys
+    idx, _ = run(w, cuda_device, return_value=False)
+    assert Q.device_status() & Q.FAULT_CMP_TABLE_COL
+    row = idx[0]
+    assert np.all((row >= 0) & (row < 512))
