@@ -1036,6 +1036,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     resolver_role<kFmt>(p, sm, rg, T, fault);
   }
 
+  // Roles run on single lanes (the MMA issue): each warp's lanes meet before
+  // the barrier (a barrier reached by part of a warp counts the whole warp).
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {

@@ -609,6 +609,9 @@ __global__ void __maxnreg__(96)
     volatile int never = 0;
     if (!mbar_wait_poll(smem_u32(sm.bar(kXbDrain)), 0, &never, kIxTimeoutNs)) atomicOr(fault, QSFM_FAULT_TIMEOUT);
   }
+  // The MMA warp ran on one lane: its lanes meet before the barrier (a
+  // barrier reached by part of a warp counts the whole warp).
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
