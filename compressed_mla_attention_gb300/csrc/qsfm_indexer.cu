@@ -631,6 +631,26 @@ constexpr int kSelCand = 8192;     // keys >= the lower bound listed in shared m
 // boundary list), selected-key bitmap, candidate keys and indices, scratch
 constexpr size_t kSelSmem = size_t(kSelBins) * 4 + size_t(kIxMaxKeys / 32) * 4 + size_t(kSelCand) * 8 + 128 * 4;
 
+// Exclusive prefix sum over the select's 512 threads with one barrier. The
+// warp totals go to half `par` of scr[0..31]; consecutive calls alternate
+// halves, so a call never overwrites totals that a warp may still be reading
+// from the call before (every warp has passed this call's barrier first).
+__device__ __forceinline__ int sel_scan(int v, int tid, int* scr, int par, int& total) {
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  int* tot = scr + 16 * par;
+  if (lane == 31) tot[warp] = incl;
+  __syncthreads();
+  const int wt = lane < kSelWarps ? tot[lane] : 0;
+  total = __reduce_add_sync(0xffffffffu, wt);
+  return __reduce_add_sync(0xffffffffu, lane < warp ? wt : 0) + incl - v;
+}
+
 // One CTA per query token. Thread tid keeps the keys of score groups
 // q = tid + 512 i (i < V; four keys 4q .. 4q+3 each) in registers, so a row
 // of up to 2048 V scores is read from the workspace once. Absent keys (past
@@ -703,6 +723,8 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
     tmax = max(tmax, max(max(u[i][0], u[i][1]), max(u[i][2], u[i][3])));
   }
   for (int i = tid; i < nw; i += kSelThreads) bits[i] = 0u;
+  if (tid == 0) scratch[99] = 0;  // candidate count
+  int sp = 0;                     // scan parity (sel_scan)
   {
     const uint32_t a = __reduce_min_sync(0xffffffffu, kmin);
     const uint32_t c = __reduce_max_sync(0xffffffffu, tmax);
@@ -732,26 +754,39 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
   const uint32_t lo = k <= min(kSelThreads, n4) ? uscr[102] : uscr[100];
 
   // 2. The candidates (keys >= lo, among them the k-th largest), listed in
-  // thread order when they fit.
+  // any order: each warp takes one slot range (a warp scan and one shared
+  // atomic); what does not fit is not written, and then the later passes
+  // run over the registers.
   int mine = 0;
 #pragma unroll
   for (int i = 0; i < V; ++i)
 #pragma unroll
     for (int e = 0; e < 4; ++e) mine += u[i][e] >= lo;
-  int ncand = 0;
-  int off = block_exclusive_scan<kSelThreads>(mine, tid, scratch, ncand);
-  const bool listed = ncand <= kSelCand;
-  if (listed) {
+  {
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int base = 0;
+    if (lane == 31 && incl > 0) base = atomicAdd(&scratch[99], incl);
+    int off = __shfl_sync(0xffffffffu, base, 31) + incl - mine;
 #pragma unroll
     for (int i = 0; i < V; ++i)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         if (u[i][e] >= lo) {
-          ckey[off] = u[i][e];
-          cidx[off] = 4 * (tid + kSelThreads * i) + e;
+          if (off < kSelCand) {
+            ckey[off] = u[i][e];
+            cidx[off] = 4 * (tid + kSelThreads * i) + e;
+          }
           ++off;
         }
   }
+  __syncthreads();
+  const int ncand = scratch[99];
+  const bool listed = ncand <= kSelCand;
 
   // 3. Radix select of the k-th largest candidate. The candidates share the
   // bits of lo and kmax above the highest bit where those two differ; the
@@ -798,7 +833,8 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
       for (int q = 0; q < per; ++q)
         if (top - q >= 0) sum += hist[top - q];
       int tot = 0;
-      const int ex = block_exclusive_scan<kSelThreads>(sum, tid, scratch, tot);
+      const int ex = sel_scan(sum, tid, scratch, sp, tot);
+      sp ^= 1;
       if (ex < remaining && remaining <= ex + sum) {  // exactly one thread
         int acc = ex;
         for (int q = 0; q < per; ++q) {
@@ -835,7 +871,7 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
   int* lidx = hist + kSelBoundary;                      // and their indices [256]
   if (!all_eq && !few)
     for (int i = tid; i < nw; i += kSelThreads) tbits[i] = 0u;
-  if (tid == 0) scratch[99] = 0;  // boundary count
+  if (tid == 0) scratch[95] = 0;  // boundary count (scratch[99] still holds the candidate count)
   __syncthreads();
   auto mark = [&](uint32_t v, int j) {
     const uint32_t hv = v & mask;
@@ -843,7 +879,7 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
       atomicOr(&bits[j >> 5], 1u << (j & 31));
     } else if (hv == prefix) {
       if (few) {
-        const int slot = atomicAdd(&scratch[99], 1);  // < eq <= 256
+        const int slot = atomicAdd(&scratch[95], 1);  // < eq <= 256
         lkey[slot] = v;
         lidx[slot] = j;
       } else {
@@ -878,7 +914,8 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
     const int w0 = 2 * tid;
     const uint32_t t0 = w0 < nw ? tbits[w0] : 0u, t1 = w0 + 1 < nw ? tbits[w0 + 1] : 0u;
     int tot = 0;
-    int r = block_exclusive_scan<kSelThreads>(__popc(t0) + __popc(t1), tid, scratch, tot);
+    int r = sel_scan(__popc(t0) + __popc(t1), tid, scratch, sp, tot);
+    sp ^= 1;
     const uint32_t m[2] = {t0, t1};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -893,7 +930,7 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
   const int w0 = 2 * tid;
   const uint32_t b0 = w0 < nw ? bits[w0] : 0u, b1 = w0 + 1 < nw ? bits[w0 + 1] : 0u;
   int tot = 0;
-  int pos = block_exclusive_scan<kSelThreads>(__popc(b0) + __popc(b1), tid, scratch, tot);
+  int pos = sel_scan(__popc(b0) + __popc(b1), tid, scratch, sp, tot);
   const uint32_t m[2] = {b0, b1};
 #pragma unroll
   for (int h = 0; h < 2; ++h)
