@@ -494,6 +494,87 @@ def run_indexer(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_pipeline(args, rank, world, local):
+    """The CSA decode step with its index rows made on the device (the CSA
+    decode batch): per step the lightning indexer (score and select kernels)
+    writes the index rows into the buffer the attention reads as
+    cmp_sparse_indices, then the plan and the attention run on them. K timed
+    steps after W warm-up steps, L2 flushed between steps outside the CUDA
+    events on the launching stream; a second pass with events between the
+    stages gives the indexer / plan + attention split."""
+    import compressed_mla_attention_gb300 as Q
+    from compressed_mla_attention_gb300 import build
+
+    build.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = W.config(2)
+    wi = W.indexer_for(w, seed=2)
+    a = W.device_inputs(w, dev)
+    a.pop("return_softmax_lse")
+    ai = W.indexer_device_inputs(wi, dev)
+    idx = torch.empty(w.total_t, 1, w.k2, dtype=torch.int32, device=dev)
+    a["cmp_sparse_indices"] = idx
+    ixws = torch.empty(w.total_t * 32768 * 4 + 4096, dtype=torch.uint8, device=dev)  # the largest score rows
+    out = torch.empty_like(a["q"])
+    plan = torch.empty(1024, dtype=torch.int32, device=dev)
+    p = Q.make_params(attn_out=out, metadata=plan, num_ctas=args.ctas, **a)
+    ws_bytes = Q.workspace_size(p)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    split = ws_bytes > 0
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        Q.lightning_indexer(ai["query"], ai["query_scale"], ai["weights"], ai["key"], ai["key_scale"],
+                            ai["block_table"], ai["seqused_k"], layout=wi.layout, batch=wi.batch,
+                            cmp_residual_k=ai["cmp_residual_k"], topk=wi.topk, mask_mode=wi.mask_mode,
+                            cmp_ratio=wi.cmp_ratio, out=idx, workspace=ixws, stream=stream)
+        if ev is not None:
+            ev.record(stream)
+        Q.metadata(p, plan, stream)
+        Q.attention(p, ws, stream)
+        if split:
+            Q.combine(p, ws, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if Q.device_status() != 0:
+        raise RuntimeError("device fault during the pipeline warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        evs[k][0].record(stream)
+        step()
+        evs[k][2].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(e[0].elapsed_time(e[2]) for e in evs)
+    for k in range(args.steps):
+        flush.zero_()
+        evs[k][0].record(stream)
+        step(evs[k][1])
+        evs[k][2].record(stream)
+    torch.cuda.synchronize()
+    if Q.device_status() != 0:
+        raise RuntimeError("device fault during the timed pipeline steps")
+    ms_ix = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms_att = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    line = {
+        "metric": "CSA decode step with device-made index rows: query-tokens/s (indexer 64 heads top-512, "
+                  "attention 64 heads D=512)",
+        "value": w.total_t / (ms / 1e3), "unit": "query-tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 indexer, f16 attention operands", "data": "synthetic",
+        "config": {"workload": w.name, "indexer": wi.name, "query_tokens": w.total_t,
+                   "l2": "flushed between steps (512 MiB write, outside the timed events)"},
+        "stage_ms": {"indexer": ms_ix, "plan_attention_combine": ms_att},
+        "gpu_launches": args.steps * (2 + (3 if split else 2)),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -509,6 +590,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--indexer", action="store_true",
                     help="time the lightning-indexer top-k on the call that feeds the CSA decode batch")
+    ap.add_argument("--pipeline", action="store_true",
+                    help="time the CSA decode step with its index rows made by the lightning indexer on the device")
     ap.add_argument("--profile-size", action="store_true",
                     help="the CSA decode batch with S2 ~ U[4K, 8K] (for ncu captures)")
     args = ap.parse_args()
@@ -524,6 +607,10 @@ def main():
     if args.indexer:
         if args.impl == "qsfm":
             run_indexer(args, rank, world, local)
+        return
+    if args.pipeline:
+        if args.impl == "qsfm":
+            run_pipeline(args, rank, world, local)
         return
     w = W.profile_case() if args.profile_size else W.config(args.workload, kv_format=args.kv_format,
                                                              n1=args.n1)

@@ -552,7 +552,7 @@ def _quantize_rows_e4m3(x: torch.Tensor):
 
 def build_indexer(name: str, *, layout: str, q_lens, sk, heads: int = 64, dim: int = 128, topk: int = 512,
                   mask_mode: int = 3, cmp_ratio: int = 4, with_residual: bool = True,
-                  seqused_q: Optional[list] = None, seed: int = 0) -> IndexerWorkload:
+                  seqused_q: Optional[list] = None, residual=None, seed: int = 0) -> IndexerWorkload:
     """One indexer call: q_lens query tokens and sk keys per batch."""
     gen = torch.Generator().manual_seed(seed)
     q_lens = np.asarray(q_lens, dtype=np.int64)
@@ -579,7 +579,9 @@ def build_indexer(name: str, *, layout: str, q_lens, sk, heads: int = 64, dim: i
     else:
         assert len(set(q_lens.tolist())) <= 1, "BSND needs equal S1"
     res = None
-    if with_residual and mask_mode == 3:
+    if residual is not None:
+        res = torch.as_tensor(np.asarray(residual), dtype=torch.int32).clone()
+    elif with_residual and mask_mode == 3:
         res = torch.from_numpy((torch.randint(0, cmp_ratio, (B,), generator=gen)).numpy().astype(np.int32))
     return IndexerWorkload(
         name=name, layout=layout, batch=B, q_lens=q_lens, cu_seqlens_q=cu, query=query, query_scale=qscale,
@@ -587,6 +589,26 @@ def build_indexer(name: str, *, layout: str, q_lens, sk, heads: int = 64, dim: i
         block_table=table, seqused_k=torch.from_numpy(sk.astype(np.int32)), cmp_residual_k=res,
         seqused_q=torch.tensor(seqused_q, dtype=torch.int32) if seqused_q is not None else None,
         topk=topk, mask_mode=mask_mode, cmp_ratio=cmp_ratio, seed=seed)
+
+
+def indexer_for(w: "Workload", seed: int = 0, heads: int = 64) -> IndexerWorkload:
+    """The indexer call that produces a CSA workload's index rows: the same
+    batches, query chunks, layout and padded query rows; one index key per
+    compressed row of the workload (seqused_k = its compressed length, the
+    generator's own s2 // cmp_ratio when the workload leaves it implicit),
+    paged in a pool of its own; the same residual, ratio and causal mask 3;
+    topk = the index row width K2. Its rows can be passed as the workload's
+    cmp_sparse_indices."""
+    if w.seqused_cmp_kv is not None:
+        sk = np.asarray(w.seqused_cmp_kv, dtype=np.int64)
+    else:
+        sk = np.asarray(w.seqused_ori_kv, dtype=np.int64) // w.cmp_ratio
+    res = (np.asarray(w.cmp_residual_kv, dtype=np.int64) if w.cmp_residual_kv is not None
+           else np.zeros(w.batch, dtype=np.int64))
+    used_q = None if w.seqused_q is None else np.asarray(w.seqused_q).tolist()
+    return build_indexer(f"indexer for {w.name}", layout=w.layout, q_lens=w.q_lens, sk=sk, heads=heads,
+                         topk=w.k2, mask_mode=3, cmp_ratio=w.cmp_ratio, seqused_q=used_q, residual=res,
+                         seed=seed)
 
 
 def indexer_decode_batch(seed: int = 2) -> IndexerWorkload:
