@@ -255,8 +255,7 @@ qsfm_status check_indexer(const qsfm_indexer_params* pp, long long* T) {
   if (p.layout_q == QSFM_LAYOUT_BSND) {
     if (p.max_s1 < 0 || p.cu_seqlens_q != nullptr) return QSFM_ERR_INVALID_ARG;
   } else if (p.layout_q == QSFM_LAYOUT_TND) {
-    if (p.total_t < 0 || (p.cu_seqlens_q == nullptr && p.batch > 0) || p.seqused_q != nullptr)
-      return QSFM_ERR_INVALID_ARG;
+    if (p.total_t < 0 || (p.cu_seqlens_q == nullptr && p.batch > 0)) return QSFM_ERR_INVALID_ARG;
   } else {
     return QSFM_ERR_INVALID_ARG;
   }

@@ -355,7 +355,10 @@ qsfm_status qsfm_debug_bounded_wait(uint64_t timeout_ns, uint64_t* elapsed_ns_ou
  *   key_scale    fp32 [num_blocks, 128, 1], paged like key
  *   block_table  int32 [B, max_blocks];  seqused_k int32 [B] (required)
  *   cmp_residual_k int32 [B] or NULL (0);  cu_seqlens_q int32 [B + 1]
- *                (required for TND);  seqused_q int32 [B] or NULL (BSND)
+ *                (required for TND);  seqused_q int32 [B] or NULL: query
+ *                rows of batch b from seqused_q[b] on are padding (all -1;
+ *                the other rows keep their positions, S1_b being the chunk
+ *                length of the layout), for BSND and TND alike
  *   sparse_indices int32 [T, 1, topk] (out)
  *   sparse_values  bf16 [T, 1, topk] (out, written when return_value != 0;
  *                the scores of the listed keys, -inf after them)

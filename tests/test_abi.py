@@ -350,7 +350,6 @@ INDEXER_INVALID = [
     ("cmp_ratio 0", dict(cmp_ratio=0), 1), ("cmp_ratio 129", dict(cmp_ratio=129), 1),
     ("BSND with cu_seqlens_q", dict(cu_seqlens_q=0x1000), 1),
     ("TND without cu_seqlens_q", dict(layout_q=1, total_t=4), 1),
-    ("TND with seqused_q", dict(layout_q=1, total_t=4, cu_seqlens_q=0x1000, seqused_q=0x1000), 1),
     ("no query", dict(query=None), 1), ("no key scale", dict(key_scale=None), 1),
     ("no block table", dict(block_table=None), 1), ("no seqused_k", dict(seqused_k=None), 1),
     ("no output", dict(sparse_indices=None), 1), ("values without buffer", dict(return_value=1), 1),
@@ -398,6 +397,14 @@ def test_indexer_rejects_too_many_query_rows(lib):
     p = _indexer_valid(lib)
     p.batch, p.max_s1 = 1 << 11, 1 << 10
     assert lib.qsfm_lightning_indexer(ctypes.byref(p), 0x1000, 1 << 40, None) == 2
+
+
+def test_indexer_tnd_takes_seqused_q(lib):
+    """TND with seqused_q is TND padding (QuantLightningIndexerV2, 约束说明):
+    accepted; only the workspace check is left to fail here."""
+    p = _indexer_valid(lib)
+    p.layout_q, p.total_t, p.cu_seqlens_q, p.seqused_q = 1, 4, 0x1000, 0x1000
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), None, 0, None) == 4
 
 
 def test_indexer_empty_call_is_ok(lib):

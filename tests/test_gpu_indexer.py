@@ -96,6 +96,8 @@ CASES = {
                          heads=48),
     "padded_queries": dict(layout="BSND", q_lens=[3, 3], sk=[200, 500], topk=20, mask_mode=3, cmp_ratio=4,
                            seqused_q=[1, 3]),
+    "tnd_padding": dict(layout="TND", q_lens=[4, 2, 5], sk=[1500, 90, 4000], topk=40, mask_mode=3, cmp_ratio=4,
+                        seqused_q=[2, 2, 0], heads=32),
     "topk_8192_long": dict(layout="BSND", q_lens=[1, 1], sk=[30000, 9000], topk=8192, mask_mode=0, heads=64),
 }
 

@@ -22,6 +22,8 @@ CASES = [
     dict(layout="BSND", q_lens=[1, 1, 1], sk=[10, 0, 130], topk=32, mask_mode=0, heads=16, dim=64),
     dict(layout="TND", q_lens=[4, 2], sk=[256, 77], topk=300, mask_mode=3, cmp_ratio=128, heads=4),
     dict(layout="BSND", q_lens=[3, 3], sk=[200, 500], topk=20, mask_mode=3, cmp_ratio=4, seqused_q=[1, 3]),
+    dict(layout="TND", q_lens=[4, 2, 5], sk=[150, 90, 400], topk=24, mask_mode=3, cmp_ratio=4, seqused_q=[2, 2, 0],
+         heads=8),
 ]
 
 
