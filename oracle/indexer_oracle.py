@@ -36,7 +36,15 @@ notes of the repository):
      and fills the rest of the row with -1 (valid first, -1 after, as
      KvQuantSparseAttnSharedKv's constraints require of its indices);
      sparse_values holds their scores (bf16), -inf where the index is -1;
-  I5 a padded query row (seqused_q) gets an all -1 row.
+  I5 a padded query row (seqused_q) gets an all -1 row (BSND and TND);
+     the other rows keep their positions (p_c takes the chunk length S1_b);
+  I6 output_idx_offset, when given, is int32 [B]: every valid index of a
+     batch-b row is reported plus output_idx_offset[b]; -1 stays -1;
+  I7 layout_k: PA_BBND keys are paged through block_table (I2); BSND keys
+     [B, S_k, 1, d] hold batch b's key j at [b, j], with seqused_k[b] keys
+     (S_k when seqused_k is absent); TND keys [T_k, 1, d] hold it at
+     cu_seqlens_k[b] + j, with cu_seqlens_k[b + 1] - cu_seqlens_k[b] keys.
+     The scales follow the keys' layout without the d axis.
 """
 
 from __future__ import annotations
@@ -46,16 +54,42 @@ import numpy as np
 from oracle.qsfm_oracle import E4M3FN_TABLE, cmp_visible_count
 
 
+def key_count(w, b: int) -> int:
+    """Keys of batch b (I2, I7)."""
+    layout = getattr(w, "layout_k", "PA_BBND")
+    if layout == "TND":
+        return int(w.cu_seqlens_k[b + 1]) - int(w.cu_seqlens_k[b])
+    if layout == "BSND" and w.seqused_k is None:
+        return int(w.key.shape[1])
+    return int(w.seqused_k[b])
+
+
+def key_rows(w, b: int, v: int):
+    """Batch b's keys 0 .. v - 1: e4m3 bytes [v, d] and fp32 scales [v] (I2, I7)."""
+    layout = getattr(w, "layout_k", "PA_BBND")
+    if layout == "PA_BBND":
+        bs = int(w.key.shape[1])
+        rows = [(int(w.block_table[b, j // bs]), j % bs) for j in range(v)]
+        k = np.stack([np.asarray(w.key[blk, off, 0]) for blk, off in rows])
+        sk = np.array([float(w.key_scale[blk, off, 0]) for blk, off in rows], dtype=np.float64)
+    elif layout == "BSND":
+        k = np.asarray(w.key[b, :v, 0])
+        sk = np.asarray(w.key_scale[b, :v, 0], dtype=np.float64)
+    else:
+        base = int(w.cu_seqlens_k[b])
+        k = np.asarray(w.key[base:base + v, 0])
+        sk = np.asarray(w.key_scale[base:base + v, 0], dtype=np.float64)
+    return k, sk
+
+
 def token_scores(w, t: int) -> np.ndarray:
     """fp64 scores of every visible key of query token t (length V)."""
     b, s = int(w.token_batch()[t]), int(w.token_pos()[t])
     v = visible_keys(w, b, s)
     if v == 0:
         return np.zeros(0)
-    bs = int(w.key.shape[1])
-    rows = [(int(w.block_table[b, j // bs]), j % bs) for j in range(v)]
-    k = E4M3FN_TABLE[np.stack([np.asarray(w.key[blk, off, 0]) for blk, off in rows]).astype(np.int64)]
-    sk = np.array([float(w.key_scale[blk, off, 0]) for blk, off in rows], dtype=np.float64)
+    kb, sk = key_rows(w, b, v)
+    k = E4M3FN_TABLE[np.asarray(kb).astype(np.int64)]
     q = E4M3FN_TABLE[np.asarray(w.query[t]).astype(np.int64)]           # [g, d]
     sq = np.asarray(w.query_scale[t], dtype=np.float64)                 # [g]
     wt = np.asarray(w.weights[t], dtype=np.float64)                     # [g]
@@ -68,7 +102,7 @@ def visible_keys(w, b: int, s: int) -> int:
     """Keys query token s of batch b may select (I3, I5)."""
     if w.seqused_q is not None and s >= int(w.seqused_q[b]):
         return 0
-    sk_len = int(w.seqused_k[b])
+    sk_len = key_count(w, b)
     if w.mask_mode == 0:
         return sk_len
     s1 = int(w.q_lens[b])
@@ -92,10 +126,13 @@ def reference(w, tokens=None):
     k = int(w.topk)
     idx = np.full((len(tokens), k), -1, dtype=np.int32)
     val = np.full((len(tokens), k), -np.inf)
+    offs = getattr(w, "output_idx_offset", None)
+    tb = w.token_batch()
     for i, t in enumerate(tokens):
         sc = token_scores(w, t)
         sel = select(sc, k)
-        idx[i, :sel.size] = sel
+        off = 0 if offs is None else int(offs[int(tb[t])])
+        idx[i, :sel.size] = sel + off
         val[i, :sel.size] = sc[sel]
     return idx, val
 

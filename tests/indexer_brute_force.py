@@ -3,7 +3,8 @@ oracle (used only to pin it on small inputs).
 
 A different route to the same definition (QuantLightningIndexerV2,
 "功能说明" formula): each batch's whole key cache is materialised by
-indexing the paged key tensor with the block table and decoded with
+indexing the paged key tensor with the block table (or slicing the BSND
+slab / TND rows) and decoded with
 torch's own float8_e4m3fn type; the scores of all keys come from one
 einsum per batch, in the order the formula writes them
 ([1]_{1 x g} @ [(W @ [1]_{1 x S_k}) * ReLU((Sq @ Sk^T) * (Q @ K^T))]);
@@ -18,12 +19,26 @@ import torch
 
 
 def _cache(w, b):
-    n = int(w.seqused_k[b])
-    bs = w.key.shape[1]
-    blocks = w.block_table[b, :(n + bs - 1) // bs].long()
-    raw = w.key[blocks].reshape(-1, w.key.shape[-1])[:n]
-    sk = w.key_scale[blocks].reshape(-1)[:n].to(torch.float64)
-    return raw.contiguous().view(torch.float8_e4m3fn).to(torch.float64), sk
+    """Batch b's whole key cache, decoded: paged keys by indexing the pool
+    with the block table, BSND keys by slicing the batch's slab to seqused_k
+    (all of it when absent), TND keys by slicing rows cu_seqlens_k[b] ..
+    cu_seqlens_k[b + 1]."""
+    layout = getattr(w, "layout_k", "PA_BBND")
+    if layout == "PA_BBND":
+        n = int(w.seqused_k[b])
+        bs = w.key.shape[1]
+        blocks = w.block_table[b, :(n + bs - 1) // bs].long()
+        raw = w.key[blocks].reshape(-1, w.key.shape[-1])[:n]
+        sk = w.key_scale[blocks].reshape(-1)[:n]
+    elif layout == "BSND":
+        n = int(w.key.shape[1]) if w.seqused_k is None else int(w.seqused_k[b])
+        raw = w.key[b, :n, 0]
+        sk = w.key_scale[b, :n, 0]
+    else:
+        lo, hi = int(w.cu_seqlens_k[b]), int(w.cu_seqlens_k[b + 1])
+        raw = w.key[lo:hi, 0]
+        sk = w.key_scale[lo:hi, 0]
+    return raw.contiguous().view(torch.float8_e4m3fn).to(torch.float64), sk.to(torch.float64)
 
 
 def _visible(c, p_c, r):
@@ -59,8 +74,10 @@ def brute_force(w):
                 cand = list(range(n))
             ranked = sorted(cand, key=lambda j: (-float(scores[j]), j))[:k]
             ranked.sort()
+            offs = getattr(w, "output_idx_offset", None)
+            shift = 0 if offs is None else int(offs[b])
             for i, j in enumerate(ranked):
-                idx[t, i] = j
+                idx[t, i] = j + shift
                 val[t, i] = scores[j]
             t += 1
     return idx, val

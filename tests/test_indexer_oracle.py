@@ -24,6 +24,11 @@ CASES = [
     dict(layout="BSND", q_lens=[3, 3], sk=[200, 500], topk=20, mask_mode=3, cmp_ratio=4, seqused_q=[1, 3]),
     dict(layout="TND", q_lens=[4, 2, 5], sk=[150, 90, 400], topk=24, mask_mode=3, cmp_ratio=4, seqused_q=[2, 2, 0],
          heads=8),
+    dict(layout="BSND", q_lens=[2, 2], sk=[300, 900], topk=40, mask_mode=3, cmp_ratio=4, layout_k="BSND",
+         output_idx_offset=[1000, 5]),
+    dict(layout="TND", q_lens=[3, 1, 5], sk=[40, 700, 129], topk=50, mask_mode=3, cmp_ratio=3, heads=8,
+         layout_k="TND", output_idx_offset=[0, 40, 740]),
+    dict(layout="BSND", q_lens=[1, 1], sk=[260, 260], topk=30, mask_mode=0, layout_k="BSND", bsnd_seqused=False),
 ]
 
 
@@ -161,4 +166,47 @@ def test_largest_index_first_on_ties_is_caught(monkeypatch):
 def test_visibility_off_by_one_is_caught(monkeypatch):
     real = I.visible_keys
     monkeypatch.setattr(I, "visible_keys", lambda w, b, s: real(w, b, s) + (1 if w.mask_mode == 3 else 0))
+    assert any(_fails(p) for p in _brute_pins())
+
+
+def test_key_layouts_give_the_same_rows():
+    """The same logical keys stored paged, as BSND slabs and as TND rows
+    (the generator stores one draw three ways) give identical rows and
+    scores; an offset shifts every valid index of its batch and no -1."""
+    base = dict(layout="TND", q_lens=[3, 2], sk=[500, 140], topk=200, mask_mode=3, cmp_ratio=4, seed=40)
+    ref = I.reference(W.build_indexer("pa", **base))
+    for lk in ("BSND", "TND"):
+        got = I.reference(W.build_indexer(lk, layout_k=lk, **base))
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+    idx, _ = I.reference(W.build_indexer("off", layout_k="TND", output_idx_offset=[7, 500], **base))
+    tb = np.repeat([0, 1], [3, 2])
+    shift = np.where(ref[0] >= 0, np.array([7, 500])[tb][:, None], 0)
+    assert np.array_equal(idx, ref[0] + shift)
+
+
+def test_tnd_key_base_off_by_one_is_caught(monkeypatch):
+    real = I.key_rows
+
+    def shifted(w, b, v):
+        if getattr(w, "layout_k", "PA_BBND") == "TND" and b > 0:
+            base = int(w.cu_seqlens_k[b]) + 1
+            return np.asarray(w.key[base:base + v, 0]), np.asarray(w.key_scale[base:base + v, 0], dtype=np.float64)
+        return real(w, b, v)
+
+    monkeypatch.setattr(I, "key_rows", shifted)
+    assert any(_fails(p) for p in _brute_pins())
+
+
+def test_missing_offset_is_caught(monkeypatch):
+    real = I.reference
+
+    def no_offset(w, tokens=None):
+        saved = w.output_idx_offset
+        w.output_idx_offset = None
+        try:
+            return real(w, tokens)
+        finally:
+            w.output_idx_offset = saved
+
+    monkeypatch.setattr(I, "reference", no_offset)
     assert any(_fails(p) for p in _brute_pins())

@@ -516,16 +516,19 @@ class IndexerWorkload:
     query: torch.Tensor  # uint8 e4m3fn bytes [T, g, d]
     query_scale: torch.Tensor  # fp32 [T, g]
     weights: torch.Tensor  # fp32 [T, g]
-    key: torch.Tensor  # uint8 e4m3fn bytes [blocks, 128, 1, d]
-    key_scale: torch.Tensor  # fp32 [blocks, 128, 1]
-    block_table: torch.Tensor  # int32 [B, width]
-    seqused_k: torch.Tensor  # int32 [B]
+    key: torch.Tensor  # uint8 e4m3fn bytes: PA_BBND [blocks, 128, 1, d], BSND [B, Sk, 1, d], TND [Tk, 1, d]
+    key_scale: torch.Tensor  # fp32, the key's shape without d
+    block_table: Optional[torch.Tensor]  # int32 [B, width] (PA_BBND)
+    seqused_k: Optional[torch.Tensor]  # int32 [B] (PA_BBND; BSND, default Sk; None for TND)
     cmp_residual_k: Optional[torch.Tensor]  # int32 [B]
     seqused_q: Optional[torch.Tensor]  # int32 [B]
     topk: int
     mask_mode: int
     cmp_ratio: int
     seed: int
+    layout_k: str = "PA_BBND"  # "PA_BBND", "BSND" or "TND"
+    cu_seqlens_k: Optional[torch.Tensor] = None  # int32 [B+1] (TND keys)
+    output_idx_offset: Optional[torch.Tensor] = None  # int32 [B]
 
     @property
     def total_t(self) -> int:
@@ -534,6 +537,14 @@ class IndexerWorkload:
     @property
     def heads(self) -> int:
         return int(self.query.shape[1])
+
+    def key_len(self, b: int) -> int:
+        """Keys of batch b (a length, not a rule of the method)."""
+        if self.layout_k == "TND":
+            return int(self.cu_seqlens_k[b + 1] - self.cu_seqlens_k[b])
+        if self.seqused_k is None:
+            return int(self.key.shape[1])
+        return int(self.seqused_k[b])
 
     def token_batch(self) -> np.ndarray:
         return np.repeat(np.arange(self.batch), self.q_lens)
@@ -552,8 +563,13 @@ def _quantize_rows_e4m3(x: torch.Tensor):
 
 def build_indexer(name: str, *, layout: str, q_lens, sk, heads: int = 64, dim: int = 128, topk: int = 512,
                   mask_mode: int = 3, cmp_ratio: int = 4, with_residual: bool = True,
-                  seqused_q: Optional[list] = None, residual=None, seed: int = 0) -> IndexerWorkload:
-    """One indexer call: q_lens query tokens and sk keys per batch."""
+                  seqused_q: Optional[list] = None, residual=None, layout_k: str = "PA_BBND",
+                  bsnd_seqused: bool = True, output_idx_offset=None, seed: int = 0) -> IndexerWorkload:
+    """One indexer call: q_lens query tokens and sk keys per batch. The
+    logical keys of a batch are drawn the same way for every layout_k and
+    then stored paged (random block permutation), as BSND slabs [B, max sk]
+    (with seqused_k, or without when bsnd_seqused is False and every batch
+    fills its slab) or as TND rows with cu_seqlens_k."""
     gen = torch.Generator().manual_seed(seed)
     q_lens = np.asarray(q_lens, dtype=np.int64)
     sk = np.asarray(sk, dtype=np.int64)
@@ -583,10 +599,40 @@ def build_indexer(name: str, *, layout: str, q_lens, sk, heads: int = 64, dim: i
         res = torch.as_tensor(np.asarray(residual), dtype=torch.int32).clone()
     elif with_residual and mask_mode == 3:
         res = torch.from_numpy((torch.randint(0, cmp_ratio, (B,), generator=gen)).numpy().astype(np.int32))
+    key = key.view(total, BLOCK, 1, dim)
+    kscale = kscale.view(total, BLOCK, 1)
+    used_k = torch.from_numpy(sk.astype(np.int32))
+    cu_k = None
+    if layout_k != "PA_BBND":
+        # batch b's logical key j is the paged pool's row table[b, j // 128], j % 128
+        rows = [[(int(table[b, j // BLOCK]), j % BLOCK) for j in range(int(sk[b]))] for b in range(B)]
+        if layout_k == "BSND":
+            width = int(sk.max()) if B else 0
+            k2 = torch.zeros(B, width, 1, dim, dtype=torch.uint8)
+            s2 = torch.zeros(B, width, 1, dtype=torch.float32)
+            for b in range(B):
+                for j, (blk, off) in enumerate(rows[b]):
+                    k2[b, j] = key[blk, off]
+                    s2[b, j] = kscale[blk, off]
+            if not bsnd_seqused:
+                assert len(set(sk.tolist())) <= 1, "without seqused_k every batch fills its slab"
+                used_k = None
+        else:
+            flat = [r for rb in rows for r in rb]
+            k2 = torch.zeros(len(flat), 1, dim, dtype=torch.uint8)
+            s2 = torch.zeros(len(flat), 1, dtype=torch.float32)
+            for i, (blk, off) in enumerate(flat):
+                k2[i] = key[blk, off]
+                s2[i] = kscale[blk, off]
+            cu_k = torch.zeros(B + 1, dtype=torch.int32)
+            cu_k[1:] = torch.from_numpy(np.cumsum(sk)).to(torch.int32)
+            used_k = None
+        key, kscale, table = k2, s2, None
+    offs = None if output_idx_offset is None else torch.as_tensor(np.asarray(output_idx_offset), dtype=torch.int32)
     return IndexerWorkload(
         name=name, layout=layout, batch=B, q_lens=q_lens, cu_seqlens_q=cu, query=query, query_scale=qscale,
-        weights=weights, key=key.view(total, BLOCK, 1, dim), key_scale=kscale.view(total, BLOCK, 1),
-        block_table=table, seqused_k=torch.from_numpy(sk.astype(np.int32)), cmp_residual_k=res,
+        weights=weights, key=key, key_scale=kscale, layout_k=layout_k, cu_seqlens_k=cu_k, output_idx_offset=offs,
+        block_table=table, seqused_k=used_k, cmp_residual_k=res,
         seqused_q=torch.tensor(seqused_q, dtype=torch.int32) if seqused_q is not None else None,
         topk=topk, mask_mode=mask_mode, cmp_ratio=cmp_ratio, seed=seed)
 
@@ -630,4 +676,5 @@ def indexer_device_inputs(w: IndexerWorkload, device) -> dict:
     return dict(query=mv(w.query), query_scale=mv(w.query_scale), weights=mv(w.weights), key=mv(w.key),
                 key_scale=mv(w.key_scale), block_table=mv(w.block_table), seqused_k=mv(w.seqused_k),
                 cmp_residual_k=mv(w.cmp_residual_k), seqused_q=mv(w.seqused_q), cu_seqlens_q=mv(w.cu_seqlens_q),
+                cu_seqlens_k=mv(w.cu_seqlens_k), output_idx_offset=mv(w.output_idx_offset), layout_k=w.layout_k,
                 layout=w.layout, batch=w.batch, topk=w.topk, mask_mode=w.mask_mode, cmp_ratio=w.cmp_ratio)
