@@ -88,6 +88,8 @@ class IndexerParams(ctypes.Structure):
         ("query", _ptr), ("query_scale", _ptr), ("weights", _ptr), ("key", _ptr), ("key_scale", _ptr),
         ("block_table", _ptr), ("seqused_k", _ptr), ("cmp_residual_k", _ptr), ("cu_seqlens_q", _ptr),
         ("seqused_q", _ptr), ("sparse_indices", _ptr), ("sparse_values", _ptr),
+        ("layout_k", _i32), ("max_sk", _i32), ("total_k", _i32), ("cu_seqlens_k", _ptr),
+        ("output_idx_offset", _ptr),
     ]
 
 
@@ -507,6 +509,9 @@ def lightning_indexer(
     mask_mode: int = 0,
     cmp_ratio: int = 1,
     return_value: bool = False,
+    layout_k: str = "PA_BBND",
+    cu_seqlens_k=None,
+    output_idx_offset=None,
     out=None,
     values=None,
     workspace=None,
@@ -515,9 +520,12 @@ def lightning_indexer(
     """QuantLightningIndexerV2's top-k (quant mode 1) through qsfm_lightning_indexer.
 
     query uint8 e4m3fn bytes BSND [B, S1, g, 128] or TND [T, g, 128];
-    query_scale, weights fp32 [T, g]; key uint8 e4m3fn bytes [blocks, 128, 1,
-    128]; key_scale fp32 [blocks, 128, 1]; block_table int32 [B, width];
-    seqused_k int32 [B]. Returns (sparse_indices int32 [T, 1, topk],
+    query_scale, weights fp32 [T, g]. key uint8 e4m3fn bytes by layout_k:
+    "PA_BBND" [blocks, 128, 1, 128] with block_table int32 [B, width] and
+    seqused_k int32 [B]; "BSND" [B, Sk, 1, 128] with seqused_k or None;
+    "TND" [Tk, 1, 128] with cu_seqlens_k int32 [B + 1] (block_table and
+    seqused_k None). key_scale fp32, key's shape without the last axis.
+    output_idx_offset int32 [B] or None. Returns (sparse_indices int32 [T, 1, topk],
     sparse_values bf16 [T, 1, topk] or None). workspace: a device uint8
     tensor of at least indexer_workspace_size() bytes, allocated when None.
     Argument marshalling only.
@@ -544,8 +552,14 @@ def lightning_indexer(
         raise ValueError(layout)
     p.heads, p.dim = int(query.shape[-2]), int(query.shape[-1])
     p.topk, p.mask_mode, p.cmp_ratio, p.return_value = int(topk), int(mask_mode), int(cmp_ratio), int(bool(return_value))
-    p.block_size, p.num_blocks = int(key.shape[1]), int(key.shape[0])
-    p.max_blocks = int(block_table.shape[-1])
+    p.layout_k = LAYOUT_KV[layout_k]
+    if layout_k == "PA_BBND":
+        p.block_size, p.num_blocks = int(key.shape[1]), int(key.shape[0])
+        p.max_blocks = int(block_table.shape[-1])
+    elif layout_k == "BSND":
+        p.max_sk = int(key.shape[1])
+    else:
+        p.total_k = int(key.shape[0])
     dev = query.device
     if out is None:
         out = torch.empty(T, 1, int(topk), dtype=torch.int32, device=dev)
@@ -555,6 +569,7 @@ def lightning_indexer(
     p.key, p.key_scale, p.block_table = _dptr(key), _dptr(key_scale), _dptr(block_table)
     p.seqused_k, p.cmp_residual_k = _dptr(seqused_k), _dptr(cmp_residual_k)
     p.cu_seqlens_q, p.seqused_q = _dptr(cu_seqlens_q), _dptr(seqused_q)
+    p.cu_seqlens_k, p.output_idx_offset = _dptr(cu_seqlens_k), _dptr(output_idx_offset)
     p.sparse_indices = _dptr(out)
     p.sparse_values = _dptr(values) if return_value else None
     need = ctypes.c_size_t(0)

@@ -259,7 +259,21 @@ qsfm_status check_indexer(const qsfm_indexer_params* pp, long long* T) {
   } else {
     return QSFM_ERR_INVALID_ARG;
   }
-  if (p.max_blocks < 1 || p.num_blocks < 1) return QSFM_ERR_INVALID_ARG;
+  // key layouts (parameter table: layout_k, seqused_k, cu_seqlens_k,
+  // block_table): the paged layout takes the table and seqused_k, BSND
+  // slabs an optional seqused_k, TND rows cu_seqlens_k and no seqused_k
+  if (p.layout_k == QSFM_LAYOUT_KV_PA_BBND) {
+    if (p.max_blocks < 1 || p.num_blocks < 1 || p.cu_seqlens_k != nullptr) return QSFM_ERR_INVALID_ARG;
+  } else if (p.layout_k == QSFM_LAYOUT_KV_BSND) {
+    if (p.max_sk < 0 || p.block_table != nullptr || p.cu_seqlens_k != nullptr) return QSFM_ERR_INVALID_ARG;
+    if ((long long)p.batch * p.max_sk > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
+  } else if (p.layout_k == QSFM_LAYOUT_KV_TND) {
+    if (p.total_k < 0 || p.block_table != nullptr || p.seqused_k != nullptr ||
+        (p.cu_seqlens_k == nullptr && p.batch > 0))
+      return QSFM_ERR_INVALID_ARG;
+  } else {
+    return QSFM_ERR_INVALID_ARG;
+  }
   *T = p.layout_q == QSFM_LAYOUT_BSND ? (long long)p.batch * p.max_s1 : p.total_t;
   if (*T > kMaxIndexerTokens) return QSFM_ERR_UNSUPPORTED;
   return QSFM_OK;
@@ -410,13 +424,17 @@ qsfm_status qsfm_lightning_indexer(const qsfm_indexer_params* pp, void* workspac
   const qsfm_indexer_params& p = *pp;
   if (T == 0) return QSFM_OK;
   if (p.query == nullptr || p.query_scale == nullptr || p.weights == nullptr || p.key == nullptr ||
-      p.key_scale == nullptr || p.block_table == nullptr || p.seqused_k == nullptr || p.sparse_indices == nullptr)
+      p.key_scale == nullptr || p.sparse_indices == nullptr)
+    return QSFM_ERR_INVALID_ARG;
+  if (p.layout_k == QSFM_LAYOUT_KV_PA_BBND && (p.block_table == nullptr || p.seqused_k == nullptr))
     return QSFM_ERR_INVALID_ARG;
   if (p.return_value && p.sparse_values == nullptr) return QSFM_ERR_INVALID_ARG;
-  if ((long long)p.num_blocks * p.block_size > kMaxPoolRows) return QSFM_ERR_UNSUPPORTED;
+  if (p.layout_k == QSFM_LAYOUT_KV_PA_BBND && (long long)p.num_blocks * p.block_size > kMaxPoolRows)
+    return QSFM_ERR_UNSUPPORTED;
   if (!aligned(p.query, 16) || !aligned(p.key, 16) || !aligned(p.key_scale, 16)) return QSFM_ERR_INVALID_ARG;
   const void* words[] = {p.query_scale, p.weights, p.block_table, p.seqused_k, p.cmp_residual_k,
-                         p.cu_seqlens_q, p.seqused_q, p.sparse_indices, p.sparse_values};
+                         p.cu_seqlens_q, p.seqused_q, p.sparse_indices, p.sparse_values, p.cu_seqlens_k,
+                         p.output_idx_offset};
   for (const void* w : words)
     if (!aligned(w, 4)) return QSFM_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned(workspace, 16) ||

@@ -70,7 +70,7 @@ constexpr uint64_t kIxTimeoutNs = 2000000000ull;
 constexpr uint32_t kXKs = 0;                                    // [scale slot][128] f32 key scales
 constexpr uint32_t kXCw = kXKs + kIxSSlots * kIxTile * 4;       // [2][256] f32 W * Sq
 constexpr uint32_t kXRow = kXCw + 2 * kIxMaxN * 4;              // [2][32] i32: nvis per token, flag
-constexpr uint32_t kXValid = kXRow + 2 * 32 * 4;                // [scale slot] i32 tile valid
+constexpr uint32_t kXValid = kXRow + 2 * 32 * 4;                // [scale slot] i32: -1 bad block, else 0 / first key row
 constexpr uint32_t kXScan = kXValid + kIxSSlots * 4;            // [64] i32 scan scratch
 constexpr uint32_t kXBar = kXScan + 256;                        // barriers, tmem slot, flags, plan
 constexpr uint32_t kXFixed = (kXBar + 640 + 1023) & ~1023u;     // the Q slots start here
@@ -181,11 +181,28 @@ __device__ __forceinline__ void ix_token(const qsfm_indexer_params& p, int t, in
   s1e = p.seqused_q != nullptr ? min(s1, __ldg(p.seqused_q + b)) : s1;
 }
 
+// Keys of batch b: seqused_k[b] (paged; BSND, max_sk without seqused_k) or
+// the cu_seqlens_k difference (TND), never past the end of a TND key tensor.
+__device__ __forceinline__ int ix_keys(const qsfm_indexer_params& p, int b) {
+  if (p.layout_k == QSFM_LAYOUT_KV_TND) {
+    const int c0 = __ldg(p.cu_seqlens_k + b), c1 = __ldg(p.cu_seqlens_k + b + 1);
+    return (c0 < 0 || c0 > p.total_k) ? 0 : max(0, min(c1, p.total_k) - c0);
+  }
+  if (p.layout_k == QSFM_LAYOUT_KV_BSND && p.seqused_k == nullptr) return p.max_sk;
+  return __ldg(p.seqused_k + b);
+}
+
+// Key tensor row of batch b's key 0 (BSND, TND; paged keys go through the
+// block table).
+__device__ __forceinline__ long long ix_key_base(const qsfm_indexer_params& p, int b) {
+  return p.layout_k == QSFM_LAYOUT_KV_TND ? (long long)__ldg(p.cu_seqlens_k + b) : (long long)b * p.max_sk;
+}
+
 // Keys the token at position s of batch b (chunk length s1) may see: all
-// seqused_k[b] (mask_mode 0), or the compressed keys whose last original
-// token is at or before p_c (mask_mode 3). Not capped.
+// its batch's keys (mask_mode 0), or the compressed keys whose last
+// original token is at or before p_c (mask_mode 3). Not capped.
 __device__ __forceinline__ int ix_visible(const qsfm_indexer_params& p, int b, int s, int s1) {
-  const int sk = __ldg(p.seqused_k + b);
+  const int sk = ix_keys(p, b);
   if (p.mask_mode == 0) return sk;
   const int r = p.cmp_ratio;
   const int res = p.cmp_residual_k != nullptr ? __ldg(p.cmp_residual_k + b) : 0;
@@ -282,6 +299,7 @@ struct IxShape {
   int tcols;    // TMEM columns allocated (a power of two >= na * nacc)
   int qslot;    // bytes of a Q slot (gmax * hp * 128 rounded up to 1024)
   int stages;   // key stages
+  int paged;    // keys paged through the block table (else BSND / TND rows)
   __host__ __device__ uint32_t q_off(int slot) const { return kXFixed + uint32_t(slot) * uint32_t(qslot); }
   __host__ __device__ uint32_t key_off(uint32_t st) const { return kXFixed + 2u * uint32_t(qslot) + st * kXStage; }
   __host__ __device__ uint32_t smem_bytes() const { return key_off(uint32_t(stages)) + 1024; }
@@ -334,9 +352,10 @@ __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const
     const int i_lo = max(lo - w.start, 0), i_hi = min(hi - w.start, w.tiles);
     const int i_pub = i_lo + min(x.stages, i_hi - i_lo);
     bool published = false;
+    const long long kbase = x.paged ? 0 : ix_key_base(p, w.b);  // BSND / TND: batch b's key 0
     for (int i0 = i_lo; i0 < i_hi; i0 += 32) {
       int mine = -1;
-      if (i0 + lane < i_hi) mine = __ldg(p.block_table + size_t(w.b) * p.max_blocks + i0 + lane);
+      if (x.paged && i0 + lane < i_hi) mine = __ldg(p.block_table + size_t(w.b) * p.max_blocks + i0 + lane);
       const int i1 = min(i_hi, i0 + 32);
       for (int i = i0; i < i1; ++i, ++n) {
         if (i == i_pub) {
@@ -350,13 +369,21 @@ __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const
           if ((n >= ns && !ix_wait(sm, kXbEmpty + st, ((n / ns) & 1) ^ 1, fault)) ||
               (n >= kIxSSlots && !ix_wait(sm, kXbSEmpty + ss, ((n / kIxSSlots) & 1) ^ 1, fault))) {
             go = false;
+          } else if (!x.paged) {
+            // BSND / TND rows: the box may run past the batch or the tensor
+            // (zero fill, scores masked); the epilogue reads the scales
+            const int row0 = int(kbase) + i * kIxTile;
+            valid[ss] = row0;
+            mbar_arrive_expect_tx(sm.bar(kXbFull + st), kIxTile * kIxDim);
+            tma_load_2d_hint(sm.base + x.key_off(st), kmap, 0, row0, sm.bar(kXbFull + st), pol);
+            mbar_arrive(sm.bar(kXbSFull + ss));
           } else if (blk < 0 || blk >= p.num_blocks) {
             atomicOr(fault, QSFM_FAULT_CMP_BLOCK_ID);
-            valid[ss] = 0;  // the tile's scores become -inf; nothing is read
+            valid[ss] = -1;  // the tile's scores become -inf; nothing is read
             mbar_arrive(sm.bar(kXbFull + st));
             mbar_arrive(sm.bar(kXbSFull + ss));
           } else {
-            valid[ss] = 1;
+            valid[ss] = 0;
             mbar_arrive_expect_tx(sm.bar(kXbFull + st), kIxTile * kIxDim);
             tma_load_2d_hint(sm.base + x.key_off(st), kmap, 0, blk * kIxTile, sm.bar(kXbFull + st), pol);
             mbar_arrive_expect_tx(sm.bar(kXbSFull + ss), kIxTile * 4);
@@ -492,8 +519,13 @@ __device__ void ix_epilogue(const qsfm_indexer_params& p, const IxShape& x, cons
       int ok = 0;
       if (first < w.g) {
         if (!ix_warp_wait(sm, kXbSFull + ss, (n / kIxSSlots) & 1, fault)) return;  // the scales landed
-        sk = ksm[ss * kIxTile + row];
-        ok = valid[ss];
+        const int v0 = valid[ss];  // -1: a bad block; else 0 (paged) or the tile's first key row
+        ok = v0 >= 0;
+        if (x.paged) {
+          sk = ksm[ss * kIxTile + row];
+        } else if (ok && i * kIxTile + row < rowi[slot * 32 + w.g - 1]) {  // the row's keys (its last token sees most)
+          sk = __ldg(p.key_scale + v0 + row);
+        }
       }
       tc_fence_after();
       __syncwarp();
@@ -677,6 +709,11 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
     if (tid == 0) atomicOr(fault, nv > kIxMaxKeys ? QSFM_FAULT_KV_ROW : QSFM_FAULT_CMP_TABLE_COL);
     nv = x.kcap;
   }
+  if (tid == 0 && s == 0 && p.layout_k == QSFM_LAYOUT_KV_TND) {  // a batch past the key tensor (cut in ix_keys)
+    const int c0 = __ldg(p.cu_seqlens_k + b), c1 = __ldg(p.cu_seqlens_k + b + 1);
+    if (c0 < 0 || c1 > p.total_k) atomicOr(fault, QSFM_FAULT_KV_ROW);
+  }
+  const int off = p.output_idx_offset != nullptr ? __ldg(p.output_idx_offset + b) : 0;  // added to valid indices
   const int k = p.topk;
   int32_t* out = p.sparse_indices + size_t(t) * k;
   __nv_bfloat16* vals = p.return_value ? static_cast<__nv_bfloat16*>(p.sparse_values) + size_t(t) * k : nullptr;
@@ -684,7 +721,7 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
   grid_dependency_wait();  // the score kernel's rows are complete and visible
   if (nv <= k) {  // every visible key, then -1
     for (int j = tid; j < k; j += kSelThreads) {
-      out[j] = j < nv ? j : -1;
+      out[j] = j < nv ? j + off : -1;
       if (vals != nullptr) vals[j] = __float2bfloat16_rn(j < nv ? __ldcg(sc + j) : -INFINITY);
     }
     return;
@@ -936,7 +973,7 @@ __global__ void __launch_bounds__(kSelThreads, V <= 8 ? 2 : 1)
   for (int h = 0; h < 2; ++h)
     for (uint32_t v = m[h]; v != 0u; v &= v - 1u, ++pos) {
       const int j = 32 * (w0 + h) + (__ffs(v) - 1);
-      out[pos] = j;
+      out[pos] = j + off;
       if (vals != nullptr) vals[pos] = __float2bfloat16_rn(__ldcg(sc + j));
     }
 }
@@ -966,13 +1003,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return encode;
 }
 
-// The key pool viewed as [num_blocks * 128 rows, 128 bytes], boxes of one
-// block (128 x 128 bytes) with the 128-byte swizzle of the MMA's K-major
-// operand.
-cudaError_t make_key_map(const void* key, int num_blocks, CUtensorMap* map) {
+// The keys viewed as [rows, 128 bytes] (the paged pool's num_blocks * 128
+// rows, the BSND slabs' B * S_k, the TND tensor's T_k), boxes of 128 rows x
+// 128 bytes with the 128-byte swizzle of the MMA's K-major operand.
+cudaError_t make_key_map(const void* key, long long rows, CUtensorMap* map) {
   const auto encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {cuuint64_t(kIxDim), cuuint64_t(num_blocks) * kIxTile};
+  const cuuint64_t dims[2] = {cuuint64_t(kIxDim), cuuint64_t(rows > 0 ? rows : 1)};
   const cuuint64_t strides[1] = {cuuint64_t(kIxDim)};
   const cuuint32_t box[2] = {kIxDim, kIxTile};
   const cuuint32_t estr[2] = {1, 1};
@@ -1005,9 +1042,11 @@ IxShape indexer_shape(const qsfm_indexer_params& p, int T) {
   x.hp = (p.heads + 15) & ~15;
   x.gmax = kIxMaxN / x.hp < kIxMaxG ? kIxMaxN / x.hp : kIxMaxG;
   if (p.layout_q == QSFM_LAYOUT_BSND && p.max_s1 < x.gmax) x.gmax = p.max_s1;
-  const long long keys = (long long)p.max_blocks * kIxTile;
+  x.paged = p.layout_k == QSFM_LAYOUT_KV_PA_BBND;
+  const long long keys = x.paged ? (long long)p.max_blocks * kIxTile
+                                 : p.layout_k == QSFM_LAYOUT_KV_BSND ? (long long)p.max_sk : (long long)p.total_k;
   x.kcap = int(keys < kIxMaxKeys ? keys : kIxMaxKeys);
-  x.kstride = x.kcap;
+  x.kstride = x.kcap < kIxTile ? kIxTile : (x.kcap + kIxTile - 1) & ~(kIxTile - 1);  // whole tiles of scores
   x.nacc = (x.gmax * x.hp + 31) & ~31;
   x.na = kIxMaxAcc * x.nacc <= 512 ? kIxMaxAcc : 2;
   x.tcols = 32;
@@ -1030,7 +1069,9 @@ cudaError_t launch_indexer(const qsfm_indexer_params& p, int T, void* workspace,
       cudaFuncSetAttribute(ix_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(x.smem_bytes()));
   if (e != cudaSuccess) return e;
   CUtensorMap kmap, qmap;
-  if ((e = make_key_map(p.key, p.num_blocks, &kmap)) != cudaSuccess) return e;
+  const long long key_rows = x.paged ? (long long)p.num_blocks * kIxTile
+                             : p.layout_k == QSFM_LAYOUT_KV_BSND ? (long long)p.batch * p.max_sk : (long long)p.total_k;
+  if ((e = make_key_map(p.key, key_rows, &kmap)) != cudaSuccess) return e;
   if ((e = make_query_map(p.query, p.heads, T, x.hp, x.gmax, &qmap)) != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;

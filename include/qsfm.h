@@ -95,7 +95,7 @@
 extern "C" {
 #endif
 
-#define QSFM_ABI_VERSION 5
+#define QSFM_ABI_VERSION 6
 #define QSFM_NUM_HEADS 64
 #define QSFM_HEAD_DIM 512
 #define QSFM_BLOCK_SIZE 128
@@ -351,9 +351,19 @@ qsfm_status qsfm_debug_bounded_wait(uint64_t timeout_ns, uint64_t* elapsed_ns_ou
  * Layout (all device memory, caller-owned):
  *   query        e4m3fn bytes BSND [B, S1, heads, dim] / TND [T, heads, dim]
  *   query_scale  fp32 [T, heads];  weights fp32 [T, heads]
- *   key          e4m3fn bytes, paged [num_blocks, 128, 1, dim]
- *   key_scale    fp32 [num_blocks, 128, 1], paged like key
- *   block_table  int32 [B, max_blocks];  seqused_k int32 [B] (required)
+ *   key          e4m3fn bytes (parameter table: layout_k):
+ *                  PA_BBND (default) paged [num_blocks, 128, 1, dim] through
+ *                    block_table int32 [B, max_blocks], seqused_k[b] keys
+ *                    (seqused_k required);
+ *                  BSND [B, max_sk, 1, dim], batch b's key j at [b, j],
+ *                    seqused_k[b] keys (max_sk when seqused_k is NULL);
+ *                  TND [total_k, 1, dim], batch b's key j at row
+ *                    cu_seqlens_k[b] + j, cu_seqlens_k[b + 1] - cu_seqlens_k[b]
+ *                    keys (cu_seqlens_k int32 [B + 1] required, seqused_k
+ *                    NULL)
+ *   key_scale    fp32, the key's layout without the dim axis
+ *   output_idx_offset int32 [B] or NULL: every valid index of a batch-b row
+ *                is reported plus output_idx_offset[b] (-1 stays -1)
  *   cmp_residual_k int32 [B] or NULL (0);  cu_seqlens_q int32 [B + 1]
  *                (required for TND);  seqused_q int32 [B] or NULL: query
  *                rows of batch b from seqused_q[b] on are padding (all -1;
@@ -364,8 +374,9 @@ qsfm_status qsfm_debug_bounded_wait(uint64_t timeout_ns, uint64_t* elapsed_ns_ou
  *                the scores of the listed keys, -inf after them)
  * Built shapes (QSFM_ERR_UNSUPPORTED otherwise): dim = 128, 1 <= heads
  * <= 64, 1 <= topk <= 8192, block size 128, at most 2^20 query rows, at
- * most min(32768, max_blocks * 128) keys per batch (a larger seqused_k is
- * cut to that and flagged: QSFM_FAULT_KV_ROW past 32768, else
+ * most 32768 keys per batch and at most max_blocks * 128 (paged) or max_sk
+ * (BSND) of them; a larger key count is cut and flagged
+ * (QSFM_FAULT_KV_ROW past 32768 or past the end of a TND key tensor, else
  * QSFM_FAULT_CMP_TABLE_COL). A block id outside [0, num_blocks) is flagged
  * with QSFM_FAULT_CMP_BLOCK_ID, its keys score -inf and are not read.
  * Pointers: query, key, key_scale 16-byte aligned, the rest 4-byte aligned.
@@ -396,6 +407,12 @@ typedef struct qsfm_indexer_params {
   const int32_t* seqused_q;
   int32_t* sparse_indices;
   void* sparse_values;
+  /* version 6: the key layouts and the index offset */
+  int32_t layout_k;     /* qsfm_kv_layout: PA_BBND (default), BSND or TND   */
+  int32_t max_sk;       /* BSND keys: S_k, the key tensor's S dimension     */
+  int32_t total_k;      /* TND keys: T_k, the key tensor's rows             */
+  const int32_t* cu_seqlens_k;
+  const int32_t* output_idx_offset;
 } qsfm_indexer_params;
 
 /* Defaults: dim 128, heads 64, topk 2048 (the page's default), block size

@@ -39,7 +39,7 @@ def test_every_declared_function_is_exported(lib):
     assert set(names) <= set(Q.EXPORTS)
     # version 2 appended qsfm_params.kv_layout, version 3 the KV storage layouts and ori
     # picks, version 4 the lightning indexer's entry points
-    assert lib.qsfm_abi_version() == 5
+    assert lib.qsfm_abi_version() == 6
 
 
 def test_exports_are_c_symbols(lib):
@@ -355,6 +355,11 @@ INDEXER_INVALID = [
     ("no output", dict(sparse_indices=None), 1), ("values without buffer", dict(return_value=1), 1),
     ("key not 16-byte aligned", dict(key=0x1008), 1), ("key scale not 16-byte aligned", dict(key_scale=0x1004), 1),
     ("weights not 4-byte aligned", dict(weights=0x1002), 1), ("no blocks", dict(num_blocks=0), 1),
+    ("key layout 3", dict(layout_k=3), 1), ("paged keys with cu_seqlens_k", dict(cu_seqlens_k=0x1000), 1),
+    ("BSND keys with a block table", dict(layout_k=1, max_sk=300), 1),
+    ("TND keys without cu_seqlens_k", dict(layout_k=2, total_k=900, block_table=None, seqused_k=None), 1),
+    ("TND keys with seqused_k", dict(layout_k=2, total_k=900, block_table=None, cu_seqlens_k=0x1000), 1),
+    ("offsets not 4-byte aligned", dict(output_idx_offset=0x1002), 1),
 ]
 
 
@@ -419,3 +424,20 @@ def test_last_cuda_error_starts_clear(lib):
     assert lib.qsfm_last_cuda_error(ctypes.byref(name)) == 0
     assert name.value == b"cudaSuccess"
     assert lib.qsfm_last_cuda_error(None) == 0
+
+
+@pytest.mark.parametrize("change", [dict(layout_k=1, max_sk=300, block_table=None),
+                                    dict(layout_k=1, max_sk=300, block_table=None, seqused_k=None),
+                                    dict(layout_k=2, total_k=900, block_table=None, seqused_k=None,
+                                         cu_seqlens_k=0x1000, output_idx_offset=0x1000)],
+                         ids=["BSND keys", "BSND keys without seqused_k", "TND keys with offsets"])
+def test_indexer_non_paged_keys_are_accepted(lib, change):
+    """BSND and TND key layouts (parameter table: layout_k) pass validation:
+    only the missing workspace is refused."""
+    p = _indexer_valid(lib)
+    for k, v in change.items():
+        setattr(p, k, v)
+    assert lib.qsfm_lightning_indexer(ctypes.byref(p), None, 0, None) == 4
+    n = ctypes.c_size_t(0)
+    assert lib.qsfm_lightning_indexer_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    assert n.value == 2 * (384 if change["layout_k"] == 1 else 1024) * 4

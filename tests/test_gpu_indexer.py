@@ -37,7 +37,8 @@ def run(w, device, return_value=True):
                                    a["block_table"], a["seqused_k"], layout=w.layout, batch=w.batch,
                                    cu_seqlens_q=a["cu_seqlens_q"], seqused_q=a["seqused_q"],
                                    cmp_residual_k=a["cmp_residual_k"], topk=w.topk, mask_mode=w.mask_mode,
-                                   cmp_ratio=w.cmp_ratio, return_value=return_value)
+                                   cmp_ratio=w.cmp_ratio, return_value=return_value, layout_k=w.layout_k,
+                                   cu_seqlens_k=a["cu_seqlens_k"], output_idx_offset=a["output_idx_offset"])
     torch.cuda.synchronize()
     idx = idx.reshape(w.total_t, w.topk).cpu().numpy()
     val = None if val is None else val.reshape(w.total_t, w.topk).float().cpu().numpy()
@@ -51,10 +52,8 @@ def fp32_bound(w, t):
     v = I.visible_keys(w, b, s)
     if v == 0:
         return 0.0
-    bs = int(w.key.shape[1])
-    blk = w.block_table[b, :(v + bs - 1) // bs].long()
-    k = E4M3FN_TABLE[w.key[blk].reshape(-1, w.key.shape[-1])[:v].numpy().astype(np.int64)]
-    sk = w.key_scale[blk].reshape(-1)[:v].double().numpy()
+    kb, sk = I.key_rows(w, b, v)
+    k = E4M3FN_TABLE[np.asarray(kb).astype(np.int64)]
     q = E4M3FN_TABLE[w.query[t].numpy().astype(np.int64)]
     absum = (np.abs(w.weights[t].double().numpy()) * np.abs(w.query_scale[t].double().numpy())) @ (np.abs(q) @ np.abs(k).T)
     return float((absum * np.abs(sk)).max()) * 2.0 ** -24 * (q.shape[1] + q.shape[0] + 4)
@@ -70,6 +69,11 @@ def check(w, idx, val, tokens=None):
         nv = int((want >= 0).sum())
         assert int((got >= 0).sum()) == nv, t
         assert np.all(got[nv:] == -1) and np.all(np.diff(got[:nv]) > 0), t  # ascending, then -1
+        offs = getattr(w, "output_idx_offset", None)
+        if offs is not None:  # compare key indices from here on
+            shift = int(offs[int(w.token_batch()[t])])
+            got = np.where(got >= 0, got - shift, got)
+            want = np.where(want >= 0, want - shift, want)
         eps = fp32_bound(w, t)
         if I.boundary_gap(w, t) > 2 * eps:
             assert np.array_equal(got, want), t  # a unique selection: bit for bit
@@ -98,6 +102,12 @@ CASES = {
                            seqused_q=[1, 3]),
     "tnd_padding": dict(layout="TND", q_lens=[4, 2, 5], sk=[1500, 90, 4000], topk=40, mask_mode=3, cmp_ratio=4,
                         seqused_q=[2, 2, 0], heads=32),
+    "bsnd_keys_offsets": dict(layout="BSND", q_lens=[2, 2, 2], sk=[300, 2900, 5000], topk=64, mask_mode=3,
+                              cmp_ratio=4, layout_k="BSND", output_idx_offset=[0, 300, 3200]),
+    "tnd_keys": dict(layout="TND", q_lens=[3, 1, 5], sk=[1040, 700, 129], topk=50, mask_mode=3, cmp_ratio=3,
+                     heads=8, layout_k="TND", output_idx_offset=[0, 1040, 1740]),
+    "bsnd_keys_full_slabs": dict(layout="BSND", q_lens=[1, 1], sk=[700, 700], topk=100, mask_mode=0,
+                                 layout_k="BSND", bsnd_seqused=False),
     "topk_8192_long": dict(layout="BSND", q_lens=[1, 1], sk=[30000, 9000], topk=8192, mask_mode=0, heads=64),
 }
 
@@ -173,3 +183,15 @@ def test_indexer_keys_past_the_table_are_cut_and_flagged(cuda_device):
     assert Q.device_status() & Q.FAULT_CMP_TABLE_COL
     row = idx[0]
     assert np.all((row >= 0) & (row < 512))
+
+
+@pytest.mark.parametrize("layout_k", ["BSND", "TND"])
+def test_non_paged_keys_equal_paged_bitwise(cuda_device, layout_k):
+    """The same logical keys as BSND slabs or TND rows give the paged
+    layout's rows and values bit for bit (the scores of a key do not depend
+    on where its row is stored)."""
+    base = dict(layout="BSND", q_lens=[2, 2], sk=[1800, 4300], topk=256, mask_mode=3, cmp_ratio=4, seed=41)
+    ref = run(W.build_indexer("paged", **base), cuda_device)
+    got = run(W.build_indexer(layout_k, layout_k=layout_k, **base), cuda_device)
+    assert Q.device_status() == 0
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
