@@ -59,6 +59,7 @@ constexpr int kIxDim = 128;        // bytes (= e4m3 elements) per query / key ro
 constexpr int kIxTile = 128;       // keys per tile (one paged block)
 constexpr int kIxMaxStages = 12;  // key stages (as many as shared memory holds)
 constexpr int kIxSSlots = 16;      // key-scale ring (freed by the epilogue, which trails the MMAs)
+static_assert(kIxSSlots == 16, "scale slots and their phases are taken from the low bits of the tile count");
 constexpr int kIxMaxKeys = 32768;  // keys per token the select holds in shared memory
 constexpr int kIxMaxHeads = 64;
 constexpr int kIxMaxN = 256;       // MMA N = tokens of a row x padded heads
@@ -319,7 +320,11 @@ __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const
   int* valid = sm.i(kXValid);
   const uint32_t qbytes = uint32_t(x.gmax * x.hp * kIxDim);
   const uint64_t pol = l2_evict_first();
-  uint32_t n = 0;  // tiles issued
+  // tile n's stage and scale slot, and the parities of their previous use,
+  // kept as running counters (no divisions on the issuing lane)
+  const uint32_t ns = uint32_t(x.stages);
+  const uint32_t key0 = sm.base + x.key_off(0);
+  uint32_t n = 0, st = 0, st_par = 1;
   for (uint32_t qn = 0;; ++qn) {
     const int slot = int(qn & 1);
     if (qn >= 2 && !ix_warp_wait(sm, kXbQEmpty + slot, ((qn >> 1) & 1) ^ 1, fault)) return;
@@ -364,10 +369,10 @@ __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const
         }
         const int blk = __shfl_sync(0xffffffffu, mine, i - i0);
         bool go = true;
+        const uint32_t ss = n & (kIxSSlots - 1), ss_par = ((n >> 4) & 1) ^ 1;
         if (lane == 0) {
-          const uint32_t ns = uint32_t(x.stages), st = n % ns, ss = n % kIxSSlots;
-          if ((n >= ns && !ix_wait(sm, kXbEmpty + st, ((n / ns) & 1) ^ 1, fault)) ||
-              (n >= kIxSSlots && !ix_wait(sm, kXbSEmpty + ss, ((n / kIxSSlots) & 1) ^ 1, fault))) {
+          if ((n >= ns && !ix_wait(sm, kXbEmpty + st, st_par, fault)) ||
+              (n >= kIxSSlots && !ix_wait(sm, kXbSEmpty + ss, ss_par, fault))) {
             go = false;
           } else if (!x.paged) {
             // BSND / TND rows: the box may run past the batch or the tensor
@@ -375,7 +380,7 @@ __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const
             const int row0 = int(kbase) + i * kIxTile;
             valid[ss] = row0;
             mbar_arrive_expect_tx(sm.bar(kXbFull + st), kIxTile * kIxDim);
-            tma_load_2d_hint(sm.base + x.key_off(st), kmap, 0, row0, sm.bar(kXbFull + st), pol);
+            tma_load_2d_hint(key0 + st * kXStage, kmap, 0, row0, sm.bar(kXbFull + st), pol);
             mbar_arrive(sm.bar(kXbSFull + ss));
           } else if (blk < 0 || blk >= p.num_blocks) {
             atomicOr(fault, QSFM_FAULT_CMP_BLOCK_ID);
@@ -385,13 +390,17 @@ __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const
           } else {
             valid[ss] = 0;
             mbar_arrive_expect_tx(sm.bar(kXbFull + st), kIxTile * kIxDim);
-            tma_load_2d_hint(sm.base + x.key_off(st), kmap, 0, blk * kIxTile, sm.bar(kXbFull + st), pol);
+            tma_load_2d_hint(key0 + st * kXStage, kmap, 0, blk * kIxTile, sm.bar(kXbFull + st), pol);
             mbar_arrive_expect_tx(sm.bar(kXbSFull + ss), kIxTile * 4);
             bulk_g2s_hint(sm.base + kXKs + ss * (kIxTile * 4), p.key_scale + size_t(blk) * kIxTile, kIxTile * 4,
                           sm.bar(kXbSFull + ss), pol);
           }
         }
         if (__shfl_sync(0xffffffffu, go ? 1 : 0, 0) == 0) return;
+        if (++st == ns) {
+          st = 0;
+          st_par ^= 1;
+        }
       }
     }
     if (!published) publish();
@@ -404,8 +413,11 @@ __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const
 // accumulator n mod na; the row's Q slot is released after its last tile.
 __device__ void ix_mma(const qsfm_indexer_params& p, const IxShape& x, const IxSmem& sm, IxWalk w, int lo, int hi,
                        uint32_t tmem, int* fault) {
-  const uint32_t na = uint32_t(x.na);
-  uint32_t n = 0;
+  const uint32_t na = uint32_t(x.na), ns = uint32_t(x.stages), nacc = uint32_t(x.nacc);
+  const uint64_t kdesc0 = make_sdesc_sw128(sm.base + x.key_off(0), 16, 1024);
+  // tile n's stage and accumulator with the parities of their use, kept as
+  // running counters (no divisions on the issuing thread)
+  uint32_t n = 0, st = 0, st_par = 0, a = 0, a_par = 0;
   for (uint32_t qn = 0;; ++qn) {
     const int slot = int(qn & 1);
     if (!ix_wait(sm, kXbQFull + slot, (qn >> 1) & 1, fault)) return;
@@ -414,17 +426,24 @@ __device__ void ix_mma(const qsfm_indexer_params& p, const IxShape& x, const IxS
     const uint64_t bdesc = make_sdesc_sw128(sm.base + x.q_off(slot), 16, 1024);
     const int i_lo = max(lo - w.start, 0), i_hi = min(hi - w.start, w.tiles);
     for (int i = i_lo; i < i_hi; ++i, ++n) {
-      const uint32_t ns = uint32_t(x.stages), st = n % ns, a = n % na;
-      if (!ix_wait(sm, kXbFull + st, (n / ns) & 1, fault)) return;
-      if (n >= na && !ix_wait(sm, kXbTEmpty + a, ((n / na) & 1) ^ 1, fault)) return;
+      if (!ix_wait(sm, kXbFull + st, st_par, fault)) return;
+      if (n >= na && !ix_wait(sm, kXbTEmpty + a, a_par ^ 1, fault)) return;
       tc_fence_after();
-      const uint64_t adesc = make_sdesc_sw128(sm.base + x.key_off(st), 16, 1024);
-      const uint32_t d = tmem + a * uint32_t(x.nacc);
+      const uint64_t adesc = kdesc0 + uint64_t((st * kXStage) >> 4);
+      const uint32_t d = tmem + a * nacc;
 #pragma unroll
       for (int k = 0; k < kIxDim / 32; ++k)  // 32 e4m3 (32 bytes) of d per MMA
         mma_f8(d, adesc + uint64_t((k * 32) >> 4), bdesc + uint64_t((k * 32) >> 4), idesc, k > 0 ? 1u : 0u);
       mma_commit(sm.bar(kXbTFull + a));
       mma_commit(sm.bar(kXbEmpty + st));
+      if (++st == ns) {
+        st = 0;
+        st_par ^= 1;
+      }
+      if (++a == na) {
+        a = 0;
+        a_par ^= 1;
+      }
     }
     mma_commit(sm.bar(kXbQEmpty + slot));
     if (!ix_next(p, x.T, x.gmax, x.kcap, w) || w.start >= hi) return;
@@ -499,26 +518,26 @@ __device__ void ix_epilogue(const qsfm_indexer_params& p, const IxShape& x, cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3, grp = (warp - 2) >> 2;
   const int row = 32 * quarter + lane;
-  const uint32_t na = uint32_t(x.na);
+  const uint32_t na = uint32_t(x.na), nacc = uint32_t(x.nacc);
   const float* cwb = sm.f(kXCw);
   const int* rowi = sm.i(kXRow);
   const float* ksm = sm.f(kXKs);
   const int* valid = sm.i(kXValid);
-  uint32_t n = 0;
+  uint32_t n = 0, a = 0, a_par = 0;  // tile n's accumulator and the parity of its use
   for (uint32_t qn = 0;; ++qn) {
     const int slot = int(qn & 1);
     if (!ix_warp_wait(sm, kXbCwFull + slot, (qn >> 1) & 1, fault)) return;
     const bool neg = rowi[slot * 32 + kIxMaxG] != 0;
     const int i_lo = max(lo - w.start, 0), i_hi = min(hi - w.start, w.tiles);
     for (int i = i_lo; i < i_hi; ++i, ++n) {
-      const uint32_t ss = n % kIxSSlots, a = n % na;
+      const uint32_t ss = n & (kIxSSlots - 1);
       // this group's first item of the tile: gg = grp - n g (mod 4)
       const int first = int((uint32_t(grp) - n * uint32_t(w.g)) & uint32_t(kIxGroups - 1));
-      if (!ix_warp_wait(sm, kXbTFull + a, (n / na) & 1, fault)) return;
+      if (!ix_warp_wait(sm, kXbTFull + a, a_par, fault)) return;
       float sk = 0.f;
       int ok = 0;
       if (first < w.g) {
-        if (!ix_warp_wait(sm, kXbSFull + ss, (n / kIxSSlots) & 1, fault)) return;  // the scales landed
+        if (!ix_warp_wait(sm, kXbSFull + ss, (n >> 4) & 1, fault)) return;  // the scales landed
         const int v0 = valid[ss];  // -1: a bad block; else 0 (paged) or the tile's first key row
         ok = v0 >= 0;
         if (x.paged) {
@@ -533,7 +552,7 @@ __device__ void ix_epilogue(const qsfm_indexer_params& p, const IxShape& x, cons
       // producer has already seen the slot's previous use released)
       if (lane == 0) mbar_arrive(sm.bar(kXbSEmpty + ss));
       const int j = i * kIxTile + row, jw = i * kIxTile + 32 * quarter;
-      const uint32_t taddr = tmem + a * uint32_t(x.nacc) + (uint32_t(32 * quarter) << 16);
+      const uint32_t taddr = tmem + a * nacc + (uint32_t(32 * quarter) << 16);
       const bool fast = __all_sync(0xffffffffu, !neg && sk >= 0.f);
       for (int gg = first; gg < w.g; gg += kIxGroups) {
         const int nv = rowi[slot * 32 + gg];
@@ -545,6 +564,10 @@ __device__ void ix_epilogue(const qsfm_indexer_params& p, const IxShape& x, cons
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(kXbTEmpty + a));
+      if (++a == na) {
+        a = 0;
+        a_par ^= 1;
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.bar(kXbQEmpty + slot));
