@@ -307,16 +307,46 @@ struct IxShape {
 };
 
 // ------------------------------------------------------------- producer
+// The head factors W * Sq of row w's tokens (0 past the real heads), the
+// keys each token sees and whether any query scale is negative, into Q slot
+// `slot`'s shared tables; all 32 lanes of the calling warp arrive on the
+// slot's CwFull barrier.
+__device__ __forceinline__ void ix_publish(const qsfm_indexer_params& p, const IxShape& x, const IxSmem& sm,
+                                           const IxWalk& w, int slot) {
+  const int lane = threadIdx.x & 31;
+  float* cwb = sm.f(kXCw);
+  int* rowi = sm.i(kXRow);
+  bool neg = false;  // a negative query scale (not produced by amax / 448 quantisation)
+  for (int i = lane; i < w.g * x.hp; i += 32) {
+    const int gg = i / x.hp, h = i - gg * x.hp;
+    float c = 0.f;
+    if (h < p.heads) {
+      const size_t o = size_t(w.t + gg) * p.heads + h;
+      const float sq = __ldg(p.query_scale + o);
+      c = __ldg(p.weights + o) * sq;
+      neg |= sq < 0.f;
+    }
+    cwb[slot * kIxMaxN + i] = c;
+  }
+  if (lane < w.g) {
+    int b, s, s1, s1e;
+    ix_token(p, w.t + lane, b, s, s1, s1e);
+    rowi[slot * 32 + lane] = min(x.kcap, ix_visible(p, b, s, s1));
+  }
+  const bool any_neg = __any_sync(0xffffffffu, neg);
+  if (lane == 0) rowi[slot * 32 + kIxMaxG] = any_neg ? 1 : 0;
+  mbar_arrive(sm.bar(kXbCwFull + slot));
+}
+
 // Per row: the row's Q (one 3-D box: hp heads x gmax tokens), then the row's
 // key tiles in this CTA's range (the block table read 32 entries at a time;
 // per tile the key block into a stage and its scales into a scale slot).
 // Once the first stages are in flight, the row's head factors W * Sq and the
-// keys each token sees are published for the epilogue.
+// keys each token sees are published for the epilogue (the first row's by
+// an epilogue warp, at the start).
 __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const IxSmem& sm, IxWalk w, int lo,
                            int hi, int* fault, const CUtensorMap* kmap, const CUtensorMap* qmap) {
   const int lane = threadIdx.x & 31;
-  float* cwb = sm.f(kXCw);
-  int* rowi = sm.i(kXRow);
   int* valid = sm.i(kXValid);
   const uint32_t qbytes = uint32_t(x.gmax * x.hp * kIxDim);
   const uint64_t pol = l2_evict_first();
@@ -332,39 +362,20 @@ __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const
       mbar_arrive_expect_tx(sm.bar(kXbQFull + slot), qbytes);
       tma_load_3d(sm.base + x.q_off(slot), qmap, 0, 0, w.t, sm.bar(kXbQFull + slot));
     }
-    auto publish = [&]() {
-      bool neg = false;  // a negative query scale (not produced by amax / 448 quantisation)
-      for (int i = lane; i < w.g * x.hp; i += 32) {
-        const int gg = i / x.hp, h = i - gg * x.hp;
-        float c = 0.f;
-        if (h < p.heads) {
-          const size_t o = size_t(w.t + gg) * p.heads + h;
-          const float sq = __ldg(p.query_scale + o);
-          c = __ldg(p.weights + o) * sq;
-          neg |= sq < 0.f;
-        }
-        cwb[slot * kIxMaxN + i] = c;
-      }
-      if (lane < w.g) {
-        int b, s, s1, s1e;
-        ix_token(p, w.t + lane, b, s, s1, s1e);
-        rowi[slot * 32 + lane] = min(x.kcap, ix_visible(p, b, s, s1));
-      }
-      const bool any_neg = __any_sync(0xffffffffu, neg);
-      if (lane == 0) rowi[slot * 32 + kIxMaxG] = any_neg ? 1 : 0;
-      mbar_arrive(sm.bar(kXbCwFull + slot));
-    };
+    // the first row's tables are published by an epilogue warp at the start
+    // (idle then); later rows' by this warp once their first stages are in
+    // flight
     const int i_lo = max(lo - w.start, 0), i_hi = min(hi - w.start, w.tiles);
     const int i_pub = i_lo + min(x.stages, i_hi - i_lo);
-    bool published = false;
+    bool published = qn == 0;
     const long long kbase = x.paged ? 0 : ix_key_base(p, w.b);  // BSND / TND: batch b's key 0
     for (int i0 = i_lo; i0 < i_hi; i0 += 32) {
       int mine = -1;
       if (x.paged && i0 + lane < i_hi) mine = __ldg(p.block_table + size_t(w.b) * p.max_blocks + i0 + lane);
       const int i1 = min(i_hi, i0 + 32);
       for (int i = i0; i < i1; ++i, ++n) {
-        if (i == i_pub) {
-          publish();
+        if (i == i_pub && !published) {
+          ix_publish(p, x, sm, w, slot);
           published = true;
         }
         const int blk = __shfl_sync(0xffffffffu, mine, i - i0);
@@ -403,7 +414,7 @@ __device__ void ix_produce(const qsfm_indexer_params& p, const IxShape& x, const
         }
       }
     }
-    if (!published) publish();
+    if (!published) ix_publish(p, x, sm, w, slot);
     if (!ix_next(p, x.T, x.gmax, x.kcap, w) || w.start >= hi) return;
   }
 }
@@ -524,6 +535,7 @@ __device__ void ix_epilogue(const qsfm_indexer_params& p, const IxShape& x, cons
   const float* ksm = sm.f(kXKs);
   const int* valid = sm.i(kXValid);
   uint32_t n = 0, a = 0, a_par = 0;  // tile n's accumulator and the parity of its use
+  if (warp == 2) ix_publish(p, x, sm, w, 0);  // the first row's tables (the producer publishes the rest)
   for (uint32_t qn = 0;; ++qn) {
     const int slot = int(qn & 1);
     if (!ix_warp_wait(sm, kXbCwFull + slot, (qn >> 1) & 1, fault)) return;
