@@ -109,6 +109,10 @@ CASES = {
     "bsnd_keys_full_slabs": dict(layout="BSND", q_lens=[1, 1], sk=[700, 700], topk=100, mask_mode=0,
                                  layout_k="BSND", bsnd_seqused=False),
     "topk_8192_long": dict(layout="BSND", q_lens=[1, 1], sk=[30000, 9000], topk=8192, mask_mode=0, heads=64),
+    # more query rows than the score kernel has threads (its start-up scan
+    # then takes two tokens per thread), rows of four 64-head tokens (N = 256)
+    "tnd_prefill_650": dict(layout="TND", q_lens=[250, 400], sk=[500, 1200], topk=48, mask_mode=3, cmp_ratio=4,
+                            heads=64),
 }
 
 
